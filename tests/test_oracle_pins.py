@@ -1,0 +1,455 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each pin compares an oracle function with a library routine (torch CPU ops and
+torch autograd on an independently assembled model), a closed form, an
+invariant or finite differences.  The planted-mistake tests at the end show
+that plausible slips in the oracle (a wrong sign, a dropped term, a wrong
+mask or index) make at least one pin fail.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import inputs
+import oracle
+from inputs import CONFIGS, TEST_CONFIGS, IGNORE_INDEX
+from oracle import llama_step as ls
+from tests.helpers import oracle_weights, rel_l2
+
+torch.set_default_dtype(torch.float64)
+RNG = np.random.default_rng(0)
+
+
+def t64(a):
+    return torch.tensor(np.asarray(a, dtype=np.float64))
+
+
+# ------------------------------------------------------------------ pins as functions
+def pin_rmsnorm_vs_torch(d=96, rows=7, eps=1e-5):
+    x = RNG.standard_normal((rows, d)) * 3
+    g = RNG.standard_normal(d)
+    dy = RNG.standard_normal((rows, d))
+    y, cache = ls.rmsnorm_fwd(x, g, eps)
+    dx, dg = ls.rmsnorm_bwd(dy, g, cache)
+    xt, gt = t64(x).requires_grad_(), t64(g).requires_grad_()
+    yt = F.rms_norm(xt, (d,), weight=gt, eps=eps)
+    yt.backward(t64(dy))
+    return max(rel_l2(y, yt.detach()), rel_l2(dx, xt.grad), rel_l2(dg, gt.grad))
+
+
+def rope_complex_torch(x, base):
+    """RoPE as complex multiplication: (x_j + i x_{j+hd/2}) * exp(i s theta_j)."""
+    B, S, H, hd = x.shape
+    half = hd // 2
+    theta = float(base) ** (-2.0 * torch.arange(half, dtype=torch.float64) / hd)
+    ang = torch.arange(S, dtype=torch.float64)[:, None] * theta[None, :]
+    rot = torch.polar(torch.ones_like(ang), ang)[None, :, None, :]
+    yc = torch.complex(x[..., :half], x[..., half:]) * rot
+    return torch.cat([yc.real, yc.imag], dim=-1)
+
+
+def pin_rope_vs_complex(S=37, hd=64, base=500000.0):
+    x = RNG.standard_normal((2, S, 3, hd))
+    dy = RNG.standard_normal((2, S, 3, hd))
+    cos, sin = ls.rope_tables(S, hd, base)
+    y = ls.rope_fwd(x, cos, sin)
+    dx = ls.rope_bwd(dy, cos, sin)
+    xt = t64(x).requires_grad_()
+    yt = rope_complex_torch(xt, base)
+    yt.backward(t64(dy))
+    return max(rel_l2(y, yt.detach()), rel_l2(dx, xt.grad))
+
+
+def torch_causal_attention(q, k, v):
+    """q [B,S,Hq,hd], k/v [B,S,Hkv,hd] -> o [B,S,Hq,hd] via torch SDPA."""
+    grp = q.shape[2] // k.shape[2]
+    qt, kt, vt = (a.transpose(1, 2) for a in (q, k, v))
+    kt = kt.repeat_interleave(grp, dim=1)
+    vt = vt.repeat_interleave(grp, dim=1)
+    return F.scaled_dot_product_attention(qt, kt, vt, is_causal=True).transpose(1, 2)
+
+
+def pin_attention_vs_sdpa(S=33, Hq=4, Hkv=2, hd=16):
+    q = RNG.standard_normal((2, S, Hq, hd))
+    k = RNG.standard_normal((2, S, Hkv, hd))
+    v = RNG.standard_normal((2, S, Hkv, hd))
+    do = RNG.standard_normal((2, S, Hq, hd))
+    o, _ = ls.attention_fwd(q, k, v)
+    dq, dk, dv = ls.attention_bwd(do, q, k, v)
+    qt, kt, vt = (t64(a).requires_grad_() for a in (q, k, v))
+    ot = torch_causal_attention(qt, kt, vt)
+    ot.backward(t64(do))
+    return max(rel_l2(o, ot.detach()), rel_l2(dq, qt.grad), rel_l2(dk, kt.grad),
+               rel_l2(dv, vt.grad))
+
+
+def pin_swiglu_vs_torch(n=1000):
+    a = RNG.standard_normal(n) * 4
+    b = RNG.standard_normal(n)
+    dm = RNG.standard_normal(n)
+    m = ls.swiglu_fwd(a, b)
+    da, db = ls.swiglu_bwd(dm, a, b)
+    at, bt = t64(a).requires_grad_(), t64(b).requires_grad_()
+    mt = F.silu(at) * bt
+    mt.backward(t64(dm))
+    return max(rel_l2(m, mt.detach()), rel_l2(da, at.grad), rel_l2(db, bt.grad))
+
+
+def pin_ce_vs_torch(N=50, V=97):
+    z = RNG.standard_normal((N, V)) * 3
+    lab = RNG.integers(0, V, N)
+    lab[::7] = IGNORE_INDEX
+    loss, dz, _ = ls.cross_entropy_fwd_bwd(z, lab)
+    zt = t64(z).requires_grad_()
+    lt = F.cross_entropy(zt, torch.tensor(lab), ignore_index=IGNORE_INDEX)
+    lt.backward()
+    return max(abs(loss - lt.item()) / abs(lt.item()), rel_l2(dz, zt.grad))
+
+
+# ------------------------------------------------------------------ library-routine pins
+def test_rmsnorm_matches_torch():
+    assert pin_rmsnorm_vs_torch() < 1e-12
+
+
+def test_rope_matches_complex_rotation():
+    assert pin_rope_vs_complex() < 1e-12
+
+
+def test_attention_matches_torch_sdpa_gqa():
+    assert pin_attention_vs_sdpa() < 1e-12
+    assert pin_attention_vs_sdpa(S=5, Hq=3, Hkv=3, hd=8) < 1e-12
+
+
+def test_swiglu_matches_torch():
+    assert pin_swiglu_vs_torch() < 1e-12
+
+
+def test_cross_entropy_matches_torch():
+    assert pin_ce_vs_torch() < 1e-12
+
+
+# ------------------------------------------------------------------ closed forms / invariants
+def test_rmsnorm_second_moment():
+    x = RNG.standard_normal((5, 64)) * 0.01
+    eps = 1e-5
+    y, _ = ls.rmsnorm_fwd(x, np.ones(64), eps)
+    ms = np.mean(x * x, axis=1)
+    assert np.allclose(np.mean(y * y, axis=1), ms / (ms + eps), rtol=1e-12)
+
+
+def test_rope_worked_values_and_identity():
+    # hd = 4, base 10000: theta = (1, 0.01).  Position 1 rotates e0 into (cos 1, 0, sin 1, 0).
+    cos, sin = ls.rope_tables(2, 4, 10000.0)
+    e = np.eye(4)[None, None, :, :].repeat(2, axis=1).transpose(0, 1, 2, 3)  # [1,2,4(heads),4]
+    y = ls.rope_fwd(e, cos, sin)
+    assert np.allclose(y[0, 0], np.eye(4))                               # s = 0: identity
+    assert np.allclose(y[0, 1, 0], [math.cos(1), 0, math.sin(1), 0])
+    assert np.allclose(y[0, 1, 1], [0, math.cos(0.01), 0, math.sin(0.01)])
+    assert np.allclose(y[0, 1, 2], [-math.sin(1), 0, math.cos(1), 0])
+
+
+def test_rope_norm_and_relative_position():
+    S, hd = 50, 32
+    cos, sin = ls.rope_tables(S, hd, 10000.0)
+    q = np.broadcast_to(RNG.standard_normal(hd), (1, S, 1, hd)).copy()
+    k = np.broadcast_to(RNG.standard_normal(hd), (1, S, 1, hd)).copy()
+    rq, rk = ls.rope_fwd(q, cos, sin), ls.rope_fwd(k, cos, sin)
+    assert np.allclose(np.linalg.norm(rq, axis=-1), np.linalg.norm(q, axis=-1))
+    dots = np.einsum("sd,rd->sr", rq[0, :, 0], rk[0, :, 0])
+    for delta in (0, 3, 17):
+        diag = np.diagonal(dots, offset=-delta)      # pairs (s, s - delta)
+        assert np.allclose(diag, diag[0], atol=1e-12)
+    # backward is the adjoint of forward
+    x, y = RNG.standard_normal((1, S, 2, hd)), RNG.standard_normal((1, S, 2, hd))
+    assert abs(np.sum(ls.rope_fwd(x, cos, sin) * y) - np.sum(x * ls.rope_bwd(y, cos, sin))) < 1e-10
+
+
+def test_attention_lse_closed_form():
+    # identical keys: every allowed score of row s equals c_s, so lse_s = c_s + ln(s + 1)
+    S, hd = 9, 8
+    q = RNG.standard_normal((1, S, 1, hd))
+    k = np.broadcast_to(RNG.standard_normal(hd), (1, S, 1, hd)).copy()
+    v = RNG.standard_normal((1, S, 1, hd))
+    o, lse = ls.attention_fwd(q, k, v)
+    c = q[0, :, 0] @ k[0, 0, 0] / math.sqrt(hd)
+    assert np.allclose(lse[0, 0], c + np.log(np.arange(1, S + 1)))
+    assert np.allclose(o[0, :, 0], np.cumsum(v[0, :, 0], axis=0) / np.arange(1, S + 1)[:, None])
+
+
+def test_ce_zero_logits_is_ln_v_and_rows_sum_to_zero():
+    V = 2048
+    z = np.zeros((6, V))
+    lab = np.array([0, 5, IGNORE_INDEX, 2047, 3, IGNORE_INDEX])
+    loss, dz, _ = ls.cross_entropy_fwd_bwd(z, lab)
+    assert loss == pytest.approx(math.log(V), rel=1e-15)
+    z = RNG.standard_normal((6, V))
+    _, dz, _ = ls.cross_entropy_fwd_bwd(z, lab)
+    assert np.allclose(dz.sum(axis=1), 0.0, atol=1e-15)
+    assert not dz[2].any() and not dz[5].any()
+    loss0, dz0, _ = ls.cross_entropy_fwd_bwd(z, np.full(6, IGNORE_INDEX))
+    assert loss0 == 0.0 and not dz0.any()
+
+
+def test_zero_lm_head_gives_ln_v_for_whole_step():
+    cfg = TEST_CONFIGS["micro"]
+    w = oracle_weights(cfg)
+    w.lm_head = np.zeros_like(w.lm_head)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss, g = oracle.step(w, tok, lab, cfg)
+    assert loss == pytest.approx(math.log(cfg.vocab), rel=1e-14)
+    # with W_lm = 0, dH = 0, so no gradient reaches the layers or the embedding
+    assert not np.any(g["embed"]) and all(not np.any(v) for v in g["layers"][0].values())
+    # dW_lm = dZ^T H with dZ = (1/V - onehot)/n_valid
+    assert np.allclose(g["lm_head"].sum(axis=0), 0.0, atol=1e-14)
+
+
+def test_random_init_loss_statistics():
+    cfg = CONFIGS["tiny"]
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss, _ = oracle.step(w, tok, lab, cfg)
+    sigma2 = 0.02 ** 2 * cfg.hidden
+    assert loss == pytest.approx(math.log(cfg.vocab) + sigma2 / 2, rel=0.02)
+
+
+def test_causal_invariance_of_hidden_states_and_logits():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, batch=1, seq=40)
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    _, _, hid = oracle.step(w, tok, lab, cfg, return_hidden=True)
+    s_star = 23
+    tok2 = tok.copy()
+    tok2[0, s_star] = (tok2[0, s_star] + 1) % cfg.vocab
+    _, _, hid2 = oracle.step(w, tok2, lab, cfg, return_hidden=True)
+    for a, b in zip(hid["xs"], hid2["xs"]):
+        assert np.array_equal(a[:, :s_star], b[:, :s_star])
+        assert not np.array_equal(a[:, s_star:], b[:, s_star:]) or a is hid["xs"][0]
+    assert np.array_equal(hid["logits"][:s_star], hid2["logits"][:s_star])
+    assert not np.array_equal(hid["logits"][s_star:], hid2["logits"][s_star:])
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=1, batch=1, seq=24)
+    grp = cfg.n_heads // cfg.n_kv_heads
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss, g = oracle.step(w, tok, lab, cfg)
+    hd = cfg.head_dim
+    rep = lambda W: np.repeat(W.reshape(cfg.n_kv_heads, hd, -1), grp, axis=0).reshape(-1, W.shape[1])
+    mha_cfg = cfg.with_(n_kv_heads=cfg.n_heads)
+    wm = oracle_weights(cfg)
+    for lp in wm.layers:
+        lp["wk"], lp["wv"] = rep(lp["wk"]), rep(lp["wv"])
+    loss_m, gm = oracle.step(wm, tok, lab, mha_cfg)
+    assert loss_m == pytest.approx(loss, rel=1e-12)
+    for name in ("wk", "wv"):
+        summed = gm["layers"][0][name].reshape(cfg.n_kv_heads, grp, hd, -1).sum(axis=1)
+        assert rel_l2(summed.reshape(-1, cfg.hidden), g["layers"][0][name]) < 1e-11
+    assert rel_l2(gm["layers"][0]["wq"], g["layers"][0]["wq"]) < 1e-11
+
+
+# ------------------------------------------------------------------ whole step vs torch autograd
+def torch_model_loss(w, tok, lab, cfg):
+    """The decoder assembled from torch library ops (rms_norm, linear, complex
+    RoPE, SDPA, silu, cross_entropy); gradients by autograd."""
+    params = {}
+
+    def P(name, a):
+        t = t64(a).requires_grad_()
+        params[name] = t
+        return t
+
+    B, S = tok.shape
+    E = P("embed", w.embed)
+    x = F.embedding(torch.tensor(tok, dtype=torch.long), E)
+    for i, lp in enumerate(w.layers):
+        p = {k: P(f"{i}.{k}", v) for k, v in lp.items()}
+        u = F.rms_norm(x, (cfg.hidden,), weight=p["g1"], eps=cfg.rms_eps)
+        q = F.linear(u, p["wq"]).view(B, S, cfg.n_heads, cfg.head_dim)
+        k = F.linear(u, p["wk"]).view(B, S, cfg.n_kv_heads, cfg.head_dim)
+        v = F.linear(u, p["wv"]).view(B, S, cfg.n_kv_heads, cfg.head_dim)
+        q, k = rope_complex_torch(q, cfg.rope_base), rope_complex_torch(k, cfg.rope_base)
+        o = torch_causal_attention(q, k, v).reshape(B, S, -1)
+        h = x + F.linear(o, p["wo"])
+        w2 = F.rms_norm(h, (cfg.hidden,), weight=p["g2"], eps=cfg.rms_eps)
+        x = h + F.linear(F.silu(F.linear(w2, p["wg"])) * F.linear(w2, p["wu"]), p["wd"])
+    hf = F.rms_norm(x, (cfg.hidden,), weight=P("final_norm", w.final_norm), eps=cfg.rms_eps)
+    z = F.linear(hf, P("lm_head", w.lm_head)).reshape(B * S, -1)
+    loss = F.cross_entropy(z, torch.tensor(lab.reshape(-1), dtype=torch.long),
+                           ignore_index=IGNORE_INDEX)
+    loss.backward()
+    return loss.item(), {k: v.grad.numpy() for k, v in params.items()}
+
+
+def step_vs_torch_error(cfg):
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss, g = oracle.step(w, tok, lab, cfg)
+    lt, gt = torch_model_loss(w, tok, lab, cfg)
+    errs = [abs(loss - lt) / lt]
+    for i, lg in enumerate(g["layers"]):
+        errs += [rel_l2(v, gt[f"{i}.{k}"]) for k, v in lg.items()]
+    errs += [rel_l2(g[k], gt[k]) for k in ("embed", "final_norm", "lm_head")]
+    return max(errs)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small-gqa", "small-hd128"])
+def test_step_matches_torch_autograd(name):
+    cfg = CONFIGS.get(name) or TEST_CONFIGS[name]
+    assert step_vs_torch_error(cfg) < 1e-10
+
+
+def test_fp32_oracle_close_to_fp64():
+    cfg = CONFIGS["tiny"]
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    l64, g64 = oracle.step(w, tok, lab, cfg, dtype=np.float64)
+    l32, g32 = oracle.step(w, tok, lab, cfg, dtype=np.float32)
+    assert abs(l32 - l64) / l64 < 1e-6
+    for a, b in zip(g32["layers"], g64["layers"]):
+        for k in a:
+            assert rel_l2(a[k], b[k]) < 1e-5, k
+    assert rel_l2(g32["lm_head"], g64["lm_head"]) < 1e-5
+
+
+# ------------------------------------------------------------------ finite differences
+def fd_max_error(cfg, n_coords=3, seed=5):
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    # make the gains non-trivial so their gradients are exercised
+    rng = np.random.default_rng(seed)
+    for lp in w.layers:
+        lp["g1"] = lp["g1"] + 0.1 * rng.standard_normal(lp["g1"].shape)
+        lp["g2"] = lp["g2"] + 0.1 * rng.standard_normal(lp["g2"].shape)
+    w.final_norm = w.final_norm + 0.1 * rng.standard_normal(w.final_norm.shape)
+    w.layers = [{k: v.astype(np.float64) for k, v in lp.items()} for lp in w.layers]
+    w.embed, w.final_norm, w.lm_head = (a.astype(np.float64) for a in (w.embed, w.final_norm, w.lm_head))
+    _, g = oracle.step(w, tok, lab, cfg)
+
+    def tensors():
+        for i, lp in enumerate(w.layers):
+            for k in lp:
+                yield lp, k, g["layers"][i][k]
+        yield w.__dict__, "final_norm", g["final_norm"]
+        yield w.__dict__, "lm_head", g["lm_head"]
+        yield w.__dict__, "embed", g["embed"]
+
+    worst = 0.0
+    for holder, key, grad in tensors():
+        arr = holder[key]
+        flat = arr.reshape(-1)
+        idxs = rng.choice(flat.size, size=n_coords, replace=False)
+        if key == "embed":   # pick rows that are actually used
+            used = np.unique(tok)
+            idxs = used[:n_coords] * cfg.hidden + rng.integers(0, cfg.hidden, n_coords)
+        for j in idxs:
+            h = 1e-5 * max(1.0, abs(flat[j]))
+            old = flat[j]
+            flat[j] = old + h
+            lp_, _ = oracle.step(w, tok, lab, cfg)
+            flat[j] = old - h
+            lm_, _ = oracle.step(w, tok, lab, cfg)
+            flat[j] = old
+            fd = (lp_ - lm_) / (2 * h)
+            an = grad.reshape(-1)[j]
+            worst = max(worst, abs(fd - an) / max(abs(an), 1e-3))
+    return worst
+
+
+def test_finite_differences_fp64():
+    assert fd_max_error(TEST_CONFIGS["micro"]) < 1e-6
+
+
+# ------------------------------------------------------------------ Adam
+def test_adam_matches_torch_adamw_and_first_step_closed_form():
+    n = 1000
+    theta = RNG.standard_normal(n)
+    m = np.zeros(n)
+    v = np.zeros(n)
+    tt = torch.tensor(theta.copy(), dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([tt], lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    th = theta.copy()
+    for t in range(1, 4):
+        g = RNG.standard_normal(n)
+        tt.grad = torch.tensor(g)
+        opt.step()
+        th, m, v = ls.adam_update(th, g, m, v, t, 1e-3, weight_decay=0.01)
+        if t == 1:
+            step1 = theta - 1e-3 * 0.01 * theta - 1e-3 * g / (np.abs(g) + 1e-8)
+            assert rel_l2(th - theta, step1 - theta) < 1e-9
+    assert rel_l2(th - theta, tt.detach().numpy() - theta) < 1e-9
+
+
+# ------------------------------------------------------------------ planted mistakes
+def _mut_rope_sign(x, cos, sin):
+    half = x.shape[-1] // 2
+    c, s = cos[None, :, None, :], sin[None, :, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+
+
+def _mut_rope_interleaved(x, cos, sin):
+    c, s = np.repeat(cos, 2, -1)[None, :, None, :], np.repeat(sin, 2, -1)[None, :, None, :]
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * c[..., 0::2] - x2 * s[..., 0::2]
+    out[..., 1::2] = x2 * c[..., 0::2] + x1 * s[..., 0::2]
+    return out
+
+
+def _mut_rmsnorm_eps_outside(x, g, eps):
+    rstd = 1.0 / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps)
+    return x * rstd * g, (x * rstd, rstd)
+
+
+def _mut_swiglu_bwd_drop_term(dm, a, b):
+    sig = 1.0 / (1.0 + np.exp(-a))
+    return dm * b * sig, dm * a * sig
+
+
+def _mut_attention_no_diag(q, k, v):
+    B, S, Hq, hd = q.shape
+    grp = Hq // k.shape[2]
+    mask = np.triu(np.ones((S, S), dtype=bool), 0)
+    mask[0, 0] = False
+    o = np.empty_like(q)
+    lse = np.empty((B, Hq, S))
+    for b in range(B):
+        for h in range(Hq):
+            sc = q[b, :, h] @ k[b, :, h // grp].T / math.sqrt(hd)
+            sc[mask] = -np.inf
+            p = np.exp(sc - sc.max(1, keepdims=True))
+            o[b, :, h] = (p / p.sum(1, keepdims=True)) @ v[b, :, h // grp]
+    return o, lse
+
+
+def _mut_gqa_modulo(q, k, v):
+    Hkv = k.shape[2]
+    kk = k[:, :, [h % Hkv for h in range(q.shape[2])]]
+    vv = v[:, :, [h % Hkv for h in range(q.shape[2])]]
+    return _orig_attention_fwd(q, kk, vv)
+
+
+_orig_attention_fwd = ls.attention_fwd
+
+
+@pytest.mark.parametrize("target,mutant,pin", [
+    ("rope_fwd", _mut_rope_sign, pin_rope_vs_complex),
+    ("rope_fwd", _mut_rope_interleaved, pin_rope_vs_complex),
+    ("rmsnorm_fwd", _mut_rmsnorm_eps_outside, lambda: pin_rmsnorm_vs_torch(eps=0.5)),
+    ("swiglu_bwd", _mut_swiglu_bwd_drop_term, pin_swiglu_vs_torch),
+    ("attention_fwd", _mut_attention_no_diag, pin_attention_vs_sdpa),
+    ("attention_fwd", _mut_gqa_modulo, pin_attention_vs_sdpa),
+])
+def test_planted_mistake_is_caught(monkeypatch, target, mutant, pin):
+    assert pin() < 1e-10
+    monkeypatch.setattr(ls, target, mutant)
+    assert pin() > 1e-3
+
+
+def test_planted_backward_mistake_is_caught_by_finite_differences(monkeypatch):
+    monkeypatch.setattr(ls, "rmsnorm_bwd", lambda dy, g, c: (c[1] * dy * g, np.sum(dy * c[0], 0)))
+    assert fd_max_error(TEST_CONFIGS["micro"], n_coords=2) > 1e-3

@@ -1,0 +1,356 @@
+"""Benchmark: one layer-sliding fine-tuning step of the 8B-shape GQA decoder
+(32 layers, hidden 4096, 32/8 heads x 128, SwiGLU 14336, vocab 128256,
+batch 8 x seq 2048, bf16 weights streamed from pinned host memory through a
+3-slot GPU ring, host Adam on fp32 masters) on one GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b] [--impl ours|reference]
+
+Prints one JSON line.  value = tokens/s over K synchronous steps timed with
+CUDA events (device clock, Adam included); e2e = the same through the public
+call with host wall clock, including the per-step staging of the token batch
+and the read of the loss.  --impl reference times the CPU oracle on a bounded
+sample of the same workload.  N > 1 (torchrun) runs independent replicas, one
+per GPU (the step has no cross-GPU exchange on one node's replicas).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+from inputs import CONFIGS, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD  # noqa: E402
+
+METRIC = "fine-tune tokens/sec at 1 GB300; % of step roofline (tensor peak vs host-link)"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def step_flops(c, executed=True):
+    """Algorithmic FLOPs of one step.  Decoder layers: forward + recompute +
+    backward (2x forward) of the four projections and causal attention; the
+    recompute skips the down projection, whose output the backward does not
+    need (executed=True counts what runs; False counts the full 4x)."""
+    d, F, T = c.hidden, c.ffn, c.batch * c.seq
+    q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    proj = {"qkv": 2 * T * d * (q + 2 * kv), "o": 2 * T * q * d, "gu": 2 * T * d * 2 * F, "down": 2 * T * F * d}
+    attn = 2.0 * c.batch * c.n_heads * c.head_dim * c.seq * (c.seq + 1)  # QK^T + PV, causal
+    fwd = sum(proj.values()) + attn
+    rec = fwd - (proj["down"] if executed else 0)
+    bwd = 2 * sum(proj.values()) + 2.5 * attn
+    layers = c.n_layers * fwd + (c.n_layers - 1) * rec + c.n_layers * bwd if executed else \
+        c.n_layers * (fwd + fwd + 2 * fwd)
+    n_valid = c.batch * (c.seq - 1)
+    head = 3 * 2.0 * d * c.vocab * (T if executed else n_valid)
+    return layers + head
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [r for r in self.rows if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def link_probe(torch, nbytes=1 << 30):
+    """Pinned host<->device GB/s: H2D, D2H and both directions at once."""
+    h1 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    out = {}
+    for name, fn in (("h2d", lambda: d1.copy_(h1, non_blocking=True)),
+                     ("d2h", lambda: h2.copy_(d2, non_blocking=True))):
+        fn(); torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        out[name] = 3 * nbytes / (time.perf_counter() - t) / 1e9
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            d1.copy_(h1, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+    torch.cuda.synchronize()
+    out["bidir"] = 6 * nbytes / (time.perf_counter() - t) / 1e9
+    del h1, h2, d1, d2
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ oracle sample (CPU)
+def oracle_sample(c, reps=1):
+    """Time the CPU oracle (float32, as it stands) on a bounded sample of the
+    workload: one sequence through one full-shape decoder layer forward and
+    backward plus the LM head and loss on its rows.  Returns (tokens/s of the
+    whole step extrapolated to n_layers, seconds, description)."""
+    import oracle
+    from oracle import llama_step as ls
+    cs = c.with_(n_layers=1, batch=1)
+    S, d = cs.seq, cs.hidden
+    lay = {k: oracle.bf16_round(v) for k, v in inputs.split_layer(cs, inputs.layer_master(cs, 0)).items()}
+    Wlm = oracle.bf16_round(inputs.normal(1234, 2, c.vocab * d, 0.0, 0.02)).reshape(c.vocab, d)
+    gf = np.ones(d, np.float32)
+    tok, lab = inputs.tokens_and_labels(cs)
+    x = inputs.normal(1234, 3, S * d, 0.0, 0.02).reshape(1, S, d)
+    cos, sin = ls.rope_tables(S, c.head_dim, c.rope_base, np.float32)
+    t_layer = t_head = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        y, cache = ls.layer_fwd(x, lay, cs, cos, sin)
+        t1 = time.perf_counter()
+        hf, cf = ls.rmsnorm_fwd(y.reshape(S, d), gf, cs.rms_eps)
+        z = hf @ Wlm.T
+        _, dz, _ = ls.cross_entropy_fwd_bwd(z, lab.reshape(-1))
+        _ = dz.T @ hf
+        dh, _ = ls.rmsnorm_bwd(dz @ Wlm, gf, cf)
+        t2 = time.perf_counter()
+        ls.layer_bwd(dh.astype(np.float32), lay, cache, cs, cos, sin)
+        t3 = time.perf_counter()
+        t_layer += (t1 - t0) + (t3 - t2)
+        t_head += t2 - t1
+    t_layer /= reps
+    t_head /= reps
+    # the full step also recomputes each layer's forward once: count it
+    t_fwd = t_layer / 3.0
+    t_step = c.batch * (c.n_layers * (t_layer + t_fwd) + t_head)
+    desc = (f"1 sequence x {S} tokens through one {c.name} decoder layer fwd+bwd "
+            f"({t_layer:.1f}s) and the LM head + loss ({t_head:.1f}s), float32 numpy; "
+            f"extrapolated to {c.n_layers} layers (+recompute) x batch {c.batch}")
+    return c.batch * S / t_step, t_layer + t_head, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, c):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(c)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        v, s, desc = oracle_sample(c)
+        vals.append(v)
+        secs += s
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": c.batch * c.seq / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": c.name, "global_batch": c.batch, "seq_len": c.seq,
+                       "parallelism": "cpu oracle"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def load_model(sf, c, ring):
+    cfg = sf.make_config(c, ring_slots=ring, retain_grads=0)
+    m = sf.Model(cfg)
+    for l in range(c.n_layers):
+        m.load(l, inputs.layer_master(c, l))
+    for u in (UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD):
+        m.load(u, inputs.unit_master(c, u))
+    return m
+
+
+def run_ours(args, c):
+    import torch
+    import offloaded_fine_tuning_gb300 as sf
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    sf.lib(build_if_needed=True)
+    bf16_peak, bf16_sust, hbm, peak_src = peaks()
+    link = link_probe(torch)
+
+    m = load_model(sf, c, args.ring or c.ring_slots)
+    adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    tok, lab = inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + rank)
+    T = c.batch * c.seq
+    for _ in range(args.warmup):
+        assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+
+    # ---- device-clock region (CUDA events, Adam included): K synchronous steps
+    m.set_timing(True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    stats = []
+    for _ in range(args.steps):
+        st = m.train_step(tok, lab, adam)
+        assert st == sf.SF_OK, m.error()
+        stats.append(m.stats())
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    dev_ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    m.set_timing(False)
+
+    # ---- end to end through the public call: stage the batch from pinned host
+    # memory each step, run the step, read the loss back
+    pin_tok = torch.empty((c.batch, c.seq), dtype=torch.int32, pin_memory=True)
+    pin_lab = torch.empty((c.batch, c.seq), dtype=torch.int32, pin_memory=True)
+    t0 = time.perf_counter()
+    losses = []
+    for i in range(args.steps):
+        pin_tok.numpy()[...] = tok
+        pin_lab.numpy()[...] = lab
+        assert m.train_step(pin_tok.numpy(), pin_lab.numpy(), adam) == sf.SF_OK, m.error()
+        losses.append(m.loss())
+    e2e_s = time.perf_counter() - t0
+
+    times = torch.tensor([dev_ms, e2e_s * 1e3], dtype=torch.float64, device="cuda")
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    dev_ms, e2e_ms = float(times[0]), float(times[1])
+    ms_step = dev_ms / args.steps
+    value = world * T * args.steps / (dev_ms / 1e3)
+    e2e = world * T * args.steps / (e2e_ms / 1e3)
+
+    gemm_ms = sum(s["gemm_ms"] for s in stats)
+    gemm_fl = sum(s["gemm_flops"] for s in stats)
+    gemm_n = sum(s["gemm_launches"] for s in stats)
+    attn_ms = sum(s["attn_ms"] for s in stats)
+    attn_fl = sum(s["attn_flops"] for s in stats)
+    h2d = statistics.mean(s["h2d_bytes"] for s in stats)
+    d2h = statistics.mean(s["d2h_bytes"] for s in stats)
+    gpu_step = statistics.mean(s["step_ms"] for s in stats)
+    achieved = gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    F_exec = step_flops(c, executed=True)
+    t_tensor = F_exec / (bf16_sust * 1e12)
+    t_link = (h2d + d2h) / (link["bidir"] * 1e9)
+    t_roof = max(t_tensor, t_link)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, secs, desc = oracle_sample(c)
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": c.name, "global_batch": c.batch * world, "seq_len": c.seq,
+                   "layers": c.n_layers, "ring_slots": args.ring or c.ring_slots,
+                   "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
+                   "l2": "inputs larger than L2 (each step streams every layer's weights and gradients)"},
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": int(sum(s["kernel_launches"] for s in stats)),
+        "roofline": {"kernel": "gemm_tcgen05", "bound": "tensor", "achieved": achieved,
+                     "peak": bf16_sust, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_sust if achieved else None, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained (cuBLAS, long loop)",
+                     "launches": gemm_n, "gemm_ms_per_step": gemm_ms / args.steps},
+        "step_roofline": {"flops": F_exec, "t_tensor_ms": t_tensor * 1e3, "h2d_bytes": h2d,
+                          "d2h_bytes": d2h, "link_gbs": link, "t_link_ms": t_link * 1e3,
+                          "t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                          "gpu_busy_ms": gpu_step,
+                          "attn_tflops": attn_fl / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None,
+                          "host_adam_ms": statistics.mean(s["host_adam_ms"] for s in stats),
+                          "host_tail_ms": statistics.mean(s["host_wait_ms"] for s in stats)},
+        "clocks": clk,
+        "loss": losses[-1],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    m.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="8b", choices=sorted(CONFIGS))
+    ap.add_argument("--ring", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    c = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, c)
+    else:
+        run_ours(args, c)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,263 @@
+/*
+ * sf.h -- C ABI of the layer-sliding fine-tuning step on one GB300 GPU.
+ *
+ * The method (SlideFormer, "An Efficient Heterogeneous Co-Design for
+ * Fine-Tuning on a Single GPU"; abstract, and the gist.science technical
+ * summary, section 2 "Methodologie") fine-tunes a decoder whose full state
+ * stays in host memory:
+ *   - the GPU holds only a fixed ring of identical layer buffers (section 2.B,
+ *     "Pre-allocated GPU Cache Queue"); each layer's bf16 weights stream in
+ *     from pinned host memory on a copy stream (section 2.A);
+ *   - each layer's forward, and after the loss its recompute-and-backward,
+ *     run on a compute stream; the LM-head projection and cross-entropy are
+ *     fused and chunked so the full logits never exist (section 2.C, "Fused
+ *     LinearCrossEntropy");
+ *   - a finished layer's gradients stream back to host buffers that are
+ *     shared with the bf16 weight copies (section 2.B, "Gedeelde
+ *     CPU-buffers") while the next layer computes, and a per-layer Adam
+ *     updates the fp32 master weights on host threads (section 2.A and 2.B,
+ *     "Layer-Adam Optimizer").
+ * The model is a pre-norm Llama-style decoder (section 4 names Llama, Qwen
+ * and Mistral): RMSNorm, QKV projection with rotary embedding (rotate-half
+ * pairs), causal grouped-query attention, output projection, RMSNorm, SwiGLU
+ * FFN; untied embedding and LM head; loss = mean token cross-entropy over
+ * labels != SF_IGNORE_INDEX.
+ *
+ * Conventions for every entry point:
+ *   - Return value: SF_OK (0) or a negative status below.  No exception and
+ *     no abort crosses this ABI.
+ *   - The caller owns every pointer it passes.  Host inputs are copied
+ *     before the call returns; host outputs are written before it returns.
+ *   - The library owns all device memory, streams, events and pinned host
+ *     memory of a context; sf_free releases them.
+ *   - A context is used by one caller thread at a time.
+ *   - Matrices are row-major; weights use the [out_features, in_features]
+ *     layout of a linear layer; token t of a batch is t = b * seq + s.
+ */
+#ifndef SF_H_
+#define SF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define SF_OK 0
+#define SF_EINVAL (-1)   /* bad argument: null, size, range, unit, token or label */
+#define SF_ENOMEM (-2)   /* device or host allocation failed */
+#define SF_ECUDA (-3)    /* a CUDA call failed; the context is poisoned */
+#define SF_ETIMEOUT (-4) /* a bounded wait (host event poll or device pipeline) ran out */
+#define SF_ESTATE (-5)   /* call not valid in this state (poisoned ctx, grads not retained) */
+#define SF_EDEVICE (-6)  /* a kernel recorded a device-side error (see sf_last_error) */
+
+/* Units: decoder layers are 0 .. n_layers-1; the other tensors are: */
+#define SF_UNIT_EMBED (-1)      /* token embedding [vocab, hidden] */
+#define SF_UNIT_FINAL_NORM (-2) /* final RMSNorm gain [hidden] */
+#define SF_UNIT_LM_HEAD (-3)    /* LM head [vocab, hidden] */
+
+#define SF_IGNORE_INDEX (-100)
+
+typedef struct sf_ctx sf_ctx;
+
+/* Model and engine configuration.
+ *   n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab: decoder shape.
+ *     head_dim in {64, 128}; n_heads % n_kv_heads == 0; hidden, ffn, vocab
+ *     multiples of 8; hidden <= 16384.  n_heads*head_dim may differ from hidden.
+ *   max_batch, max_seq: the largest batch x seq a step may use (sizes buffers).
+ *   ring_slots: R identical GPU layer buffers, 2 <= R <= n_layers (R ==
+ *     n_layers keeps every layer resident: the non-offloaded reference mode).
+ *   lce_chunk_rows: rows of the fused LM-head/cross-entropy per chunk
+ *     (0 = automatic); the chunk's logits are the only logits ever stored.
+ *   retain_grads: 1 keeps every unit's gradient of the last step on the host
+ *     for sf_get_grads (costs a host copy per unit); 0 lets the gradient
+ *     buffers be reused.
+ *   rms_eps, rope_base: RMSNorm epsilon and RoPE base.
+ *   device: CUDA device ordinal.
+ *   adam_threads: host threads for Adam, gather and scatter (0 = all cores).
+ *   wait_timeout_ms: bound of every host-side wait on the GPU (0 = 300000). */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int32_t max_batch, max_seq;
+  int32_t ring_slots;
+  int32_t lce_chunk_rows;
+  int32_t retain_grads;
+  float rms_eps, rope_base;
+  int32_t device;
+  int32_t adam_threads;
+  int32_t wait_timeout_ms;
+} sf_config;
+
+/* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} sf_adam;
+
+/* Counters of the last sf_train_step (device times from CUDA events on the
+ * stream each kernel was launched on). */
+typedef struct {
+  double step_ms;          /* compute stream, first to last operation of the step */
+  double gemm_ms;          /* sum of tcgen05 GEMM launch durations */
+  double gemm_flops;       /* algorithmic FLOPs of those launches (2*M*N*K each) */
+  double attn_ms;          /* attention forward + backward kernels */
+  double attn_flops;       /* algorithmic causal attention FLOPs */
+  double h2d_bytes;        /* bytes copied host -> device during the step */
+  double d2h_bytes;        /* bytes copied device -> host during the step */
+  double host_adam_ms;     /* wall time the Adam workers spent updating */
+  double host_wait_ms;     /* wall time sf_train_step blocked after the GPU finished */
+  int64_t gemm_launches;
+  int64_t kernel_launches; /* all kernels of this library launched in the step */
+  int32_t timing_enabled;
+} sf_stats;
+
+/* ---------------------------------------------------------------- model API */
+
+/* Number of fp32 values of `unit` (see SF_UNIT_*): for a decoder layer the
+ * concatenation g1[d], Wq[Hq*hd, d], Wk[Hkv*hd, d], Wv[Hkv*hd, d],
+ * Wo[d, Hq*hd], g2[d], Wg[F, d], Wu[F, d], Wd[d, F].  0 for a bad unit. */
+size_t sf_unit_numel(const sf_config* cfg, int32_t unit);
+
+/* Validate cfg, allocate the ring slots, checkpoint and workspace buffers on
+ * the device, pinned host buffers for every unit, fp32 master / Adam state in
+ * host memory, streams, events and the host worker threads.  Every buffer the
+ * step needs is allocated here (the step itself allocates nothing).
+ * Errors: SF_EINVAL (bad cfg), SF_ENOMEM, SF_ECUDA. */
+int sf_init_model(const sf_config* cfg, sf_ctx** out);
+
+/* Release everything the context owns.  NULL is a no-op. */
+void sf_free(sf_ctx* ctx);
+
+/* Message of the last error on ctx ("" if none); NULL ctx gives the message
+ * of the last failed sf_init_model on this thread.  Owned by the library. */
+const char* sf_last_error(const sf_ctx* ctx);
+
+/* Set the fp32 master weights of `unit` (numel == sf_unit_numel) and reset
+ * its Adam moments; the bf16 copy that streams to the GPU is rounded from it
+ * (round-to-nearest-even).  Errors: SF_EINVAL, SF_ESTATE. */
+int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* fp32_master, size_t numel);
+
+/* One training step on tokens/labels [batch, seq] (int32, host memory):
+ * forward over all layers through the GPU ring, fused LM-head cross-entropy,
+ * recompute-and-backward over the layers in reverse order, gradient
+ * streaming to the host and, if adam != NULL, the Adam update of every unit
+ * (adam == NULL: gradients only, weights unchanged).  Synchronous: on return
+ * the loss is ready and every update is done.  tokens in [0, vocab); labels
+ * in [0, vocab) or SF_IGNORE_INDEX; batch*seq <= max_batch*max_seq and seq <=
+ * max_seq.  With no valid label the loss and all gradients are 0.
+ * Errors: SF_EINVAL, SF_ECUDA, SF_ETIMEOUT, SF_EDEVICE, SF_ESTATE. */
+int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
+                  int32_t seq, const sf_adam* adam);
+
+/* Gradient of the last step for `unit`, in sf_unit_numel order, upcast from
+ * the bf16 values that were streamed to the host (the embedding gradient is
+ * accumulated in fp32).  Needs retain_grads = 1, else SF_ESTATE. */
+int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
+
+/* Current fp32 master weights of `unit`.  Errors: SF_EINVAL. */
+int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
+
+/* Loss of the last step.  Errors: SF_ESTATE before the first step. */
+int sf_loss(sf_ctx* ctx, float* out);
+
+/* Per-kernel timing of the steps that follow: 1 records CUDA events around
+ * every GEMM and attention launch (small overhead), 0 turns it off. */
+int sf_set_timing(sf_ctx* ctx, int32_t enabled);
+
+/* Counters of the last step. */
+int sf_get_stats(const sf_ctx* ctx, sf_stats* out);
+
+/* Host-side fault injection for tests (no GPU fault is ever made):
+ *   what = 1: the Adam worker fails on unit `arg` of the next step;
+ *   what = 2: the Adam worker sleeps `arg` ms before each update;
+ *   what = 0: clear.  */
+int sf_debug_inject(sf_ctx* ctx, int32_t what, int32_t arg);
+
+/* ---------------------------------------------------------------- kernel API
+ * Single operations of the step on device pointers, launched on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream) and asynchronous like any
+ * kernel launch.  Every scratch buffer is passed in by the caller; the first
+ * call on a device also creates the 4-byte device error word that
+ * sf_op_device_error reads.
+ * Errors: SF_EINVAL for bad sizes / alignment (16-byte aligned bases and row
+ * strides that are multiples of 8 elements), SF_ECUDA for a failed launch.
+ * bf16 arguments are uint16 bit patterns of bfloat16. */
+
+/* Dense bf16 GEMM on the tcgen05 tensor cores, fp32 accumulation.
+ * layout 0 (NT): C[M,N] = alpha * A[M,K] * B[N,K]^T   (projection forward)
+ * layout 1 (NN): C[M,N] = alpha * A[M,K] * B[K,N]     (input gradient)
+ * layout 2 (TN): C[M,N] = alpha * A[K,M]^T * B[K,N]   (weight gradient)
+ * epi 0: C bf16; 1: C fp32; 2: C fp32 = R + alpha*AB (R may alias C);
+ * epi 3: C fp32 += alpha*AB.  lda/ldb/ldc/ldr are row strides in elements. */
+int sf_op_gemm(int32_t layout, int32_t epi, int64_t M, int64_t N, int64_t K, const void* A,
+               int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R,
+               int64_t ldr, float alpha, void* stream);
+
+/* y[r] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)), rstd[r] = 1/sqrt(...);
+ * x fp32 [rows, d], g bf16 [d], y bf16 [rows, d], rstd fp32 [rows]. */
+int sf_op_rmsnorm_fwd(const float* x, const uint16_t* g, uint16_t* y, float* rstd, int64_t rows,
+                      int32_t d, float eps, void* stream);
+
+/* Backward of sf_op_rmsnorm_fwd given dy (fp32 [rows, d], the gradient of y):
+ * dx = dres + rstd*(g*dy - xhat*mean(g*dy*xhat)) (fp32; dres may be NULL),
+ * dxb = bf16(dx), dg = bf16(sum_r dy*xhat) [d].  scratch: fp32 of
+ * sf_op_rmsnorm_bwd_scratch(rows, d) elements. */
+int sf_op_rmsnorm_bwd(const float* x, const uint16_t* g, const float* rstd, const float* dy,
+                      const float* dres, float* dx, uint16_t* dxb, uint16_t* dg, float* scratch,
+                      int64_t rows, int32_t d, void* stream);
+int64_t sf_op_rmsnorm_bwd_scratch(int64_t rows, int32_t d);
+
+/* Host table of (cos, sin) of s * base^(-2j/head_dim), s < seq, j < head_dim/2,
+ * written as float pairs [seq, head_dim/2, 2] to `out` (host memory). */
+int sf_rope_table(int32_t seq, int32_t head_dim, float rope_base, float* out);
+
+/* Rotary embedding in place on the first `heads` heads of each row of
+ * x [tokens, ld] (bf16; position s = token % seq): pair (j, j + hd/2) rotated by
+ * the table angle; inverse = 1 rotates by the opposite angle.  table: device
+ * copy of sf_rope_table. */
+int sf_op_rope(uint16_t* x, int64_t ld, int64_t tokens, int32_t seq, int32_t heads,
+               int32_t head_dim, const float* table, int32_t inverse, void* stream);
+
+/* Causal GQA attention forward.  qkv bf16 [B*S, (Hq+2Hkv)*hd] (Q heads, then K
+ * heads, then V heads); o bf16 [B*S, Hq*hd]; lse fp32 [B, Hq, S] (natural
+ * log-sum-exp of the scaled scores).  Scale 1/sqrt(hd). */
+int sf_op_attn_fwd(const uint16_t* qkv, uint16_t* o, float* lse, int32_t B, int32_t S,
+                   int32_t Hq, int32_t Hkv, int32_t hd, void* stream);
+
+/* Backward of sf_op_attn_fwd: writes dQ, dK, dV into dqkv (same layout as qkv);
+ * when table != NULL the inverse rotary embedding is applied to dQ and dK (the
+ * gradient reaches the pre-rotation projections).  Scratch: delta fp32
+ * [B*Hq*S], dq_acc fp32 [B*S*Hq*hd]. */
+int sf_op_attn_bwd(const uint16_t* qkv, const uint16_t* o, const uint16_t* dout,
+                   const float* lse, float* delta, float* dq_acc, uint16_t* dqkv, int32_t B,
+                   int32_t S, int32_t Hq, int32_t Hkv, int32_t hd, const float* table,
+                   void* stream);
+
+/* m = silu(a) * b with ab = [a | b] bf16 [rows, 2*ffn]; m bf16 [rows, ffn]. */
+int sf_op_swiglu_fwd(const uint16_t* ab, uint16_t* m, int64_t rows, int32_t ffn, void* stream);
+/* dab = [dm * b * s(1 + a(1-s)) | dm * silu(a)], s = sigmoid(a). */
+int sf_op_swiglu_bwd(const uint16_t* dm, const uint16_t* ab, uint16_t* dab, int64_t rows,
+                     int32_t ffn, void* stream);
+
+/* Fused chunked LM-head + cross-entropy forward and backward on device data:
+ * z = h W^T (never stored beyond one chunk of `chunk_rows` rows),
+ * loss = (1/n_valid) sum_valid (logsumexp(z_t) - z_t[label_t]),
+ * dh = dZ W (fp32 [n, d]), dw = dZ^T h (fp32 [v, d]) with
+ * dZ = (softmax(z) - onehot)/n_valid on valid rows, 0 on ignored rows.
+ * h bf16 [n, d], w bf16 [v, d], labels int32 [n] (device), loss fp32 [1].
+ * n_valid is the number of labels != SF_IGNORE_INDEX (the caller counts it).
+ * workspace: sf_op_lce_workspace_bytes(n, v, chunk_rows) bytes, 256-aligned. */
+int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64_t n, int32_t d,
+              int32_t v, int64_t n_valid, int64_t chunk_rows, void* workspace, float* loss,
+              float* dh, float* dw, void* stream);
+int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows);
+
+/* Read and clear the device error word of the kernel API on the current
+ * device (nonzero: a bounded device wait ran out).  Synchronises the device. */
+int sf_op_device_error(int32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SF_H_ */

@@ -53,6 +53,8 @@ def _load():
             lib.synth_normal_f32.argtypes = [u64, u64, u64, i64, f64, f64, vp]
             lib.synth_randint_i32.argtypes = [u64, u64, u64, i64, i64, vp]
             lib.synth_uniform_f64.argtypes = [u64, u64, u64, i64, vp]
+            lib.synth_set_threads.argtypes = [ctypes.c_int]
+            lib.synth_set_threads(int(os.environ.get("SYNTH_THREADS", "0")) or (os.cpu_count() or 1))
             _lib = lib
     return _lib
 
@@ -132,14 +134,16 @@ def _stream(unit: int, tensor_idx: int) -> int:
 def layer_master(cfg: ModelConfig, layer: int, seed: int = SEED_WEIGHTS) -> np.ndarray:
     """fp32 master weights of decoder layer ``layer`` as one flat array, in the
     unit order g1, Wq, Wk, Wv, Wo, g2, Wg, Wu, Wd (matrices N(0, 0.02), gains 1)."""
-    parts = []
+    out = np.empty(unit_numel(cfg, layer), dtype=np.float32)
+    off = 0
     for idx, (name, shape) in enumerate(layer_tensor_shapes(cfg)):
         n = int(np.prod(shape))
         if name in ("g1", "g2"):
-            parts.append(np.ones(n, dtype=np.float32))
+            out[off:off + n] = 1.0
         else:
-            parts.append(normal(seed, _stream(layer, idx), n, 0.0, 0.02))
-    return np.concatenate(parts)
+            normal(seed, _stream(layer, idx), n, 0.0, 0.02, out=out[off:off + n])
+        off += n
+    return out
 
 
 def unit_master(cfg: ModelConfig, unit: int, seed: int = SEED_WEIGHTS) -> np.ndarray:

@@ -19,8 +19,14 @@
  * (OOPSLA 2014), with Vigna's published constants.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stddef.h>
+
+/* Worker threads for the generators (the draws do not depend on it). */
+void synth_set_threads(int n) {
+  if (n > 0) omp_set_num_threads(n);
+}
 
 static inline uint64_t sm64(uint64_t z) {
   z += 0x9E3779B97F4A7C15ULL;
@@ -35,20 +41,24 @@ static inline uint64_t key_of(uint64_t seed, uint64_t stream) {
 
 static inline double u53(uint64_t w) { return (double)(w >> 11) * 0x1.0p-53; }
 
-/* out[j] = mean + std * normal(offset + j), j in [0, n); float32 output. */
+/* out[j] = mean + std * normal(offset + j), j in [0, n); float32 output.
+ * Each Box-Muller pair is computed once and gives both of its draws. */
 void synth_normal_f32(uint64_t seed, uint64_t stream, uint64_t offset,
                       int64_t n, double mean, double std, float* out) {
+  if (n <= 0) return;
   const uint64_t key = key_of(seed, stream);
   const double two_pi = 6.283185307179586476925286766559;
+  const uint64_t first = offset & ~1ULL, last = offset + (uint64_t)n;  /* [first, last) */
+  const int64_t pairs = (int64_t)((last - first + 1ULL) / 2ULL);
 #pragma omp parallel for schedule(static)
-  for (int64_t j = 0; j < n; ++j) {
-    uint64_t i = offset + (uint64_t)j;
-    uint64_t p = i & ~1ULL;
+  for (int64_t q = 0; q < pairs; ++q) {
+    const uint64_t p = first + 2ULL * (uint64_t)q;
     double u0 = u53(sm64(key + p));
     double u1 = u53(sm64(key + p + 1ULL));
     double r = sqrt(-2.0 * log(1.0 - u0));
-    double z = (i & 1ULL) ? r * sin(two_pi * u1) : r * cos(two_pi * u1);
-    out[j] = (float)(mean + std * z);
+    double ph = two_pi * u1;
+    if (p >= offset) out[p - offset] = (float)(mean + std * (r * cos(ph)));
+    if (p + 1ULL >= offset && p + 1ULL < last) out[p + 1ULL - offset] = (float)(mean + std * (r * sin(ph)));
   }
 }
 

@@ -1,0 +1,418 @@
+// Memory-bound kernels of the decoder step: RMSNorm forward/backward, RoPE,
+// SwiGLU forward/backward, the row softmax of the fused LM-head cross-entropy,
+// reductions and casts.  All of them stream rows with 16-byte vector accesses
+// and reduce with warp shuffles; none of them is a contraction.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "sf_internal.h"
+
+namespace sf {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Block-wide sum; every thread gets the result.  `sh` holds >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  float t = (lane < nw) ? sh[lane] : 0.f;
+  return warp_sum(t);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+// ------------------------------------------------------------------ RMSNorm forward
+// One CTA per row: y = bf16(g * x * rstd), rstd = 1/sqrt(mean(x^2) + eps).
+__global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
+                                   __nv_bfloat16* __restrict__ y, float* __restrict__ rstd_out,
+                                   int d, float eps) {
+  __shared__ float sh[32];
+  const int64_t row = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + row * d);
+  const int n4 = d >> 2;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 v = xr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum(ss, sh);
+  const float rstd = rsqrtf(ss / d + eps);
+  if (threadIdx.x == 0) rstd_out[row] = rstd;
+  const uint2* gr = reinterpret_cast<const uint2*>(g);
+  uint2* yr = reinterpret_cast<uint2*>(y + row * d);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 v = xr[i];
+    uint2 gu = gr[i];
+    float2 g01 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.x));
+    float2 g23 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.y));
+    __nv_bfloat162 o01 = __floats2bfloat162_rn(v.x * rstd * g01.x, v.y * rstd * g01.y);
+    __nv_bfloat162 o23 = __floats2bfloat162_rn(v.z * rstd * g23.x, v.w * rstd * g23.y);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&o01);
+    o.y = *reinterpret_cast<uint32_t*>(&o23);
+    yr[i] = o;
+  }
+}
+
+void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float* rstd,
+                 int64_t rows, int d, float eps, cudaStream_t st) {
+  if (rows <= 0) return;
+  rmsnorm_fwd_kernel<<<(unsigned)rows, 256, 0, st>>>(x, g, y, rstd, d, eps);
+}
+
+// ------------------------------------------------------------------ RMSNorm backward
+// CTAs stride over rows; thread t owns the float4 columns t, t+256, ... (CH of
+// them) so the gain gradient sum over the CTA's rows stays in registers.  The
+// second pass over a row re-reads x and dy, which are still in L1/L2.
+constexpr int kNormThreads = 256;
+
+template <int CH>
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_bwd_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
+                       const float* __restrict__ rstd, const float* __restrict__ dy,
+                       const float* __restrict__ dres, float* __restrict__ dx,
+                       __nv_bfloat16* __restrict__ dxb, float* __restrict__ dg_part,
+                       int64_t rows, int d) {
+  __shared__ float sh[32];
+  const int n4 = d >> 2;
+  float4 gacc[CH], gg[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    gacc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    gg[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int i = threadIdx.x + c * kNormThreads;
+    if (i < n4) {
+      uint2 gu = reinterpret_cast<const uint2*>(g)[i];
+      float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.x));
+      float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.y));
+      gg[c] = make_float4(a.x, a.y, b.x, b.y);
+    }
+  }
+  const float inv_d = 1.f / d;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float r = rstd[row];
+    const float4* xr = reinterpret_cast<const float4*>(x + row * d);
+    const float4* dyr = reinterpret_cast<const float4*>(dy + row * d);
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int i = threadIdx.x + c * kNormThreads;
+      if (i < n4) {
+        const float4 xv = xr[i], dv = dyr[i];
+        const float4 xh = make_float4(xv.x * r, xv.y * r, xv.z * r, xv.w * r);
+        dot += gg[c].x * dv.x * xh.x + gg[c].y * dv.y * xh.y + gg[c].z * dv.z * xh.z +
+               gg[c].w * dv.w * xh.w;
+        gacc[c].x += dv.x * xh.x; gacc[c].y += dv.y * xh.y;
+        gacc[c].z += dv.z * xh.z; gacc[c].w += dv.w * xh.w;
+      }
+    }
+    dot = block_sum(dot, sh) * inv_d;
+    float4* dxr = reinterpret_cast<float4*>(dx + row * d);
+    const float4* drr = dres ? reinterpret_cast<const float4*>(dres + row * d) : nullptr;
+    uint2* dbr = reinterpret_cast<uint2*>(dxb + row * d);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int i = threadIdx.x + c * kNormThreads;
+      if (i < n4) {
+        const float4 xv = xr[i], dv = dyr[i];
+        float4 o;
+        o.x = r * (gg[c].x * dv.x - xv.x * r * dot);
+        o.y = r * (gg[c].y * dv.y - xv.y * r * dot);
+        o.z = r * (gg[c].z * dv.z - xv.z * r * dot);
+        o.w = r * (gg[c].w * dv.w - xv.w * r * dot);
+        if (drr) {
+          const float4 q = drr[i];
+          o.x += q.x; o.y += q.y; o.z += q.z; o.w += q.w;
+        }
+        dxr[i] = o;
+        __nv_bfloat162 a = __floats2bfloat162_rn(o.x, o.y), b = __floats2bfloat162_rn(o.z, o.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&a);
+        u.y = *reinterpret_cast<uint32_t*>(&b);
+        dbr[i] = u;
+      }
+    }
+  }
+  float4* part = reinterpret_cast<float4*>(dg_part + (int64_t)blockIdx.x * d);
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int i = threadIdx.x + c * kNormThreads;
+    if (i < n4) part[i] = gacc[c];
+  }
+}
+
+int rmsnorm_bwd_parts(int64_t rows) {
+  const int p = 2 * num_sms();
+  return rows < p ? (int)(rows > 0 ? rows : 1) : p;
+}
+
+void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, const float* dy,
+                 const float* dres, float* dx, __nv_bfloat16* dxb, float* dg_part, int parts,
+                 int64_t rows, int d, cudaStream_t st) {
+  const int need = (d / 4 + kNormThreads - 1) / kNormThreads;  // float4 chunks per thread
+#define SF_NORM_BWD(CH) \
+  rmsnorm_bwd_kernel<CH><<<parts, kNormThreads, 0, st>>>(x, g, rstd, dy, dres, dx, dxb, dg_part, rows, d)
+  if (need <= 1) SF_NORM_BWD(1);
+  else if (need <= 2) SF_NORM_BWD(2);
+  else if (need <= 4) SF_NORM_BWD(4);
+  else if (need <= 8) SF_NORM_BWD(8);
+  else if (need <= 12) SF_NORM_BWD(12);
+  else SF_NORM_BWD(16);
+#undef SF_NORM_BWD
+}
+
+// out[j] = bf16(sum_p part[p, j])   (fixed order: deterministic)
+__global__ void reduce_parts_kernel(const float* __restrict__ part, int parts, int d,
+                                    __nv_bfloat16* __restrict__ out) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= d) return;
+  float s = 0.f;
+  for (int p = 0; p < parts; ++p) s += part[(int64_t)p * d + j];
+  out[j] = __float2bfloat16_rn(s);
+}
+
+void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st) {
+  reduce_parts_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d, out);
+}
+
+// ------------------------------------------------------------------ RoPE
+// In place on the first `heads` heads of each token row of qkv.  cs[s*hd/2 + j]
+// = (cos, sin) of s * base^(-2j/hd).  inverse = 1 rotates by the opposite angle
+// (the transpose, used on gradients).  One thread per (token, head, 8 pairs).
+__global__ void rope_kernel(__nv_bfloat16* __restrict__ qkv, int64_t ld, int64_t tokens, int seq,
+                            int heads, int hd, const float2* __restrict__ cs, int inverse) {
+  const int half = hd >> 1;
+  const int groups = half >> 3;  // 8 pairs per thread
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = tokens * heads * groups;
+  if (idx >= total) return;
+  const int grp = (int)(idx % groups);
+  const int64_t th = idx / groups;
+  const int h = (int)(th % heads);
+  const int64_t t = th / heads;
+  const int s = (int)(t % seq);
+  __nv_bfloat16* base = qkv + t * ld + (int64_t)h * hd + grp * 8;
+  float x1[8], x2[8];
+  unpack8(*reinterpret_cast<const uint4*>(base), x1);
+  unpack8(*reinterpret_cast<const uint4*>(base + half), x2);
+  const float2* c = cs + (int64_t)s * half + grp * 8;
+  float y1[8], y2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float co = c[i].x, si = inverse ? -c[i].y : c[i].y;
+    y1[i] = x1[i] * co - x2[i] * si;
+    y2[i] = x2[i] * co + x1[i] * si;
+  }
+  *reinterpret_cast<uint4*>(base) = pack8(y1);
+  *reinterpret_cast<uint4*>(base + half) = pack8(y2);
+}
+
+void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
+                  int head_dim, const float2* cs, int inverse, cudaStream_t st) {
+  const int64_t total = tokens * heads * (head_dim / 16);
+  if (total <= 0) return;
+  rope_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(qkv, ld, tokens, seq, heads,
+                                                                head_dim, cs, inverse);
+}
+
+// ------------------------------------------------------------------ SwiGLU
+// ab row = [a (ffn) | b (ffn)];  m = silu(a) * b.
+__global__ void swiglu_fwd_kernel(const __nv_bfloat16* __restrict__ ab, __nv_bfloat16* __restrict__ m,
+                                  int64_t rows, int ffn) {
+  const int per_row = ffn >> 3;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const int64_t r = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  float a[8], b[8], o[8];
+  unpack8(*reinterpret_cast<const uint4*>(ab + r * 2 * ffn + c), a);
+  unpack8(*reinterpret_cast<const uint4*>(ab + r * 2 * ffn + ffn + c), b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = a[i] / (1.f + __expf(-a[i])) * b[i];
+  *reinterpret_cast<uint4*>(m + r * ffn + c) = pack8(o);
+}
+
+void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn, cudaStream_t st) {
+  const int64_t total = rows * (ffn / 8);
+  if (total <= 0) return;
+  swiglu_fwd_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(ab, m, rows, ffn);
+}
+
+// da = dm * b * s * (1 + a (1 - s)),  db = dm * a * s,  s = sigmoid(a)
+__global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ dm,
+                                  const __nv_bfloat16* __restrict__ ab,
+                                  __nv_bfloat16* __restrict__ dab, int64_t rows, int ffn) {
+  const int per_row = ffn >> 3;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const int64_t r = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  float a[8], b[8], g[8], da[8], db[8];
+  unpack8(*reinterpret_cast<const uint4*>(ab + r * 2 * ffn + c), a);
+  unpack8(*reinterpret_cast<const uint4*>(ab + r * 2 * ffn + ffn + c), b);
+  unpack8(*reinterpret_cast<const uint4*>(dm + r * ffn + c), g);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float s = 1.f / (1.f + __expf(-a[i]));
+    da[i] = g[i] * b[i] * s * (1.f + a[i] * (1.f - s));
+    db[i] = g[i] * a[i] * s;
+  }
+  *reinterpret_cast<uint4*>(dab + r * 2 * ffn + c) = pack8(da);
+  *reinterpret_cast<uint4*>(dab + r * 2 * ffn + ffn + c) = pack8(db);
+}
+
+void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16* dab, int64_t rows,
+                int ffn, cudaStream_t st) {
+  const int64_t total = rows * (ffn / 8);
+  if (total <= 0) return;
+  swiglu_bwd_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(dm, ab, dab, rows, ffn);
+}
+
+// ------------------------------------------------------------------ cross-entropy rows
+// One CTA per logits row (bf16, in place):  lse by an online max / sum-exp
+// pass, then dz = (exp(z - lse) - [v == label]) * inv_n written over z; rows
+// whose label is ignore (-100) get dz = 0 and loss 0.
+constexpr int kCeThreads = 512;
+
+__global__ void __launch_bounds__(kCeThreads)
+    ce_rows_kernel(__nv_bfloat16* __restrict__ z, const int32_t* __restrict__ labels, int64_t vocab,
+                   float inv_n, float* __restrict__ loss_rows) {
+  __shared__ float shm[32], shs[32];
+  const int64_t row = blockIdx.x;
+  __nv_bfloat16* zr = z + row * vocab;
+  const int label = labels[row];
+  const int64_t n8 = vocab >> 3;  // vocab % 8 == 0 (checked by the caller)
+  const uint4* zv = reinterpret_cast<const uint4*>(zr);
+  if (label < 0) {
+    uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) reinterpret_cast<uint4*>(zr)[i] = zero;
+    if (threadIdx.x == 0) loss_rows[row] = 0.f;
+    return;
+  }
+  float m = -FLT_MAX, s = 0.f;
+  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
+    float f[8];
+    unpack8(zv[i], f);
+    float lm = f[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) lm = fmaxf(lm, f[k]);
+    if (lm > m) {
+      s *= __expf(m - lm);
+      m = lm;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += __expf(f[k] - m);
+  }
+  // combine (m, s) across the block
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float wm = warp_max(m);
+  s *= __expf(m - wm);
+  s = warp_sum(s);
+  if (lane == 0) { shm[w] = wm; shs[w] = s; }
+  __syncthreads();
+  float bm = -FLT_MAX;
+  for (int i = 0; i < nw; ++i) bm = fmaxf(bm, shm[i]);
+  float bs = 0.f;
+  for (int i = 0; i < nw; ++i) bs += shs[i] * __expf(shm[i] - bm);
+  const float lse = bm + __logf(bs);
+  const float z_label = __bfloat162float(zr[label]);
+  __syncthreads();  // everyone has read zr[label] before it is overwritten
+  if (threadIdx.x == 0) loss_rows[row] = lse - z_label;
+  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
+    float f[8];
+    unpack8(zv[i], f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float p = __expf(f[k] - lse);
+      if (i * 8 + k == label) p -= 1.f;
+      f[k] = p * inv_n;
+    }
+    reinterpret_cast<uint4*>(zr)[i] = pack8(f);
+  }
+}
+
+void ce_rows(__nv_bfloat16* z, const int32_t* labels, int64_t rows, int64_t vocab, float inv_n,
+             float* loss_rows, cudaStream_t st) {
+  if (rows <= 0) return;
+  ce_rows_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, labels, vocab, inv_n, loss_rows);
+}
+
+// ------------------------------------------------------------------ reductions / casts
+// out[0] = scale * sum(x) in a fixed order (one CTA).
+__global__ void sum_kernel(const float* __restrict__ x, int64_t n, float scale, float* out) {
+  __shared__ float sh[32];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) acc += x[i];
+  float v = block_sum((float)acc, sh);
+  if (threadIdx.x == 0) out[0] = v * scale;
+}
+
+void sum_f32(const float* x, int64_t n, float scale, float* out, cudaStream_t st) {
+  sum_kernel<<<1, 1024, 0, st>>>(x, n, scale, out);
+}
+
+__global__ void cast_f32_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y, int64_t n) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i + 8 <= n) {
+    float4 a = reinterpret_cast<const float4*>(x + i)[0], b = reinterpret_cast<const float4*>(x + i)[1];
+    float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    *reinterpret_cast<uint4*>(y + i) = pack8(f);
+  } else {
+    for (int64_t j = i; j < n; ++j) y[j] = __float2bfloat16_rn(x[j]);
+  }
+}
+
+void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st) {
+  const int64_t threads = (n + 7) / 8;
+  if (threads <= 0) return;
+  cast_f32_bf16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(x, y, n);
+}
+
+__global__ void cast_bf16_f32_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i + 8 <= n) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(x + i), f);
+    reinterpret_cast<float4*>(y + i)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(y + i)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  } else {
+    for (int64_t j = i; j < n; ++j) y[j] = __bfloat162float(x[j]);
+  }
+}
+
+void cast_bf16_f32(const __nv_bfloat16* x, float* y, int64_t n, cudaStream_t st) {
+  const int64_t threads = (n + 7) / 8;
+  if (threads <= 0) return;
+  cast_bf16_f32_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(x, y, n);
+}
+
+}  // namespace sf

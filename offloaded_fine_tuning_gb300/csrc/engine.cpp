@@ -1,0 +1,1247 @@
+// Layer-sliding training engine: the model API of sf.h.
+//
+// SlideFormer ("An Efficient Heterogeneous Co-Design for Fine-Tuning on a
+// Single GPU", gist.science technical summary):
+//   2.A  layers slide through the GPU; one host thread drives separate CUDA
+//        streams for transfers and compute; after layer i's backward its
+//        gradients go to the host while the GPU runs layer i-1's backward and
+//        prefetches layer i-2; the CPU updates layer i meanwhile.
+//   2.B  a pre-allocated queue of identical GPU buffers holds the active
+//        layers; gradients and the fp32->bf16 conversions share fixed host
+//        buffers; Adam state lives in host memory and is updated per layer.
+//   2.C  fused LinearCrossEntropy keeps the logits out of memory.
+//
+// This engine: R ring slots (weights + gradients of one layer each) on the
+// device; streams C (compute), U (host->device) and D (device->host) fenced
+// by events; one pinned bf16 pack per layer that first carries the weights to
+// the GPU and then receives that layer's gradients, which the host Adam
+// workers turn back into the next step's bf16 weights in place.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <condition_variable>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <functional>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "sf.h"
+#include "sf_internal.h"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using Clock = std::chrono::steady_clock;
+
+thread_local std::string g_init_error;
+
+inline uint16_t f2bf(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+inline float bf2f(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ thread pool
+// parallel_for over [0, n) in chunks; the calling thread takes part.  One
+// parallel_for runs at a time (callers are serialised).
+class Pool {
+ public:
+  explicit Pool(int threads) {
+    for (int i = 1; i < threads; ++i) workers_.emplace_back([this] { work(); });
+  }
+  ~Pool() {
+    {
+      std::lock_guard<std::mutex> l(m_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : workers_) t.join();
+  }
+  int size() const { return (int)workers_.size() + 1; }
+  void parallel_for(int64_t n, int64_t chunk, const std::function<void(int64_t, int64_t)>& fn) {
+    if (n <= 0) return;
+    std::lock_guard<std::mutex> run(run_m_);
+    {
+      std::lock_guard<std::mutex> l(m_);
+      fn_ = &fn;
+      n_ = n;
+      chunk_ = std::max<int64_t>(1, chunk);
+      next_.store(0);
+      active_ = (int)workers_.size();
+      ++gen_;
+    }
+    cv_.notify_all();
+    run_chunks();
+    std::unique_lock<std::mutex> l(m_);
+    done_cv_.wait(l, [&] { return active_ == 0; });
+    fn_ = nullptr;
+  }
+
+ private:
+  void run_chunks() {
+    while (true) {
+      const int64_t b = next_.fetch_add(chunk_);
+      if (b >= n_) break;
+      (*fn_)(b, std::min(b + chunk_, n_));
+    }
+  }
+  void work() {
+    uint64_t seen = 0;
+    std::unique_lock<std::mutex> l(m_);
+    while (true) {
+      cv_.wait(l, [&] { return stop_ || gen_ != seen; });
+      if (stop_) return;
+      seen = gen_;
+      l.unlock();
+      run_chunks();
+      l.lock();
+      if (--active_ == 0) done_cv_.notify_all();
+    }
+  }
+  std::vector<std::thread> workers_;
+  std::mutex m_, run_m_;
+  std::condition_variable cv_, done_cv_;
+  const std::function<void(int64_t, int64_t)>* fn_ = nullptr;
+  int64_t n_ = 0, chunk_ = 1;
+  std::atomic<int64_t> next_{0};
+  int active_ = 0;
+  uint64_t gen_ = 0;
+  bool stop_ = false;
+};
+
+// One host copy of a unit's state.  pack = bf16 weights to stream in, then
+// (after the unit's backward) its bf16 gradients, then the updated weights.
+struct HostUnit {
+  int64_t elems = 0;          // padded pack length
+  uint16_t* pack = nullptr;   // pinned
+  std::unique_ptr<float[]> master, m, v;
+  std::vector<uint16_t> retained;  // last step's gradients (retain_grads)
+};
+
+// (offset in the caller's unpadded order, offset in the padded pack, count)
+struct Seg {
+  int64_t src, dst, n;
+};
+
+}  // namespace
+
+struct sf_ctx {
+  sf_config cfg{};
+  std::string err;
+  bool poisoned = false;
+  int L = 0, R = 0;
+  int64_t d = 0, qdim = 0, kvdim = 0, qkvdim = 0, F = 0, V = 0, Tmax = 0, Smax = 0;
+  int64_t off_g1 = 0, off_qkv = 0, off_o = 0, off_g2 = 0, off_gu = 0, off_d = 0, pack_elems = 0;
+  std::vector<Seg> segs;
+  int64_t chunk_rows = 0;
+  int dg_parts = 0;
+
+  // device
+  std::vector<void*> dev_allocs;
+  std::vector<bf16*> ring;  // R slots of 2 * pack_elems (weights, then grads)
+  float* X = nullptr;       // (L+1) * T * d checkpoints of the residual stream
+  bf16 *u = nullptr, *qkv = nullptr, *o = nullptr, *w2 = nullptr, *ab = nullptr, *mb = nullptr;
+  float *rstd1 = nullptr, *rstd2 = nullptr, *rstdf = nullptr, *lse = nullptr, *h = nullptr;
+  float *dX = nullptr, *dw2 = nullptr, *dh = nullptr, *du = nullptr, *dq_acc = nullptr,
+        *delta = nullptr, *dg_part = nullptr;
+  bf16 *dXb = nullptr, *dm = nullptr, *dab = nullptr, *dhb = nullptr, *dob = nullptr,
+       *dqkv = nullptr;
+  bf16 *hf = nullptr, *Wlm = nullptr, *gf = nullptr, *dWlm16 = nullptr, *dgf = nullptr,
+       *logits = nullptr, *x0b = nullptr;
+  float *dhf = nullptr, *dWlm32 = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
+  float2* rope_cs = nullptr;
+  int32_t* labels_dev = nullptr;
+  int* dev_err = nullptr;
+
+  // host
+  std::vector<HostUnit> layers;
+  HostUnit lm, fn;  // LM head [V*d], final norm [d]
+  std::unique_ptr<float[]> E, Em, Ev, dE;
+  uint16_t* x0_pin = nullptr;    // gathered embeddings, later the input gradient dX0
+  int32_t* lab_pin = nullptr;
+  float* loss_pin = nullptr;
+  int* err_pin = nullptr;
+  std::vector<void*> pinned;
+
+  // streams and events
+  cudaStream_t sC = nullptr, sU = nullptr, sD = nullptr;
+  std::vector<cudaEvent_t> ev_loaded, ev_free, ev_grads, ev_d2h;  // per slot x3, per layer
+  cudaEvent_t ev_x0 = nullptr, ev_lm = nullptr, ev_head = nullptr, ev_head_d2h = nullptr,
+              ev_dx0 = nullptr, ev_start = nullptr, ev_end = nullptr, ev_end_d = nullptr;
+  std::vector<cudaEvent_t> all_events;
+
+  // timing
+  bool timing = false;
+  std::vector<cudaEvent_t> t_ev;  // pairs
+  size_t t_used = 0;
+  std::vector<int> t_kind;        // 0 gemm, 1 attention
+  std::vector<double> t_flops;
+  sf_stats stats{};
+  int64_t launches = 0;
+
+  // host workers
+  std::unique_ptr<Pool> pool;
+  std::thread adam_thread;
+  std::mutex aq_m;
+  std::condition_variable aq_cv, aq_done_cv;
+  struct Task {
+    int unit;
+    cudaEvent_t ev;
+  };
+  std::deque<Task> aq;
+  int aq_pending = 0;
+  int aq_status = SF_OK;
+  std::string aq_err;
+  bool aq_stop = false;
+  const sf_adam* cur_adam = nullptr;
+  sf_adam adam_copy{};
+  bool adam_on = false;
+  int64_t adam_t = 0;
+  double adam_ms = 0.0;
+  std::atomic<int> inject_fail_unit{-1000};
+  std::atomic<int> inject_sleep_ms{0};
+
+  bool have_loss = false;
+  float loss = 0.f;
+  int64_t wait_ms = 300000;
+
+  void set_err(const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    err = buf;
+  }
+};
+
+namespace {
+
+#define CK(call)                                                                     \
+  do {                                                                               \
+    cudaError_t e_ = (call);                                                         \
+    if (e_ != cudaSuccess) {                                                         \
+      ctx->set_err("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, \
+                   __LINE__);                                                        \
+      ctx->poisoned = true;                                                          \
+      return SF_ECUDA;                                                               \
+    }                                                                                \
+  } while (0)
+
+bool dev_alloc(sf_ctx* ctx, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 256;
+  if (cudaMalloc(p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    ctx->set_err("cudaMalloc of %zu bytes failed", bytes);
+    return false;
+  }
+  ctx->dev_allocs.push_back(*p);
+  return true;
+}
+template <class T>
+bool dalloc(sf_ctx* ctx, T** p, int64_t n) {
+  return dev_alloc(ctx, reinterpret_cast<void**>(p), (size_t)n * sizeof(T));
+}
+template <class T>
+bool halloc(sf_ctx* ctx, T** p, int64_t n) {
+  void* q = nullptr;
+  size_t bytes = std::max<size_t>(256, (size_t)n * sizeof(T));
+  if (cudaHostAlloc(&q, bytes, cudaHostAllocPortable) != cudaSuccess) {
+    cudaGetLastError();
+    ctx->set_err("cudaHostAlloc of %zu bytes failed", bytes);
+    return false;
+  }
+  ctx->pinned.push_back(q);
+  *p = reinterpret_cast<T*>(q);
+  return true;
+}
+bool new_floats(sf_ctx* ctx, std::unique_ptr<float[]>& p, int64_t n) {
+  p.reset(new (std::nothrow) float[std::max<int64_t>(n, 1)]);
+  if (!p) ctx->set_err("host allocation of %lld floats failed", (long long)n);
+  return (bool)p;
+}
+
+// Bounded host wait on an event.
+int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
+  const auto deadline = Clock::now() + std::chrono::milliseconds(ctx->wait_ms);
+  while (true) {
+    cudaError_t r = cudaEventQuery(ev);
+    if (r == cudaSuccess) return SF_OK;
+    if (r != cudaErrorNotReady) {
+      ctx->set_err("waiting for %s: %s", what, cudaGetErrorString(r));
+      ctx->poisoned = true;
+      return SF_ECUDA;
+    }
+    if (Clock::now() > deadline) {
+      ctx->set_err("timed out after %lld ms waiting for %s", (long long)ctx->wait_ms, what);
+      return SF_ETIMEOUT;
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+// ------------------------------------------------------------------ Adam on host
+// One unit: optional copy of the gradients, then either the Adam update of the
+// fp32 master (refreshing the bf16 pack in place) or, without an optimizer, a
+// refresh of the pack from the unchanged master.
+void host_update(sf_ctx* ctx, HostUnit& hu, bool retain) {
+  if (retain) {
+    hu.retained.resize((size_t)hu.elems);
+    uint16_t* dst = hu.retained.data();
+    const uint16_t* src = hu.pack;
+    ctx->pool->parallel_for(hu.elems, 1 << 18, [&](int64_t b, int64_t e) {
+      std::memcpy(dst + b, src + b, (size_t)(e - b) * 2);
+    });
+  }
+  uint16_t* p = hu.pack;
+  float* w = hu.master.get();
+  if (!ctx->adam_on) {
+    ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
+    });
+    return;
+  }
+  const sf_adam a = ctx->adam_copy;
+  const float b1 = a.beta1, b2 = a.beta2, lr = a.lr, eps = a.eps, wd = a.weight_decay;
+  const float bc1 = 1.f - std::pow(b1, (float)ctx->adam_t);
+  const float bc2 = 1.f - std::pow(b2, (float)ctx->adam_t);
+  float* m = hu.m.get();
+  float* v = hu.v.get();
+  ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) {
+      const float g = bf2f(p[i]);
+      const float mi = b1 * m[i] + (1.f - b1) * g;
+      const float vi = b2 * v[i] + (1.f - b2) * g * g;
+      float th = w[i];
+      th = th - lr * wd * th - lr * (mi / bc1) / (std::sqrt(vi / bc2) + eps);
+      m[i] = mi;
+      v[i] = vi;
+      w[i] = th;
+      p[i] = f2bf(th);
+    }
+  });
+}
+
+void adam_loop(sf_ctx* ctx) {
+  while (true) {
+    sf_ctx::Task t;
+    {
+      std::unique_lock<std::mutex> l(ctx->aq_m);
+      ctx->aq_cv.wait(l, [&] { return ctx->aq_stop || !ctx->aq.empty(); });
+      if (ctx->aq_stop && ctx->aq.empty()) return;
+      t = ctx->aq.front();
+      ctx->aq.pop_front();
+    }
+    int st = SF_OK;
+    std::string why;
+    {
+      const auto deadline = Clock::now() + std::chrono::milliseconds(ctx->wait_ms);
+      while (true) {
+        cudaError_t r = cudaEventQuery(t.ev);
+        if (r == cudaSuccess) break;
+        if (r != cudaErrorNotReady) {
+          st = SF_ECUDA;
+          why = std::string("gradient copy of unit failed: ") + cudaGetErrorString(r);
+          break;
+        }
+        if (Clock::now() > deadline) {
+          st = SF_ETIMEOUT;
+          why = "timed out waiting for a gradient copy";
+          break;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+      }
+    }
+    if (st == SF_OK && ctx->inject_sleep_ms.load() > 0)
+      std::this_thread::sleep_for(std::chrono::milliseconds(ctx->inject_sleep_ms.load()));
+    if (st == SF_OK && ctx->inject_fail_unit.load() == t.unit) {
+      st = SF_ESTATE;
+      why = "injected Adam worker failure on unit " + std::to_string(t.unit);
+      // the gradients are dropped: put the unchanged weights back into the pack
+      const bool on = ctx->adam_on;
+      ctx->adam_on = false;
+      if (t.unit >= 0) {
+        host_update(ctx, ctx->layers[t.unit], false);
+      } else {
+        host_update(ctx, ctx->lm, false);
+        host_update(ctx, ctx->fn, false);
+      }
+      ctx->adam_on = on;
+    }
+    if (st == SF_ETIMEOUT || st == SF_ECUDA) ctx->poisoned = true;  // the pack is in an unknown state
+    if (st == SF_OK) {
+      const auto t0 = Clock::now();
+      const bool retain = ctx->cfg.retain_grads != 0;
+      if (t.unit >= 0) {
+        host_update(ctx, ctx->layers[t.unit], retain);
+      } else {  // LM head and final norm
+        host_update(ctx, ctx->lm, retain);
+        host_update(ctx, ctx->fn, retain);
+      }
+      ctx->adam_ms += std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+    }
+    {
+      std::lock_guard<std::mutex> l(ctx->aq_m);
+      if (st != SF_OK && ctx->aq_status == SF_OK) {
+        ctx->aq_status = st;
+        ctx->aq_err = why;
+      }
+      --ctx->aq_pending;
+    }
+    ctx->aq_done_cv.notify_all();
+  }
+}
+
+void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev) {
+  {
+    std::lock_guard<std::mutex> l(ctx->aq_m);
+    ctx->aq.push_back({unit, ev});
+    ++ctx->aq_pending;
+  }
+  ctx->aq_cv.notify_one();
+}
+
+int wait_tasks(sf_ctx* ctx) {
+  std::unique_lock<std::mutex> l(ctx->aq_m);
+  const bool ok = ctx->aq_done_cv.wait_for(l, std::chrono::milliseconds(ctx->wait_ms),
+                                           [&] { return ctx->aq_pending == 0; });
+  if (!ok) {
+    ctx->set_err("timed out waiting for the host Adam workers");
+    return SF_ETIMEOUT;
+  }
+  if (ctx->aq_status != SF_OK) {
+    ctx->set_err("%s", ctx->aq_err.c_str());
+    int st = ctx->aq_status;
+    ctx->aq_status = SF_OK;
+    return st;
+  }
+  return SF_OK;
+}
+
+// ------------------------------------------------------------------ timing helpers
+struct Timed {
+  sf_ctx* ctx;
+  int kind;
+  double flops;
+  cudaEvent_t b = nullptr, e = nullptr;
+  Timed(sf_ctx* c, int k, double f) : ctx(c), kind(k), flops(f) {
+    if (!ctx->timing) return;
+    while (ctx->t_ev.size() < 2 * (ctx->t_used + 1)) {
+      cudaEvent_t x;
+      if (cudaEventCreate(&x) != cudaSuccess) return;
+      ctx->t_ev.push_back(x);
+    }
+    b = ctx->t_ev[2 * ctx->t_used];
+    e = ctx->t_ev[2 * ctx->t_used + 1];
+    ++ctx->t_used;
+    ctx->t_kind.push_back(kind);
+    ctx->t_flops.push_back(flops);
+    cudaEventRecord(b, ctx->sC);
+  }
+  ~Timed() {
+    if (e) cudaEventRecord(e, ctx->sC);
+  }
+};
+
+int gemm(sf_ctx* ctx, int layout, int epi, int64_t M, int64_t N, int64_t K, const void* A,
+         int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R = nullptr,
+         int64_t ldr = 0, float alpha = 1.f) {
+  sf::GemmArgs g;
+  g.layout = layout; g.epi = epi; g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.R = R; g.ldr = ldr;
+  g.alpha = alpha;
+  int st;
+  char why[128] = {0};
+  {
+    Timed t(ctx, 0, 2.0 * M * N * K);
+    st = sf::gemm(g, ctx->dev_err, ctx->sC, why);
+  }
+  ctx->launches += 1;
+  ctx->stats.gemm_launches += 1;
+  if (st != 0) {
+    ctx->set_err("%s", why);
+    if (st == -3) ctx->poisoned = true;
+    return st == -3 ? SF_ECUDA : SF_EINVAL;
+  }
+  return SF_OK;
+}
+
+double attn_fwd_flops(int64_t B, int64_t S, int64_t Hq, int64_t hd) {
+  // QK^T and PV over the causal half (diagonal included): 2 * 2 * hd * S(S+1)/2 per head
+  return 2.0 * B * Hq * hd * (double)S * (double)(S + 1);
+}
+
+#define RET(x)                    \
+  do {                            \
+    int r_ = (x);                 \
+    if (r_ != SF_OK) return r_;   \
+  } while (0)
+
+// ------------------------------------------------------------------ layer compute
+struct LayerW {
+  const bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+};
+struct LayerG {
+  bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+};
+LayerW slot_w(sf_ctx* c, int s) {
+  const bf16* b = c->ring[s];
+  return {b + c->off_g1, b + c->off_qkv, b + c->off_o, b + c->off_g2, b + c->off_gu, b + c->off_d};
+}
+LayerG slot_g(sf_ctx* c, int s) {
+  bf16* b = c->ring[s] + c->pack_elems;
+  return {b + c->off_g1, b + c->off_qkv, b + c->off_o, b + c->off_g2, b + c->off_gu, b + c->off_d};
+}
+
+// Forward of one layer from X_l (fp32) to X_{l+1}; with `full == false` the
+// final down projection is skipped (recompute for the backward needs only the
+// intermediates).
+int layer_forward(sf_ctx* c, const LayerW& w, const float* Xin, float* Xout, int B, int S,
+                  bool full) {
+  sf_ctx* ctx = c;
+  const int64_t T = (int64_t)B * S, d = c->d, F = c->F;
+  const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
+  sf::rmsnorm_fwd(Xin, w.g1, c->u, c->rstd1, T, (int)d, c->cfg.rms_eps, c->sC);
+  RET(gemm(c, sf::kNT, sf::kEpiBF16, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim));
+  sf::rope_inplace(c->qkv, c->qkvdim, T, S, Hq + Hkv, hd, c->rope_cs, 0, c->sC);
+  {
+    Timed t(c, 1, attn_fwd_flops(B, S, Hq, hd));
+    if (sf::attn_fwd(c->qkv, c->o, c->lse, B, S, Hq, Hkv, hd, c->sC) != 0) {
+      ctx->set_err("attention forward launch failed");
+      return SF_ECUDA;
+    }
+  }
+  RET(gemm(c, sf::kNT, sf::kEpiF32Add, T, d, c->qdim, c->o, c->qdim, w.wo, c->qdim, c->h, d,
+           Xin, d));
+  sf::rmsnorm_fwd(c->h, w.g2, c->w2, c->rstd2, T, (int)d, c->cfg.rms_eps, c->sC);
+  RET(gemm(c, sf::kNT, sf::kEpiBF16, T, 2 * F, d, c->w2, d, w.wgu, d, c->ab, 2 * F));
+  sf::swiglu_fwd(c->ab, c->mb, T, (int)F, c->sC);
+  c->launches += 5;
+  if (full)
+    RET(gemm(c, sf::kNT, sf::kEpiF32Add, T, d, F, c->mb, F, w.wd, F, Xout, d, c->h, d));
+  return SF_OK;
+}
+
+// Backward of one layer.  On entry dX / dXb hold dLoss/dX_{l+1}; on exit they
+// hold dLoss/dX_l.  Weight gradients go into the slot's gradient area (bf16).
+int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin, int B, int S) {
+  sf_ctx* ctx = c;
+  const int64_t T = (int64_t)B * S, d = c->d, F = c->F;
+  const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
+  // down projection: X_{l+1} = h + m Wd^T
+  RET(gemm(c, sf::kNN, sf::kEpiBF16, T, F, d, c->dXb, d, w.wd, F, c->dm, F));
+  RET(gemm(c, sf::kTN, sf::kEpiBF16, d, F, T, c->dXb, d, c->mb, F, g.wd, F));
+  sf::swiglu_bwd(c->dm, c->ab, c->dab, T, (int)F, c->sC);
+  // gate/up projection from w2 = RMSNorm(h; g2)
+  RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, 2 * F, c->dab, 2 * F, w.wgu, d, c->dw2, d));
+  RET(gemm(c, sf::kTN, sf::kEpiBF16, 2 * F, d, T, c->dab, 2 * F, c->w2, d, g.wgu, d));
+  sf::rmsnorm_bwd(c->h, w.g2, c->rstd2, c->dw2, c->dX, c->dh, c->dhb, c->dg_part, c->dg_parts,
+                  T, (int)d, c->sC);
+  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, g.g2, c->sC);
+  // output projection: h = X_l + o Wo^T
+  RET(gemm(c, sf::kNN, sf::kEpiBF16, T, c->qdim, d, c->dhb, d, w.wo, c->qdim, c->dob, c->qdim));
+  RET(gemm(c, sf::kTN, sf::kEpiBF16, d, c->qdim, T, c->dhb, d, c->o, c->qdim, g.wo, c->qdim));
+  {
+    Timed t(c, 1, 2.5 * attn_fwd_flops(B, S, Hq, hd));
+    if (sf::attn_bwd(c->qkv, c->o, c->dob, c->lse, c->delta, c->dq_acc, c->dqkv, B, S, Hq, Hkv,
+                     hd, c->rope_cs, c->sC) != 0) {
+      ctx->set_err("attention backward launch failed");
+      return SF_ECUDA;
+    }
+  }
+  // QKV projection from u = RMSNorm(X_l; g1)
+  RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, c->qkvdim, c->dqkv, c->qkvdim, w.wqkv, d, c->du, d));
+  RET(gemm(c, sf::kTN, sf::kEpiBF16, c->qkvdim, d, T, c->dqkv, c->qkvdim, c->u, d, g.wqkv, d));
+  sf::rmsnorm_bwd(Xin, w.g1, c->rstd1, c->du, c->dh, c->dX, c->dXb, c->dg_part, c->dg_parts, T,
+                  (int)d, c->sC);
+  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, g.g1, c->sC);
+  c->launches += 8;  // swiglu, 2 norm, 2 reduce, 3 attention (GEMMs are counted in gemm())
+  return SF_OK;
+}
+
+// Final norm + fused chunked LM head / cross-entropy + final norm backward.
+int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
+  sf_ctx* ctx = c;
+  const int64_t d = c->d, V = c->V;
+  const float* XL = c->X + (int64_t)c->L * T * d;
+  sf::rmsnorm_fwd(XL, c->gf, c->hf, c->rstdf, T, (int)d, c->cfg.rms_eps, c->sC);
+  const float inv_n = n_valid > 0 ? 1.f / (float)n_valid : 0.f;
+  for (int64_t r0 = 0; r0 < T; r0 += c->chunk_rows) {
+    const int64_t n = std::min(c->chunk_rows, T - r0);
+    RET(gemm(c, sf::kNT, sf::kEpiBF16, n, V, d, c->hf + r0 * d, d, c->Wlm, d, c->logits, V));
+    sf::ce_rows(c->logits, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0, c->sC);
+    RET(gemm(c, sf::kNN, sf::kEpiF32, n, d, V, c->logits, V, c->Wlm, d, c->dhf + r0 * d, d));
+    RET(gemm(c, sf::kTN, r0 == 0 ? sf::kEpiF32 : sf::kEpiF32Acc, V, d, n, c->logits, V,
+             c->hf + r0 * d, d, c->dWlm32, d));
+    c->launches += 1;
+  }
+  sf::sum_f32(c->loss_rows, T, inv_n, c->loss_dev, c->sC);
+  sf::rmsnorm_bwd(XL, c->gf, c->rstdf, c->dhf, nullptr, c->dX, c->dXb, c->dg_part, c->dg_parts,
+                  T, (int)d, c->sC);
+  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, c->dgf, c->sC);
+  sf::cast_f32_bf16(c->dWlm32, c->dWlm16, V * d, c->sC);
+  c->launches += 5;
+  return SF_OK;
+}
+
+size_t unit_numel_cfg(const sf_config* c, int32_t unit) {
+  if (!c) return 0;
+  const int64_t d = c->hidden, q = (int64_t)c->n_heads * c->head_dim,
+                kv = (int64_t)c->n_kv_heads * c->head_dim, F = c->ffn;
+  if (unit >= 0) {
+    if (unit >= c->n_layers) return 0;
+    return (size_t)(2 * d + q * d + 2 * kv * d + d * q + 3 * F * d);
+  }
+  if (unit == SF_UNIT_EMBED || unit == SF_UNIT_LM_HEAD) return (size_t)c->vocab * (size_t)d;
+  if (unit == SF_UNIT_FINAL_NORM) return (size_t)d;
+  return 0;
+}
+
+const char* validate(const sf_config* c) {
+  if (!c) return "null config";
+  if (c->n_layers < 1) return "n_layers must be >= 1";
+  if (c->hidden < 8 || c->hidden % 8 || c->hidden > 16384) return "hidden must be a multiple of 8 in [8, 16384]";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) return "n_heads must be a positive multiple of n_kv_heads";
+  if (c->ffn < 8 || c->ffn % 8) return "ffn must be a positive multiple of 8";
+  if (c->vocab < 8 || c->vocab % 8) return "vocab must be a positive multiple of 8";
+  if (c->max_batch < 1 || c->max_seq < 1) return "max_batch and max_seq must be >= 1";
+  if ((int64_t)c->max_batch * c->max_seq > (int64_t)1 << 26) return "max_batch * max_seq too large";
+  if (c->ring_slots < 2 || c->ring_slots > std::max(2, c->n_layers)) return "ring_slots must be in [2, max(2, n_layers)]";
+  if (c->lce_chunk_rows < 0) return "lce_chunk_rows must be >= 0";
+  if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.f)) return "rms_eps must be > 0 and rope_base > 1";
+  return nullptr;
+}
+
+int init(sf_ctx* ctx) {
+  const sf_config& cf = ctx->cfg;
+  ctx->L = cf.n_layers;
+  ctx->R = std::min(cf.ring_slots, cf.n_layers);
+  ctx->d = cf.hidden;
+  ctx->qdim = (int64_t)cf.n_heads * cf.head_dim;
+  ctx->kvdim = (int64_t)cf.n_kv_heads * cf.head_dim;
+  ctx->qkvdim = ctx->qdim + 2 * ctx->kvdim;
+  ctx->F = cf.ffn;
+  ctx->V = cf.vocab;
+  ctx->Smax = cf.max_seq;
+  ctx->Tmax = (int64_t)cf.max_batch * cf.max_seq;
+  ctx->wait_ms = cf.wait_timeout_ms > 0 ? cf.wait_timeout_ms : 300000;
+  const int64_t d = ctx->d, T = ctx->Tmax, F = ctx->F, V = ctx->V, L = ctx->L;
+  // padded pack: each group starts on a 256-byte boundary
+  constexpr int64_t A = 128;
+  ctx->off_g1 = 0;
+  ctx->off_qkv = round_up(d, A);
+  ctx->off_o = round_up(ctx->off_qkv + ctx->qkvdim * d, A);
+  ctx->off_g2 = round_up(ctx->off_o + d * ctx->qdim, A);
+  ctx->off_gu = round_up(ctx->off_g2 + d, A);
+  ctx->off_d = round_up(ctx->off_gu + 2 * F * d, A);
+  ctx->pack_elems = round_up(ctx->off_d + d * F, A);
+  int64_t src = 0;
+  auto seg = [&](int64_t dst, int64_t n) {
+    ctx->segs.push_back({src, dst, n});
+    src += n;
+  };
+  seg(ctx->off_g1, d);
+  seg(ctx->off_qkv, ctx->qkvdim * d);
+  seg(ctx->off_o, d * ctx->qdim);
+  seg(ctx->off_g2, d);
+  seg(ctx->off_gu, 2 * F * d);
+  seg(ctx->off_d, d * F);
+  if (cf.lce_chunk_rows > 0) {
+    ctx->chunk_rows = std::min<int64_t>(cf.lce_chunk_rows, T);
+  } else {
+    int64_t c = ((int64_t)1 << 30) / (2 * V);
+    c = std::max<int64_t>(128, c / 128 * 128);
+    ctx->chunk_rows = std::min<int64_t>(c, T);
+  }
+  ctx->dg_parts = sf::rmsnorm_bwd_parts(T);
+
+  if (cudaSetDevice(cf.device) != cudaSuccess) {
+    cudaGetLastError();
+    ctx->set_err("cudaSetDevice(%d) failed", cf.device);
+    return SF_ECUDA;
+  }
+  int threads = cf.adam_threads > 0 ? cf.adam_threads : (int)std::thread::hardware_concurrency();
+  ctx->pool.reset(new Pool(std::max(1, threads)));
+
+  // ---- device buffers
+  bool ok = true;
+  ctx->ring.resize(ctx->R);
+  for (int s = 0; s < ctx->R && ok; ++s) ok = dalloc(ctx, &ctx->ring[s], 2 * ctx->pack_elems);
+  ok = ok && dalloc(ctx, &ctx->X, (L + 1) * T * d);
+  ok = ok && dalloc(ctx, &ctx->u, T * d) && dalloc(ctx, &ctx->qkv, T * ctx->qkvdim) &&
+       dalloc(ctx, &ctx->o, T * ctx->qdim) && dalloc(ctx, &ctx->w2, T * d) &&
+       dalloc(ctx, &ctx->ab, T * 2 * F) && dalloc(ctx, &ctx->mb, T * F) &&
+       dalloc(ctx, &ctx->rstd1, T) && dalloc(ctx, &ctx->rstd2, T) && dalloc(ctx, &ctx->rstdf, T) &&
+       dalloc(ctx, &ctx->lse, T * cf.n_heads) && dalloc(ctx, &ctx->h, T * d);
+  ok = ok && dalloc(ctx, &ctx->dX, T * d) && dalloc(ctx, &ctx->dw2, T * d) &&
+       dalloc(ctx, &ctx->dh, T * d) && dalloc(ctx, &ctx->du, T * d) &&
+       dalloc(ctx, &ctx->dq_acc, T * ctx->qdim) && dalloc(ctx, &ctx->delta, T * cf.n_heads) &&
+       dalloc(ctx, &ctx->dg_part, (int64_t)ctx->dg_parts * d) && dalloc(ctx, &ctx->dXb, T * d) &&
+       dalloc(ctx, &ctx->dm, T * F) && dalloc(ctx, &ctx->dab, T * 2 * F) &&
+       dalloc(ctx, &ctx->dhb, T * d) && dalloc(ctx, &ctx->dob, T * ctx->qdim) &&
+       dalloc(ctx, &ctx->dqkv, T * ctx->qkvdim);
+  ok = ok && dalloc(ctx, &ctx->hf, T * d) && dalloc(ctx, &ctx->Wlm, V * d) &&
+       dalloc(ctx, &ctx->gf, round_up(d, A)) && dalloc(ctx, &ctx->dWlm16, V * d) &&
+       dalloc(ctx, &ctx->dgf, round_up(d, A)) && dalloc(ctx, &ctx->logits, ctx->chunk_rows * V) &&
+       dalloc(ctx, &ctx->x0b, T * d) && dalloc(ctx, &ctx->dhf, T * d) &&
+       dalloc(ctx, &ctx->dWlm32, V * d) && dalloc(ctx, &ctx->loss_rows, T) &&
+       dalloc(ctx, &ctx->loss_dev, 1) && dalloc(ctx, &ctx->labels_dev, T) &&
+       dalloc(ctx, &ctx->rope_cs, ctx->Smax * cf.head_dim / 2) && dalloc(ctx, &ctx->dev_err, 1);
+  if (!ok) return SF_ENOMEM;
+  // gradient areas: padding stays zero forever
+  for (int s = 0; s < ctx->R; ++s)
+    CK(cudaMemset(ctx->ring[s], 0, (size_t)2 * ctx->pack_elems * sizeof(bf16)));
+  CK(cudaMemset(ctx->dev_err, 0, sizeof(int)));
+  {
+    std::vector<float> tab((size_t)ctx->Smax * cf.head_dim);
+    sf_rope_table((int32_t)ctx->Smax, cf.head_dim, cf.rope_base, tab.data());
+    CK(cudaMemcpy(ctx->rope_cs, tab.data(), tab.size() * sizeof(float), cudaMemcpyHostToDevice));
+  }
+
+  // ---- host buffers
+  ctx->layers.resize(L);
+  auto host_unit = [&](HostUnit& hu, int64_t elems) -> bool {
+    hu.elems = elems;
+    if (!halloc(ctx, &hu.pack, elems)) return false;
+    if (!new_floats(ctx, hu.master, elems) || !new_floats(ctx, hu.m, elems) ||
+        !new_floats(ctx, hu.v, elems))
+      return false;
+    float* a = hu.master.get();
+    float* b = hu.m.get();
+    float* c = hu.v.get();
+    uint16_t* p = hu.pack;
+    ctx->pool->parallel_for(elems, 1 << 18, [&](int64_t s, int64_t e) {
+      std::memset(a + s, 0, (size_t)(e - s) * 4);
+      std::memset(b + s, 0, (size_t)(e - s) * 4);
+      std::memset(c + s, 0, (size_t)(e - s) * 4);
+      std::memset(p + s, 0, (size_t)(e - s) * 2);
+    });
+    return true;
+  };
+  for (int l = 0; l < L && ok; ++l) ok = host_unit(ctx->layers[l], ctx->pack_elems);
+  ok = ok && host_unit(ctx->lm, V * d) && host_unit(ctx->fn, round_up(d, A));
+  ok = ok && new_floats(ctx, ctx->E, V * d) && new_floats(ctx, ctx->Em, V * d) &&
+       new_floats(ctx, ctx->Ev, V * d) && new_floats(ctx, ctx->dE, V * d);
+  ok = ok && halloc(ctx, &ctx->x0_pin, T * d) && halloc(ctx, &ctx->lab_pin, T) &&
+       halloc(ctx, &ctx->loss_pin, 1) && halloc(ctx, &ctx->err_pin, 1);
+  if (!ok) return SF_ENOMEM;
+  {
+    float* a = ctx->E.get();
+    float* b = ctx->Em.get();
+    float* c = ctx->Ev.get();
+    float* e2 = ctx->dE.get();
+    ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t s, int64_t e) {
+      std::memset(a + s, 0, (size_t)(e - s) * 4);
+      std::memset(b + s, 0, (size_t)(e - s) * 4);
+      std::memset(c + s, 0, (size_t)(e - s) * 4);
+      std::memset(e2 + s, 0, (size_t)(e - s) * 4);
+    });
+  }
+
+  // ---- streams and events
+  CK(cudaStreamCreateWithFlags(&ctx->sC, cudaStreamNonBlocking));
+  CK(cudaStreamCreateWithFlags(&ctx->sU, cudaStreamNonBlocking));
+  CK(cudaStreamCreateWithFlags(&ctx->sD, cudaStreamNonBlocking));
+  auto mk = [&](cudaEvent_t* e, bool timed) -> int {
+    CK(cudaEventCreateWithFlags(e, timed ? cudaEventDefault : cudaEventDisableTiming));
+    ctx->all_events.push_back(*e);
+    return SF_OK;
+  };
+  ctx->ev_loaded.resize(ctx->R);
+  ctx->ev_free.resize(ctx->R);
+  ctx->ev_grads.resize(ctx->R);
+  ctx->ev_d2h.resize(L);
+  for (int s = 0; s < ctx->R; ++s) {
+    RET(mk(&ctx->ev_loaded[s], false));
+    RET(mk(&ctx->ev_free[s], false));
+    RET(mk(&ctx->ev_grads[s], false));
+  }
+  for (int l = 0; l < L; ++l) RET(mk(&ctx->ev_d2h[l], false));
+  RET(mk(&ctx->ev_x0, false));
+  RET(mk(&ctx->ev_lm, false));
+  RET(mk(&ctx->ev_head, false));
+  RET(mk(&ctx->ev_head_d2h, false));
+  RET(mk(&ctx->ev_dx0, false));
+  RET(mk(&ctx->ev_start, true));
+  RET(mk(&ctx->ev_end, true));
+  RET(mk(&ctx->ev_end_d, false));
+  ctx->adam_thread = std::thread(adam_loop, ctx);
+  return SF_OK;
+}
+
+void destroy(sf_ctx* ctx) {
+  if (ctx->adam_thread.joinable()) {
+    {
+      std::lock_guard<std::mutex> l(ctx->aq_m);
+      ctx->aq_stop = true;
+    }
+    ctx->aq_cv.notify_all();
+    ctx->adam_thread.join();
+  }
+  if (ctx->sC) cudaStreamSynchronize(ctx->sC);
+  if (ctx->sU) cudaStreamSynchronize(ctx->sU);
+  if (ctx->sD) cudaStreamSynchronize(ctx->sD);
+  for (auto e : ctx->all_events) cudaEventDestroy(e);
+  for (auto e : ctx->t_ev) cudaEventDestroy(e);
+  for (auto s : {ctx->sC, ctx->sU, ctx->sD})
+    if (s) cudaStreamDestroy(s);
+  for (void* p : ctx->dev_allocs) cudaFree(p);
+  for (void* p : ctx->pinned) cudaFreeHost(p);
+  ctx->pool.reset();
+}
+
+// Copy `unit`'s fp32 values between the caller's order and the padded pack.
+void scatter_unit(sf_ctx* ctx, const float* in, float* master) {
+  for (const Seg& s : ctx->segs) {
+    const float* a = in + s.src;
+    float* b = master + s.dst;
+    ctx->pool->parallel_for(s.n, 1 << 18, [&](int64_t x, int64_t y) {
+      std::memcpy(b + x, a + x, (size_t)(y - x) * 4);
+    });
+  }
+}
+
+int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S,
+         const sf_adam* adam) {
+  const int64_t T = (int64_t)B * S, d = ctx->d, V = ctx->V;
+  const int L = ctx->L, R = ctx->R;
+  const auto t_host0 = Clock::now();
+  // ---- validate on the host, count valid labels
+  int64_t n_valid = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    if (tokens[t] < 0 || tokens[t] >= V) {
+      ctx->set_err("token %d at position %lld outside [0, %lld)", tokens[t], (long long)t, (long long)V);
+      return SF_EINVAL;
+    }
+    const int32_t y = labels[t];
+    if (y == SF_IGNORE_INDEX) continue;
+    if (y < 0 || y >= V) {
+      ctx->set_err("label %d at position %lld outside [0, %lld) and not ignore_index", y, (long long)t, (long long)V);
+      return SF_EINVAL;
+    }
+    ++n_valid;
+  }
+  // host updates left over from a step that timed out still own the pinned packs
+  RET(wait_tasks(ctx));
+  ctx->adam_on = adam != nullptr;
+  if (adam) {
+    ctx->adam_copy = *adam;
+    ++ctx->adam_t;
+  }
+  ctx->stats = sf_stats{};
+  ctx->stats.timing_enabled = ctx->timing ? 1 : 0;
+  ctx->t_used = 0;
+  ctx->t_kind.clear();
+  ctx->t_flops.clear();
+  ctx->launches = 0;
+  ctx->adam_ms = 0.0;
+  double h2d = 0, d2h = 0;
+
+  // ---- A0: gather bf16 embedding rows into the pinned input buffer
+  {
+    const float* E = ctx->E.get();
+    uint16_t* x0 = ctx->x0_pin;
+    ctx->pool->parallel_for(T, 64, [&](int64_t b, int64_t e) {
+      for (int64_t t = b; t < e; ++t) {
+        const float* src = E + (int64_t)tokens[t] * d;
+        uint16_t* dst = x0 + t * d;
+        for (int64_t j = 0; j < d; ++j) dst[j] = f2bf(src[j]);
+      }
+    });
+    std::memcpy(ctx->lab_pin, labels, (size_t)T * 4);
+  }
+  CK(cudaEventRecord(ctx->ev_start, ctx->sC));
+  CK(cudaStreamWaitEvent(ctx->sU, ctx->ev_start, 0));
+  CK(cudaMemcpyAsync(ctx->x0b, ctx->x0_pin, (size_t)T * d * 2, cudaMemcpyHostToDevice, ctx->sU));
+  CK(cudaMemcpyAsync(ctx->labels_dev, ctx->lab_pin, (size_t)T * 4, cudaMemcpyHostToDevice, ctx->sU));
+  CK(cudaEventRecord(ctx->ev_x0, ctx->sU));
+  h2d += (double)T * d * 2 + (double)T * 4;
+  CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_x0, 0));
+  sf::cast_bf16_f32(ctx->x0b, ctx->X, T * d, ctx->sC);
+  ctx->launches += 1;
+
+  const size_t pack_bytes = (size_t)ctx->pack_elems * 2;
+  auto h2d_layer = [&](int l) -> int {
+    const int s = l % R;
+    CK(cudaStreamWaitEvent(ctx->sU, ctx->ev_free[s], 0));
+    CK(cudaMemcpyAsync(ctx->ring[s], ctx->layers[l].pack, pack_bytes, cudaMemcpyHostToDevice, ctx->sU));
+    CK(cudaEventRecord(ctx->ev_loaded[s], ctx->sU));
+    h2d += (double)pack_bytes;
+    return SF_OK;
+  };
+  // slots start free
+  for (int s = 0; s < R; ++s) CK(cudaEventRecord(ctx->ev_free[s], ctx->sC));
+
+  // ---- forward through the ring (A1-A9)
+  for (int l = 0; l < L; ++l) {
+    const int s = l % R;
+    RET(h2d_layer(l));
+    if (l == L - 1) {  // the LM head and final norm follow the last layer on the copy stream
+      CK(cudaMemcpyAsync(ctx->Wlm, ctx->lm.pack, (size_t)V * d * 2, cudaMemcpyHostToDevice, ctx->sU));
+      CK(cudaMemcpyAsync(ctx->gf, ctx->fn.pack, (size_t)ctx->fn.elems * 2, cudaMemcpyHostToDevice, ctx->sU));
+      CK(cudaEventRecord(ctx->ev_lm, ctx->sU));
+      h2d += (double)V * d * 2 + (double)ctx->fn.elems * 2;
+    }
+    CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_loaded[s], 0));
+    const float* Xin = ctx->X + (int64_t)l * T * d;
+    float* Xout = ctx->X + (int64_t)(l + 1) * T * d;
+    RET(layer_forward(ctx, slot_w(ctx, s), Xin, Xout, B, S, true));
+    CK(cudaEventRecord(ctx->ev_free[s], ctx->sC));
+  }
+
+  // ---- A10: fused LM head + cross-entropy, forward and backward
+  CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_lm, 0));
+  RET(head_fwd_bwd(ctx, T, n_valid));
+  CK(cudaEventRecord(ctx->ev_head, ctx->sC));
+  CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_head, 0));
+  CK(cudaMemcpyAsync(ctx->lm.pack, ctx->dWlm16, (size_t)V * d * 2, cudaMemcpyDeviceToHost, ctx->sD));
+  CK(cudaMemcpyAsync(ctx->fn.pack, ctx->dgf, (size_t)ctx->fn.elems * 2, cudaMemcpyDeviceToHost, ctx->sD));
+  CK(cudaEventRecord(ctx->ev_head_d2h, ctx->sD));
+  d2h += (double)V * d * 2 + (double)ctx->fn.elems * 2;
+  post_task(ctx, SF_UNIT_LM_HEAD, ctx->ev_head_d2h);
+
+  // ---- A11-A15: recompute + backward, gradients out, prefetch the next layers in
+  for (int l = L - 1; l >= 0; --l) {
+    const int s = l % R;
+    const bool resident = l >= L - R;  // still in its slot from the forward
+    if (!resident) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_loaded[s], 0));
+    const LayerW w = slot_w(ctx, s);
+    const float* Xin = ctx->X + (int64_t)l * T * d;
+    // the last layer's intermediates are still in the workspace from the forward
+    if (l != L - 1) RET(layer_forward(ctx, w, Xin, nullptr, B, S, false));
+    RET(layer_backward(ctx, w, slot_g(ctx, s), Xin, B, S));
+    CK(cudaEventRecord(ctx->ev_grads[s], ctx->sC));
+    CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_grads[s], 0));
+    CK(cudaMemcpyAsync(ctx->layers[l].pack, ctx->ring[s] + ctx->pack_elems, pack_bytes,
+                       cudaMemcpyDeviceToHost, ctx->sD));
+    CK(cudaEventRecord(ctx->ev_d2h[l], ctx->sD));
+    CK(cudaEventRecord(ctx->ev_free[s], ctx->sD));
+    d2h += (double)pack_bytes;
+    post_task(ctx, l, ctx->ev_d2h[l]);
+    const int nl = l - R;  // the next layer that is not resident goes into this slot
+    if (nl >= 0) RET(h2d_layer(nl));
+  }
+
+  // ---- A16: input gradient to the host, loss
+  sf::cast_f32_bf16(ctx->dX, ctx->x0b, T * d, ctx->sC);
+  ctx->launches += 1;
+  CK(cudaMemcpyAsync(ctx->err_pin, ctx->dev_err, sizeof(int), cudaMemcpyDeviceToHost, ctx->sC));
+  CK(cudaEventRecord(ctx->ev_end, ctx->sC));
+  CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_end, 0));
+  CK(cudaMemcpyAsync(ctx->x0_pin, ctx->x0b, (size_t)T * d * 2, cudaMemcpyDeviceToHost, ctx->sD));
+  CK(cudaMemcpyAsync(ctx->loss_pin, ctx->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, ctx->sD));
+  CK(cudaEventRecord(ctx->ev_dx0, ctx->sD));
+  d2h += (double)T * d * 2 + 4;
+
+  int st = wait_event(ctx, ctx->ev_dx0, "the input gradient copy");
+  if (st != SF_OK) {
+    wait_tasks(ctx);
+    return st;
+  }
+  const auto t_gpu_done = Clock::now();
+  if (*ctx->err_pin != 0) {
+    ctx->set_err("device wait limit reached in a kernel (code %d)", *ctx->err_pin);
+    ctx->poisoned = true;
+    wait_tasks(ctx);
+    return SF_EDEVICE;
+  }
+  // embedding gradient (scatter-add by column ranges: no races) and its update
+  {
+    float* dE = ctx->dE.get();
+    const uint16_t* g = ctx->x0_pin;
+    ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t b, int64_t e) {
+      std::memset(dE + b, 0, (size_t)(e - b) * 4);
+    });
+    ctx->pool->parallel_for(d, 64, [&](int64_t c0, int64_t c1) {
+      for (int64_t t = 0; t < T; ++t) {
+        float* row = dE + (int64_t)tokens[t] * d;
+        const uint16_t* gr = g + t * d;
+        for (int64_t j = c0; j < c1; ++j) row[j] += bf2f(gr[j]);
+      }
+    });
+    if (ctx->adam_on) {
+      const sf_adam a = ctx->adam_copy;
+      const float bc1 = 1.f - std::pow(a.beta1, (float)ctx->adam_t);
+      const float bc2 = 1.f - std::pow(a.beta2, (float)ctx->adam_t);
+      float* w = ctx->E.get();
+      float* m = ctx->Em.get();
+      float* v = ctx->Ev.get();
+      ctx->pool->parallel_for(V * d, 1 << 16, [&](int64_t b, int64_t e) {
+        for (int64_t i = b; i < e; ++i) {
+          const float gi = dE[i];
+          const float mi = a.beta1 * m[i] + (1.f - a.beta1) * gi;
+          const float vi = a.beta2 * v[i] + (1.f - a.beta2) * gi * gi;
+          float th = w[i];
+          th = th - a.lr * a.weight_decay * th - a.lr * (mi / bc1) / (std::sqrt(vi / bc2) + a.eps);
+          m[i] = mi;
+          v[i] = vi;
+          w[i] = th;
+        }
+      });
+    }
+  }
+  st = wait_tasks(ctx);
+  if (st != SF_OK) return st;
+  ctx->loss = *ctx->loss_pin;
+  ctx->have_loss = true;
+
+  // ---- counters
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, ctx->ev_start, ctx->ev_end) == cudaSuccess) ctx->stats.step_ms = ms;
+  for (size_t i = 0; i < ctx->t_used; ++i) {
+    float x = 0.f;
+    if (cudaEventElapsedTime(&x, ctx->t_ev[2 * i], ctx->t_ev[2 * i + 1]) != cudaSuccess) continue;
+    if (ctx->t_kind[i] == 0) {
+      ctx->stats.gemm_ms += x;
+      ctx->stats.gemm_flops += ctx->t_flops[i];
+    } else {
+      ctx->stats.attn_ms += x;
+      ctx->stats.attn_flops += ctx->t_flops[i];
+    }
+  }
+  cudaGetLastError();
+  ctx->stats.h2d_bytes = h2d;
+  ctx->stats.d2h_bytes = d2h;
+  ctx->stats.host_adam_ms = ctx->adam_ms;
+  ctx->stats.host_wait_ms = std::chrono::duration<double, std::milli>(Clock::now() - t_gpu_done).count();
+  ctx->stats.kernel_launches = ctx->launches;
+  (void)t_host0;
+  return SF_OK;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+extern "C" {
+
+size_t sf_unit_numel(const sf_config* cfg, int32_t unit) { return unit_numel_cfg(cfg, unit); }
+
+int sf_init_model(const sf_config* cfg, sf_ctx** out) {
+  if (!out) {
+    g_init_error = "null output pointer";
+    return SF_EINVAL;
+  }
+  *out = nullptr;
+  if (const char* why = validate(cfg)) {
+    g_init_error = why;
+    return SF_EINVAL;
+  }
+  sf_ctx* ctx = new (std::nothrow) sf_ctx();
+  if (!ctx) {
+    g_init_error = "out of host memory";
+    return SF_ENOMEM;
+  }
+  ctx->cfg = *cfg;
+  int st;
+  try {
+    st = init(ctx);
+  } catch (...) {
+    ctx->set_err("host allocation failed during init");
+    st = SF_ENOMEM;
+  }
+  if (st != SF_OK) {
+    g_init_error = ctx->err;
+    destroy(ctx);
+    delete ctx;
+    return st;
+  }
+  g_init_error.clear();
+  *out = ctx;
+  return SF_OK;
+}
+
+void sf_free(sf_ctx* ctx) {
+  if (!ctx) return;
+  destroy(ctx);
+  delete ctx;
+}
+
+const char* sf_last_error(const sf_ctx* ctx) { return ctx ? ctx->err.c_str() : g_init_error.c_str(); }
+
+int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t numel) {
+  if (!ctx) return SF_EINVAL;
+  if (ctx->poisoned) return SF_ESTATE;
+  if (!w || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
+    ctx->set_err("sf_load_layer_weights: bad unit %d or numel %zu", unit, numel);
+    return SF_EINVAL;
+  }
+  HostUnit* hu = nullptr;
+  float *master = nullptr, *m = nullptr, *v = nullptr;
+  int64_t n = (int64_t)numel;
+  if (unit >= 0) {
+    hu = &ctx->layers[unit];
+    scatter_unit(ctx, w, hu->master.get());
+  } else if (unit == SF_UNIT_EMBED) {
+    master = ctx->E.get();
+    m = ctx->Em.get();
+    v = ctx->Ev.get();
+  } else {
+    hu = unit == SF_UNIT_LM_HEAD ? &ctx->lm : &ctx->fn;
+  }
+  if (hu && unit < 0) {
+    float* dst = hu->master.get();
+    ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
+      std::memcpy(dst + b, w + b, (size_t)(e - b) * 4);
+    });
+  }
+  if (hu) {
+    master = hu->master.get();
+    m = hu->m.get();
+    v = hu->v.get();
+    n = hu->elems;
+    uint16_t* p = hu->pack;
+    ctx->pool->parallel_for(n, 1 << 16, [&](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i) p[i] = f2bf(master[i]);
+    });
+  } else {
+    ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
+      std::memcpy(master + b, w + b, (size_t)(e - b) * 4);
+    });
+  }
+  ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
+    std::memset(m + b, 0, (size_t)(e - b) * 4);
+    std::memset(v + b, 0, (size_t)(e - b) * 4);
+  });
+  return SF_OK;
+}
+
+int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
+                  int32_t seq, const sf_adam* adam) {
+  if (!ctx) return SF_EINVAL;
+  if (ctx->poisoned) {
+    ctx->set_err("context is poisoned by an earlier CUDA error");
+    return SF_ESTATE;
+  }
+  if (!tokens || !labels || batch < 1 || seq < 1 || seq > ctx->Smax ||
+      (int64_t)batch * seq > ctx->Tmax) {
+    ctx->set_err("sf_train_step: bad arguments (batch %d, seq %d)", batch, seq);
+    return SF_EINVAL;
+  }
+  if (adam && !(adam->lr >= 0.f && adam->beta1 >= 0.f && adam->beta1 < 1.f &&
+                adam->beta2 >= 0.f && adam->beta2 < 1.f && adam->eps > 0.f)) {
+    ctx->set_err("sf_train_step: bad Adam hyper-parameters");
+    return SF_EINVAL;
+  }
+  if (cudaSetDevice(ctx->cfg.device) != cudaSuccess) {
+    ctx->set_err("cudaSetDevice failed");
+    return SF_ECUDA;
+  }
+  int st;
+  try {
+    st = step(ctx, tokens, labels, batch, seq, adam);
+  } catch (...) {
+    ctx->set_err("host exception in the step");
+    ctx->poisoned = true;
+    st = SF_ESTATE;
+  }
+  if (st != SF_OK && st != SF_EINVAL) {
+    // leave no copy, kernel or host update of this step in flight
+    const std::string why = ctx->err;
+    cudaStreamSynchronize(ctx->sC);
+    cudaStreamSynchronize(ctx->sU);
+    cudaStreamSynchronize(ctx->sD);
+    wait_tasks(ctx);
+    ctx->err = why;
+    if (st == SF_ECUDA || st == SF_EDEVICE) ctx->poisoned = true;
+  }
+  return st;
+}
+
+int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
+  if (!ctx || !out || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
+    if (ctx) ctx->set_err("sf_get_grads: bad unit %d or numel %zu", unit, numel);
+    return SF_EINVAL;
+  }
+  if (!ctx->cfg.retain_grads || !ctx->have_loss) {
+    ctx->set_err("sf_get_grads needs retain_grads = 1 and a finished step");
+    return SF_ESTATE;
+  }
+  if (unit == SF_UNIT_EMBED) {
+    std::memcpy(out, ctx->dE.get(), numel * 4);
+    return SF_OK;
+  }
+  const HostUnit& hu = unit >= 0 ? ctx->layers[unit] : (unit == SF_UNIT_LM_HEAD ? ctx->lm : ctx->fn);
+  const uint16_t* g = hu.retained.data();
+  if (unit >= 0) {
+    for (const Seg& s : ctx->segs)
+      for (int64_t i = 0; i < s.n; ++i) out[s.src + i] = bf2f(g[s.dst + i]);
+  } else {
+    for (size_t i = 0; i < numel; ++i) out[i] = bf2f(g[i]);
+  }
+  return SF_OK;
+}
+
+int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
+  if (!ctx || !out || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
+    if (ctx) ctx->set_err("sf_get_weights: bad unit %d or numel %zu", unit, numel);
+    return SF_EINVAL;
+  }
+  if (unit == SF_UNIT_EMBED) {
+    std::memcpy(out, ctx->E.get(), numel * 4);
+    return SF_OK;
+  }
+  const HostUnit& hu = unit >= 0 ? ctx->layers[unit] : (unit == SF_UNIT_LM_HEAD ? ctx->lm : ctx->fn);
+  if (unit >= 0) {
+    for (const Seg& s : ctx->segs) std::memcpy(out + s.src, hu.master.get() + s.dst, (size_t)s.n * 4);
+  } else {
+    std::memcpy(out, hu.master.get(), numel * 4);
+  }
+  return SF_OK;
+}
+
+int sf_loss(sf_ctx* ctx, float* out) {
+  if (!ctx || !out) return SF_EINVAL;
+  if (!ctx->have_loss) {
+    ctx->set_err("no step has finished yet");
+    return SF_ESTATE;
+  }
+  *out = ctx->loss;
+  return SF_OK;
+}
+
+int sf_set_timing(sf_ctx* ctx, int32_t enabled) {
+  if (!ctx) return SF_EINVAL;
+  ctx->timing = enabled != 0;
+  return SF_OK;
+}
+
+int sf_get_stats(const sf_ctx* ctx, sf_stats* out) {
+  if (!ctx || !out) return SF_EINVAL;
+  *out = ctx->stats;
+  return SF_OK;
+}
+
+int sf_debug_inject(sf_ctx* ctx, int32_t what, int32_t arg) {
+  if (!ctx) return SF_EINVAL;
+  if (what == 0) {
+    ctx->inject_fail_unit = -1000;
+    ctx->inject_sleep_ms = 0;
+  } else if (what == 1) {
+    ctx->inject_fail_unit = arg;
+  } else if (what == 2) {
+    ctx->inject_sleep_ms = std::max(0, arg);
+  } else {
+    return SF_EINVAL;
+  }
+  return SF_OK;
+}
+
+}  // extern "C"

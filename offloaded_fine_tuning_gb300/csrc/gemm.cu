@@ -1,0 +1,432 @@
+// Dense bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), operands
+// staged by TMA.  Every dense contraction of the decoder step runs here: the
+// QKV, O, gate/up and down projections forward, their dX and dW products
+// backward, and the three LM-head products of the fused cross-entropy.
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: A and B tiles of BK = 64 into a STAGES-deep ring
+//   warp 1      MMA issuer: tcgen05.mma 128 x BN x 16 into a TMEM accumulator;
+//               also allocates / frees TMEM (512 columns = 2 accumulators)
+//   warps 2-5   epilogue: tcgen05.ld rows out of TMEM, convert, store
+// Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
+// tile i+1.  Tiles are visited in groups of 8 M-tiles so that the B panel of
+// a group stays in L2.  All operands use the 128-byte swizzle: a K-major tile
+// is [rows][64] with 128-byte rows; an MN-major tile is a set of [64 K rows]
+// x [64 MN] boxes placed 8 KB apart.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ptx.cuh"
+#include "sf_internal.h"
+
+namespace sf {
+
+struct GemmParams {
+  int M, N, K;
+  void* C;
+  int64_t ldc;
+  const float* R;
+  int64_t ldr;
+  float alpha;
+  int* err;
+};
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int BAR_OFF = STAGES * (A_BYTES + B_BYTES);
+  // full[S], empty[S], tfull[2], tempty[2], drain; then tmem slot and abort flag
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn) {
+  constexpr int G = 8;
+  const int per_group = G * num_n;
+  const int group = tile / per_group;
+  const int first_m = group * G;
+  const int gsize = min(num_m - first_m, G);
+  const int r = tile % per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 32 accumulator columns [col, col+32) of one output row.
+template <int EPI>
+__device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
+                                          const uint32_t (&r)[32]) {
+  const float a = p.alpha;
+  const bool full = (col + 32 <= p.N);
+  if constexpr (EPI == kEpiBF16) {
+    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
+    if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * a, __uint_as_float(r[8 * q + 1]) * a);
+        v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * a, __uint_as_float(r[8 * q + 3]) * a);
+        v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * a, __uint_as_float(r[8 * q + 5]) * a);
+        v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * a, __uint_as_float(r[8 * q + 7]) * a);
+        reinterpret_cast<uint4*>(c)[q] = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col + j < p.N) c[j] = __float2bfloat16_rn(__uint_as_float(r[j]) * a);
+    }
+  } else {
+    float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
+    const float* rr = nullptr;
+    if constexpr (EPI == kEpiF32Add) rr = p.R + (int64_t)row * p.ldr + col;
+    if constexpr (EPI == kEpiF32Acc) rr = c;
+    if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0) &&
+        (rr == nullptr || (reinterpret_cast<uintptr_t>(rr) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v = make_float4(__uint_as_float(r[4 * q + 0]) * a, __uint_as_float(r[4 * q + 1]) * a,
+                               __uint_as_float(r[4 * q + 2]) * a, __uint_as_float(r[4 * q + 3]) * a);
+        if constexpr (EPI == kEpiF32Add || EPI == kEpiF32Acc) {
+          const float4 b = reinterpret_cast<const float4*>(rr)[q];
+          v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+        }
+        reinterpret_cast<float4*>(c)[q] = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col + j < p.N) {
+          float v = __uint_as_float(r[j]) * a;
+          if constexpr (EPI == kEpiF32Add || EPI == kEpiF32Acc) v += rr[j];
+          c[j] = v;
+        }
+      }
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN, int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = (p.M + kBM - 1) / kBM;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int nk = (p.K + kBK - 1) / kBK;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- producer
+    int stage = 0;
+    uint32_t phase = 0;
+    long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, num_m, num_n, tm, tn);
+      const int m0 = tm * kBM, n0 = tn * BN;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
+        const int k0 = kb * kBK;
+        const uint32_t a_dst = sA + stage * A_BYTES, b_dst = sB + stage * B_BYTES;
+        if constexpr (A_MN) {
+#pragma unroll
+          for (int j = 0; j < kBM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, full_bar(stage), m0 + 64 * j, k0);
+        } else {
+          tma_load_2d(a_dst, &tmA, full_bar(stage), k0, m0);
+        }
+        if constexpr (B_MN) {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0);
+        } else {
+          tma_load_2d(b_dst, &tmB, full_bar(stage), k0, n0);
+        }
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {
+      record_error(p.err, kDevGemmTimeout);
+      *abort_flag = 1;
+      // let the copies already issued land before the CTA's shared memory goes away
+      const long n = issued < STAGES ? issued : STAGES;
+      for (long i = 0; i < n; ++i) {
+        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+        mbar_wait(full_bar(stage), phase, nullptr);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int iter = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
+      const int acc = iter & 1;
+      const uint32_t acc_phase = (iter >> 1) & 1;
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_base = sA + stage * A_BYTES, b_base = sB + stage * B_BYTES;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          uint64_t ad, bd;
+          if constexpr (A_MN) ad = smem_desc_sw128(a_base + k * 2048, 8192, 1024);
+          else ad = smem_desc_sw128(a_base + k * 32, 16, 1024);
+          if constexpr (B_MN) bd = smem_desc_sw128(b_base + k * 2048, 8192, 1024);
+          else bd = smem_desc_sw128(b_base + k * 32, 16, 1024);
+          umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        umma_commit(empty_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      umma_commit(tfull_bar(acc));
+    }
+    if (!ok) {
+      record_error(p.err, kDevGemmTimeout);
+      *abort_flag = 1;
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    int iter = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
+      int tm, tn;
+      tile_coords(tile, num_m, num_n, tm, tn);
+      const int acc = iter & 1;
+      const uint32_t acc_phase = (iter >> 1) & 1;
+      bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) { record_error(p.err, kDevGemmTimeout); *abort_flag = 1; }
+        break;
+      }
+      tc_fence_after();
+      const int row = tm * kBM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      for (int c = 0; c < BN; c += 32) {
+        const int col = tn * BN + c;
+        if (col >= p.N) break;  // uniform across the warp
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c, r);
+        tmem_ld_wait();
+        if (row < p.M) epi_store<EPI>(p, row, col, r);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride ld
+// (elements), box [box_rows, 64] with the 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                     int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <bool A_MN, bool B_MN, int BN, int EPI>
+static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                    cudaStream_t st, char* why) {
+  using Cfg = GemmCfg<BN>;
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess) {
+      snprintf(why, 64, "gemm: cannot reserve %d B shared memory", Cfg::SMEM);
+      return -3;
+    }
+    attr_set = true;
+  }
+  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, kThreads, Cfg::SMEM, st>>>(ta, tb, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    snprintf(why, 64, "gemm launch: %s", cudaGetErrorString(e));
+    return -3;
+  }
+  return 0;
+}
+
+template <bool A_MN, bool B_MN, int BN>
+static int launch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                      cudaStream_t st, char* why) {
+  switch (epi) {
+    case kEpiBF16: return launch_t<A_MN, B_MN, BN, kEpiBF16>(ta, tb, p, st, why);
+    case kEpiF32: return launch_t<A_MN, B_MN, BN, kEpiF32>(ta, tb, p, st, why);
+    case kEpiF32Add: return launch_t<A_MN, B_MN, BN, kEpiF32Add>(ta, tb, p, st, why);
+    case kEpiF32Acc: return launch_t<A_MN, B_MN, BN, kEpiF32Acc>(ta, tb, p, st, why);
+  }
+  snprintf(why, 64, "gemm: bad epilogue %d", epi);
+  return -1;
+}
+
+int gemm_check(const GemmArgs& a, char* why) {
+  if (a.M == 0 || a.N == 0) return 0;
+  if (a.M < 0 || a.N < 0 || a.K <= 0 || a.M > INT32_MAX || a.N > INT32_MAX || a.K > INT32_MAX) {
+    snprintf(why, 64, "gemm: bad sizes");
+    return -1;
+  }
+  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiF32Acc) {
+    snprintf(why, 64, "gemm: bad layout %d or epilogue %d", a.layout, a.epi);
+    return -1;
+  }
+  if (!a.A || !a.B || !a.C || (a.epi == kEpiF32Add && !a.R)) {
+    snprintf(why, 64, "gemm: null operand");
+    return -1;
+  }
+  // TMA: 16-byte aligned bases and row strides.
+  if ((reinterpret_cast<uintptr_t>(a.A) & 15) || (reinterpret_cast<uintptr_t>(a.B) & 15) ||
+      (a.lda % 8) || (a.ldb % 8)) {
+    snprintf(why, 64, "gemm: operands must be 16-byte aligned");
+    return -1;
+  }
+  const bool a_mn = (a.layout == kTN);
+  const bool b_mn = (a.layout == kNN || a.layout == kTN);
+  // row extents of the stored matrices must fit their leading dimensions
+  const int64_t a_cols = a_mn ? a.M : a.K, b_cols = b_mn ? a.N : a.K;
+  if (a.lda < a_cols || a.ldb < b_cols || a.ldc < a.N || (a.epi == kEpiF32Add && a.ldr < a.N)) {
+    snprintf(why, 64, "gemm: leading dimension too small");
+    return -1;
+  }
+  return 0;
+}
+
+int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
+  if (a.M == 0 || a.N == 0) return 0;
+  if (int c = gemm_check(a, why)) return c;
+  const bool a_mn = (a.layout == kTN);
+  const bool b_mn = (a.layout == kNN || a.layout == kTN);
+  const int BN = (a.N > 128) ? 256 : 128;
+  CUtensorMap ta, tb;
+  bool ok = a_mn ? make_map(&ta, a.A, a.M, a.K, a.lda, 64, 64)
+                 : make_map(&ta, a.A, a.K, a.M, a.lda, 64, kBM);
+  ok = ok && (b_mn ? make_map(&tb, a.B, a.N, a.K, a.ldb, 64, 64)
+                   : make_map(&tb, a.B, a.K, a.N, a.ldb, 64, BN));
+  if (!ok) {
+    snprintf(why, 64, "gemm: tensor map encode failed");
+    return -3;
+  }
+  GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err};
+  if (BN == 256) {
+    if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, p, st, why);
+    if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, p, st, why);
+    return launch_epi<true, true, 256>(a.epi, ta, tb, p, st, why);
+  }
+  if (a.layout == kNT) return launch_epi<false, false, 128>(a.epi, ta, tb, p, st, why);
+  if (a.layout == kNN) return launch_epi<false, true, 128>(a.epi, ta, tb, p, st, why);
+  return launch_epi<true, true, 128>(a.epi, ta, tb, p, st, why);
+}
+
+}  // namespace sf

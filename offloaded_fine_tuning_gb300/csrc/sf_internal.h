@@ -1,0 +1,69 @@
+// Internal launchers of the CUDA kernels (host-side declarations).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace sf {
+
+// Operand layouts of C[M,N] = A * B (all matrices row-major in memory):
+//   kNT: A [M,K] (K contiguous), B [N,K] (K contiguous)   -> Y = X W^T
+//   kNN: A [M,K] (K contiguous), B [K,N] (N contiguous)   -> dX = dY W
+//   kTN: A [K,M] (M contiguous), B [K,N] (N contiguous)   -> dW = dY^T X
+enum GemmLayout : int { kNT = 0, kNN = 1, kTN = 2 };
+// Epilogues: C bf16 = alpha*acc | C f32 = alpha*acc | C f32 = R + alpha*acc | C f32 += alpha*acc
+enum GemmEpi : int { kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3 };
+
+struct GemmArgs {
+  int layout = kNT, epi = kEpiBF16;
+  int64_t M = 0, N = 0, K = 0;
+  const void* A = nullptr;
+  int64_t lda = 0;
+  const void* B = nullptr;
+  int64_t ldb = 0;
+  void* C = nullptr;
+  int64_t ldc = 0;
+  const float* R = nullptr;
+  int64_t ldr = 0;
+  float alpha = 1.f;
+};
+
+// Returns 0, or a negative status with a message in `why` (64 chars at least).
+int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why);
+// Host-side argument check only (no CUDA call): 0 or -1.
+int gemm_check(const GemmArgs& a, char* why);
+
+// ---- elementwise / normalisation kernels (elementwise.cu)
+void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float* rstd,
+                 int64_t rows, int d, float eps, cudaStream_t st);
+// dx = dres + rstd*(g*dy - xhat*mean(g*dy*xhat)); dxb = bf16(dx); dg partials [parts, d]
+void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, const float* dy,
+                 const float* dres, float* dx, __nv_bfloat16* dxb, float* dg_part, int parts,
+                 int64_t rows, int d, cudaStream_t st);
+int rmsnorm_bwd_parts(int64_t rows);
+void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st);
+void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
+                  int head_dim, const float2* cs, int inverse, cudaStream_t st);
+void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn,
+                cudaStream_t st);
+void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16* dab,
+                int64_t rows, int ffn, cudaStream_t st);
+void ce_rows(__nv_bfloat16* z, const int32_t* labels, int64_t rows, int64_t vocab,
+             float inv_n, float* loss_rows, cudaStream_t st);
+void sum_f32(const float* x, int64_t n, float scale, float* out, cudaStream_t st);
+void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st);
+void cast_bf16_f32(const __nv_bfloat16* x, float* y, int64_t n, cudaStream_t st);
+
+// ---- attention (attention.cu).  qkv [T, (Hq+2Hkv)*hd] bf16, token t = b*S + s.
+int attn_fwd(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq,
+             int Hkv, int hd, cudaStream_t st);
+// dq_acc: fp32 scratch [T, Hq*hd] (zeroed inside); delta: fp32 scratch [B, Hq, S].
+// Writes dQ (RoPE-inverse applied when cs != null), dK (same) and dV into dqkv.
+int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+             const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S,
+             int Hq, int Hkv, int hd, const float2* cs, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace sf

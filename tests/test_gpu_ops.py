@@ -1,0 +1,363 @@
+"""Per-kernel parity through the C ABI: each CUDA kernel against the oracle's
+function (or the plain definition, for the GEMM) on the same seeded inputs.
+
+Tolerances: fp32 results of bf16 inputs (fp32 accumulation) within rel-L2
+1e-5 of the float64 result; results stored in bf16 within rel-L2 4e-3 (bf16
+has 8 significant bits: rounding alone gives ~2e-3)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import oracle
+from tests.gpu_util import bf16_values, cuda, host, stream, sync
+from tests.helpers import rel_l2
+
+pytestmark = pytest.mark.gpu
+sf = pytest.importorskip("offloaded_fine_tuning_gb300")
+
+F32_RL2 = 1e-5
+BF16_RL2 = 4e-3
+
+
+def f32_tol(K):
+    """fp32 accumulation over K products: rounding error grows like sqrt(K)."""
+    return F32_RL2 * max(1.0, math.sqrt(K / 1024.0))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    sf.lib(build_if_needed=True)
+    yield
+    assert sf.device_error() == 0
+
+
+def rnd(seed, shape, std=1.0):
+    return inputs.normal(seed, 77, int(np.prod(shape)), 0.0, std).reshape(shape)
+
+
+# ------------------------------------------------------------------ GEMM
+GEMM_CASES = [
+    # layout, epi, M, N, K
+    (sf.NT, sf.EPI_BF16, 300, 520, 200),
+    (sf.NT, sf.EPI_F32, 128, 256, 64),
+    (sf.NT, sf.EPI_F32_ADD, 257, 384, 136),
+    (sf.NT, sf.EPI_BF16, 5, 72, 8),
+    (sf.NN, sf.EPI_F32, 300, 520, 200),
+    (sf.NN, sf.EPI_BF16, 640, 136, 520),
+    (sf.NN, sf.EPI_F32, 70, 40, 1000),
+    (sf.TN, sf.EPI_BF16, 520, 296, 200),
+    (sf.TN, sf.EPI_F32, 136, 264, 777 + 7),
+    (sf.TN, sf.EPI_F32_ACC, 384, 512, 256),
+    (sf.NT, sf.EPI_BF16, 1024, 2304, 1536),
+    (sf.TN, sf.EPI_F32, 1152, 1024, 2048),
+]
+
+
+def run_gemm(layout, epi, M, N, K, alpha=1.0, seed=1):
+    a_shape = (K, M) if layout == sf.TN else (M, K)
+    b_shape = (N, K) if layout == sf.NT else (K, N)
+    A = bf16_values(rnd(seed, a_shape))
+    B = bf16_values(rnd(seed + 1, b_shape))
+    Am = A.T if layout == sf.TN else A
+    Bm = B.T if layout == sf.NT else B
+    ref = alpha * (Am.astype(np.float64) @ Bm.astype(np.float64))
+    dA, dB = cuda(A, torch.bfloat16), cuda(B, torch.bfloat16)
+    R = None
+    if epi == sf.EPI_BF16:
+        C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    elif epi == sf.EPI_F32:
+        C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    else:
+        R0 = rnd(seed + 2, (M, N))
+        ref = ref + R0
+        C = cuda(R0, torch.float32)
+        R = C if epi == sf.EPI_F32_ACC else cuda(R0, torch.float32)
+    st = sf.op_gemm(layout, epi, M, N, K, dA.data_ptr(), a_shape[1], dB.data_ptr(), b_shape[1],
+                    C.data_ptr(), N, R.data_ptr() if (R is not None and epi == sf.EPI_F32_ADD) else 0,
+                    N, alpha, stream())
+    assert st == 0
+    sync()
+    return host(C), ref
+
+
+@pytest.mark.parametrize("layout,epi,M,N,K", GEMM_CASES)
+def test_gemm_matches_definition(layout, epi, M, N, K):
+    got, ref = run_gemm(layout, epi, M, N, K)
+    tol = BF16_RL2 if epi == sf.EPI_BF16 else f32_tol(K)
+    assert rel_l2(got, ref) < tol
+    # and elementwise: no tile or tail is wrong
+    scale = np.abs(ref).max()
+    assert np.abs(got - ref).max() < (2e-2 if epi == sf.EPI_BF16 else 1e-4) * scale
+
+
+def test_gemm_alpha_and_residual_alias():
+    got, ref = run_gemm(sf.NT, sf.EPI_F32, 200, 200, 96, alpha=0.25)
+    assert rel_l2(got, ref) < F32_RL2
+    # residual add in place (R aliases C), as the residual stream uses it
+    M, N, K = 130, 256, 72
+    A = bf16_values(rnd(5, (M, K)))
+    B = bf16_values(rnd(6, (N, K)))
+    R0 = rnd(7, (M, N))
+    C = cuda(R0, torch.float32)
+    dA, dB = cuda(A, torch.bfloat16), cuda(B, torch.bfloat16)  # keep alive until the kernel ran
+    st = sf.op_gemm(sf.NT, sf.EPI_F32_ADD, M, N, K, dA.data_ptr(), K, dB.data_ptr(), K,
+                    C.data_ptr(), N, C.data_ptr(), N, 1.0, stream())
+    assert st == 0
+    sync()
+    assert rel_l2(host(C), R0 + A.astype(np.float64) @ B.T) < F32_RL2
+
+
+def test_gemm_full_size_sampled_rows():
+    """8B-shape QKV projection (16384 x 6144 x 4096) and gate/up weight
+    gradient (28672 x 4096 x 16384): sampled output rows against float64."""
+    rng = np.random.default_rng(3)
+    for layout, M, N, K in [(sf.NT, 16384, 6144, 4096), (sf.TN, 28672, 4096, 16384)]:
+        a_shape = (K, M) if layout == sf.TN else (M, K)
+        b_shape = (N, K) if layout == sf.NT else (K, N)
+        dA = cuda(rnd(11, a_shape), torch.bfloat16)
+        dB = cuda(rnd(12, b_shape), torch.bfloat16)
+        C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        assert sf.op_gemm(layout, sf.EPI_F32, M, N, K, dA.data_ptr(), a_shape[1], dB.data_ptr(),
+                          b_shape[1], C.data_ptr(), N, 0, 0, 1.0, stream()) == 0
+        sync()
+        rows = np.sort(rng.choice(M, 12, replace=False))
+        rows[-1] = M - 1
+        Bm = host(dB).astype(np.float64)
+        Bm = Bm.T if layout == sf.NT else Bm
+        Ar = host(dA[:, rows].T if layout == sf.TN else dA[rows]).astype(np.float64)
+        ref = Ar @ Bm
+        assert rel_l2(host(C[rows]), ref) < f32_tol(K)
+        del dA, dB, C
+        torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ RMSNorm
+@pytest.mark.parametrize("rows,d", [(37, 256), (300, 4096), (5, 12288), (1, 8)])
+def test_rmsnorm_fwd_bwd(rows, d):
+    x = rnd(1, (rows, d), 2.0)
+    g = bf16_values(1.0 + 0.1 * rnd(2, (d,)))
+    dy = rnd(3, (rows, d))
+    dres = rnd(4, (rows, d))
+    y_ref, cache = oracle.rmsnorm_fwd(x.astype(np.float64), g.astype(np.float64), 1e-5)
+    dx_ref, dg_ref = oracle.rmsnorm_bwd(dy.astype(np.float64), g.astype(np.float64), cache)
+    dx_ref = dx_ref + dres
+    X, G, DY, DR = cuda(x, torch.float32), cuda(g, torch.bfloat16), cuda(dy, torch.float32), cuda(dres, torch.float32)
+    Y = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    RS = torch.empty(rows, dtype=torch.float32, device="cuda")
+    assert sf.op_rmsnorm_fwd(X.data_ptr(), G.data_ptr(), Y.data_ptr(), RS.data_ptr(), rows, d, 1e-5, stream()) == 0
+    DX = torch.empty((rows, d), dtype=torch.float32, device="cuda")
+    DXB = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    DG = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+    SC = torch.empty(sf.rmsnorm_bwd_scratch(rows, d), dtype=torch.float32, device="cuda")
+    assert sf.op_rmsnorm_bwd(X.data_ptr(), G.data_ptr(), RS.data_ptr(), DY.data_ptr(), DR.data_ptr(),
+                             DX.data_ptr(), DXB.data_ptr(), DG.data_ptr(), SC.data_ptr(), rows, d, stream()) == 0
+    sync()
+    assert rel_l2(host(Y), y_ref) < BF16_RL2
+    assert rel_l2(host(RS), cache[1][:, 0]) < F32_RL2
+    assert rel_l2(host(DX), dx_ref) < F32_RL2 * 10
+    assert rel_l2(host(DXB), dx_ref) < BF16_RL2
+    assert rel_l2(host(DG), dg_ref) < BF16_RL2
+
+
+# ------------------------------------------------------------------ RoPE
+@pytest.mark.parametrize("hd,base", [(64, 10000.0), (128, 500000.0)])
+def test_rope_fwd_and_inverse(hd, base):
+    B, S, H = 2, 70, 3
+    x = bf16_values(rnd(1, (B, S, H, hd)))
+    cos, sin = oracle.rope_tables(S, hd, base)
+    tab = cuda(sf.rope_table(S, hd, base), torch.float32)
+    for inverse, fn in ((0, oracle.rope_fwd), (1, oracle.rope_bwd)):
+        X = cuda(x.reshape(B * S, H * hd), torch.bfloat16)
+        assert sf.op_rope(X.data_ptr(), H * hd, B * S, S, H, hd, tab.data_ptr(), inverse, stream()) == 0
+        sync()
+        ref = fn(x.astype(np.float64), cos, sin).reshape(B * S, H * hd)
+        assert rel_l2(host(X), ref) < BF16_RL2
+
+
+# ------------------------------------------------------------------ SwiGLU
+def test_swiglu_fwd_bwd():
+    rows, F = 333, 1000
+    a = bf16_values(rnd(1, (rows, F), 3.0))
+    b = bf16_values(rnd(2, (rows, F)))
+    dm = bf16_values(rnd(3, (rows, F)))
+    AB = cuda(np.concatenate([a, b], axis=1), torch.bfloat16)
+    M = torch.empty((rows, F), dtype=torch.bfloat16, device="cuda")
+    DAB = torch.empty((rows, 2 * F), dtype=torch.bfloat16, device="cuda")
+    assert sf.op_swiglu_fwd(AB.data_ptr(), M.data_ptr(), rows, F, stream()) == 0
+    DM = cuda(dm, torch.bfloat16)
+    assert sf.op_swiglu_bwd(DM.data_ptr(), AB.data_ptr(), DAB.data_ptr(), rows, F, stream()) == 0
+    sync()
+    a64, b64 = a.astype(np.float64), b.astype(np.float64)
+    assert rel_l2(host(M), oracle.swiglu_fwd(a64, b64)) < BF16_RL2
+    da, db = oracle.swiglu_bwd(dm.astype(np.float64), a64, b64)
+    got = host(DAB)
+    assert rel_l2(got[:, :F], da) < BF16_RL2 and rel_l2(got[:, F:], db) < BF16_RL2
+
+
+# ------------------------------------------------------------------ attention
+ATTN_CASES = [(2, 200, 6, 2, 64), (1, 130, 4, 1, 128), (1, 64, 2, 2, 64), (2, 1, 4, 2, 128),
+              (1, 300, 12, 1, 128)]
+
+
+def attn_inputs(B, S, Hq, Hkv, hd, seed=1):
+    W = (Hq + 2 * Hkv) * hd
+    qkv = bf16_values(rnd(seed, (B * S, W)))
+    do = bf16_values(rnd(seed + 1, (B * S, Hq * hd)))
+    return qkv, do
+
+
+def split_qkv(qkv, B, S, Hq, Hkv, hd):
+    q = qkv[:, :Hq * hd].reshape(B, S, Hq, hd)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(B, S, Hkv, hd)
+    v = qkv[:, (Hq + Hkv) * hd:].reshape(B, S, Hkv, hd)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,hd", ATTN_CASES)
+def test_attention_fwd_bwd(B, S, Hq, Hkv, hd):
+    qkv, do = attn_inputs(B, S, Hq, Hkv, hd)
+    q, k, v = (a.astype(np.float64) for a in split_qkv(qkv, B, S, Hq, Hkv, hd))
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v)
+    QKV = cuda(qkv, torch.bfloat16)
+    O = torch.empty((B * S, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    assert sf.op_attn_fwd(QKV.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, S, Hq, Hkv, hd, stream()) == 0
+    sync()
+    assert rel_l2(host(O), o_ref.reshape(B * S, -1)) < BF16_RL2
+    assert np.abs(host(LSE) - lse_ref).max() < 1e-4 * max(1.0, np.abs(lse_ref).max())
+    # backward from the kernel's own O and LSE (as in the step), without RoPE
+    dq_ref, dk_ref, dv_ref = oracle.attention_bwd(do.reshape(B, S, Hq, hd).astype(np.float64), q, k, v)
+    DO = cuda(do, torch.bfloat16)
+    DQKV = torch.zeros_like(QKV)
+    DEL = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    DQA = torch.empty((B * S, Hq * hd), dtype=torch.float32, device="cuda")
+    assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(), DEL.data_ptr(),
+                          DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0, stream()) == 0
+    sync()
+    gq, gk, gv = split_qkv(host(DQKV), B, S, Hq, Hkv, hd)
+    assert rel_l2(gq, dq_ref) < 1e-2
+    assert rel_l2(gk, dk_ref) < 1e-2
+    assert rel_l2(gv, dv_ref) < 1e-2
+
+
+def test_attention_bwd_with_inverse_rope():
+    B, S, Hq, Hkv, hd, base = 1, 96, 4, 2, 128, 500000.0
+    qkv, do = attn_inputs(B, S, Hq, Hkv, hd, seed=9)
+    q, k, v = (a.astype(np.float64) for a in split_qkv(qkv, B, S, Hq, Hkv, hd))
+    cos, sin = oracle.rope_tables(S, hd, base)
+    dq, dk, dv = oracle.attention_bwd(do.reshape(B, S, Hq, hd).astype(np.float64), q, k, v)
+    QKV = cuda(qkv, torch.bfloat16)
+    O = torch.empty((B * S, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    sf.op_attn_fwd(QKV.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, S, Hq, Hkv, hd, stream())
+    tab = cuda(sf.rope_table(S, hd, base), torch.float32)
+    DQKV = torch.zeros_like(QKV)
+    DEL = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    DQA = torch.empty((B * S, Hq * hd), dtype=torch.float32, device="cuda")
+    DO = cuda(do, torch.bfloat16)
+    assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(),
+                          DEL.data_ptr(), DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd,
+                          tab.data_ptr(), stream()) == 0
+    sync()
+    gq, gk, gv = split_qkv(host(DQKV), B, S, Hq, Hkv, hd)
+    assert rel_l2(gq, oracle.rope_bwd(dq, cos, sin)) < 1e-2
+    assert rel_l2(gk, oracle.rope_bwd(dk, cos, sin)) < 1e-2
+    assert rel_l2(gv, dv) < 1e-2
+
+
+def test_attention_full_size_sampled_heads():
+    """8B shape: B=8, S=2048, 32 query / 8 kv heads of 128.  Forward output of
+    sampled (batch, head) pairs and the backward of one whole kv group."""
+    B, S, Hq, Hkv, hd = 8, 2048, 32, 8, 128
+    qkv, do = attn_inputs(B, S, Hq, Hkv, hd, seed=21)
+    QKV = cuda(qkv, torch.bfloat16)
+    O = torch.empty((B * S, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    assert sf.op_attn_fwd(QKV.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, S, Hq, Hkv, hd, stream()) == 0
+    DQKV = torch.zeros_like(QKV)
+    DEL = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    DQA = torch.empty((B * S, Hq * hd), dtype=torch.float32, device="cuda")
+    DO = cuda(do, torch.bfloat16)
+    assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(),
+                          DEL.data_ptr(), DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0, stream()) == 0
+    sync()
+    o_all, dqkv_all = host(O), host(DQKV)
+    b, g = 5, 6  # one batch row, one kv group (query heads 24..27)
+    rows = slice(b * S, (b + 1) * S)
+    q, k, v = (a.astype(np.float64) for a in split_qkv(qkv[rows], 1, S, Hq, Hkv, hd))
+    heads = list(range(g * 4, g * 4 + 4))
+    o_ref, _ = oracle.attention_fwd(q[:, :, heads], k[:, :, [g]], v[:, :, [g]])
+    o_got = o_all[rows].reshape(1, S, Hq, hd)[:, :, heads]
+    assert rel_l2(o_got, o_ref) < BF16_RL2
+    dq, dk, dv = oracle.attention_bwd(do[rows].reshape(1, S, Hq, hd)[:, :, heads].astype(np.float64),
+                                      q[:, :, heads], k[:, :, [g]], v[:, :, [g]])
+    gq, gk, gv = split_qkv(dqkv_all[rows], 1, S, Hq, Hkv, hd)
+    assert rel_l2(gq[:, :, heads], dq) < 1e-2
+    assert rel_l2(gk[:, :, [g]], dk) < 1e-2
+    assert rel_l2(gv[:, :, [g]], dv) < 1e-2
+
+
+# ------------------------------------------------------------------ fused LM head + CE
+def lce_run(h, w, lab, chunk):
+    n, d = h.shape
+    V = w.shape[0]
+    n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
+    H, W, Y = cuda(h, torch.bfloat16), cuda(w, torch.bfloat16), cuda(lab, torch.int32)
+    ws = torch.empty(sf.lce_workspace_bytes(n, V, chunk), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    dh = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    dw = torch.empty((V, d), dtype=torch.float32, device="cuda")
+    assert sf.op_lce(H.data_ptr(), W.data_ptr(), Y.data_ptr(), n, d, V, n_valid, chunk, ws.data_ptr(),
+                     loss.data_ptr(), dh.data_ptr(), dw.data_ptr(), stream()) == 0
+    sync()
+    return float(host(loss)[0]), host(dh), host(dw)
+
+
+@pytest.mark.parametrize("chunk", [128, 500, 1000])
+def test_lce_matches_unfused_cross_entropy(chunk):
+    from inputs.configs import LceConfig
+    c = LceConfig("small", 384, 3000, 2, 250, 0.1)
+    h, w, lab = inputs.lce_inputs(c)
+    h, w = bf16_values(h), bf16_values(w)
+    z = h.astype(np.float64) @ w.astype(np.float64).T
+    loss_ref, dz, _ = oracle.cross_entropy_fwd_bwd(z, lab)
+    loss, dh, dw = lce_run(h, w, lab, chunk)
+    assert abs(loss - loss_ref) / loss_ref < 1e-3
+    assert rel_l2(dh, dz @ w.astype(np.float64)) < 1e-2
+    assert rel_l2(dw, dz.T @ h.astype(np.float64)) < 1e-2
+    ign = lab == sf.IGNORE_INDEX
+    assert not np.any(dh[ign])
+
+
+def test_lce_all_ignored_gives_zero():
+    h = bf16_values(rnd(1, (64, 128)))
+    w = bf16_values(rnd(2, (256, 128), 0.02))
+    loss, dh, dw = lce_run(h, w, np.full(64, sf.IGNORE_INDEX, dtype=np.int32), 32)
+    assert loss == 0.0 and not dh.any() and not dw.any()
+
+
+def test_lce_stress_shape_properties():
+    """Large-vocab stress shape (16384 x 3584, V = 152064, 10% ignored): loss near
+    ln V + sigma^2/2, exact on sampled rows' dh, dW columns sum to ~0, chunking-invariant."""
+    from inputs import LCE_STRESS as c
+    h, w, lab = inputs.lce_inputs(c)
+    h, w = bf16_values(h), bf16_values(w)
+    loss, dh, dw = lce_run(h, w, lab, 4096)
+    sigma2 = 0.02 ** 2 * c.hidden
+    assert loss == pytest.approx(math.log(c.vocab) + sigma2 / 2, rel=0.02)
+    n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
+    rows = [0, 1, 777, 16383] + [int(i) for i in np.nonzero(lab == sf.IGNORE_INDEX)[0][:2]]
+    W64 = w.astype(np.float64)
+    for r in rows:
+        z = h[r].astype(np.float64) @ W64.T
+        _, dz, _ = oracle.cross_entropy_fwd_bwd(z[None, :], lab[r:r + 1])
+        ref = dz[0] * (1.0 / n_valid) @ W64  # oracle normalises by this row alone; rescale
+        assert rel_l2(dh[r], ref) < 1e-2 or (not ref.any() and not dh[r].any())
+    col_sum = dw.sum(axis=0)
+    assert np.abs(col_sum).max() < 1e-3 * np.abs(dw).max() * math.sqrt(c.vocab)
+    loss2, dh2, dw2 = lce_run(h, w, lab, 2048)
+    assert abs(loss2 - loss) / loss < 1e-5
+    assert rel_l2(dh2, dh) < 1e-5 and rel_l2(dw2, dw) < 1e-4

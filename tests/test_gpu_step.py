@@ -1,0 +1,162 @@
+"""Whole-step parity through the C ABI: sf_train_step against the CPU oracle
+on the same seeded weights, tokens and labels.
+
+Bar: loss relative error <= 1e-3; per-tensor gradient relative L2 error
+<= 2e-2 (bf16 compute with fp32 accumulation against the float64 oracle)."""
+import numpy as np
+import pytest
+
+import inputs
+import oracle
+from inputs import CONFIGS, TEST_CONFIGS, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD, IGNORE_INDEX
+from inputs.configs import layer_tensor_shapes
+from tests.helpers import GRAD_RL2, LOSS_RTOL, masters, oracle_weights, rel_l2
+
+pytestmark = pytest.mark.gpu
+sf = pytest.importorskip("offloaded_fine_tuning_gb300")
+
+
+def make_model(cfg, mast, **kw):
+    kw.setdefault("retain_grads", 1)
+    m = sf.Model(sf.make_config(cfg, **kw))
+    for u, a in mast.items():
+        m.load(u, a)
+    return m
+
+
+def compare(cfg, m, loss_ref, g_ref, tol=GRAD_RL2):
+    errs = {"loss": abs(m.loss() - loss_ref) / abs(loss_ref)}
+    for l in range(cfg.n_layers):
+        flat = m.grads(l)
+        off = 0
+        for name, shape in layer_tensor_shapes(cfg):
+            n = int(np.prod(shape))
+            errs[f"{l}.{name}"] = rel_l2(flat[off:off + n].reshape(shape), g_ref["layers"][l][name])
+            off += n
+    errs["embed"] = rel_l2(m.grads(UNIT_EMBED).reshape(cfg.vocab, cfg.hidden), g_ref["embed"])
+    errs["final_norm"] = rel_l2(m.grads(UNIT_FINAL_NORM), g_ref["final_norm"])
+    errs["lm_head"] = rel_l2(m.grads(UNIT_LM_HEAD).reshape(cfg.vocab, cfg.hidden), g_ref["lm_head"])
+    bad = {k: v for k, v in errs.items() if v > (LOSS_RTOL if k == "loss" else tol)}
+    assert not bad, f"outside tolerance: {bad}"
+    return errs
+
+
+@pytest.mark.parametrize("name", ["tiny", "small-gqa", "small-hd128"])
+def test_step_matches_oracle(name):
+    cfg = CONFIGS.get(name) or TEST_CONFIGS[name]
+    sf.lib(build_if_needed=True)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
+    with make_model(cfg, mast) as m:
+        assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+        compare(cfg, m, loss_ref, g_ref)
+        # a second identical step gives bit-identical results (no state leaks between steps)
+        g0, l0 = m.grads(0), m.loss()
+        assert m.train_step(tok, lab) == sf.SF_OK
+        assert m.loss() == l0 and np.array_equal(m.grads(0), g0)
+
+
+def test_ring_size_invariance_is_bitwise():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=4)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    results = []
+    for R in (2, 3, 4):
+        with make_model(cfg, mast, ring_slots=R) as m:
+            assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+            results.append((m.loss(), [m.grads(u) for u in (0, 1, 2, 3, UNIT_EMBED, UNIT_LM_HEAD)]))
+    for loss, gs in results[1:]:
+        assert loss == results[0][0]
+        for a, b in zip(gs, results[0][1]):
+            assert np.array_equal(a, b)
+
+
+def test_lce_chunking_does_not_change_the_step():
+    cfg = TEST_CONFIGS["small-gqa"]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    out = []
+    for chunk in (0, 96, 400):
+        with make_model(cfg, mast, lce_chunk_rows=chunk) as m:
+            assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+            out.append((m.loss(), m.grads(1), m.grads(UNIT_LM_HEAD)))
+    for loss, g1, glm in out[1:]:
+        assert abs(loss - out[0][0]) <= 1e-6 * abs(out[0][0])
+        assert rel_l2(g1, out[0][1]) < 1e-3 and rel_l2(glm, out[0][2]) < 1e-3
+
+
+def test_multi_step_adam_tracks_oracle():
+    cfg = CONFIGS["tiny"]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lr = 1e-4
+    adam = sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    # oracle: float32 masters, bf16 compute weights re-rounded after each update
+    theta = {u: a.astype(np.float32).copy() for u, a in mast.items()}
+    mom = {u: (np.zeros_like(a), np.zeros_like(a)) for u, a in theta.items()}
+    with make_model(cfg, mast) as m:
+        for t in range(1, 4):
+            loss_ref, g = oracle.step(oracle_weights(cfg, theta), tok, lab, cfg)
+            assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+            assert abs(m.loss() - loss_ref) / loss_ref < LOSS_RTOL
+            for u in theta:
+                if u >= 0:
+                    gu = np.concatenate([g["layers"][u][n].reshape(-1) for n, _ in layer_tensor_shapes(cfg)])
+                else:
+                    gu = {UNIT_EMBED: g["embed"], UNIT_FINAL_NORM: g["final_norm"],
+                          UNIT_LM_HEAD: g["lm_head"]}[u].reshape(-1)
+                th, mm, vv = oracle.adam_update(theta[u], gu.astype(np.float32), *mom[u], t, lr)
+                theta[u], mom[u] = th.astype(np.float32), (mm.astype(np.float32), vv.astype(np.float32))
+        for u in (0, 1, UNIT_EMBED, UNIT_LM_HEAD, UNIT_FINAL_NORM):
+            w = m.weights(u)
+            assert rel_l2(w - mast[u], theta[u] - mast[u]) < 0.1
+            assert rel_l2(w, theta[u]) < 1e-3
+
+
+def test_no_valid_label_gives_zero_loss_and_decay_only_update():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2)
+    mast = masters(cfg)
+    tok, _ = inputs.tokens_and_labels(cfg)
+    lab = np.full_like(tok, IGNORE_INDEX)
+    lr, wd = 1e-2, 0.1
+    with make_model(cfg, mast) as m:
+        assert m.train_step(tok, lab, sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=wd)) == 0
+        assert m.loss() == 0.0
+        for u in (0, 1, UNIT_EMBED, UNIT_LM_HEAD, UNIT_FINAL_NORM):
+            assert not m.grads(u).any()
+            # zero gradient: Adam moves nothing but the decoupled decay
+            w = m.weights(u)
+            np.testing.assert_allclose(w, mast[u] * np.float32(1 - lr * wd), rtol=5e-7, atol=0)
+
+
+def test_invalid_step_arguments_are_rejected():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2)
+    with make_model(cfg, masters(cfg)) as m:
+        tok, lab = inputs.tokens_and_labels(cfg)
+        bad = tok.copy(); bad[0, 3] = cfg.vocab
+        assert m.train_step(bad, lab) == sf.SF_EINVAL
+        badl = lab.copy(); badl[1, 0] = -5
+        assert m.train_step(tok, badl) == sf.SF_EINVAL
+        big = np.zeros((cfg.batch + 1, cfg.seq), dtype=np.int32)
+        assert m.train_step(big, big) == sf.SF_EINVAL
+        assert m.train_step(tok, lab) == sf.SF_OK  # the context is still usable
+
+
+def test_adam_worker_failure_and_timeout_are_reported():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    adam = sf.Adam(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    mast = masters(cfg)
+    with make_model(cfg, mast, wait_timeout_ms=300) as m:
+        m.inject(1, 1)          # the update of layer 1 fails on the host
+        assert m.train_step(tok, lab, adam) == sf.SF_ESTATE
+        assert "injected" in m.error()
+        m.inject(0)
+        # the failed unit kept its weights; the step after it runs normally
+        np.testing.assert_array_equal(m.weights(1), mast[1])
+        assert m.train_step(tok, lab, adam) == sf.SF_OK
+        m.inject(2, 1500)       # host updates slower than the wait bound
+        assert m.train_step(tok, lab, adam) == sf.SF_ETIMEOUT
+        assert "timed out" in m.error()
+        m.inject(0)

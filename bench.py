@@ -235,10 +235,12 @@ def run_ours(args, c):
 
     m = load_model(sf, c, args.ring or c.ring_slots)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
-    tok, lab = inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + rank)
+    # a fresh batch each step (rank-specific seeds for replicas)
+    n_batches = args.warmup + 2 * args.steps
+    batches = [inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + 1000 * rank + i) for i in range(n_batches)]
     T = c.batch * c.seq
-    for _ in range(args.warmup):
-        assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+    for i in range(args.warmup):
+        assert m.train_step(*batches[i], adam) == sf.SF_OK, m.error()
 
     # ---- device-clock region (CUDA events, Adam included): K synchronous steps
     m.set_timing(True)
@@ -250,8 +252,8 @@ def run_ours(args, c):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     stats = []
-    for _ in range(args.steps):
-        st = m.train_step(tok, lab, adam)
+    for i in range(args.steps):
+        st = m.train_step(*batches[args.warmup + i], adam)
         assert st == sf.SF_OK, m.error()
         stats.append(m.stats())
     e1.record()
@@ -269,6 +271,7 @@ def run_ours(args, c):
     t0 = time.perf_counter()
     losses = []
     for i in range(args.steps):
+        tok, lab = batches[args.warmup + args.steps + i]
         pin_tok.numpy()[...] = tok
         pin_lab.numpy()[...] = lab
         assert m.train_step(pin_tok.numpy(), pin_lab.numpy(), adam) == sf.SF_OK, m.error()

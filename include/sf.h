@@ -253,6 +253,30 @@ int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64
               float* dh, float* dw, void* stream);
 int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows);
 
+/* sf_op_rmsnorm_bwd_noalloc: the same operation and results as
+ * sf_op_rmsnorm_bwd, for callers that cannot allocate device memory (for
+ * instance code inside a host application whose memory manager owns the
+ * whole device budget, or a latency-critical loop where a cudaMalloc, which
+ * can synchronise the device and can fail, is not acceptable).  It takes no
+ * scratch argument and calls no allocating routine: the partial sums of the
+ * gain gradient live in a fixed array of SF_STATIC_SCRATCH_FLOATS floats
+ * (16 MiB) that the library reserves on every GPU that loads it, until the
+ * process exits.  The paper has no counterpart to this entry point.
+ *   - Size limit: returns SF_EINVAL when the row partition needs more than
+ *     SF_STATIC_SCRATCH_FLOATS floats, i.e. when P * d > 4194304 with
+ *     P = min(rows, 2 * number of SMs) (on a 152-SM GPU: any rows for
+ *     d <= 13792, at most 256 rows for d = 16384).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race and must not be issued.  Each
+ *     call overwrites every partial it reads, so nothing has to be cleared.
+ * Other arguments, layouts and errors: as sf_op_rmsnorm_bwd. */
+#define SF_STATIC_SCRATCH_FLOATS 4194304
+int sf_op_rmsnorm_bwd_noalloc(const float* x, const uint16_t* g, const float* rstd,
+                              const float* dy, const float* dres, float* dx, uint16_t* dxb,
+                              uint16_t* dg, int64_t rows, int32_t d, void* stream);
+
 /* Read and clear the device error word of the kernel API on the current
  * device (nonzero: a bounded device wait ran out).  Synchronises the device. */
 int sf_op_device_error(int32_t* out);

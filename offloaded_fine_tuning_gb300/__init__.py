@@ -80,6 +80,7 @@ _SIGS = {
     "sf_op_rmsnorm_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _F32, _VP]),
     "sf_op_rmsnorm_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_op_rmsnorm_bwd_scratch": (_I64, [_I64, _I32]),
+    "sf_op_rmsnorm_bwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_rope_table": (ctypes.c_int, [_I32, _I32, _F32, _VP]),
     "sf_op_rope": (ctypes.c_int, [_VP, _I64, _I64, _I32, _I32, _I32, _VP, _I32, _VP]),
     "sf_op_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
@@ -232,6 +233,14 @@ def op_rmsnorm_fwd(x, g, y, rstd, rows, d, eps, stream=0) -> int:
 
 def op_rmsnorm_bwd(x, g, rstd, dy, dres, dx, dxb, dg, scratch, rows, d, stream=0) -> int:
     return lib().sf_op_rmsnorm_bwd(x, g, rstd, dy, dres or None, dx, dxb, dg, scratch, rows, d, _s(stream))
+
+
+def op_rmsnorm_bwd_noalloc(x, g, rstd, dy, dres, dx, dxb, dg, rows, d, stream=0) -> int:
+    """sf_op_rmsnorm_bwd without a scratch argument (library-owned fixed array)."""
+    return lib().sf_op_rmsnorm_bwd_noalloc(x, g, rstd, dy, dres or None, dx, dxb, dg, rows, d, _s(stream))
+
+
+STATIC_SCRATCH_FLOATS = 4194304
 
 
 def rmsnorm_bwd_scratch(rows, d) -> int:

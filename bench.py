@@ -208,8 +208,8 @@ def run_reference(args, c):
 
 
 # ------------------------------------------------------------------ our arm
-def load_model(sf, c, ring):
-    cfg = sf.make_config(c, ring_slots=ring, retain_grads=0)
+def load_model(sf, c, ring, async_update):
+    cfg = sf.make_config(c, ring_slots=ring, retain_grads=0, async_update=async_update)
     m = sf.Model(cfg)
     for l in range(c.n_layers):
         m.load(l, inputs.layer_master(c, l))
@@ -233,7 +233,7 @@ def run_ours(args, c):
     bf16_peak, bf16_sust, hbm, peak_src = peaks()
     link = link_probe(torch)
 
-    m = load_model(sf, c, args.ring or c.ring_slots)
+    m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
     # a fresh batch each step (rank-specific seeds for replicas)
     n_batches = args.warmup + 2 * args.steps
@@ -242,7 +242,8 @@ def run_ours(args, c):
     for i in range(args.warmup):
         assert m.train_step(*batches[i], adam) == sf.SF_OK, m.error()
 
-    # ---- device-clock region (CUDA events, Adam included): K synchronous steps
+    m.sync()  # no warm-up update runs into the timed region
+    # ---- device-clock region (CUDA events, host Adam included): K steps
     m.set_timing(True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -256,6 +257,7 @@ def run_ours(args, c):
         st = m.train_step(*batches[args.warmup + i], adam)
         assert st == sf.SF_OK, m.error()
         stats.append(m.stats())
+    m.sync()  # the last step's host updates belong to the timed work
     e1.record()
     torch.cuda.synchronize()
     if dist:
@@ -276,6 +278,7 @@ def run_ours(args, c):
         pin_lab.numpy()[...] = lab
         assert m.train_step(pin_tok.numpy(), pin_lab.numpy(), adam) == sf.SF_OK, m.error()
         losses.append(m.loss())
+    m.sync()
     e2e_s = time.perf_counter() - t0
 
     times = torch.tensor([dev_ms, e2e_s * 1e3], dtype=torch.float64, device="cuda")
@@ -312,6 +315,7 @@ def run_ours(args, c):
         "config": {"workload": c.name, "global_batch": c.batch * world, "seq_len": c.seq,
                    "layers": c.n_layers, "ring_slots": args.ring or c.ring_slots,
                    "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
+                   "host_updates": "synchronous" if args.sync_updates else "overlap next step",
                    "l2": "inputs larger than L2 (each step streams every layer's weights and gradients)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps},
@@ -347,6 +351,8 @@ def main():
     ap.add_argument("--ring", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sync-updates", action="store_true",
+                    help="finish every host update before a step returns (no cross-step overlap)")
     args = ap.parse_args()
     c = CONFIGS[args.config]
     if args.impl == "reference":

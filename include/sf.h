@@ -77,7 +77,13 @@ typedef struct sf_ctx sf_ctx;
  *   rms_eps, rope_base: RMSNorm epsilon and RoPE base.
  *   device: CUDA device ordinal.
  *   adam_threads: host threads for Adam, gather and scatter (0 = all cores).
- *   wait_timeout_ms: bound of every host-side wait on the GPU (0 = 300000). */
+ *   wait_timeout_ms: bound of every host-side wait on the GPU (0 = 300000).
+ *   async_update: 0 = sf_train_step returns after every host update of the
+ *     step is done; 1 = it returns once the loss is ready and the updates
+ *     still running overlap the next step (which waits for a unit's update
+ *     just before that unit is needed).  Results are identical either way;
+ *     sf_get_grads, sf_get_weights and sf_load_layer_weights wait for the
+ *     pending updates first. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -88,6 +94,7 @@ typedef struct {
   int32_t device;
   int32_t adam_threads;
   int32_t wait_timeout_ms;
+  int32_t async_update;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -142,11 +149,12 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* fp32_master, s
  * forward over all layers through the GPU ring, fused LM-head cross-entropy,
  * recompute-and-backward over the layers in reverse order, gradient
  * streaming to the host and, if adam != NULL, the Adam update of every unit
- * (adam == NULL: gradients only, weights unchanged).  Synchronous: on return
- * the loss is ready and every update is done.  tokens in [0, vocab); labels
- * in [0, vocab) or SF_IGNORE_INDEX; batch*seq <= max_batch*max_seq and seq <=
- * max_seq.  With no valid label the loss and all gradients are 0.
- * Errors: SF_EINVAL, SF_ECUDA, SF_ETIMEOUT, SF_EDEVICE, SF_ESTATE. */
+ * (adam == NULL: gradients only, weights unchanged).  On return the loss is
+ * ready and, unless async_update is set, every update is done.  tokens in
+ * [0, vocab); labels in [0, vocab) or SF_IGNORE_INDEX; batch*seq <=
+ * max_batch*max_seq and seq <= max_seq.  With no valid label the loss and all
+ * gradients are 0.  Errors: SF_EINVAL, SF_ECUDA, SF_ETIMEOUT, SF_EDEVICE,
+ * SF_ESTATE. */
 int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
                   int32_t seq, const sf_adam* adam);
 
@@ -157,6 +165,11 @@ int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
 
 /* Current fp32 master weights of `unit`.  Errors: SF_EINVAL. */
 int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
+
+/* Wait (bounded by wait_timeout_ms) until every host update posted by the
+ * steps so far is done; returns the first error a pending update reported.
+ * A no-op when async_update is 0.  Errors: SF_ETIMEOUT, SF_ESTATE. */
+int sf_sync(sf_ctx* ctx);
 
 /* Loss of the last step.  Errors: SF_ESTATE before the first step. */
 int sf_loss(sf_ctx* ctx, float* out);

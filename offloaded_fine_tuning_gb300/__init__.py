@@ -41,7 +41,7 @@ class Config(ctypes.Structure):
                  "max_batch", "max_seq", "ring_slots", "lce_chunk_rows", "retain_grads")] + \
                [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
                 ("device", ctypes.c_int32), ("adam_threads", ctypes.c_int32),
-                ("wait_timeout_ms", ctypes.c_int32)]
+                ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32)]
 
 
 class Adam(ctypes.Structure):
@@ -72,6 +72,7 @@ _SIGS = {
     "sf_get_grads": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_get_weights": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_loss": (ctypes.c_int, [_VP, ctypes.POINTER(_F32)]),
+    "sf_sync": (ctypes.c_int, [_VP]),
     "sf_set_timing": (ctypes.c_int, [_VP, _I32]),
     "sf_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(Stats)]),
     "sf_debug_inject": (ctypes.c_int, [_VP, _I32, _I32]),
@@ -124,7 +125,8 @@ def _check(st: int, ctx=None, what=""):
 
 
 def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_grads=1,
-                lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0) -> Config:
+                lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0,
+                async_update=0) -> Config:
     """sf_config from a shape object with the fields of inputs.ModelConfig."""
     return Config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
                   n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, ffn=shape.ffn,
@@ -132,7 +134,8 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   max_seq=max_seq or shape.seq,
                   ring_slots=ring_slots or shape.ring_slots, lce_chunk_rows=lce_chunk_rows,
                   retain_grads=retain_grads, rms_eps=shape.rms_eps, rope_base=shape.rope_base,
-                  device=device, adam_threads=adam_threads, wait_timeout_ms=wait_timeout_ms)
+                  device=device, adam_threads=adam_threads, wait_timeout_ms=wait_timeout_ms,
+                  async_update=async_update)
 
 
 def unit_numel(cfg: Config, unit: int) -> int:
@@ -205,6 +208,10 @@ class Model:
         out = np.empty(self.numel(unit), dtype=np.float32)
         _check(lib().sf_get_weights(self.h, unit, out.ctypes.data, out.size), self.h, "sf_get_weights")
         return out
+
+    def sync(self):
+        """Wait for the host updates still running (async_update mode)."""
+        _check(lib().sf_sync(self.h), self.h, "sf_sync")
 
     def set_timing(self, on: bool):
         _check(lib().sf_set_timing(self.h, 1 if on else 0), self.h, "sf_set_timing")

@@ -204,9 +204,17 @@ struct sf_ctx {
   struct Task {
     int unit;
     cudaEvent_t ev;
+    int prio;  // the order the next step needs the unit in: embedding, layers, LM head
+    Clock::time_point deadline;
+    bool adam_on;   // the step's optimizer settings, fixed when the task is posted
+    sf_adam adam;
+    int64_t t;
   };
   std::deque<Task> aq;
   int aq_pending = 0;
+  std::vector<char> unit_pending;  // [L + 2]: layers, LM head + final norm (L), embedding (L + 1)
+  std::vector<int32_t> tok_copy;   // tokens of the step whose embedding update is pending
+  bool async = false;
   int aq_status = SF_OK;
   std::string aq_err;
   bool aq_stop = false;
@@ -301,7 +309,8 @@ int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
 // One unit: optional copy of the gradients, then either the Adam update of the
 // fp32 master (refreshing the bf16 pack in place) or, without an optimizer, a
 // refresh of the pack from the unchanged master.
-void host_update(sf_ctx* ctx, HostUnit& hu, bool retain) {
+void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_adam& a,
+                 int64_t step_t) {
   if (retain) {
     hu.retained.resize((size_t)hu.elems);
     uint16_t* dst = hu.retained.data();
@@ -312,16 +321,15 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain) {
   }
   uint16_t* p = hu.pack;
   float* w = hu.master.get();
-  if (!ctx->adam_on) {
+  if (!adam_on) {
     ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
       for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
     });
     return;
   }
-  const sf_adam a = ctx->adam_copy;
   const float b1 = a.beta1, b2 = a.beta2, lr = a.lr, eps = a.eps, wd = a.weight_decay;
-  const float bc1 = 1.f - std::pow(b1, (float)ctx->adam_t);
-  const float bc2 = 1.f - std::pow(b2, (float)ctx->adam_t);
+  const float bc1 = 1.f - std::pow(b1, (float)step_t);
+  const float bc2 = 1.f - std::pow(b2, (float)step_t);
   float* m = hu.m.get();
   float* v = hu.v.get();
   ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
@@ -339,83 +347,165 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain) {
   });
 }
 
+int unit_slot(const sf_ctx* ctx, int unit) {
+  if (unit >= 0) return unit;
+  return unit == SF_UNIT_EMBED ? ctx->L + 1 : ctx->L;  // LM head and final norm share a task
+}
+
+// Embedding: zero dE, scatter-add the bf16 input gradient by column ranges (no
+// races), then the Adam update of the fp32 embedding (no bf16 copy: the
+// gather reads the fp32 master).
+void embed_update(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
+  const int64_t d = ctx->d, V = ctx->V, T = (int64_t)ctx->tok_copy.size();
+  const int32_t* tokens = ctx->tok_copy.data();
+  float* dE = ctx->dE.get();
+  const uint16_t* g = ctx->x0_pin;
+  ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t b, int64_t e) {
+    std::memset(dE + b, 0, (size_t)(e - b) * 4);
+  });
+  ctx->pool->parallel_for(d, 64, [&](int64_t c0, int64_t c1) {
+    for (int64_t t = 0; t < T; ++t) {
+      float* row = dE + (int64_t)tokens[t] * d;
+      const uint16_t* gr = g + t * d;
+      for (int64_t j = c0; j < c1; ++j) row[j] += bf2f(gr[j]);
+    }
+  });
+  if (!adam_on) return;
+  const float bc1 = 1.f - std::pow(a.beta1, (float)step_t);
+  const float bc2 = 1.f - std::pow(a.beta2, (float)step_t);
+  float* w = ctx->E.get();
+  float* m = ctx->Em.get();
+  float* v = ctx->Ev.get();
+  ctx->pool->parallel_for(V * d, 1 << 16, [&](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) {
+      const float gi = dE[i];
+      const float mi = a.beta1 * m[i] + (1.f - a.beta1) * gi;
+      const float vi = a.beta2 * v[i] + (1.f - a.beta2) * gi * gi;
+      float th = w[i];
+      th = th - a.lr * a.weight_decay * th - a.lr * (mi / bc1) / (std::sqrt(vi / bc2) + a.eps);
+      m[i] = mi;
+      v[i] = vi;
+      w[i] = th;
+    }
+  });
+}
+
+void finish_task(sf_ctx* ctx, const sf_ctx::Task& t, int st, const std::string& why) {
+  {
+    std::lock_guard<std::mutex> l(ctx->aq_m);
+    if (st != SF_OK && ctx->aq_status == SF_OK) {
+      ctx->aq_status = st;
+      ctx->aq_err = why;
+    }
+    ctx->unit_pending[unit_slot(ctx, t.unit)] = 0;
+    --ctx->aq_pending;
+  }
+  ctx->aq_done_cv.notify_all();
+}
+
+void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
+  if (ctx->inject_sleep_ms.load() > 0)
+    std::this_thread::sleep_for(std::chrono::milliseconds(ctx->inject_sleep_ms.load()));
+  if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED) {
+    // the gradients are dropped: put the unchanged weights back into the pack
+    if (t.unit >= 0) {
+      host_update(ctx, ctx->layers[t.unit], false, false, t.adam, t.t);
+    } else {
+      host_update(ctx, ctx->lm, false, false, t.adam, t.t);
+      host_update(ctx, ctx->fn, false, false, t.adam, t.t);
+    }
+    finish_task(ctx, t, SF_ESTATE, "injected Adam worker failure on unit " + std::to_string(t.unit));
+    return;
+  }
+  const auto t0 = Clock::now();
+  const bool retain = ctx->cfg.retain_grads != 0;
+  if (t.unit >= 0) {
+    host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t);
+  } else if (t.unit == SF_UNIT_EMBED) {
+    embed_update(ctx, t.adam_on, t.adam, t.t);
+  } else {  // LM head and final norm
+    host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t);
+    host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t);
+  }
+  ctx->adam_ms += std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+  finish_task(ctx, t, SF_OK, std::string());
+}
+
+// The update coordinator: of the units whose gradient copy has landed, update
+// the one the next step needs first (embedding, then layers 0 .. L-1, then the
+// LM head), so that the next step's forward can start before every update is
+// done.  A copy that fails, or does not land within the bound, fails its task.
 void adam_loop(sf_ctx* ctx) {
+  std::vector<sf_ctx::Task> mine;
   while (true) {
-    sf_ctx::Task t;
     {
       std::unique_lock<std::mutex> l(ctx->aq_m);
-      ctx->aq_cv.wait(l, [&] { return ctx->aq_stop || !ctx->aq.empty(); });
-      if (ctx->aq_stop && ctx->aq.empty()) return;
-      t = ctx->aq.front();
-      ctx->aq.pop_front();
-    }
-    int st = SF_OK;
-    std::string why;
-    {
-      const auto deadline = Clock::now() + std::chrono::milliseconds(ctx->wait_ms);
-      while (true) {
-        cudaError_t r = cudaEventQuery(t.ev);
-        if (r == cudaSuccess) break;
-        if (r != cudaErrorNotReady) {
-          st = SF_ECUDA;
-          why = std::string("gradient copy of unit failed: ") + cudaGetErrorString(r);
-          break;
-        }
-        if (Clock::now() > deadline) {
-          st = SF_ETIMEOUT;
-          why = "timed out waiting for a gradient copy";
-          break;
-        }
-        std::this_thread::sleep_for(std::chrono::microseconds(20));
+      if (mine.empty()) ctx->aq_cv.wait(l, [&] { return ctx->aq_stop || !ctx->aq.empty(); });
+      while (!ctx->aq.empty()) {
+        mine.push_back(ctx->aq.front());
+        ctx->aq.pop_front();
       }
+      if (mine.empty() && ctx->aq_stop) return;
     }
-    if (st == SF_OK && ctx->inject_sleep_ms.load() > 0)
-      std::this_thread::sleep_for(std::chrono::milliseconds(ctx->inject_sleep_ms.load()));
-    if (st == SF_OK && ctx->inject_fail_unit.load() == t.unit) {
-      st = SF_ESTATE;
-      why = "injected Adam worker failure on unit " + std::to_string(t.unit);
-      // the gradients are dropped: put the unchanged weights back into the pack
-      const bool on = ctx->adam_on;
-      ctx->adam_on = false;
-      if (t.unit >= 0) {
-        host_update(ctx, ctx->layers[t.unit], false);
-      } else {
-        host_update(ctx, ctx->lm, false);
-        host_update(ctx, ctx->fn, false);
+    int best = -1;
+    for (size_t i = 0; i < mine.size();) {
+      const cudaError_t r = cudaEventQuery(mine[i].ev);
+      if (r == cudaSuccess) {
+        if (best < 0 || mine[i].prio < mine[best].prio) best = (int)i;
+        ++i;
+        continue;
       }
-      ctx->adam_on = on;
-    }
-    if (st == SF_ETIMEOUT || st == SF_ECUDA) ctx->poisoned = true;  // the pack is in an unknown state
-    if (st == SF_OK) {
-      const auto t0 = Clock::now();
-      const bool retain = ctx->cfg.retain_grads != 0;
-      if (t.unit >= 0) {
-        host_update(ctx, ctx->layers[t.unit], retain);
-      } else {  // LM head and final norm
-        host_update(ctx, ctx->lm, retain);
-        host_update(ctx, ctx->fn, retain);
+      if (r != cudaErrorNotReady || Clock::now() > mine[i].deadline) {
+        const bool to = (r == cudaErrorNotReady);
+        ctx->poisoned = true;  // the pack is in an unknown state
+        finish_task(ctx, mine[i], to ? SF_ETIMEOUT : SF_ECUDA,
+                    to ? std::string("timed out waiting for a gradient copy")
+                       : std::string("gradient copy failed: ") + cudaGetErrorString(r));
+        mine.erase(mine.begin() + i);
+        if (best > (int)i) --best;
+        continue;
       }
-      ctx->adam_ms += std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+      ++i;
     }
-    {
-      std::lock_guard<std::mutex> l(ctx->aq_m);
-      if (st != SF_OK && ctx->aq_status == SF_OK) {
-        ctx->aq_status = st;
-        ctx->aq_err = why;
-      }
-      --ctx->aq_pending;
+    if (best < 0) {
+      std::this_thread::sleep_for(std::chrono::microseconds(20));
+      continue;
     }
-    ctx->aq_done_cv.notify_all();
+    const sf_ctx::Task t = mine[best];
+    mine.erase(mine.begin() + best);
+    run_task(ctx, t);
   }
 }
 
 void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev) {
   {
     std::lock_guard<std::mutex> l(ctx->aq_m);
-    ctx->aq.push_back({unit, ev});
+    const int prio = unit == SF_UNIT_EMBED ? -1 : (unit >= 0 ? unit : ctx->L);
+    ctx->aq.push_back({unit, ev, prio, Clock::now() + std::chrono::milliseconds(ctx->wait_ms),
+                       ctx->adam_on, ctx->adam_copy, ctx->adam_t});
+    ctx->unit_pending[unit_slot(ctx, unit)] = 1;
     ++ctx->aq_pending;
   }
   ctx->aq_cv.notify_one();
+}
+
+// Bounded wait until the host update of one unit (posted by an earlier step) is done.
+int wait_unit(sf_ctx* ctx, int unit) {
+  std::unique_lock<std::mutex> l(ctx->aq_m);
+  const int u = unit_slot(ctx, unit);
+  const bool ok = ctx->aq_done_cv.wait_for(l, std::chrono::milliseconds(ctx->wait_ms),
+                                           [&] { return !ctx->unit_pending[u]; });
+  if (!ok) {
+    ctx->set_err("timed out waiting for the host update of unit %d", unit);
+    return SF_ETIMEOUT;
+  }
+  if (ctx->aq_status != SF_OK) {
+    ctx->set_err("%s", ctx->aq_err.c_str());
+    const int st = ctx->aq_status;
+    ctx->aq_status = SF_OK;
+    return st;
+  }
+  return SF_OK;
 }
 
 int wait_tasks(sf_ctx* ctx) {
@@ -783,6 +873,8 @@ int init(sf_ctx* ctx) {
   RET(mk(&ctx->ev_start, true));
   RET(mk(&ctx->ev_end, true));
   RET(mk(&ctx->ev_end_d, false));
+  ctx->unit_pending.assign(L + 2, 0);
+  ctx->async = cf.async_update != 0;
   ctx->adam_thread = std::thread(adam_loop, ctx);
   return SF_OK;
 }
@@ -839,8 +931,13 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     }
     ++n_valid;
   }
-  // host updates left over from a step that timed out still own the pinned packs
-  RET(wait_tasks(ctx));
+  // The embedding update of the previous step reads its tokens and the pinned
+  // input-gradient buffer, which this step is about to overwrite.  Without
+  // async_update every update of the previous step is finished here (also the
+  // ones left over by a step that timed out, which still own the pinned packs).
+  if (ctx->async) RET(wait_unit(ctx, SF_UNIT_EMBED));
+  else RET(wait_tasks(ctx));
+  ctx->tok_copy.assign(tokens, tokens + T);
   ctx->adam_on = adam != nullptr;
   if (adam) {
     ctx->adam_copy = *adam;
@@ -893,8 +990,10 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   // ---- forward through the ring (A1-A9)
   for (int l = 0; l < L; ++l) {
     const int s = l % R;
+    if (ctx->async) RET(wait_unit(ctx, l));  // the previous step's update of this layer
     RET(h2d_layer(l));
     if (l == L - 1) {  // the LM head and final norm follow the last layer on the copy stream
+      if (ctx->async) RET(wait_unit(ctx, SF_UNIT_LM_HEAD));
       CK(cudaMemcpyAsync(ctx->Wlm, ctx->lm.pack, (size_t)V * d * 2, cudaMemcpyHostToDevice, ctx->sU));
       CK(cudaMemcpyAsync(ctx->gf, ctx->fn.pack, (size_t)ctx->fn.elems * 2, cudaMemcpyHostToDevice, ctx->sU));
       CK(cudaEventRecord(ctx->ev_lm, ctx->sU));
@@ -963,43 +1062,12 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     wait_tasks(ctx);
     return SF_EDEVICE;
   }
-  // embedding gradient (scatter-add by column ranges: no races) and its update
-  {
-    float* dE = ctx->dE.get();
-    const uint16_t* g = ctx->x0_pin;
-    ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t b, int64_t e) {
-      std::memset(dE + b, 0, (size_t)(e - b) * 4);
-    });
-    ctx->pool->parallel_for(d, 64, [&](int64_t c0, int64_t c1) {
-      for (int64_t t = 0; t < T; ++t) {
-        float* row = dE + (int64_t)tokens[t] * d;
-        const uint16_t* gr = g + t * d;
-        for (int64_t j = c0; j < c1; ++j) row[j] += bf2f(gr[j]);
-      }
-    });
-    if (ctx->adam_on) {
-      const sf_adam a = ctx->adam_copy;
-      const float bc1 = 1.f - std::pow(a.beta1, (float)ctx->adam_t);
-      const float bc2 = 1.f - std::pow(a.beta2, (float)ctx->adam_t);
-      float* w = ctx->E.get();
-      float* m = ctx->Em.get();
-      float* v = ctx->Ev.get();
-      ctx->pool->parallel_for(V * d, 1 << 16, [&](int64_t b, int64_t e) {
-        for (int64_t i = b; i < e; ++i) {
-          const float gi = dE[i];
-          const float mi = a.beta1 * m[i] + (1.f - a.beta1) * gi;
-          const float vi = a.beta2 * v[i] + (1.f - a.beta2) * gi * gi;
-          float th = w[i];
-          th = th - a.lr * a.weight_decay * th - a.lr * (mi / bc1) / (std::sqrt(vi / bc2) + a.eps);
-          m[i] = mi;
-          v[i] = vi;
-          w[i] = th;
-        }
-      });
-    }
+  // embedding gradient and update: a host task like the others
+  post_task(ctx, SF_UNIT_EMBED, ctx->ev_dx0);
+  if (!ctx->async) {
+    st = wait_tasks(ctx);
+    if (st != SF_OK) return st;
   }
-  st = wait_tasks(ctx);
-  if (st != SF_OK) return st;
   ctx->loss = *ctx->loss_pin;
   ctx->have_loss = true;
 
@@ -1079,6 +1147,7 @@ const char* sf_last_error(const sf_ctx* ctx) { return ctx ? ctx->err.c_str() : g
 int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t numel) {
   if (!ctx) return SF_EINVAL;
   if (ctx->poisoned) return SF_ESTATE;
+  if (int st = wait_tasks(ctx)) return st;
   if (!w || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
     ctx->set_err("sf_load_layer_weights: bad unit %d or numel %zu", unit, numel);
     return SF_EINVAL;
@@ -1170,6 +1239,7 @@ int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
     if (ctx) ctx->set_err("sf_get_grads: bad unit %d or numel %zu", unit, numel);
     return SF_EINVAL;
   }
+  if (int st = wait_tasks(ctx)) return st;
   if (!ctx->cfg.retain_grads || !ctx->have_loss) {
     ctx->set_err("sf_get_grads needs retain_grads = 1 and a finished step");
     return SF_ESTATE;
@@ -1194,6 +1264,7 @@ int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
     if (ctx) ctx->set_err("sf_get_weights: bad unit %d or numel %zu", unit, numel);
     return SF_EINVAL;
   }
+  if (int st = wait_tasks(ctx)) return st;
   if (unit == SF_UNIT_EMBED) {
     std::memcpy(out, ctx->E.get(), numel * 4);
     return SF_OK;
@@ -1205,6 +1276,11 @@ int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
     std::memcpy(out, hu.master.get(), numel * 4);
   }
   return SF_OK;
+}
+
+int sf_sync(sf_ctx* ctx) {
+  if (!ctx) return SF_EINVAL;
+  return wait_tasks(ctx);
 }
 
 int sf_loss(sf_ctx* ctx, float* out) {

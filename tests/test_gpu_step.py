@@ -72,6 +72,24 @@ def test_ring_size_invariance_is_bitwise():
             assert np.array_equal(a, b)
 
 
+def test_async_update_gives_bitwise_identical_training():
+    """Updates overlapping the next step (async_update) change no result."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=4)
+    mast = masters(cfg)
+    batches = [inputs.tokens_and_labels(cfg, seed=42 + i) for i in range(3)]
+    adam = sf.Adam(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    units = (0, 3, UNIT_EMBED, UNIT_LM_HEAD, UNIT_FINAL_NORM)
+    out = []
+    for asyn in (0, 1):
+        with make_model(cfg, mast, async_update=asyn, ring_slots=2) as m:
+            losses = [m.step(t, l, adam) for t, l in batches]
+            m.sync()
+            out.append((losses, [m.weights(u) for u in units], [m.grads(u) for u in units]))
+    assert out[0][0] == out[1][0]
+    for a, b in zip(out[0][1] + out[0][2], out[1][1] + out[1][2]):
+        assert np.array_equal(a, b)
+
+
 def test_lce_chunking_does_not_change_the_step():
     cfg = TEST_CONFIGS["small-gqa"]
     mast = masters(cfg)

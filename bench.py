@@ -342,6 +342,62 @@ def run_ours(args, c):
         dist.destroy_process_group()
 
 
+def run_op(args, c):
+    """Time one kernel at the workload's shapes on device-resident data (CUDA
+    events on the launching stream, inputs larger than L2).  Prints one JSON line."""
+    import torch
+    import offloaded_fine_tuning_gb300 as sf
+    sf.lib(build_if_needed=True)
+    torch.manual_seed(0)
+    st = torch.cuda.current_stream().cuda_stream
+    B, S, Hq, Hkv, hd = c.batch, c.seq, c.n_heads, c.n_kv_heads, c.head_dim
+    T = B * S
+    W = (Hq + 2 * Hkv) * hd
+    attn_fwd_flops = 2.0 * B * Hq * hd * S * (S + 1)
+    bf16_peak, bf16_sust, hbm, src = peaks()
+    if args.op.startswith("attn"):
+        qkv = torch.randn(T, W, device="cuda").to(torch.bfloat16)
+        o = torch.empty(T, Hq * hd, device="cuda", dtype=torch.bfloat16)
+        lse = torch.empty(B, Hq, S, device="cuda")
+        dout = torch.randn(T, Hq * hd, device="cuda").to(torch.bfloat16)
+        dqkv = torch.empty_like(qkv)
+        delta = torch.empty(B, Hq, S, device="cuda")
+        dqa = torch.empty(T, Hq * hd, device="cuda")
+        fwd = lambda: sf.op_attn_fwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), B, S, Hq, Hkv, hd, st)
+        bwd = lambda: sf.op_attn_bwd(qkv.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                                     delta.data_ptr(), dqa.data_ptr(), dqkv.data_ptr(), B, S, Hq, Hkv, hd, 0, st)
+        assert fwd() == 0
+        run, flops = (fwd, attn_fwd_flops) if args.op == "attn_fwd" else (bwd, 2.5 * attn_fwd_flops)
+        shape = {"B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "hd": hd}
+    else:
+        M, N, K = (int(x) for x in args.shape.split(","))
+        layout = {"nt": sf.NT, "nn": sf.NN, "tn": sf.TN}[args.layout]
+        a_shape = (K, M) if layout == sf.TN else (M, K)
+        b_shape = (N, K) if layout == sf.NT else (K, N)
+        A = torch.randn(*a_shape, device="cuda").to(torch.bfloat16)
+        Bm = torch.randn(*b_shape, device="cuda").to(torch.bfloat16)
+        C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        run = lambda: sf.op_gemm(layout, sf.EPI_BF16, M, N, K, A.data_ptr(), a_shape[1], Bm.data_ptr(),
+                                 b_shape[1], C.data_ptr(), N, 0, 0, 1.0, st)
+        flops = 2.0 * M * N * K
+        shape = {"M": M, "N": N, "K": K, "layout": args.layout}
+    for _ in range(args.warmup):
+        assert run() == 0
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    assert sf.device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"op": args.op, "workload": c.name, "shape": shape, "ms": ms, "tflops": tf,
+                      "peak": bf16_peak, "frac": tf / bf16_peak,
+                      "peak_source": f"{src} bf16 burst (kernel timed alone)"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -353,9 +409,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sync-updates", action="store_true",
                     help="finish every host update before a step returns (no cross-step overlap)")
+    ap.add_argument("--op", default="", choices=["", "attn_fwd", "attn_bwd", "gemm"],
+                    help="time one kernel instead of the training step")
+    ap.add_argument("--shape", default="16384,6144,4096", help="M,N,K for --op gemm")
+    ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])
     args = ap.parse_args()
     c = CONFIGS[args.config]
-    if args.impl == "reference":
+    if args.op:
+        run_op(args, c)
+    elif args.impl == "reference":
         run_reference(args, c)
     else:
         run_ours(args, c)

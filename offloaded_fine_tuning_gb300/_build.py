@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsfslide.so")
-SOURCES = ["gemm.cu", "attention.cu", "elementwise.cu", "engine.cpp", "ops.cpp", "noalloc.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "elementwise.cu", "engine.cpp", "ops.cpp", "noalloc.cu", "attention_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

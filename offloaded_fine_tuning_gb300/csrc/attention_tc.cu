@@ -1,0 +1,724 @@
+// Causal grouped-query attention forward on the tcgen05 tensor cores.
+//
+// Online softmax over key blocks (Milakov & Gimelshein 2018; the blocking of
+// Dao et al., FlashAttention 2022), laid out for sm_103a: one CTA owns 128
+// query rows of one head; per 128-key block the tensor core computes
+// S = Q K^T into one of two TMEM buffers, four softmax warps (one thread per
+// query row, so row max and row sum need no shuffles) turn S into bf16 P in
+// shared memory, and the tensor core accumulates O += P V in TMEM.  S of the
+// next block is computed while the softmax warps work on the current one.
+//
+//   warp 0     TMA: Q once, then K and V blocks into a 2-stage ring
+//   warp 1     MMA issuer (tcgen05.mma, one thread); TMEM owner (512 columns:
+//              S0 | S1 | O)
+//   warps 2-5  softmax: tcgen05.ld of a row of S, scale, causal mask,
+//              max / exp2 / sum, rescale of the O row in TMEM when the row
+//              max grows, swizzled store of the row of P
+//
+// Operands: Q, K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
+// columns per box); V is the MN-major operand of P V ([128 keys][64 hd] boxes);
+// P is written by the softmax threads in the same swizzled K-major layout the
+// TMA would produce.  The qkv rows are read through a 3-D tensor map
+// (column, position, batch), so rows past the sequence end arrive as zeros.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ptx.cuh"
+#include "sf_internal.h"
+
+namespace sf {
+
+namespace {
+
+constexpr int kAttThreads = 192;
+
+template <int HD>
+struct AttCfg {
+  static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = TILE;
+  static constexpr int OFF_V = OFF_K + 2 * TILE;
+  static constexpr int OFF_P = OFF_V + 2 * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * 16384;  // P: 128 rows x 128 keys
+  static constexpr int NBAR = 12;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+};
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ out,
+                       float* __restrict__ lse, int S, int Hq, int Hkv, float scale_log2,
+                       int* err) {
+  using C = AttCfg<HD>;
+  constexpr int NB = HD / 64;  // 64-column boxes per tile
+  constexpr uint32_t ID_S = umma_idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID_O = umma_idesc_bf16(128, HD, false, true);
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t O_COL = 256;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sP = s0 + C::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  const uint32_t q_full = b0;
+  auto kv_full = [&](int s) { return b0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (3 + s); };
+  auto s_full = [&](int s) { return b0 + 8u * (5 + s); };
+  auto s_free = [&](int s) { return b0 + 8u * (7 + s); };
+  const uint32_t p_full = b0 + 8u * 9, o_done = b0 + 8u * 10, drain = b0 + 8u * 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (S + 127) / 128;
+  const int qb = nqb - 1 - (int)blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (Hq / Hkv);
+  const int q0 = qb * 128;
+  const int nkv = qb + 1;
+  const int colQ = h * HD, colK = (Hq + g) * HD, colV = (Hq + Hkv + g) * HD;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(s_free(s), 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    mbar_arrive_expect_tx(q_full, C::TILE);
+#pragma unroll
+    for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, colQ + 64 * c, q0, b);
+    bool ok = true;
+    int issued = 0;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!mbar_wait(kv_empty(st), ph ^ 1u, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(kv_full(st), 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < NB; ++c) {
+        tma_load_3d(sK + st * C::TILE + c * 16384, &tm, kv_full(st), colK + 64 * c, j * 128, b);
+        tma_load_3d(sV + st * C::TILE + c * 16384, &tm, kv_full(st), colV + 64 * c, j * 128, b);
+      }
+      issued = j + 1;
+    }
+    if (!ok) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      // let the copies already issued land before the CTA's shared memory goes away
+      mbar_wait(q_full, 0, nullptr);
+      for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+        mbar_wait(kv_full(j & 1), (j >> 1) & 1, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait(q_full, 0, abort_flag);
+    for (int j = 0; ok && j <= nkv; ++j) {
+      if (j < nkv) {  // S_j = Q K_j^T into S buffer j % 2
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(kv_full(st), ph, abort_flag) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem_base + st * 128, smem_desc_sw128(sQ + off, 16, 1024),
+                    smem_desc_sw128(sK + st * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full(st));
+      }
+      if (j > 0) {  // O += P_{j-1} V_{j-1}
+        const int jp = j - 1, st = jp & 1;
+        if (!mbar_wait(p_full, jp & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          umma_bf16(tmem_base + O_COL,
+                    smem_desc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
+                    (jp > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(kv_empty(st));
+      }
+    }
+    if (!ok) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- softmax
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int q = q0 + row;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int st = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full(st), (j >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free(st));
+      const bool diag = (j == qb);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        float v = s[i] * scale_log2;
+        if (diag && j * 128 + i > q) v = -INFINITY;
+        s[i] = v;
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m, mx);
+      float ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const float p = exp2f(s[i] - m_new);
+        s[i] = p;
+        ps += p;
+      }
+      const float corr = exp2f(m - m_new);  // 0 on the first block (m = -inf)
+      if (j > 0) {
+        // P_{j-1} V_{j-1} is done: the P buffer is free and the O row is current
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, m_new > m)) {
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+            tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      l = l * corr + ps;
+      m = m_new;
+      // row of P, bf16, in the 128-byte swizzled K-major layout
+      const uint32_t prow = sP + (uint32_t)row * 128u;
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const float* p8 = s + kb * 64 + jj * 8;
+          const uint32_t addr = prow + kb * 16384 + (uint32_t)((jj ^ (row & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack2_bf16(p8[0], p8[1])), "r"(pack2_bf16(p8[2], p8[3])),
+                       "r"(pack2_bf16(p8[4], p8[5])), "r"(pack2_bf16(p8[6], p8[7]))
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = out + ((int64_t)b * S + q) * ((int64_t)Hq * HD) + (int64_t)h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+        tmem_ld_wait();
+        if (q < S) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack2_bf16(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
+            v.y = pack2_bf16(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
+            v.z = pack2_bf16(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
+            v.w = pack2_bf16(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * k) = v;
+          }
+        }
+      }
+      if (q < S) lse[((int64_t)b * Hq + h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
+    } else if (lane == 0) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ backward
+// One CTA per (128-key block j, kv head g, batch b).  It walks every query
+// head of the group and every 128-query block i >= j.  Per (head, block):
+//   MMA:     S^T = K Q^T -> TMEM[0,128),  dP^T = V dO^T -> TMEM[128,256)
+//   threads: one per key row: P^T = exp2(S^T*scale*log2e - lse*log2e) (causal),
+//            dS^T = P^T * (dP^T - D), both to shared memory (bf16, swizzled)
+//   MMA:     dV += P^T dO, dK += dS^T Q (TMEM, kept over the whole walk);
+//            dQ = dS K -> TMEM[0,hd) (the S^T columns, already consumed)
+//   threads: one per query row: dQ added into the fp32 dq_acc (vector atomics)
+// dS^T is stored once and read both as the K-major A of dK and as the
+// MN-major A (dS) of dQ.  At the end the threads write dK (scaled, inverse
+// RoPE) and dV of their key rows.
+namespace {
+template <int HD>
+struct AttBwdCfg {
+  static constexpr int TILE = HD / 64 * 16384;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int OFF_DO = 3 * TILE;
+  static constexpr int OFF_PT = 4 * TILE;
+  static constexpr int OFF_DST = OFF_PT + 32768;
+  static constexpr int OFF_LD = OFF_DST + 32768;  // lse*log2e and D, 2 buffers x 128 each
+  static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
+  static constexpr int NBAR = 10;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+};
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                       const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
+                       const float* __restrict__ delta, float* __restrict__ dq_acc,
+                       __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ cs, int S,
+                       int Hq, int Hkv, float scale, float scale_log2, int* err) {
+  using C = AttBwdCfg<HD>;
+  constexpr int NB = HD / 64;
+  constexpr uint32_t ID_SQ = umma_idesc_bf16(128, 128, false, false);  // S^T, dP^T
+  constexpr uint32_t ID_KV = umma_idesc_bf16(128, HD, false, true);    // dV, dK
+  constexpr uint32_t ID_Q = umma_idesc_bf16(128, HD, true, true);      // dQ
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t COL_DP = 128, COL_DV = 256, COL_DK = 256 + HD;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
+  const uint32_t sPt = s0 + C::OFF_PT, sDSt = s0 + C::OFF_DST;
+  float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);  // [2][lse 128 | D 128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  const uint32_t kv_full = b0, qdo_full = b0 + 8, qdo_empty = b0 + 16, sp_full = b0 + 24,
+                 ps_full = b0 + 32, dq_full = b0 + 40, dq_free = b0 + 48, acc_done = b0 + 56,
+                 drain = b0 + 64;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int grp = Hq / Hkv;
+  const int k0 = j * 128;
+  const int nqb = (S + 127) / 128;
+  const int n_it = grp * (nqb - j);  // (head, query block) pairs
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(sp_full, 1);
+    mbar_init(ps_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+      tma_load_3d(sK + c * 16384, &tm_qkv, kv_full, (Hq + g) * HD + 64 * c, k0, b);
+      tma_load_3d(sV + c * 16384, &tm_qkv, kv_full, (Hq + Hkv + g) * HD + 64 * c, k0, b);
+    }
+    bool ok = true;
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = g * grp + it / (nqb - j);
+      const int q0 = (j + it % (nqb - j)) * 128;
+      if (!mbar_wait(qdo_empty, (it & 1) ^ 1, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(qdo_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < NB; ++c) {
+        tma_load_3d(sQ + c * 16384, &tm_qkv, qdo_full, h * HD + 64 * c, q0, b);
+        tma_load_3d(sDO + c * 16384, &tm_do, qdo_full, h * HD + 64 * c, q0, b);
+      }
+      issued = it + 1;
+    }
+    if (!ok) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      mbar_wait(kv_full, 0, nullptr);
+      if (issued > 0) mbar_wait(qdo_full, (issued - 1) & 1, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait(kv_full, 0, abort_flag);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const uint32_t ph = it & 1;
+      if (!mbar_wait(qdo_full, ph, abort_flag) || !mbar_wait(dq_free, ph ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        umma_bf16(tmem_base, smem_desc_sw128(sK + off, 16, 1024), smem_desc_sw128(sQ + off, 16, 1024),
+                  ID_SQ, kk > 0 ? 1u : 0u);
+        umma_bf16(tmem_base + COL_DP, smem_desc_sw128(sV + off, 16, 1024),
+                  smem_desc_sw128(sDO + off, 16, 1024), ID_SQ, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(sp_full);
+      if (!mbar_wait(ps_full, ph, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {  // contraction over the 128 queries
+        const uint32_t a_off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+        umma_bf16(tmem_base + COL_DV, smem_desc_sw128(sPt + a_off, 16, 1024),
+                  smem_desc_sw128(sDO + kk * 2048, 16384, 1024), ID_KV, acc);
+        umma_bf16(tmem_base + COL_DK, smem_desc_sw128(sDSt + a_off, 16, 1024),
+                  smem_desc_sw128(sQ + kk * 2048, 16384, 1024), ID_KV, acc);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // contraction over the 128 keys
+        umma_bf16(tmem_base, smem_desc_sw128(sDSt + kk * 2048, 16384, 1024),
+                  smem_desc_sw128(sK + kk * 2048, 16384, 1024), ID_Q, kk > 0 ? 1u : 0u);
+      umma_commit(dq_full);
+      umma_commit(qdo_empty);
+    }
+    if (ok) {
+      umma_commit(acc_done);
+    } else {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- softmax-gradient threads
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row for S^T / dP^T, query row for dQ
+    const int key = k0 + r;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const int tid = threadIdx.x - 64;  // 0..127
+    const int64_t ldo = (int64_t)Hq * HD;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = g * grp + it / (nqb - j);
+      const int q0 = (j + it % (nqb - j)) * 128;
+      const uint32_t ph = it & 1;
+      float* bL = sLD + (it & 1) * 256;
+      float* bD = bL + 128;
+      {
+        const int q = q0 + tid;
+        const int64_t o = ((int64_t)b * Hq + h) * S + q;
+        bL[tid] = (q < S) ? lse[o] * 1.4426950408889634f : 0.f;
+        bD[tid] = (q < S) ? delta[o] : 0.f;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      ok = __all_sync(0xffffffffu, mbar_wait(sp_full, ph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t rowoff = (uint32_t)r * 128u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(lane_base + 32 * c, sr);
+        tmem_ld_32x32b_x32(lane_base + COL_DP + 32 * c, dr);
+        tmem_ld_wait();
+        float p[32], ds[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qq = 32 * c + e;
+          const int q = q0 + qq;
+          float pv = 0.f;
+          if (q < S && key <= q) pv = exp2f(__uint_as_float(sr[e]) * scale_log2 - bL[qq]);
+          p[e] = pv;
+          ds[e] = pv * (__uint_as_float(dr[e]) - bD[qq]);
+        }
+        const uint32_t box = (uint32_t)(c >> 1) * 16384u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int jj = (c & 1) * 4 + k;
+          const uint32_t off = box + rowoff + (uint32_t)((jj ^ (r & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sPt + off),
+                       "r"(pack2_bf16(p[8 * k], p[8 * k + 1])), "r"(pack2_bf16(p[8 * k + 2], p[8 * k + 3])),
+                       "r"(pack2_bf16(p[8 * k + 4], p[8 * k + 5])), "r"(pack2_bf16(p[8 * k + 6], p[8 * k + 7]))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDSt + off),
+                       "r"(pack2_bf16(ds[8 * k], ds[8 * k + 1])), "r"(pack2_bf16(ds[8 * k + 2], ds[8 * k + 3])),
+                       "r"(pack2_bf16(ds[8 * k + 4], ds[8 * k + 5])), "r"(pack2_bf16(ds[8 * k + 6], ds[8 * k + 7]))
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ps_full);
+      // dQ rows of this query block (thread = query row)
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, ph, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int q = q0 + r;
+      float* dst = dq_acc + ((int64_t)b * S + q) * ldo + (int64_t)h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_base + 32 * c, v);
+        tmem_ld_wait();
+        if (q < S) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * k),
+                      make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                  __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      // dK: pairs (d, d + HD/2) get the inverse rotation of the key's position
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t x1[32], x2[32];
+        tmem_ld_32x32b_x32(lane_base + COL_DK + 32 * c, x1);
+        tmem_ld_32x32b_x32(lane_base + COL_DK + HD / 2 + 32 * c, x2);
+        tmem_ld_wait();
+        if (key < S) {
+          const int64_t ld = (int64_t)(Hq + 2 * Hkv) * HD;
+          __nv_bfloat16* krow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + g) * HD;
+          uint32_t o1[16], o2[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float a1 = __uint_as_float(x1[e]) * scale, b1 = __uint_as_float(x1[e + 1]) * scale;
+            float a2 = __uint_as_float(x2[e]) * scale, b2 = __uint_as_float(x2[e + 1]) * scale;
+            if (cs) {
+              const float2 ca = cs[(int64_t)key * (HD / 2) + 32 * c + e];
+              const float2 cb = cs[(int64_t)key * (HD / 2) + 32 * c + e + 1];
+              const float y1a = a1 * ca.x + a2 * ca.y, y2a = a2 * ca.x - a1 * ca.y;
+              const float y1b = b1 * cb.x + b2 * cb.y, y2b = b2 * cb.x - b1 * cb.y;
+              a1 = y1a; a2 = y2a; b1 = y1b; b2 = y2b;
+            }
+            o1[e / 2] = pack2_bf16(a1, b1);
+            o2[e / 2] = pack2_bf16(a2, b2);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            *reinterpret_cast<uint4*>(krow + 32 * c + 8 * k) = make_uint4(o1[4 * k], o1[4 * k + 1], o1[4 * k + 2], o1[4 * k + 3]);
+            *reinterpret_cast<uint4*>(krow + HD / 2 + 32 * c + 8 * k) = make_uint4(o2[4 * k], o2[4 * k + 1], o2[4 * k + 2], o2[4 * k + 3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_base + COL_DV + 32 * c, v);
+        tmem_ld_wait();
+        if (key < S) {
+          const int64_t ld = (int64_t)(Hq + 2 * Hkv) * HD;
+          __nv_bfloat16* vrow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + Hkv + g) * HD;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = pack2_bf16(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1]));
+            u.y = pack2_bf16(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3]));
+            u.z = pack2_bf16(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5]));
+            u.w = pack2_bf16(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7]));
+            *reinterpret_cast<uint4*>(vrow + 32 * c + 8 * k) = u;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_att() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+template <int HD>
+int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq, int Hkv,
+           int* err, cudaStream_t st) {
+  using C = AttCfg<HD>;
+  auto fn = encode_fn_att();
+  if (!fn) return -3;
+  const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD;
+  CUtensorMap tm;
+  cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(S * W * 2)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(qkv), dims, strides,
+         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -3;
+  static bool set = false;
+  if (!set) {
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return -3;
+    set = true;
+  }
+  dim3 grid((S + 127) / 128, Hq, B);
+  attn_fwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(tm, o, lse, S, Hq, Hkv,
+                                                             1.4426950408889634f / sqrtf((float)HD), err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+template <int HD>
+int bwd_tc(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+           const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq,
+           int Hkv, const float2* cs, int* err, cudaStream_t st) {
+  using C = AttBwdCfg<HD>;
+  auto fn = encode_fn_att();
+  if (!fn) return -3;
+  const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
+  CUtensorMap tq, td;
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t dq[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t sq[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(S * W * 2)};
+  cuuint64_t dd[3] = {(cuuint64_t)WO, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t sd[2] = {(cuuint64_t)(WO * 2), (cuuint64_t)(S * WO * 2)};
+  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(qkv), dq, sq, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      fn(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(dout), dd, sd, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -3;
+  static bool set = false;
+  if (!set) {
+    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return -3;
+    set = true;
+  }
+  const int64_t T = (int64_t)B * S;
+  if (cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess) return -3;
+  attn_delta(o, dout, delta, B, S, Hq, HD, st);
+  const float scale = 1.f / sqrtf((float)HD);
+  dim3 grid((S + 127) / 128, Hkv, B);
+  attn_bwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(
+      tq, td, lse, delta, dq_acc, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
+  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, st);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
+int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+             const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S,
+             int Hq, int Hkv, int hd, const float2* cs, int* err, cudaStream_t st) {
+  if (B <= 0 || S <= 0) return 0;
+  if (Hkv <= 0 || Hq % Hkv) return -1;
+  if (hd == 64) return bwd_tc<64>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
+  if (hd == 128) return bwd_tc<128>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
+  return -1;
+}
+
+int attn_fwd(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq, int Hkv,
+             int hd, int* err, cudaStream_t st) {
+  if (B <= 0 || S <= 0) return 0;
+  if (Hkv <= 0 || Hq % Hkv) return -1;
+  if ((reinterpret_cast<uintptr_t>(qkv) & 15) != 0) return -1;
+  if (hd == 64) return fwd_tc<64>(qkv, o, lse, B, S, Hq, Hkv, err, st);
+  if (hd == 128) return fwd_tc<128>(qkv, o, lse, B, S, Hq, Hkv, err, st);
+  return -1;
+}
+
+}  // namespace sf

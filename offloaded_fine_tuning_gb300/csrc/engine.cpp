@@ -613,7 +613,7 @@ int layer_forward(sf_ctx* c, const LayerW& w, const float* Xin, float* Xout, int
   sf::rope_inplace(c->qkv, c->qkvdim, T, S, Hq + Hkv, hd, c->rope_cs, 0, c->sC);
   {
     Timed t(c, 1, attn_fwd_flops(B, S, Hq, hd));
-    if (sf::attn_fwd(c->qkv, c->o, c->lse, B, S, Hq, Hkv, hd, c->sC) != 0) {
+    if (sf::attn_fwd(c->qkv, c->o, c->lse, B, S, Hq, Hkv, hd, c->dev_err, c->sC) != 0) {
       ctx->set_err("attention forward launch failed");
       return SF_ECUDA;
     }
@@ -651,7 +651,7 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   {
     Timed t(c, 1, 2.5 * attn_fwd_flops(B, S, Hq, hd));
     if (sf::attn_bwd(c->qkv, c->o, c->dob, c->lse, c->delta, c->dq_acc, c->dqkv, B, S, Hq, Hkv,
-                     hd, c->rope_cs, c->sC) != 0) {
+                     hd, c->rope_cs, c->dev_err, c->sC) != 0) {
       ctx->set_err("attention backward launch failed");
       return SF_ECUDA;
     }

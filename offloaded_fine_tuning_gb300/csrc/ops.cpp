@@ -122,8 +122,10 @@ int sf_op_attn_fwd(const uint16_t* qkv, uint16_t* o, float* lse, int32_t B, int3
   if (B < 0 || S_ < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || (hd != 64 && hd != 128)) return SF_EINVAL;
   if (B == 0 || S_ == 0) return SF_OK;
   if (!qkv || !o || !lse || !al16(qkv) || !al16(o)) return SF_EINVAL;
+  int* err = dev_err_word();
+  if (!err) return SF_ECUDA;
   if (sf::attn_fwd(reinterpret_cast<const bf16*>(qkv), reinterpret_cast<bf16*>(o), lse, B, S_,
-                   Hq, Hkv, hd, S(stream)) != 0)
+                   Hq, Hkv, hd, err, S(stream)) != 0)
     return SF_ECUDA;
   return SF_OK;
 }
@@ -136,10 +138,12 @@ int sf_op_attn_bwd(const uint16_t* qkv, const uint16_t* o, const uint16_t* dout,
   if (B == 0 || S_ == 0) return SF_OK;
   if (!qkv || !o || !dout || !lse || !delta || !dq_acc || !dqkv) return SF_EINVAL;
   if (!al16(qkv) || !al16(o) || !al16(dout) || !al16(dq_acc) || !al16(dqkv)) return SF_EINVAL;
+  int* err = dev_err_word();
+  if (!err) return SF_ECUDA;
   if (sf::attn_bwd(reinterpret_cast<const bf16*>(qkv), reinterpret_cast<const bf16*>(o),
                    reinterpret_cast<const bf16*>(dout), lse, delta, dq_acc,
                    reinterpret_cast<bf16*>(dqkv), B, S_, Hq, Hkv, hd,
-                   reinterpret_cast<const float2*>(table), S(stream)) != 0)
+                   reinterpret_cast<const float2*>(table), err, S(stream)) != 0)
     return SF_ECUDA;
   return SF_OK;
 }

@@ -56,13 +56,22 @@ void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st)
 void cast_bf16_f32(const __nv_bfloat16* x, float* y, int64_t n, cudaStream_t st);
 
 // ---- attention (attention.cu).  qkv [T, (Hq+2Hkv)*hd] bf16, token t = b*S + s.
+// Forward on tcgen05 (attention_tc.cu); a bounded wait that runs out writes
+// kDevAttnTimeout to *err.
 int attn_fwd(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq,
-             int Hkv, int hd, cudaStream_t st);
-// dq_acc: fp32 scratch [T, Hq*hd] (zeroed inside); delta: fp32 scratch [B, Hq, S].
-// Writes dQ (RoPE-inverse applied when cs != null), dK (same) and dV into dqkv.
+             int Hkv, int hd, int* err, cudaStream_t st);
+// Backward on tcgen05 (attention_tc.cu).  dq_acc: fp32 scratch [T, Hq*hd]
+// (zeroed inside); delta: fp32 scratch [B, Hq, S].  Writes dQ and dK (inverse
+// RoPE applied when cs != null) and dV into dqkv.
 int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
              const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S,
-             int Hq, int Hkv, int hd, const float2* cs, cudaStream_t st);
+             int Hq, int Hkv, int hd, const float2* cs, int* err, cudaStream_t st);
+// delta[b, h, s] = sum_j dO * O over one head's row (attention.cu)
+void attn_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, int B, int S,
+                int Hq, int hd, cudaStream_t st);
+// dQ = scale * dq_acc, inverse RoPE, into the query columns of dqkv (attention.cu)
+void attn_dq_finalize(const float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq, int Hkv,
+                      int hd, float scale, const float2* cs, cudaStream_t st);
 
 int num_sms();
 

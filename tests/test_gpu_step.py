@@ -178,3 +178,38 @@ def test_adam_worker_failure_and_timeout_are_reported():
         assert m.train_step(tok, lab, adam) == sf.SF_ETIMEOUT
         assert "timed out" in m.error()
         m.inject(0)
+
+
+# ------------------------------------------------------------------ full-size shapes
+@pytest.mark.parametrize("name,seq", [("8b", 2048), ("123b-slice", 1024)])
+def test_one_full_shape_layer_matches_oracle(name, seq):
+    """One decoder layer at the full width of the 8B and 123B-slice shapes
+    (GQA 4:1 and 12:1, head_dim 128, full vocabulary), one sequence, against
+    the float32 oracle (float32 is within ~1e-6 of float64, far inside the bar)."""
+    cfg = CONFIGS[name].with_(n_layers=1, batch=1, seq=seq)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg, dtype=np.float32)
+    with make_model(cfg, mast, ring_slots=2) as m:
+        assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+        compare(cfg, m, loss_ref, g_ref)
+
+
+def test_full_1p3b_step_properties():
+    """The whole 24-layer 1.3B-shape step (8 x 1024 tokens): loss near
+    ln V + sigma^2/2 (random init), finite gradients, and ring sizes 2 and 3
+    give bit-identical results."""
+    import math
+    cfg = CONFIGS["1.3b"]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    out = []
+    for R in (2, 3):
+        with make_model(cfg, mast, ring_slots=R) as m:
+            assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+            out.append((m.loss(), m.grads(0), m.grads(cfg.n_layers - 1), m.grads(UNIT_LM_HEAD)))
+    loss = out[0][0]
+    assert loss == pytest.approx(math.log(cfg.vocab) + 0.02 ** 2 * cfg.hidden / 2, rel=0.02)
+    assert out[1][0] == loss
+    for a, b in zip(out[0][1:], out[1][1:]):
+        assert np.isfinite(a).all() and np.array_equal(a, b)

@@ -243,6 +243,7 @@ def run_ours(args, c):
         assert m.train_step(*batches[i], adam) == sf.SF_OK, m.error()
 
     m.sync()  # no warm-up update runs into the timed region
+    m.trace()  # start the host timeline at the timed region
     # ---- device-clock region (CUDA events, host Adam included): K steps
     m.set_timing(True)
     clocks = ClockSampler(local)
@@ -259,6 +260,7 @@ def run_ours(args, c):
         stats.append(m.stats())
     m.sync()  # the last step's host updates belong to the timed work
     e1.record()
+    timeline = m.trace()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -302,6 +304,9 @@ def run_ours(args, c):
     t_tensor = F_exec / (bf16_sust * 1e12)
     t_link = (h2d + d2h) / (link["bidir"] * 1e9)
     t_roof = max(t_tensor, t_link)
+    if args.trace:
+        with open(args.trace, "w") as f:
+            json.dump(timeline, f)
     if rank != 0:
         return
     cpu = None
@@ -409,6 +414,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sync-updates", action="store_true",
                     help="finish every host update before a step returns (no cross-step overlap)")
+    ap.add_argument("--trace", default="", help="write the host timeline of the timed steps (JSON)")
     ap.add_argument("--op", default="", choices=["", "attn_fwd", "attn_bwd", "gemm"],
                     help="time one kernel instead of the training step")
     ap.add_argument("--shape", default="16384,6144,4096", help="M,N,K for --op gemm")

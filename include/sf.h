@@ -181,6 +181,20 @@ int sf_set_timing(sf_ctx* ctx, int32_t enabled);
 /* Counters of the last step. */
 int sf_get_stats(const sf_ctx* ctx, sf_stats* out);
 
+/* Host timeline of the engine, for showing overlap: one record per event,
+ * t_ms from context creation (steady clock).  kind: 1 step begins, 2 batch
+ * gathered, 3 wait for a unit's update begins, 4 that wait ends, 5 update task
+ * begins (unit), 6 update task ends (unit), 7 the step's GPU work is done,
+ * 8 step returns.  unit: layer index or SF_UNIT_*, -9 when not applicable.
+ * The last 8192 records are kept; sf_get_trace copies up to cap of them
+ * (oldest first) into out, sets *n and clears the record. */
+typedef struct {
+  double t_ms;
+  int32_t kind;
+  int32_t unit;
+} sf_trace_event;
+int sf_get_trace(sf_ctx* ctx, sf_trace_event* out, int32_t cap, int32_t* n);
+
 /* Host-side fault injection for tests (no GPU fault is ever made):
  *   what = 1: the Adam worker fails on unit `arg` of the next step;
  *   what = 2: the Adam worker sleeps `arg` ms before each update;

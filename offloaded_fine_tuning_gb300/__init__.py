@@ -59,6 +59,13 @@ class Stats(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class TraceEvent(ctypes.Structure):
+    _fields_ = [("t_ms", ctypes.c_double), ("kind", ctypes.c_int32), ("unit", ctypes.c_int32)]
+
+
+TRACE_KINDS = {1: "step_begin", 2: "gathered", 3: "wait_unit_begin", 4: "wait_unit_end",
+               5: "update_begin", 6: "update_end", 7: "gpu_done", 8: "step_return"}
+
 _lib = None
 
 _VP, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -76,6 +83,7 @@ _SIGS = {
     "sf_set_timing": (ctypes.c_int, [_VP, _I32]),
     "sf_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(Stats)]),
     "sf_debug_inject": (ctypes.c_int, [_VP, _I32, _I32]),
+    "sf_get_trace": (ctypes.c_int, [_VP, ctypes.POINTER(TraceEvent), _I32, ctypes.POINTER(_I32)]),
     "sf_op_gemm": (ctypes.c_int, [_I32, _I32, _I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64,
                                   _VP, _I64, _F32, _VP]),
     "sf_op_rmsnorm_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _F32, _VP]),
@@ -220,6 +228,13 @@ class Model:
         s = Stats()
         _check(lib().sf_get_stats(self.h, ctypes.byref(s)), self.h, "sf_get_stats")
         return s.as_dict()
+
+    def trace(self, cap: int = 8192) -> list:
+        """Host timeline records since the last call: (t_ms, kind name, unit)."""
+        buf = (TraceEvent * cap)()
+        n = _I32()
+        _check(lib().sf_get_trace(self.h, buf, cap, ctypes.byref(n)), self.h, "sf_get_trace")
+        return [(buf[i].t_ms, TRACE_KINDS.get(buf[i].kind, buf[i].kind), buf[i].unit) for i in range(n.value)]
 
     def inject(self, what: int, arg: int = 0):
         _check(lib().sf_debug_inject(self.h, what, arg), self.h, "sf_debug_inject")

@@ -44,10 +44,17 @@ struct AttCfg {
   static constexpr int OFF_K = TILE;
   static constexpr int OFF_V = OFF_K + 2 * TILE;
   static constexpr int OFF_P = OFF_V + 2 * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * 16384;  // P: 128 rows x 128 keys
-  static constexpr int NBAR = 12;
+  static constexpr int OFF_BAR = OFF_P + 2 * 32768;  // P: 2 buffers of 128 rows x 128 keys
+  static constexpr int NBAR = 14;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
+
+// 2^x on the special-function unit (relative error ~2^-22, flushes denormals).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -80,7 +87,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   auto kv_empty = [&](int s) { return b0 + 8u * (3 + s); };
   auto s_full = [&](int s) { return b0 + 8u * (5 + s); };
   auto s_free = [&](int s) { return b0 + 8u * (7 + s); };
-  const uint32_t p_full = b0 + 8u * 9, o_done = b0 + 8u * 10, drain = b0 + 8u * 11;
+  auto p_full = [&](int s) { return b0 + 8u * (9 + s); };
+  auto o_done = [&](int s) { return b0 + 8u * (11 + s); };
+  const uint32_t drain = b0 + 8u * 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -101,8 +110,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       mbar_init(s_full(s), 1);
       mbar_init(s_free(s), 128);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(p_full(s), 128);
+      mbar_init(o_done(s), 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -166,16 +177,16 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       if (j > 0) {  // O += P_{j-1} V_{j-1}
         const int jp = j - 1, st = jp & 1;
-        if (!mbar_wait(p_full, jp & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(p_full(st), (jp >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           umma_bf16(tmem_base + O_COL,
-                    smem_desc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(sP + st * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                     smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
                     (jp > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(o_done);
+        umma_commit(o_done(st));
         umma_commit(kv_empty(st));
       }
     }
@@ -191,6 +202,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int row = quarter * 32 + lane;
     const int q = q0 + row;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    // m: the row max in log2 units that the exponentials are taken against.
+    // It only moves when a block's max exceeds it by more than 8 (a factor of
+    // 256), so O in TMEM is rarely rescaled; the result O / l does not depend
+    // on the choice of m.
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
@@ -209,46 +224,53 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(s_free(st));
-      const bool diag = (j == qb);
       float mx = -INFINITY;
+      if (j == qb) {  // diagonal block: keys after the query are masked
+        const int lim = q - j * 128;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        float v = s[i] * scale_log2;
-        if (diag && j * 128 + i > q) v = -INFINITY;
-        s[i] = v;
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < 128; ++i) {
+          if (i > lim) s[i] = -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
       }
-      const float m_new = fmaxf(m, mx);
+      mx *= scale_log2;  // the scale is positive: the max commutes with it
+      const bool grow = mx > m + 8.f;
+      const float m_new = grow ? mx : m;
+      const float corr = ex2_approx(m - m_new);  // 1 without growth, 0 on the first block
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // P_{j-1} V_{j-1} must have landed before the O row is rescaled
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+          tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
+        }
+        tmem_st_wait();
+      }
       float ps = 0.f;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        const float p = exp2f(s[i] - m_new);
+        const float p = ex2_approx(fmaf(s[i], scale_log2, -m_new));
         s[i] = p;
         ps += p;
       }
-      const float corr = exp2f(m - m_new);  // 0 on the first block (m = -inf)
-      if (j > 0) {
-        // P_{j-1} V_{j-1} is done: the P buffer is free and the O row is current
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, m_new > m)) {
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-            tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
-          }
-          tmem_st_wait();
-        }
-      }
       l = l * corr + ps;
       m = m_new;
+      if (j >= 2) {  // P buffer st was read by P_{j-2} V_{j-2}
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done(st), ((j - 2) >> 1) & 1, abort_flag));
+        if (!ok) break;
+      }
       // row of P, bf16, in the 128-byte swizzled K-major layout
-      const uint32_t prow = sP + (uint32_t)row * 128u;
+      const uint32_t prow = sP + st * 32768 + (uint32_t)row * 128u;
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
@@ -263,9 +285,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full(st));
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, abort_flag));
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
@@ -473,18 +495,31 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int tid = threadIdx.x - 64;  // 0..127
     const int64_t ldo = (int64_t)Hq * HD;
     bool ok = true;
+    // lse (log2 units) and D of the query block, one value per thread, loaded
+    // one block ahead so the global latency is off the critical path
+    auto fetch = [&](int it_, float& lv, float& dv) {
+      lv = 0.f;
+      dv = 0.f;
+      if (it_ >= n_it) return;
+      const int h_ = g * grp + it_ / (nqb - j);
+      const int q_ = (j + it_ % (nqb - j)) * 128 + tid;
+      if (q_ < S) {
+        const int64_t o = ((int64_t)b * Hq + h_) * S + q_;
+        lv = lse[o] * 1.4426950408889634f;
+        dv = delta[o];
+      }
+    };
+    float next_l, next_d;
+    fetch(0, next_l, next_d);
     for (int it = 0; it < n_it; ++it) {
       const int h = g * grp + it / (nqb - j);
       const int q0 = (j + it % (nqb - j)) * 128;
       const uint32_t ph = it & 1;
       float* bL = sLD + (it & 1) * 256;
       float* bD = bL + 128;
-      {
-        const int q = q0 + tid;
-        const int64_t o = ((int64_t)b * Hq + h) * S + q;
-        bL[tid] = (q < S) ? lse[o] * 1.4426950408889634f : 0.f;
-        bD[tid] = (q < S) ? delta[o] : 0.f;
-      }
+      bL[tid] = next_l;
+      bD[tid] = next_d;
+      fetch(it + 1, next_l, next_d);
       asm volatile("bar.sync 1, 128;" ::: "memory");
       ok = __all_sync(0xffffffffu, mbar_wait(sp_full, ph, abort_flag));
       if (!ok) break;
@@ -502,7 +537,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           const int qq = 32 * c + e;
           const int q = q0 + qq;
           float pv = 0.f;
-          if (q < S && key <= q) pv = exp2f(__uint_as_float(sr[e]) * scale_log2 - bL[qq]);
+          if (q < S && key <= q) pv = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -bL[qq]));
           p[e] = pv;
           ds[e] = pv * (__uint_as_float(dr[e]) - bD[qq]);
         }

@@ -226,6 +226,12 @@ struct sf_ctx {
   std::atomic<int> inject_fail_unit{-1000};
   std::atomic<int> inject_sleep_ms{0};
 
+  // host timeline (sf_get_trace)
+  std::mutex tr_m;
+  std::vector<sf_trace_event> trace;
+  size_t tr_head = 0;
+  Clock::time_point t0 = Clock::now();
+
   bool have_loss = false;
   float loss = 0.f;
   int64_t wait_ms = 300000;
@@ -241,6 +247,18 @@ struct sf_ctx {
 };
 
 namespace {
+
+void trace(sf_ctx* ctx, int kind, int unit) {
+  const double t = std::chrono::duration<double, std::milli>(Clock::now() - ctx->t0).count();
+  std::lock_guard<std::mutex> l(ctx->tr_m);
+  constexpr size_t kCap = 8192;
+  if (ctx->trace.size() < kCap) {
+    ctx->trace.push_back({t, kind, unit});
+  } else {
+    ctx->trace[ctx->tr_head] = {t, kind, unit};
+    ctx->tr_head = (ctx->tr_head + 1) % kCap;
+  }
+}
 
 #define CK(call)                                                                     \
   do {                                                                               \
@@ -306,6 +324,50 @@ int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
 }
 
 // ------------------------------------------------------------------ Adam on host
+// The element loops take restrict-qualified pointers so that the compiler
+// vectorises them (the update is bound by host memory bandwidth).
+struct AdamK {
+  float b1, b2, lr, eps, wd, bc1, bc2;
+};
+
+void adam_bf16_span(uint16_t* __restrict p, float* __restrict w, float* __restrict m,
+                    float* __restrict v, int64_t b, int64_t e, const AdamK k) {
+  for (int64_t i = b; i < e; ++i) {
+    const float g = bf2f(p[i]);
+    const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
+    const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
+    float th = w[i];
+    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    m[i] = mi;
+    v[i] = vi;
+    w[i] = th;
+    p[i] = f2bf(th);
+  }
+}
+
+void adam_f32_span(const float* __restrict g, float* __restrict w, float* __restrict m,
+                   float* __restrict v, int64_t b, int64_t e, const AdamK k) {
+  for (int64_t i = b; i < e; ++i) {
+    const float gi = g[i];
+    const float mi = k.b1 * m[i] + (1.f - k.b1) * gi;
+    const float vi = k.b2 * v[i] + (1.f - k.b2) * gi * gi;
+    float th = w[i];
+    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    m[i] = mi;
+    v[i] = vi;
+    w[i] = th;
+  }
+}
+
+void refresh_bf16_span(uint16_t* __restrict p, const float* __restrict w, int64_t b, int64_t e) {
+  for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
+}
+
+AdamK adam_consts(const sf_adam& a, int64_t step_t) {
+  return {a.beta1, a.beta2, a.lr, a.eps, a.weight_decay, 1.f - std::pow(a.beta1, (float)step_t),
+          1.f - std::pow(a.beta2, (float)step_t)};
+}
+
 // One unit: optional copy of the gradients, then either the Adam update of the
 // fp32 master (refreshing the bf16 pack in place) or, without an optimizer, a
 // refresh of the pack from the unchanged master.
@@ -322,28 +384,15 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_
   uint16_t* p = hu.pack;
   float* w = hu.master.get();
   if (!adam_on) {
-    ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
-      for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
-    });
+    ctx->pool->parallel_for(hu.elems, 1 << 16,
+                            [p, w](int64_t b, int64_t e) { refresh_bf16_span(p, w, b, e); });
     return;
   }
-  const float b1 = a.beta1, b2 = a.beta2, lr = a.lr, eps = a.eps, wd = a.weight_decay;
-  const float bc1 = 1.f - std::pow(b1, (float)step_t);
-  const float bc2 = 1.f - std::pow(b2, (float)step_t);
+  const AdamK k = adam_consts(a, step_t);
   float* m = hu.m.get();
   float* v = hu.v.get();
-  ctx->pool->parallel_for(hu.elems, 1 << 16, [&](int64_t b, int64_t e) {
-    for (int64_t i = b; i < e; ++i) {
-      const float g = bf2f(p[i]);
-      const float mi = b1 * m[i] + (1.f - b1) * g;
-      const float vi = b2 * v[i] + (1.f - b2) * g * g;
-      float th = w[i];
-      th = th - lr * wd * th - lr * (mi / bc1) / (std::sqrt(vi / bc2) + eps);
-      m[i] = mi;
-      v[i] = vi;
-      w[i] = th;
-      p[i] = f2bf(th);
-    }
+  ctx->pool->parallel_for(hu.elems, 1 << 16, [p, w, m, v, k](int64_t b, int64_t e) {
+    adam_bf16_span(p, w, m, v, b, e, k);
   });
 }
 
@@ -371,22 +420,13 @@ void embed_update(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
     }
   });
   if (!adam_on) return;
-  const float bc1 = 1.f - std::pow(a.beta1, (float)step_t);
-  const float bc2 = 1.f - std::pow(a.beta2, (float)step_t);
+  const AdamK k = adam_consts(a, step_t);
   float* w = ctx->E.get();
   float* m = ctx->Em.get();
   float* v = ctx->Ev.get();
-  ctx->pool->parallel_for(V * d, 1 << 16, [&](int64_t b, int64_t e) {
-    for (int64_t i = b; i < e; ++i) {
-      const float gi = dE[i];
-      const float mi = a.beta1 * m[i] + (1.f - a.beta1) * gi;
-      const float vi = a.beta2 * v[i] + (1.f - a.beta2) * gi * gi;
-      float th = w[i];
-      th = th - a.lr * a.weight_decay * th - a.lr * (mi / bc1) / (std::sqrt(vi / bc2) + a.eps);
-      m[i] = mi;
-      v[i] = vi;
-      w[i] = th;
-    }
+  const float* gE = dE;
+  ctx->pool->parallel_for(V * d, 1 << 16, [gE, w, m, v, k](int64_t b, int64_t e) {
+    adam_f32_span(gE, w, m, v, b, e, k);
   });
 }
 
@@ -418,6 +458,7 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
     return;
   }
   const auto t0 = Clock::now();
+  trace(ctx, 5, t.unit);
   const bool retain = ctx->cfg.retain_grads != 0;
   if (t.unit >= 0) {
     host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t);
@@ -428,6 +469,7 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
     host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t);
   }
   ctx->adam_ms += std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+  trace(ctx, 6, t.unit);
   finish_task(ctx, t, SF_OK, std::string());
 }
 
@@ -491,6 +533,12 @@ void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev) {
 
 // Bounded wait until the host update of one unit (posted by an earlier step) is done.
 int wait_unit(sf_ctx* ctx, int unit) {
+  trace(ctx, 3, unit);
+  struct End {
+    sf_ctx* c;
+    int u;
+    ~End() { trace(c, 4, u); }
+  } end{ctx, unit};
   std::unique_lock<std::mutex> l(ctx->aq_m);
   const int u = unit_slot(ctx, unit);
   const bool ok = ctx->aq_done_cv.wait_for(l, std::chrono::milliseconds(ctx->wait_ms),
@@ -916,6 +964,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   const int64_t T = (int64_t)B * S, d = ctx->d, V = ctx->V;
   const int L = ctx->L, R = ctx->R;
   const auto t_host0 = Clock::now();
+  trace(ctx, 1, -9);
   // ---- validate on the host, count valid labels
   int64_t n_valid = 0;
   for (int64_t t = 0; t < T; ++t) {
@@ -965,6 +1014,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     });
     std::memcpy(ctx->lab_pin, labels, (size_t)T * 4);
   }
+  trace(ctx, 2, -9);
   CK(cudaEventRecord(ctx->ev_start, ctx->sC));
   CK(cudaStreamWaitEvent(ctx->sU, ctx->ev_start, 0));
   CK(cudaMemcpyAsync(ctx->x0b, ctx->x0_pin, (size_t)T * d * 2, cudaMemcpyHostToDevice, ctx->sU));
@@ -1056,6 +1106,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     return st;
   }
   const auto t_gpu_done = Clock::now();
+  trace(ctx, 7, -9);
   if (*ctx->err_pin != 0) {
     ctx->set_err("device wait limit reached in a kernel (code %d)", *ctx->err_pin);
     ctx->poisoned = true;
@@ -1092,6 +1143,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   ctx->stats.host_wait_ms = std::chrono::duration<double, std::milli>(Clock::now() - t_gpu_done).count();
   ctx->stats.kernel_launches = ctx->launches;
   (void)t_host0;
+  trace(ctx, 8, -9);
   return SF_OK;
 }
 
@@ -1302,6 +1354,18 @@ int sf_set_timing(sf_ctx* ctx, int32_t enabled) {
 int sf_get_stats(const sf_ctx* ctx, sf_stats* out) {
   if (!ctx || !out) return SF_EINVAL;
   *out = ctx->stats;
+  return SF_OK;
+}
+
+int sf_get_trace(sf_ctx* ctx, sf_trace_event* out, int32_t cap, int32_t* n) {
+  if (!ctx || !n || cap < 0 || (cap > 0 && !out)) return SF_EINVAL;
+  std::lock_guard<std::mutex> l(ctx->tr_m);
+  const size_t sz = ctx->trace.size();
+  const size_t take = std::min<size_t>(sz, (size_t)cap);
+  for (size_t i = 0; i < take; ++i) out[i] = ctx->trace[(ctx->tr_head + sz - take + i) % sz];
+  *n = (int32_t)take;
+  ctx->trace.clear();
+  ctx->tr_head = 0;
   return SF_OK;
 }
 

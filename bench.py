@@ -104,6 +104,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    replica sets the whole job's time); identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(tokens_per_rank_step, steps, world, slowest_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / (slowest_ms / 1e3)
+
+
 def link_probe(torch, nbytes=1 << 30):
     """Pinned host<->device GB/s: H2D, D2H and both directions at once."""
     h1 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
@@ -283,13 +299,10 @@ def run_ours(args, c):
     m.sync()
     e2e_s = time.perf_counter() - t0
 
-    times = torch.tensor([dev_ms, e2e_s * 1e3], dtype=torch.float64, device="cuda")
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    dev_ms, e2e_ms = float(times[0]), float(times[1])
+    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_s * 1e3], dist, device="cuda")
     ms_step = dev_ms / args.steps
-    value = world * T * args.steps / (dev_ms / 1e3)
-    e2e = world * T * args.steps / (e2e_ms / 1e3)
+    value = job_throughput(T, args.steps, world, dev_ms)
+    e2e = job_throughput(T, args.steps, world, e2e_ms)
 
     gemm_ms = sum(s["gemm_ms"] for s in stats)
     gemm_fl = sum(s["gemm_flops"] for s in stats)

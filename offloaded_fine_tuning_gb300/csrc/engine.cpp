@@ -135,6 +135,11 @@ struct HostUnit {
   std::vector<uint16_t> retained;  // last step's gradients (retain_grads)
 };
 
+// Adam constants of one step (bias corrections folded in by adam_consts).
+struct AdamK {
+  float b1, b2, lr, eps, wd, bc1, bc2;
+};
+
 // (offset in the caller's unpadded order, offset in the padded pack, count)
 struct Seg {
   int64_t src, dst, n;
@@ -209,10 +214,20 @@ struct sf_ctx {
     bool adam_on;   // the step's optimizer settings, fixed when the task is posted
     sf_adam adam;
     int64_t t;
+    int arg;        // row range of a deferred embedding-update task
   };
   std::deque<Task> aq;
   int aq_pending = 0;
-  std::vector<char> unit_pending;  // [L + 2]: layers, LM head + final norm (L), embedding (L + 1)
+  // pending tasks per unit slot [L + 3]: layers, LM head + final norm (L),
+  // embedding gradient (L + 1), deferred embedding-row updates (L + 2)
+  std::vector<int> unit_pending;
+  // A deferred embedding update: e_state[row] is 0 (to update), 1 (being
+  // updated) or 2 (done), so every row is updated exactly once whether the
+  // next step's gather or a background task reaches it first.
+  std::unique_ptr<std::atomic<uint8_t>[]> e_state;
+  bool e_pending = false;
+  AdamK e_k{};
+  std::vector<int32_t> e_rows;  // rows of dE that hold the last step's gradient
   std::vector<int32_t> tok_copy;   // tokens of the step whose embedding update is pending
   bool async = false;
   int aq_status = SF_OK;
@@ -326,9 +341,6 @@ int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
 // ------------------------------------------------------------------ Adam on host
 // The element loops take restrict-qualified pointers so that the compiler
 // vectorises them (the update is bound by host memory bandwidth).
-struct AdamK {
-  float b1, b2, lr, eps, wd, bc1, bc2;
-};
 
 void adam_bf16_span(uint16_t* __restrict p, float* __restrict w, float* __restrict m,
                     float* __restrict v, int64_t b, int64_t e, const AdamK k) {
@@ -396,38 +408,72 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_
   });
 }
 
+constexpr int kUnitEmbedRest = -10;  // internal: background embedding-row updates
+constexpr int kEmbedRestTasks = 16;
+
 int unit_slot(const sf_ctx* ctx, int unit) {
   if (unit >= 0) return unit;
-  return unit == SF_UNIT_EMBED ? ctx->L + 1 : ctx->L;  // LM head and final norm share a task
+  if (unit == SF_UNIT_EMBED) return ctx->L + 1;
+  if (unit == kUnitEmbedRest) return ctx->L + 2;
+  return ctx->L;  // LM head and final norm share a task
 }
 
-// Embedding: zero dE, scatter-add the bf16 input gradient by column ranges (no
-// races), then the Adam update of the fp32 embedding (no bf16 copy: the
-// gather reads the fp32 master).
-void embed_update(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
-  const int64_t d = ctx->d, V = ctx->V, T = (int64_t)ctx->tok_copy.size();
-  const int32_t* tokens = ctx->tok_copy.data();
-  float* dE = ctx->dE.get();
-  const uint16_t* g = ctx->x0_pin;
-  ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t b, int64_t e) {
-    std::memset(dE + b, 0, (size_t)(e - b) * 4);
+// Adam update of embedding row r, exactly once per pending update.
+void e_update_row(sf_ctx* ctx, int64_t r) {
+  std::atomic<uint8_t>& st = ctx->e_state[r];
+  uint8_t expect = 0;
+  if (st.compare_exchange_strong(expect, 1, std::memory_order_acq_rel)) {
+    const int64_t d = ctx->d, o = r * d;
+    adam_f32_span(ctx->dE.get() + o, ctx->E.get() + o, ctx->Em.get() + o, ctx->Ev.get() + o, 0, d,
+                  ctx->e_k);
+    st.store(2, std::memory_order_release);
+  } else {
+    while (st.load(std::memory_order_acquire) != 2) std::this_thread::yield();
+  }
+}
+
+void e_update_rows(sf_ctx* ctx, int64_t r0, int64_t r1) {
+  ctx->pool->parallel_for(r1 - r0, 64, [ctx, r0](int64_t b, int64_t e) {
+    for (int64_t r = r0 + b; r < r0 + e; ++r) e_update_row(ctx, r);
   });
-  ctx->pool->parallel_for(d, 64, [&](int64_t c0, int64_t c1) {
+}
+
+void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg = 0);
+
+// Embedding gradient: zero the rows of dE the previous gradient touched,
+// scatter-add the bf16 input gradient (by column ranges: no races).  The Adam
+// update of the embedding is then deferred: the next step's gather updates the
+// rows its tokens need, and background tasks of the lowest priority update
+// the rest while the update thread would otherwise wait for gradients.
+void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
+  const int64_t d = ctx->d, V = ctx->V, T = (int64_t)ctx->tok_copy.size();
+  if (ctx->e_pending) e_update_rows(ctx, 0, V);  // finish a previous update first
+  ctx->e_pending = false;
+  float* dE = ctx->dE.get();
+  {
+    const int32_t* rows = ctx->e_rows.data();
+    ctx->pool->parallel_for((int64_t)ctx->e_rows.size(), 64, [rows, dE, d](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i) std::memset(dE + (int64_t)rows[i] * d, 0, (size_t)d * 4);
+    });
+  }
+  const int32_t* tokens = ctx->tok_copy.data();
+  const uint16_t* g = ctx->x0_pin;
+  ctx->pool->parallel_for(d, 64, [tokens, dE, g, T, d](int64_t c0, int64_t c1) {
     for (int64_t t = 0; t < T; ++t) {
-      float* row = dE + (int64_t)tokens[t] * d;
-      const uint16_t* gr = g + t * d;
+      float* __restrict row = dE + (int64_t)tokens[t] * d;
+      const uint16_t* __restrict gr = g + t * d;
       for (int64_t j = c0; j < c1; ++j) row[j] += bf2f(gr[j]);
     }
   });
+  ctx->e_rows.assign(ctx->tok_copy.begin(), ctx->tok_copy.end());
+  std::sort(ctx->e_rows.begin(), ctx->e_rows.end());
+  ctx->e_rows.erase(std::unique(ctx->e_rows.begin(), ctx->e_rows.end()), ctx->e_rows.end());
   if (!adam_on) return;
-  const AdamK k = adam_consts(a, step_t);
-  float* w = ctx->E.get();
-  float* m = ctx->Em.get();
-  float* v = ctx->Ev.get();
-  const float* gE = dE;
-  ctx->pool->parallel_for(V * d, 1 << 16, [gE, w, m, v, k](int64_t b, int64_t e) {
-    adam_f32_span(gE, w, m, v, b, e, k);
-  });
+  ctx->e_k = adam_consts(a, step_t);
+  for (int64_t r = 0; r < V; ++r) ctx->e_state[r].store(0, std::memory_order_relaxed);
+  std::atomic_thread_fence(std::memory_order_release);
+  ctx->e_pending = true;
+  for (int i = 0; i < kEmbedRestTasks; ++i) post_task(ctx, kUnitEmbedRest, nullptr, i);
 }
 
 void finish_task(sf_ctx* ctx, const sf_ctx::Task& t, int st, const std::string& why) {
@@ -437,7 +483,7 @@ void finish_task(sf_ctx* ctx, const sf_ctx::Task& t, int st, const std::string& 
       ctx->aq_status = st;
       ctx->aq_err = why;
     }
-    ctx->unit_pending[unit_slot(ctx, t.unit)] = 0;
+    --ctx->unit_pending[unit_slot(ctx, t.unit)];
     --ctx->aq_pending;
   }
   ctx->aq_done_cv.notify_all();
@@ -446,7 +492,7 @@ void finish_task(sf_ctx* ctx, const sf_ctx::Task& t, int st, const std::string& 
 void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   if (ctx->inject_sleep_ms.load() > 0)
     std::this_thread::sleep_for(std::chrono::milliseconds(ctx->inject_sleep_ms.load()));
-  if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED) {
+  if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED && t.unit != kUnitEmbedRest) {
     // the gradients are dropped: put the unchanged weights back into the pack
     if (t.unit >= 0) {
       host_update(ctx, ctx->layers[t.unit], false, false, t.adam, t.t);
@@ -463,7 +509,10 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   if (t.unit >= 0) {
     host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t);
   } else if (t.unit == SF_UNIT_EMBED) {
-    embed_update(ctx, t.adam_on, t.adam, t.t);
+    embed_grad(ctx, t.adam_on, t.adam, t.t);
+  } else if (t.unit == kUnitEmbedRest) {
+    const int64_t V = ctx->V;
+    e_update_rows(ctx, V * t.arg / kEmbedRestTasks, V * (t.arg + 1) / kEmbedRestTasks);
   } else {  // LM head and final norm
     host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t);
     host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t);
@@ -491,7 +540,7 @@ void adam_loop(sf_ctx* ctx) {
     }
     int best = -1;
     for (size_t i = 0; i < mine.size();) {
-      const cudaError_t r = cudaEventQuery(mine[i].ev);
+      const cudaError_t r = mine[i].ev ? cudaEventQuery(mine[i].ev) : cudaSuccess;  // null: no copy to wait for
       if (r == cudaSuccess) {
         if (best < 0 || mine[i].prio < mine[best].prio) best = (int)i;
         ++i;
@@ -519,13 +568,15 @@ void adam_loop(sf_ctx* ctx) {
   }
 }
 
-void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev) {
+void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg) {
   {
     std::lock_guard<std::mutex> l(ctx->aq_m);
-    const int prio = unit == SF_UNIT_EMBED ? -1 : (unit >= 0 ? unit : ctx->L);
+    const int prio = unit == SF_UNIT_EMBED ? -1
+                     : unit == kUnitEmbedRest ? ctx->L + 1
+                     : (unit >= 0 ? unit : ctx->L);
     ctx->aq.push_back({unit, ev, prio, Clock::now() + std::chrono::milliseconds(ctx->wait_ms),
-                       ctx->adam_on, ctx->adam_copy, ctx->adam_t});
-    ctx->unit_pending[unit_slot(ctx, unit)] = 1;
+                       ctx->adam_on, ctx->adam_copy, ctx->adam_t, arg});
+    ++ctx->unit_pending[unit_slot(ctx, unit)];
     ++ctx->aq_pending;
   }
   ctx->aq_cv.notify_one();
@@ -542,7 +593,7 @@ int wait_unit(sf_ctx* ctx, int unit) {
   std::unique_lock<std::mutex> l(ctx->aq_m);
   const int u = unit_slot(ctx, unit);
   const bool ok = ctx->aq_done_cv.wait_for(l, std::chrono::milliseconds(ctx->wait_ms),
-                                           [&] { return !ctx->unit_pending[u]; });
+                                           [&] { return ctx->unit_pending[u] == 0; });
   if (!ok) {
     ctx->set_err("timed out waiting for the host update of unit %d", unit);
     return SF_ETIMEOUT;
@@ -921,7 +972,10 @@ int init(sf_ctx* ctx) {
   RET(mk(&ctx->ev_start, true));
   RET(mk(&ctx->ev_end, true));
   RET(mk(&ctx->ev_end_d, false));
-  ctx->unit_pending.assign(L + 2, 0);
+  ctx->unit_pending.assign(L + 3, 0);
+  ctx->e_state.reset(new (std::nothrow) std::atomic<uint8_t>[(size_t)V]);
+  if (!ctx->e_state) return SF_ENOMEM;
+  for (int64_t r = 0; r < V; ++r) ctx->e_state[r].store(2, std::memory_order_relaxed);
   ctx->async = cf.async_update != 0;
   ctx->adam_thread = std::thread(adam_loop, ctx);
   return SF_OK;
@@ -1005,8 +1059,10 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   {
     const float* E = ctx->E.get();
     uint16_t* x0 = ctx->x0_pin;
+    const bool upd = ctx->e_pending;  // rows still owed the previous step's update
     ctx->pool->parallel_for(T, 64, [&](int64_t b, int64_t e) {
       for (int64_t t = b; t < e; ++t) {
+        if (upd) e_update_row(ctx, tokens[t]);
         const float* src = E + (int64_t)tokens[t] * d;
         uint16_t* dst = x0 + t * d;
         for (int64_t j = 0; j < d; ++j) dst[j] = f2bf(src[j]);

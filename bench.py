@@ -248,6 +248,7 @@ def run_ours(args, c):
     sf.lib(build_if_needed=True)
     bf16_peak, bf16_sust, hbm, peak_src = peaks()
     link = link_probe(torch)
+    host_gbs = sf.probe_host_bandwidth(0, 8 << 30)
 
     m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
@@ -317,6 +318,13 @@ def run_ours(args, c):
     t_tensor = F_exec / (bf16_sust * 1e12)
     t_link = (h2d + d2h) / (link["bidir"] * 1e9)
     t_roof = max(t_tensor, t_link)
+    # host memory: the Adam update of every unit (28 B per layer / LM-head
+    # parameter: bf16 grad in, fp32 master, m, v read and written, bf16 out;
+    # 24 B per embedding parameter, whose gradient is fp32) plus the DMA copies
+    P_l = inputs.unit_numel(c, 0)
+    adam_bytes = 28.0 * (c.n_layers * P_l + c.vocab * c.hidden + c.hidden) + 24.0 * c.vocab * c.hidden
+    host_bytes = adam_bytes + h2d + d2h
+    t_host = host_bytes / (host_gbs * 1e9)
     if args.trace:
         with open(args.trace, "w") as f:
             json.dump(timeline, f)
@@ -346,6 +354,9 @@ def run_ours(args, c):
         "step_roofline": {"flops": F_exec, "t_tensor_ms": t_tensor * 1e3, "h2d_bytes": h2d,
                           "d2h_bytes": d2h, "link_gbs": link, "t_link_ms": t_link * 1e3,
                           "t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                          "host_memory": {"bytes": host_bytes, "adam_bytes": adam_bytes,
+                                          "probe_gbs": host_gbs, "t_ms": t_host * 1e3,
+                                          "frac": t_host * 1e3 / ms_step},
                           "gpu_busy_ms": gpu_step,
                           "attn_tflops": attn_fl / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None,
                           "host_adam_ms": statistics.mean(s["host_adam_ms"] for s in stats),

@@ -195,6 +195,13 @@ typedef struct {
 } sf_trace_event;
 int sf_get_trace(sf_ctx* ctx, sf_trace_event* out, int32_t cap, int32_t* n);
 
+/* Host memory bandwidth with the access pattern of the host Adam update:
+ * per element, read 2 + 12 bytes and write 12 + 2 bytes, over `bytes` bytes
+ * of freshly allocated host memory, on `threads` threads (0 = all cores);
+ * best of three passes, in GB/s of read plus written bytes.  Allocates and
+ * frees its own buffers.  Errors: SF_EINVAL, SF_ENOMEM. */
+int sf_probe_host_bandwidth(int32_t threads, int64_t bytes, double* gbs);
+
 /* Host-side fault injection for tests (no GPU fault is ever made):
  *   what = 1: the Adam worker fails on unit `arg` of the next step;
  *   what = 2: the Adam worker sleeps `arg` ms before each update;

@@ -84,6 +84,7 @@ _SIGS = {
     "sf_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(Stats)]),
     "sf_debug_inject": (ctypes.c_int, [_VP, _I32, _I32]),
     "sf_get_trace": (ctypes.c_int, [_VP, ctypes.POINTER(TraceEvent), _I32, ctypes.POINTER(_I32)]),
+    "sf_probe_host_bandwidth": (ctypes.c_int, [_I32, _I64, ctypes.POINTER(ctypes.c_double)]),
     "sf_op_gemm": (ctypes.c_int, [_I32, _I32, _I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64,
                                   _VP, _I64, _F32, _VP]),
     "sf_op_rmsnorm_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _F32, _VP]),
@@ -302,6 +303,13 @@ def lce_workspace_bytes(n, v, chunk_rows) -> int:
 
 def op_lce(h, w, labels, n, d, v, n_valid, chunk_rows, workspace, loss, dh, dw, stream=0) -> int:
     return lib().sf_op_lce(h, w, labels, n, d, v, n_valid, chunk_rows, workspace, loss, dh, dw, _s(stream))
+
+
+def probe_host_bandwidth(threads: int = 0, nbytes: int = 4 << 30) -> float:
+    """GB/s of host memory traffic with the host Adam's access pattern."""
+    out = ctypes.c_double()
+    _check(lib().sf_probe_host_bandwidth(threads, nbytes, ctypes.byref(out)), None, "sf_probe_host_bandwidth")
+    return out.value
 
 
 def device_error() -> int:

@@ -1413,6 +1413,47 @@ int sf_get_stats(const sf_ctx* ctx, sf_stats* out) {
   return SF_OK;
 }
 
+int sf_probe_host_bandwidth(int32_t threads, int64_t bytes, double* gbs) {
+  if (!gbs || bytes < (1 << 20) || threads < 0) return SF_EINVAL;
+  const int nt = threads > 0 ? threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  const int64_t n = bytes / 28;
+  std::unique_ptr<uint16_t[]> p(new (std::nothrow) uint16_t[n]);
+  std::unique_ptr<float[]> w(new (std::nothrow) float[n]), m(new (std::nothrow) float[n]),
+      v(new (std::nothrow) float[n]);
+  if (!p || !w || !m || !v) return SF_ENOMEM;
+  Pool pool(nt);
+  uint16_t* pp = p.get();
+  float *ww = w.get(), *mm = m.get(), *vv = v.get();
+  pool.parallel_for(n, 1 << 16, [pp, ww, mm, vv](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) {
+      pp[i] = 0x3c00;
+      ww[i] = 1.f;
+      mm[i] = 0.f;
+      vv[i] = 0.f;
+    }
+  });
+  double best = 1e30;
+  for (int rep = 0; rep < 3; ++rep) {
+    const auto t0 = Clock::now();
+    pool.parallel_for(n, 1 << 16, [pp, ww, mm, vv](int64_t b, int64_t e) {
+      uint16_t* __restrict P = pp;
+      float* __restrict W = ww;
+      float* __restrict M = mm;
+      float* __restrict Vv = vv;
+      for (int64_t i = b; i < e; ++i) {
+        const float g = bf2f(P[i]);
+        M[i] += g;
+        Vv[i] += g;
+        W[i] += g;
+        P[i] = f2bf(W[i]);
+      }
+    });
+    best = std::min(best, std::chrono::duration<double>(Clock::now() - t0).count());
+  }
+  *gbs = 28.0 * (double)n / best / 1e9;
+  return SF_OK;
+}
+
 int sf_get_trace(sf_ctx* ctx, sf_trace_event* out, int32_t cap, int32_t* n) {
   if (!ctx || !n || cap < 0 || (cap > 0 && !out)) return SF_EINVAL;
   std::lock_guard<std::mutex> l(ctx->tr_m);

@@ -213,3 +213,16 @@ def test_full_1p3b_step_properties():
     assert out[1][0] == loss
     for a, b in zip(out[0][1:], out[1][1:]):
         assert np.isfinite(a).all() and np.array_equal(a, b)
+
+
+def test_full_1p3b_step_matches_oracle():
+    """The whole 1.3B-shape step (24 layers, hidden 2048, 16 x 64 heads, FFN
+    5504, vocab 32000, 8 x 1024 tokens) against the float32 oracle, tensor by
+    tensor (the oracle needs a few minutes of the host's cores)."""
+    cfg = CONFIGS["1.3b"]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    with make_model(cfg, mast) as m:
+        assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+        loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg, dtype=np.float32)
+        compare(cfg, m, loss_ref, g_ref)

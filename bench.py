@@ -224,8 +224,9 @@ def run_reference(args, c):
 
 
 # ------------------------------------------------------------------ our arm
-def load_model(sf, c, ring, async_update):
-    cfg = sf.make_config(c, ring_slots=ring, retain_grads=0, async_update=async_update)
+def load_model(sf, c, ring, async_update, offload_activations=0):
+    cfg = sf.make_config(c, ring_slots=ring, retain_grads=0, async_update=async_update,
+                         offload_activations=offload_activations)
     m = sf.Model(cfg)
     for l in range(c.n_layers):
         m.load(l, inputs.layer_master(c, l))
@@ -250,7 +251,8 @@ def run_ours(args, c):
     link = link_probe(torch)
     host_gbs = sf.probe_host_bandwidth(0, 8 << 30)
 
-    m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1)
+    m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1,
+                   1 if args.offload_activations else 0)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
     # a fresh batch each step (rank-specific seeds for replicas)
     n_batches = args.warmup + 2 * args.steps
@@ -342,6 +344,7 @@ def run_ours(args, c):
                    "layers": c.n_layers, "ring_slots": args.ring or c.ring_slots,
                    "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
                    "host_updates": "synchronous" if args.sync_updates else "overlap next step",
+                   "activations": "sliding (host)" if args.offload_activations else "resident",
                    "l2": "inputs larger than L2 (each step streams every layer's weights and gradients)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps},
@@ -427,6 +430,62 @@ def run_op(args, c):
                       "peak_source": f"{src} bf16 burst (kernel timed alone)"}), flush=True)
 
 
+def run_sweep(args, c):
+    """The overlap condition of the layer-sliding backward: per decoder layer,
+    is the GPU backward (with its recompute) at least as long as copying the
+    layer's gradients to the host plus the host Adam update?  Measured per
+    batch size; the critical batch is the smallest one where it holds."""
+    import torch
+    import offloaded_fine_tuning_gb300 as sf
+    sf.lib(build_if_needed=True)
+    batches = [int(x) for x in args.sweep_batch.split(",")]
+    cfg = sf.make_config(c, max_batch=max(batches), ring_slots=args.ring or c.ring_slots,
+                         retain_grads=0, async_update=0)
+    m = sf.Model(cfg)
+    for l in range(c.n_layers):
+        m.load(l, inputs.layer_master(c, l))
+    for u in (UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD):
+        m.load(u, inputs.unit_master(c, u))
+    adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    rows = []
+    for B in batches:
+        cb = c.with_(batch=B)
+        tok, lab = inputs.tokens_and_labels(cb, seed=inputs.SEED_TOKENS + B)
+        m.set_timing(False)
+        for _ in range(args.warmup):
+            assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+        m.set_timing(True)
+        st = []
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+            st.append(m.stats())
+        wall = (time.perf_counter() - t0) / args.steps
+        avg = {k: statistics.mean(x[k] for x in st) for k in
+               ("fwd_layer_ms", "bwd_layer_ms", "d2h_layer_ms", "update_layer_ms")}
+        need = avg["d2h_layer_ms"] + avg["update_layer_ms"]
+        rows.append({"batch": B, "tokens": B * c.seq, **{k: round(v, 3) for k, v in avg.items()},
+                     "d2h_plus_update_ms": round(need, 3), "overlapped": avg["bwd_layer_ms"] >= need,
+                     "step_ms": round(wall * 1e3, 1), "tokens_per_s": round(B * c.seq / wall, 1)})
+        print(json.dumps(rows[-1]), flush=True)
+    crit = None
+    for a, b in zip(rows, rows[1:]):
+        fa = a["bwd_layer_ms"] - a["d2h_plus_update_ms"]
+        fb = b["bwd_layer_ms"] - b["d2h_plus_update_ms"]
+        if fa < 0 <= fb:
+            crit = a["batch"] + (b["batch"] - a["batch"]) * (-fa) / (fb - fa)
+    if crit is None and rows and rows[0]["overlapped"]:
+        crit = rows[0]["batch"]
+    if crit is None and len(rows) >= 2:  # extrapolate the (linear in batch) backward time
+        a, b = rows[-2], rows[-1]
+        slope = (b["bwd_layer_ms"] - a["bwd_layer_ms"]) / (b["batch"] - a["batch"])
+        if slope > 0:
+            crit = b["batch"] + (b["d2h_plus_update_ms"] - b["bwd_layer_ms"]) / slope
+    print(json.dumps({"sweep": "critical batch", "workload": c.name, "seq_len": c.seq,
+                      "critical_batch": crit, "condition": "T_bwd >= T_grad_d2h + T_update"}), flush=True)
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -436,8 +495,12 @@ def main():
     ap.add_argument("--ring", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--offload-activations", action="store_true",
+                    help="sliding activations: layer checkpoints go to pinned host memory")
     ap.add_argument("--sync-updates", action="store_true",
                     help="finish every host update before a step returns (no cross-step overlap)")
+    ap.add_argument("--sweep-batch", default="",
+                    help="comma-separated batch sizes: measure the backward overlap condition per layer")
     ap.add_argument("--trace", default="", help="write the host timeline of the timed steps (JSON)")
     ap.add_argument("--op", default="", choices=["", "attn_fwd", "attn_bwd", "gemm"],
                     help="time one kernel instead of the training step")
@@ -445,7 +508,9 @@ def main():
     ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])
     args = ap.parse_args()
     c = CONFIGS[args.config]
-    if args.op:
+    if args.sweep_batch:
+        run_sweep(args, c)
+    elif args.op:
         run_op(args, c)
     elif args.impl == "reference":
         run_reference(args, c)

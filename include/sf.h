@@ -83,7 +83,12 @@ typedef struct sf_ctx sf_ctx;
  *     still running overlap the next step (which waits for a unit's update
  *     just before that unit is needed).  Results are identical either way;
  *     sf_get_grads, sf_get_weights and sf_load_layer_weights wait for the
- *     pending updates first. */
+ *     pending updates first.
+ *   offload_activations: 0 = every layer's input checkpoint (fp32 [T, d])
+ *     stays in device memory; 1 = sliding activations: after a layer's
+ *     forward its checkpoint is copied to pinned host memory and brought back
+ *     just before that layer's backward, the device keeping a window of four
+ *     (results are identical). */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -95,6 +100,7 @@ typedef struct {
   int32_t adam_threads;
   int32_t wait_timeout_ms;
   int32_t async_update;
+  int32_t offload_activations;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -117,6 +123,11 @@ typedef struct {
   int64_t gemm_launches;
   int64_t kernel_launches; /* all kernels of this library launched in the step */
   int32_t timing_enabled;
+  /* per decoder layer, averaged over the step (timing enabled): */
+  double fwd_layer_ms;     /* forward compute (compute stream) */
+  double bwd_layer_ms;     /* recompute + backward compute (compute stream) */
+  double d2h_layer_ms;     /* gradient pack copy to the host (copy stream) */
+  double update_layer_ms;  /* host Adam of one layer (wall time, update thread) */
 } sf_stats;
 
 /* ---------------------------------------------------------------- model API */

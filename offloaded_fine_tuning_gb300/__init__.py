@@ -41,7 +41,8 @@ class Config(ctypes.Structure):
                  "max_batch", "max_seq", "ring_slots", "lce_chunk_rows", "retain_grads")] + \
                [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
                 ("device", ctypes.c_int32), ("adam_threads", ctypes.c_int32),
-                ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32)]
+                ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32),
+                ("offload_activations", ctypes.c_int32)]
 
 
 class Adam(ctypes.Structure):
@@ -53,7 +54,9 @@ class Stats(ctypes.Structure):
                 ("step_ms", "gemm_ms", "gemm_flops", "attn_ms", "attn_flops", "h2d_bytes",
                  "d2h_bytes", "host_adam_ms", "host_wait_ms")] + \
                [("gemm_launches", ctypes.c_int64), ("kernel_launches", ctypes.c_int64),
-                ("timing_enabled", ctypes.c_int32)]
+                ("timing_enabled", ctypes.c_int32)] + \
+               [(n, ctypes.c_double) for n in
+                ("fwd_layer_ms", "bwd_layer_ms", "d2h_layer_ms", "update_layer_ms")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -135,7 +138,7 @@ def _check(st: int, ctx=None, what=""):
 
 def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_grads=1,
                 lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0,
-                async_update=0) -> Config:
+                async_update=0, offload_activations=0) -> Config:
     """sf_config from a shape object with the fields of inputs.ModelConfig."""
     return Config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
                   n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, ffn=shape.ffn,
@@ -144,7 +147,7 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   ring_slots=ring_slots or shape.ring_slots, lce_chunk_rows=lce_chunk_rows,
                   retain_grads=retain_grads, rms_eps=shape.rms_eps, rope_base=shape.rope_base,
                   device=device, adam_threads=adam_threads, wait_timeout_ms=wait_timeout_ms,
-                  async_update=async_update)
+                  async_update=async_update, offload_activations=offload_activations)
 
 
 def unit_numel(cfg: Config, unit: int) -> int:

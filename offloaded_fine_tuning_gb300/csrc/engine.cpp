@@ -161,7 +161,10 @@ struct sf_ctx {
   // device
   std::vector<void*> dev_allocs;
   std::vector<bf16*> ring;  // R slots of 2 * pack_elems (weights, then grads)
-  float* X = nullptr;       // (L+1) * T * d checkpoints of the residual stream
+  float* X = nullptr;       // checkpoints of the residual stream: L+1 slots, or 4 when they slide
+  bool xoff = false;        // sliding activations: checkpoints live in pinned host memory
+  float* x_pin = nullptr;   // [L][Tmax * d] host copies of the checkpoints
+  cudaEvent_t ev_xused[4] = {}, ev_xfree[4] = {}, ev_xready[4] = {};
   bf16 *u = nullptr, *qkv = nullptr, *o = nullptr, *w2 = nullptr, *ab = nullptr, *mb = nullptr;
   float *rstd1 = nullptr, *rstd2 = nullptr, *rstdf = nullptr, *lse = nullptr, *h = nullptr;
   float *dX = nullptr, *dw2 = nullptr, *dh = nullptr, *du = nullptr, *dq_acc = nullptr,
@@ -234,6 +237,8 @@ struct sf_ctx {
   std::string aq_err;
   bool aq_stop = false;
   const sf_adam* cur_adam = nullptr;
+  double upd_layer_ms = 0.0;  // host Adam time of layer tasks since the last stats
+  int64_t upd_layer_n = 0;
   sf_adam adam_copy{};
   bool adam_on = false;
   int64_t adam_t = 0;
@@ -517,7 +522,13 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
     host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t);
     host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t);
   }
-  ctx->adam_ms += std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+  const double ms = std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+  ctx->adam_ms += ms;
+  if (t.unit >= 0) {
+    std::lock_guard<std::mutex> l(ctx->aq_m);
+    ctx->upd_layer_ms += ms;
+    ++ctx->upd_layer_n;
+  }
   trace(ctx, 6, t.unit);
   finish_task(ctx, t, SF_OK, std::string());
 }
@@ -630,7 +641,10 @@ struct Timed {
   int kind;
   double flops;
   cudaEvent_t b = nullptr, e = nullptr;
-  Timed(sf_ctx* c, int k, double f) : ctx(c), kind(k), flops(f) {
+  cudaStream_t st;
+  // kind: 0 GEMM, 1 attention, 2 layer forward, 3 layer backward, 4 gradient D2H
+  Timed(sf_ctx* c, int k, double f, cudaStream_t s = nullptr)
+      : ctx(c), kind(k), flops(f), st(s ? s : c->sC) {
     if (!ctx->timing) return;
     while (ctx->t_ev.size() < 2 * (ctx->t_used + 1)) {
       cudaEvent_t x;
@@ -642,10 +656,10 @@ struct Timed {
     ++ctx->t_used;
     ctx->t_kind.push_back(kind);
     ctx->t_flops.push_back(flops);
-    cudaEventRecord(b, ctx->sC);
+    cudaEventRecord(b, st);
   }
   ~Timed() {
-    if (e) cudaEventRecord(e, ctx->sC);
+    if (e) cudaEventRecord(e, st);
   }
 };
 
@@ -682,6 +696,14 @@ double attn_fwd_flops(int64_t B, int64_t S, int64_t Hq, int64_t hd) {
     int r_ = (x);                 \
     if (r_ != SF_OK) return r_;   \
   } while (0)
+
+// Device address of checkpoint l (the input of layer l; l = L is the final
+// hidden state).  Resident: one slot per checkpoint.  Sliding: a window of
+// four slots, the others in pinned host memory.
+float* xck(sf_ctx* c, int l, int64_t T) {
+  if (c->xoff) return c->X + (int64_t)(l % 4) * c->Tmax * c->d;
+  return c->X + (int64_t)l * T * c->d;
+}
 
 // ------------------------------------------------------------------ layer compute
 struct LayerW {
@@ -769,7 +791,7 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
 int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
   sf_ctx* ctx = c;
   const int64_t d = c->d, V = c->V;
-  const float* XL = c->X + (int64_t)c->L * T * d;
+  const float* XL = xck(c, c->L, T);
   sf::rmsnorm_fwd(XL, c->gf, c->hf, c->rstdf, T, (int)d, c->cfg.rms_eps, c->sC);
   const float inv_n = n_valid > 0 ? 1.f / (float)n_valid : 0.f;
   for (int64_t r0 = 0; r0 < T; r0 += c->chunk_rows) {
@@ -874,7 +896,8 @@ int init(sf_ctx* ctx) {
   bool ok = true;
   ctx->ring.resize(ctx->R);
   for (int s = 0; s < ctx->R && ok; ++s) ok = dalloc(ctx, &ctx->ring[s], 2 * ctx->pack_elems);
-  ok = ok && dalloc(ctx, &ctx->X, (L + 1) * T * d);
+  ctx->xoff = cf.offload_activations != 0;
+  ok = ok && dalloc(ctx, &ctx->X, (ctx->xoff ? 4 : L + 1) * T * d);
   ok = ok && dalloc(ctx, &ctx->u, T * d) && dalloc(ctx, &ctx->qkv, T * ctx->qkvdim) &&
        dalloc(ctx, &ctx->o, T * ctx->qdim) && dalloc(ctx, &ctx->w2, T * d) &&
        dalloc(ctx, &ctx->ab, T * 2 * F) && dalloc(ctx, &ctx->mb, T * F) &&
@@ -929,6 +952,7 @@ int init(sf_ctx* ctx) {
   ok = ok && host_unit(ctx->lm, V * d) && host_unit(ctx->fn, round_up(d, A));
   ok = ok && new_floats(ctx, ctx->E, V * d) && new_floats(ctx, ctx->Em, V * d) &&
        new_floats(ctx, ctx->Ev, V * d) && new_floats(ctx, ctx->dE, V * d);
+  if (ok && ctx->xoff) ok = halloc(ctx, &ctx->x_pin, L * T * d);
   ok = ok && halloc(ctx, &ctx->x0_pin, T * d) && halloc(ctx, &ctx->lab_pin, T) &&
        halloc(ctx, &ctx->loss_pin, 1) && halloc(ctx, &ctx->err_pin, 1);
   if (!ok) return SF_ENOMEM;
@@ -964,6 +988,11 @@ int init(sf_ctx* ctx) {
     RET(mk(&ctx->ev_grads[s], false));
   }
   for (int l = 0; l < L; ++l) RET(mk(&ctx->ev_d2h[l], false));
+  for (int i = 0; i < 4; ++i) {
+    RET(mk(&ctx->ev_xused[i], false));
+    RET(mk(&ctx->ev_xfree[i], false));
+    RET(mk(&ctx->ev_xready[i], false));
+  }
   RET(mk(&ctx->ev_x0, false));
   RET(mk(&ctx->ev_lm, false));
   RET(mk(&ctx->ev_head, false));
@@ -1078,7 +1107,8 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   CK(cudaEventRecord(ctx->ev_x0, ctx->sU));
   h2d += (double)T * d * 2 + (double)T * 4;
   CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_x0, 0));
-  sf::cast_bf16_f32(ctx->x0b, ctx->X, T * d, ctx->sC);
+  if (ctx->xoff) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_xused[0], 0));  // previous step's X_0
+  sf::cast_bf16_f32(ctx->x0b, xck(ctx, 0, T), T * d, ctx->sC);
   ctx->launches += 1;
 
   const size_t pack_bytes = (size_t)ctx->pack_elems * 2;
@@ -1106,16 +1136,41 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
       h2d += (double)V * d * 2 + (double)ctx->fn.elems * 2;
     }
     CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_loaded[s], 0));
-    const float* Xin = ctx->X + (int64_t)l * T * d;
-    float* Xout = ctx->X + (int64_t)(l + 1) * T * d;
-    RET(layer_forward(ctx, slot_w(ctx, s), Xin, Xout, B, S, true));
+    const float* Xin = xck(ctx, l, T);
+    float* Xout = xck(ctx, l + 1, T);
+    // sliding: X_{l+1}'s slot held X_{l-3}, whose copy to the host must be done
+    if (ctx->xoff && l + 1 >= 4) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_xfree[(l + 1) % 4], 0));
+    {
+      Timed tl(ctx, 2, 0.0);
+      RET(layer_forward(ctx, slot_w(ctx, s), Xin, Xout, B, S, true));
+    }
     CK(cudaEventRecord(ctx->ev_free[s], ctx->sC));
+    if (ctx->xoff) {  // the checkpoint slides to the host while the next layers compute
+      CK(cudaEventRecord(ctx->ev_xused[l % 4], ctx->sC));
+      CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_xused[l % 4], 0));
+      CK(cudaMemcpyAsync(ctx->x_pin + (int64_t)l * T * d, Xin, (size_t)T * d * 4,
+                         cudaMemcpyDeviceToHost, ctx->sD));
+      CK(cudaEventRecord(ctx->ev_xfree[l % 4], ctx->sD));
+      d2h += (double)T * d * 4;
+    }
   }
 
   // ---- A10: fused LM head + cross-entropy, forward and backward
   CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_lm, 0));
   RET(head_fwd_bwd(ctx, T, n_valid));
   CK(cudaEventRecord(ctx->ev_head, ctx->sC));
+  // sliding: bring checkpoint l back into slot l % 4 once that slot's last user
+  // is done (the head for the slot of X_L, else the backward of layer l + 4)
+  auto h2d_ck = [&](int l, cudaEvent_t after) -> int {
+    CK(cudaStreamWaitEvent(ctx->sU, after, 0));
+    CK(cudaStreamWaitEvent(ctx->sU, ctx->ev_xfree[l % 4], 0));
+    CK(cudaMemcpyAsync(xck(ctx, l, T), ctx->x_pin + (int64_t)l * T * d, (size_t)T * d * 4,
+                       cudaMemcpyHostToDevice, ctx->sU));
+    CK(cudaEventRecord(ctx->ev_xready[l % 4], ctx->sU));
+    h2d += (double)T * d * 4;
+    return SF_OK;
+  };
+  if (ctx->xoff && L - 4 >= 0) RET(h2d_ck(L - 4, ctx->ev_head));
   CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_head, 0));
   CK(cudaMemcpyAsync(ctx->lm.pack, ctx->dWlm16, (size_t)V * d * 2, cudaMemcpyDeviceToHost, ctx->sD));
   CK(cudaMemcpyAsync(ctx->fn.pack, ctx->dgf, (size_t)ctx->fn.elems * 2, cudaMemcpyDeviceToHost, ctx->sD));
@@ -1129,14 +1184,25 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     const bool resident = l >= L - R;  // still in its slot from the forward
     if (!resident) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_loaded[s], 0));
     const LayerW w = slot_w(ctx, s);
-    const float* Xin = ctx->X + (int64_t)l * T * d;
+    const float* Xin = xck(ctx, l, T);
+    if (ctx->xoff && l <= L - 4) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_xready[l % 4], 0));
     // the last layer's intermediates are still in the workspace from the forward
-    if (l != L - 1) RET(layer_forward(ctx, w, Xin, nullptr, B, S, false));
-    RET(layer_backward(ctx, w, slot_g(ctx, s), Xin, B, S));
+    {
+      Timed tl(ctx, 3, 0.0);
+      if (l != L - 1) RET(layer_forward(ctx, w, Xin, nullptr, B, S, false));
+      RET(layer_backward(ctx, w, slot_g(ctx, s), Xin, B, S));
+    }
     CK(cudaEventRecord(ctx->ev_grads[s], ctx->sC));
+    if (ctx->xoff) {
+      CK(cudaEventRecord(ctx->ev_xused[l % 4], ctx->sC));
+      if (l - 4 >= 0) RET(h2d_ck(l - 4, ctx->ev_xused[l % 4]));
+    }
     CK(cudaStreamWaitEvent(ctx->sD, ctx->ev_grads[s], 0));
-    CK(cudaMemcpyAsync(ctx->layers[l].pack, ctx->ring[s] + ctx->pack_elems, pack_bytes,
-                       cudaMemcpyDeviceToHost, ctx->sD));
+    {
+      Timed tl(ctx, 4, 0.0, ctx->sD);
+      CK(cudaMemcpyAsync(ctx->layers[l].pack, ctx->ring[s] + ctx->pack_elems, pack_bytes,
+                         cudaMemcpyDeviceToHost, ctx->sD));
+    }
     CK(cudaEventRecord(ctx->ev_d2h[l], ctx->sD));
     CK(cudaEventRecord(ctx->ev_free[s], ctx->sD));
     d2h += (double)pack_bytes;
@@ -1187,10 +1253,22 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     if (ctx->t_kind[i] == 0) {
       ctx->stats.gemm_ms += x;
       ctx->stats.gemm_flops += ctx->t_flops[i];
-    } else {
+    } else if (ctx->t_kind[i] == 1) {
       ctx->stats.attn_ms += x;
       ctx->stats.attn_flops += ctx->t_flops[i];
+    } else if (ctx->t_kind[i] == 2) {
+      ctx->stats.fwd_layer_ms += x / L;
+    } else if (ctx->t_kind[i] == 3) {
+      ctx->stats.bwd_layer_ms += x / L;
+    } else {
+      ctx->stats.d2h_layer_ms += x / L;
     }
+  }
+  {
+    std::lock_guard<std::mutex> l(ctx->aq_m);
+    ctx->stats.update_layer_ms = ctx->upd_layer_n ? ctx->upd_layer_ms / ctx->upd_layer_n : 0.0;
+    ctx->upd_layer_ms = 0.0;
+    ctx->upd_layer_n = 0;
   }
   cudaGetLastError();
   ctx->stats.h2d_bytes = h2d;

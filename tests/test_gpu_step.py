@@ -90,6 +90,29 @@ def test_async_update_gives_bitwise_identical_training():
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("layers,asyn", [(6, 0), (6, 1), (3, 0)])
+def test_sliding_activations_are_bitwise_identical(layers, asyn):
+    """Checkpoints copied to the host after the forward and brought back for
+    the backward (a 4-slot device window) change no result."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=layers)
+    mast = masters(cfg)
+    batches = [inputs.tokens_and_labels(cfg, seed=50 + i) for i in range(2)]
+    adam = sf.Adam(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    units = (0, layers - 1, UNIT_EMBED, UNIT_LM_HEAD)
+    out, d2h = [], []
+    for off in (0, 1):
+        with make_model(cfg, mast, ring_slots=2, async_update=asyn, offload_activations=off) as m:
+            losses = [m.step(t, l, adam) for t, l in batches]
+            m.sync()
+            out.append((losses, [m.grads(u) for u in units], [m.weights(u) for u in units]))
+            d2h.append(m.stats()["d2h_bytes"])
+    # every layer's fp32 checkpoint went to the host once per step
+    assert d2h[1] - d2h[0] == layers * cfg.batch * cfg.seq * cfg.hidden * 4
+    assert out[0][0] == out[1][0]
+    for a, b in zip(out[0][1] + out[0][2], out[1][1] + out[1][2]):
+        assert np.array_equal(a, b)
+
+
 def test_lce_chunking_does_not_change_the_step():
     cfg = TEST_CONFIGS["small-gqa"]
     mast = masters(cfg)
@@ -218,11 +241,24 @@ def test_full_1p3b_step_properties():
 def test_full_1p3b_step_matches_oracle():
     """The whole 1.3B-shape step (24 layers, hidden 2048, 16 x 64 heads, FFN
     5504, vocab 32000, 8 x 1024 tokens) against the float32 oracle, tensor by
-    tensor (the oracle needs a few minutes of the host's cores)."""
+    tensor (the oracle needs a couple of minutes of the host's cores).
+
+    Tolerance: at this depth bf16 storage of activations by itself moves the
+    gradients by more than 2e-2.  tests/golden/bf16_depth_error.json (written
+    by tests/golden/make_bf16_depth_error.py from the oracle with bf16
+    rounding at the points where this path stores bf16) gives that error; the
+    path must stay within 1.5x of it (the loss keeps the 1e-3 bar)."""
+    import json
+    import os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "bf16_depth_error.json")))
     cfg = CONFIGS["1.3b"]
+    assert gold["workload"] == cfg.name
     mast = masters(cfg)
     tok, lab = inputs.tokens_and_labels(cfg)
     with make_model(cfg, mast) as m:
         assert m.train_step(tok, lab) == sf.SF_OK, m.error()
         loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg, dtype=np.float32)
-        compare(cfg, m, loss_ref, g_ref)
+        tol_layers = max(GRAD_RL2, 1.5 * gold["layer_max"])
+        errs = compare(cfg, m, loss_ref, g_ref, tol=tol_layers)
+    assert errs["lm_head"] <= max(GRAD_RL2, 1.5 * gold["lm_head"])
+    assert errs["final_norm"] <= max(GRAD_RL2, 1.5 * gold["final_norm"])

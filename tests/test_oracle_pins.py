@@ -453,3 +453,21 @@ def test_planted_mistake_is_caught(monkeypatch, target, mutant, pin):
 def test_planted_backward_mistake_is_caught_by_finite_differences(monkeypatch):
     monkeypatch.setattr(ls, "rmsnorm_bwd", lambda dy, g, c: (c[1] * dy * g, np.sum(dy * c[0], 0)))
     assert fd_max_error(TEST_CONFIGS["micro"], n_coords=2) > 1e-3
+
+
+def test_bf16_depth_error_golden_is_from_the_rounding_model():
+    """The stored depth error was written by tests/golden/make_bf16_depth_error.py;
+    re-derive its shallow end here: with two layers of the same widths the
+    bf16-activation error stays under the 2e-2 bar, and it grows with depth."""
+    import json
+    import os
+    from tests.bf16_rounding_model import step_bf16_activations
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "bf16_depth_error.json")))
+    assert gold["layer_max"] > 2e-2 and gold["loss_rel"] < 1e-3
+    cfg = CONFIGS["1.3b"].with_(n_layers=2, batch=1, seq=64)
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    _, g0 = oracle.step(w, tok, lab, cfg)
+    _, g1 = step_bf16_activations(w, tok, lab, cfg)
+    shallow = max(rel_l2(g1["layers"][i][k], g0["layers"][i][k]) for i in range(2) for k in g0["layers"][i])
+    assert shallow < 2e-2 < gold["layer_max"]

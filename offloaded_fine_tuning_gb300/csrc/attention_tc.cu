@@ -347,7 +347,7 @@ struct AttBwdCfg {
   static constexpr int OFF_DST = OFF_PT + 32768;
   static constexpr int OFF_LD = OFF_DST + 32768;  // lse*log2e and D, 2 buffers x 128 each
   static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
-  static constexpr int NBAR = 10;
+  static constexpr int NBAR = 11;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 }  // namespace
@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const uint32_t kv_full = b0, qdo_full = b0 + 8, qdo_empty = b0 + 16, sp_full = b0 + 24,
                  ps_full = b0 + 32, dq_full = b0 + 40, dq_free = b0 + 48, acc_done = b0 + 56,
                  drain = b0 + 64;
+  auto ld_full = [&](int i) { return b0 + 72u + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -399,6 +400,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(ld_full(0), 128);
+    mbar_init(ld_full(1), 128);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
@@ -517,11 +520,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const uint32_t ph = it & 1;
       float* bL = sLD + (it & 1) * 256;
       float* bD = bL + 128;
+      // The buffer written here was last read for block it - 2, and every
+      // thread finished that before the MMA warp could issue block it - 1,
+      // whose S^T this thread has already waited for.
       bL[tid] = next_l;
       bD[tid] = next_d;
+      mbar_arrive(ld_full(it & 1));
       fetch(it + 1, next_l, next_d);
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      ok = __all_sync(0xffffffffu, mbar_wait(sp_full, ph, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(ld_full(it & 1), (it >> 1) & 1, abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sp_full, ph, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const uint32_t rowoff = (uint32_t)r * 128u;
@@ -648,6 +655,356 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   }
 }
 
+// Backward for head_dim 128 with 64-query blocks: the Q and dO tiles are
+// double-buffered (the next block loads while this one computes), and dQ is
+// formed transposed, dQ^T = K^T dS^T (M = head_dim = 128), one thread per
+// head-dim lane, so its atomics are coalesced across a warp.  TMEM columns:
+// S^T [0,64), dP^T [64,128), dQ^T [128,192), dV [256,384), dK [384,512).
+namespace {
+struct AttBwd2Cfg {
+  static constexpr int KV = 32768;  // 128 keys x 128 hd
+  static constexpr int QT = 16384;  // 64 queries x 128 hd
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV;
+  static constexpr int OFF_Q = 2 * KV;           // 2 buffers
+  static constexpr int OFF_DO = OFF_Q + 2 * QT;  // 2 buffers
+  static constexpr int OFF_PT = OFF_DO + 2 * QT;  // 128 keys x 64 queries
+  static constexpr int OFF_DST = OFF_PT + 16384;
+  static constexpr int OFF_LD = OFF_DST + 16384;  // [2][lse 64 | D 64]
+  static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
+  static constexpr int NBAR = 14;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+};
+}  // namespace
+
+__global__ void __launch_bounds__(kAttThreads, 1)
+    attn_bwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
+                        const float* __restrict__ delta, float* __restrict__ dq_acc,
+                        __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ cs, int S,
+                        int Hq, int Hkv, float scale, float scale_log2, int* err) {
+  using C = AttBwd2Cfg;
+  constexpr int HD = 128;
+  constexpr uint32_t ID_SP = umma_idesc_bf16(128, 64, false, false);  // S^T, dP^T
+  constexpr uint32_t ID_KV = umma_idesc_bf16(128, HD, false, true);   // dV, dK
+  constexpr uint32_t ID_Q = umma_idesc_bf16(128, 64, true, true);     // dQ^T
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
+  const uint32_t sPt = s0 + C::OFF_PT, sDSt = s0 + C::OFF_DST;
+  float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  const uint32_t kv_full = b0;
+  auto qdo_full = [&](int i) { return b0 + 8u * (1 + i); };
+  auto qdo_empty = [&](int i) { return b0 + 8u * (3 + i); };
+  const uint32_t sp_full = b0 + 40, ps_full = b0 + 48, pds_free = b0 + 56, dq_full = b0 + 64,
+                 dq_free = b0 + 72, acc_done = b0 + 80, drain = b0 + 88;
+  auto ld_full = [&](int i) { return b0 + 8u * (12 + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int grp = Hq / Hkv;
+  const int k0 = j * 128;
+  const int nqb = (S + 63) / 64;
+  const int first = 2 * j;  // first 64-query block that can see these keys
+  const int per_head = nqb - first;
+  const int n_it = grp * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(qdo_full(i), 1);
+      mbar_init(qdo_empty(i), 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ps_full, 128);
+    mbar_init(pds_free, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(ld_full(0), 64);
+    mbar_init(ld_full(1), 64);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    mbar_arrive_expect_tx(kv_full, 2 * C::KV);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      tma_load_3d(sK + c * 16384, &tm_kv, kv_full, (Hq + g) * HD + 64 * c, k0, b);
+      tma_load_3d(sV + c * 16384, &tm_kv, kv_full, (Hq + Hkv + g) * HD + 64 * c, k0, b);
+    }
+    bool ok = true;
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int bi = it & 1;
+      const int h = g * grp + it / per_head;
+      const int q0 = (first + it % per_head) * 64;
+      if (!mbar_wait(qdo_empty(bi), ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(qdo_full(bi), 2 * C::QT);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sQ + bi * C::QT + c * 8192, &tm_q, qdo_full(bi), h * HD + 64 * c, q0, b);
+        tma_load_3d(sDO + bi * C::QT + c * 8192, &tm_do, qdo_full(bi), h * HD + 64 * c, q0, b);
+      }
+      issued = it + 1;
+    }
+    if (!ok) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      mbar_wait(kv_full, 0, nullptr);
+      for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
+        mbar_wait(qdo_full(it & 1), (it >> 1) & 1, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait(kv_full, 0, abort_flag);
+    for (int it = 0; ok && it <= n_it; ++it) {
+      if (it < n_it) {  // S^T and dP^T of block it
+        const int bi = it & 1;
+        if (!mbar_wait(qdo_full(bi), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (it >= 1 && !mbar_wait(ps_full, (it - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;   // K / V: 128-row boxes
+          const uint32_t qa = (kk >> 2) * 8192 + (kk & 3) * 32;    // Q / dO: 64-row boxes
+          umma_bf16(tmem_base, smem_desc_sw128(sK + ka, 16, 1024),
+                    smem_desc_sw128(sQ + bi * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem_base + COL_DP, smem_desc_sw128(sV + ka, 16, 1024),
+                    smem_desc_sw128(sDO + bi * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(sp_full);
+      }
+      if (it >= 1) {  // dV, dK, dQ^T of block it - 1
+        const int ip = it - 1, bi = ip & 1;
+        if (it == n_it && !mbar_wait(ps_full, ip & 1, abort_flag)) { ok = false; break; }
+        if (ip >= 1 && !mbar_wait(dq_free, (ip - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // over the 64 queries
+          const uint32_t acc = (ip > 0 || kk > 0) ? 1u : 0u;
+          umma_bf16(tmem_base + COL_DV, smem_desc_sw128(sPt + kk * 32, 16, 1024),
+                    smem_desc_sw128(sDO + bi * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
+          umma_bf16(tmem_base + COL_DK, smem_desc_sw128(sDSt + kk * 32, 16, 1024),
+                    smem_desc_sw128(sQ + bi * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // over the 128 keys
+          umma_bf16(tmem_base + COL_DQ, smem_desc_sw128(sK + kk * 2048, 16384, 1024),
+                    smem_desc_sw128(sDSt + kk * 2048, 16384, 1024), ID_Q, kk > 0 ? 1u : 0u);
+        umma_commit(dq_full);
+        umma_commit(qdo_empty(bi));
+        umma_commit(pds_free);
+      }
+    }
+    if (ok) {
+      umma_commit(acc_done);
+    } else {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- threads
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row of S^T / dP^T; head-dim lane of dQ^T
+    const int key = k0 + r;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const int tid = threadIdx.x - 64;
+    const int64_t ldo = (int64_t)Hq * HD;
+    bool ok = true;
+    auto fetch = [&](int it_, float& lv, float& dv) {
+      lv = 0.f;
+      dv = 0.f;
+      if (it_ >= n_it || tid >= 64) return;
+      const int h_ = g * grp + it_ / per_head;
+      const int q_ = (first + it_ % per_head) * 64 + tid;
+      if (q_ < S) {
+        const int64_t o = ((int64_t)b * Hq + h_) * S + q_;
+        lv = lse[o] * 1.4426950408889634f;
+        dv = delta[o];
+      }
+    };
+    // dQ^T of block it_ (queries of head h_ from q0_): thread = head-dim lane r
+    auto emit_dq = [&](int it_) {
+      const int h_ = g * grp + it_ / per_head;
+      const int q0_ = (first + it_ % per_head) * 64;
+      float* col = dq_acc + ((int64_t)b * S + q0_) * ldo + (int64_t)h_ * HD + r;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_base + COL_DQ + 32 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (q0_ + 32 * c + e < S) atomicAdd(col + (int64_t)(32 * c + e) * ldo, __uint_as_float(v[e]));
+      }
+    };
+    float next_l, next_d;
+    fetch(0, next_l, next_d);
+    const uint32_t rowoff = (uint32_t)r * 128u;
+    for (int it = 0; it < n_it; ++it) {
+      const int q0 = (first + it % per_head) * 64;
+      float* bL = sLD + (it & 1) * 128;
+      float* bD = bL + 64;
+      // The buffer written here was last read for block it - 2, and every
+      // thread finished that before the MMA warp could issue block it - 1,
+      // whose S^T this thread has already waited for.
+      if (tid < 64) {
+        bL[tid] = next_l;
+        bD[tid] = next_d;
+        mbar_arrive(ld_full(it & 1));
+      }
+      fetch(it + 1, next_l, next_d);
+      ok = __all_sync(0xffffffffu, mbar_wait(ld_full(it & 1), (it >> 1) & 1, abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sp_full, it & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(lane_base + 32 * c, sr);
+        tmem_ld_32x32b_x32(lane_base + COL_DP + 32 * c, dr);
+        tmem_ld_wait();
+        float p[32], ds[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int qq = 32 * c + e;
+          const int q = q0 + qq;
+          float pv = 0.f;
+          if (q < S && key <= q) pv = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -bL[qq]));
+          p[e] = pv;
+          ds[e] = pv * (__uint_as_float(dr[e]) - bD[qq]);
+        }
+        if (c == 0 && it >= 1) {  // P^T, dS^T of the previous block consumed
+          ok = __all_sync(0xffffffffu, mbar_wait(pds_free, (it - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int jj = c * 4 + k;
+          const uint32_t off = rowoff + (uint32_t)((jj ^ (r & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sPt + off),
+                       "r"(pack2_bf16(p[8 * k], p[8 * k + 1])), "r"(pack2_bf16(p[8 * k + 2], p[8 * k + 3])),
+                       "r"(pack2_bf16(p[8 * k + 4], p[8 * k + 5])), "r"(pack2_bf16(p[8 * k + 6], p[8 * k + 7]))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDSt + off),
+                       "r"(pack2_bf16(ds[8 * k], ds[8 * k + 1])), "r"(pack2_bf16(ds[8 * k + 2], ds[8 * k + 3])),
+                       "r"(pack2_bf16(ds[8 * k + 4], ds[8 * k + 5])), "r"(pack2_bf16(ds[8 * k + 6], ds[8 * k + 7]))
+                       : "memory");
+        }
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ps_full);
+      if (it >= 1) {  // dQ of the previous block, then its TMEM columns are free
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        emit_dq(it - 1);
+        tc_fence_before();
+        mbar_arrive(dq_free);
+      }
+    }
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (n_it - 1) & 1, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        emit_dq(n_it - 1);
+      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const int64_t ld = (int64_t)(Hq + 2 * Hkv) * HD;
+      // dK: pairs (d, d + HD/2) get the inverse rotation of the key's position
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t x1[32], x2[32];
+        tmem_ld_32x32b_x32(lane_base + COL_DK + 32 * c, x1);
+        tmem_ld_32x32b_x32(lane_base + COL_DK + HD / 2 + 32 * c, x2);
+        tmem_ld_wait();
+        if (key < S) {
+          __nv_bfloat16* krow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + g) * HD;
+          uint32_t o1[16], o2[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float a1 = __uint_as_float(x1[e]) * scale, b1 = __uint_as_float(x1[e + 1]) * scale;
+            float a2 = __uint_as_float(x2[e]) * scale, b2 = __uint_as_float(x2[e + 1]) * scale;
+            if (cs) {
+              const float2 ca = cs[(int64_t)key * (HD / 2) + 32 * c + e];
+              const float2 cb = cs[(int64_t)key * (HD / 2) + 32 * c + e + 1];
+              const float y1a = a1 * ca.x + a2 * ca.y, y2a = a2 * ca.x - a1 * ca.y;
+              const float y1b = b1 * cb.x + b2 * cb.y, y2b = b2 * cb.x - b1 * cb.y;
+              a1 = y1a; a2 = y2a; b1 = y1b; b2 = y2b;
+            }
+            o1[e / 2] = pack2_bf16(a1, b1);
+            o2[e / 2] = pack2_bf16(a2, b2);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            *reinterpret_cast<uint4*>(krow + 32 * c + 8 * k) = make_uint4(o1[4 * k], o1[4 * k + 1], o1[4 * k + 2], o1[4 * k + 3]);
+            *reinterpret_cast<uint4*>(krow + HD / 2 + 32 * c + 8 * k) = make_uint4(o2[4 * k], o2[4 * k + 1], o2[4 * k + 2], o2[4 * k + 3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_base + COL_DV + 32 * c, v);
+        tmem_ld_wait();
+        if (key < S) {
+          __nv_bfloat16* vrow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + Hkv + g) * HD;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            u.x = pack2_bf16(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1]));
+            u.y = pack2_bf16(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3]));
+            u.z = pack2_bf16(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5]));
+            u.w = pack2_bf16(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7]));
+            *reinterpret_cast<uint4*>(vrow + 32 * c + 8 * k) = u;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -734,6 +1091,48 @@ int bwd_tc(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
+int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+            const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq,
+            int Hkv, const float2* cs, int* err, cudaStream_t st) {
+  using C = AttBwd2Cfg;
+  constexpr int HD = 128;
+  auto fn = encode_fn_att();
+  if (!fn) return -3;
+  const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
+  CUtensorMap tkv, tq, td;
+  cuuint32_t box_kv[3] = {64, 128, 1}, box_q[3] = {64, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t dq[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t sq[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(S * W * 2)};
+  cuuint64_t dd[3] = {(cuuint64_t)WO, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t sd[2] = {(cuuint64_t)(WO * 2), (cuuint64_t)(S * WO * 2)};
+  auto enc = [&](CUtensorMap* m, const void* base, cuuint64_t* dims, cuuint64_t* strides,
+                 cuuint32_t* box) {
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!enc(&tkv, qkv, dq, sq, box_kv) || !enc(&tq, qkv, dq, sq, box_q) ||
+      !enc(&td, dout, dd, sd, box_q))
+    return -3;
+  static bool set = false;
+  if (!set) {
+    if (cudaFuncSetAttribute(attn_bwd_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return -3;
+    set = true;
+  }
+  const int64_t T = (int64_t)B * S;
+  if (cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess) return -3;
+  attn_delta(o, dout, delta, B, S, Hq, HD, st);
+  const float scale = 1.f / sqrtf((float)HD);
+  dim3 grid((S + 127) / 128, Hkv, B);
+  attn_bwd_tc2_kernel<<<grid, kAttThreads, C::SMEM, st>>>(
+      tkv, tq, td, lse, delta, dq_acc, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
+  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, st);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 }  // namespace
 
 int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
@@ -742,7 +1141,7 @@ int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat
   if (B <= 0 || S <= 0) return 0;
   if (Hkv <= 0 || Hq % Hkv) return -1;
   if (hd == 64) return bwd_tc<64>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
-  if (hd == 128) return bwd_tc<128>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
+  if (hd == 128) return bwd_tc2(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
   return -1;
 }
 

@@ -88,7 +88,13 @@ typedef struct sf_ctx sf_ctx;
  *     stays in device memory; 1 = sliding activations: after a layer's
  *     forward its checkpoint is copied to pinned host memory and brought back
  *     just before that layer's backward, the device keeping a window of four
- *     (results are identical). */
+ *     (results are identical).
+ *   deterministic: 0 = the attention backward adds the dQ contributions of
+ *     its key blocks into one fp32 buffer in whatever order they arrive, so
+ *     the last bits of a gradient can differ between two identical steps;
+ *     1 = every key block writes its own slot and the slots are summed in key
+ *     order (bit-reproducible steps, ~ceil(max_seq/128) x more dQ scratch in
+ *     device memory and one extra pass over it). */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -101,6 +107,7 @@ typedef struct {
   int32_t wait_timeout_ms;
   int32_t async_update;
   int32_t offload_activations;
+  int32_t deterministic;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -273,11 +280,14 @@ int sf_op_attn_fwd(const uint16_t* qkv, uint16_t* o, float* lse, int32_t B, int3
 /* Backward of sf_op_attn_fwd: writes dQ, dK, dV into dqkv (same layout as qkv);
  * when table != NULL the inverse rotary embedding is applied to dQ and dK (the
  * gradient reaches the pre-rotation projections).  Scratch: delta fp32
- * [B*Hq*S], dq_acc fp32 [B*S*Hq*hd]. */
+ * [B*Hq*S]; dq_acc fp32 [B*S*Hq*hd] when deterministic == 0 (contributions
+ * added in arrival order), or [ceil(S/128) * B*S*Hq*hd] when deterministic
+ * != 0 (one slot per 128-key block, summed in key order: the result is
+ * bit-reproducible).  dq_acc must be 16-byte aligned. */
 int sf_op_attn_bwd(const uint16_t* qkv, const uint16_t* o, const uint16_t* dout,
                    const float* lse, float* delta, float* dq_acc, uint16_t* dqkv, int32_t B,
                    int32_t S, int32_t Hq, int32_t Hkv, int32_t hd, const float* table,
-                   void* stream);
+                   int32_t deterministic, void* stream);
 
 /* m = silu(a) * b with ab = [a | b] bf16 [rows, 2*ffn]; m bf16 [rows, ffn]. */
 int sf_op_swiglu_fwd(const uint16_t* ab, uint16_t* m, int64_t rows, int32_t ffn, void* stream);

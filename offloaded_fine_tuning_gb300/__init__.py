@@ -42,7 +42,7 @@ class Config(ctypes.Structure):
                [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
                 ("device", ctypes.c_int32), ("adam_threads", ctypes.c_int32),
                 ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32),
-                ("offload_activations", ctypes.c_int32)]
+                ("offload_activations", ctypes.c_int32), ("deterministic", ctypes.c_int32)]
 
 
 class Adam(ctypes.Structure):
@@ -98,7 +98,7 @@ _SIGS = {
     "sf_op_rope": (ctypes.c_int, [_VP, _I64, _I64, _I32, _I32, _I32, _VP, _I32, _VP]),
     "sf_op_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
     "sf_op_attn_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
-                                      _I32, _VP, _VP]),
+                                      _I32, _VP, _I32, _VP]),
     "sf_op_swiglu_fwd": (ctypes.c_int, [_VP, _VP, _I64, _I32, _VP]),
     "sf_op_swiglu_bwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_op_lce": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, _I32, _I64, _I64, _VP, _VP, _VP, _VP, _VP]),
@@ -138,7 +138,7 @@ def _check(st: int, ctx=None, what=""):
 
 def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_grads=1,
                 lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0,
-                async_update=0, offload_activations=0) -> Config:
+                async_update=0, offload_activations=0, deterministic=0) -> Config:
     """sf_config from a shape object with the fields of inputs.ModelConfig."""
     return Config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
                   n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, ffn=shape.ffn,
@@ -147,7 +147,8 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   ring_slots=ring_slots or shape.ring_slots, lce_chunk_rows=lce_chunk_rows,
                   retain_grads=retain_grads, rms_eps=shape.rms_eps, rope_base=shape.rope_base,
                   device=device, adam_threads=adam_threads, wait_timeout_ms=wait_timeout_ms,
-                  async_update=async_update, offload_activations=offload_activations)
+                  async_update=async_update, offload_activations=offload_activations,
+                  deterministic=deterministic)
 
 
 def unit_numel(cfg: Config, unit: int) -> int:
@@ -287,9 +288,15 @@ def op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, stream=0) -> int:
     return lib().sf_op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, _s(stream))
 
 
-def op_attn_bwd(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, hd, table=0, stream=0) -> int:
+def op_attn_bwd(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, hd, table=0, stream=0,
+                deterministic=0) -> int:
     return lib().sf_op_attn_bwd(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, hd,
-                                table or None, _s(stream))
+                                table or None, deterministic, _s(stream))
+
+
+def attn_dq_scratch_floats(B, S, Hq, hd, deterministic=0) -> int:
+    """Floats of the dq_acc scratch sf_op_attn_bwd needs."""
+    return (((S + 127) // 128) if deterministic else 1) * B * S * Hq * hd
 
 
 def op_swiglu_fwd(ab, m, rows, ffn, stream=0) -> int:

@@ -27,6 +27,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "sf_internal.h"
@@ -48,6 +49,18 @@ struct AttCfg {
   static constexpr int NBAR = 14;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
+
+// Grid position in longest-first order: the CTAs are dispatched roughly in
+// linear block order, so every CTA of rank 0 (the most work) is placed before
+// any CTA of rank 1, and so on, whatever the other two coordinates.
+__device__ __forceinline__ void grid_rank_first(int& rank, int& y, int& z) {
+  const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  const int per = (int)(gridDim.y * gridDim.z);
+  rank = lin / per;
+  const int rem = lin - rank * per;
+  y = rem % (int)gridDim.y;
+  z = rem / (int)gridDim.y;
+}
 
 // 2^x on the special-function unit (relative error ~2^-22, flushes denormals).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -95,8 +108,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (S + 127) / 128;
-  const int qb = nqb - 1 - (int)blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, h, b;
+  grid_rank_first(rank, h, b);
+  const int qb = nqb - 1 - rank;  // longest rows first
   const int g = h / (Hq / Hkv);
   const int q0 = qb * 128;
   const int nkv = qb + 1;
@@ -352,7 +366,7 @@ struct AttBwdCfg {
 };
 }  // namespace
 
-template <int HD>
+template <int HD, bool DET>
 __global__ void __launch_bounds__(kAttThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                        const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
@@ -384,7 +398,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  int j, g, b;
+  grid_rank_first(j, g, b);  // key block 0 sees the most query blocks
   const int grp = Hq / Hkv;
   const int k0 = j * 128;
   const int nqb = (S + 127) / 128;
@@ -571,7 +586,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int q = q0 + r;
-      float* dst = dq_acc + ((int64_t)b * S + q) * ldo + (int64_t)h * HD;
+      // deterministic: this key block's own slot, plain stores
+      const int64_t row = DET ? ((int64_t)j * gridDim.z + b) * S + q : (int64_t)b * S + q;
+      float* dst = dq_acc + row * ldo + (int64_t)h * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t v[32];
@@ -579,10 +596,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tmem_ld_wait();
         if (q < S) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * k),
-                      make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                  __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])));
+          for (int k = 0; k < 8; ++k) {
+            const float4 x = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                         __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+            if (DET)
+              *reinterpret_cast<float4*>(dst + 32 * c + 4 * k) = x;
+            else
+              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * k), x);
+          }
         }
       }
       tc_fence_before();
@@ -655,33 +676,46 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   }
 }
 
-// Backward for head_dim 128 with 64-query blocks: the Q and dO tiles are
-// double-buffered (the next block loads while this one computes), and dQ is
-// formed transposed, dQ^T = K^T dS^T (M = head_dim = 128), one thread per
-// head-dim lane, so its atomics are coalesced across a warp.  TMEM columns:
-// S^T [0,64), dP^T [64,128), dQ^T [128,192), dV [256,384), dK [384,512).
+// Backward for head_dim 128 with 64-query blocks.  The Q and dO tiles have
+// three stages, so loads run two blocks ahead.  dQ is formed transposed,
+// dQ^T = K^T dS^T (M = head_dim = 128), one thread per head-dim lane; each
+// warp stages its 32 x 32 piece in shared memory and the TMA unit adds it
+// into the fp32 dQ buffer (cp.reduce.async.bulk), so no thread issues atomics;
+// in the deterministic variant it stores the piece into this key block's own
+// slot instead, and the slots are summed in key order afterwards.  The threads copy S^T and dP^T into
+// registers and release those TMEM columns at once, so the MMA warp computes
+// the next block's S^T and dP^T, and this block's dV, dK and dQ^T, while
+// they work.  TMEM columns: S^T [0,64), dP^T [64,128), dQ^T two buffers
+// [128,256), dV [256,384), dK [384,512).  Every mbarrier below completes at
+// most once before its waiter has seen the previous completion (each has a
+// dependency chain through its waiter), so parity waits are unambiguous.
 namespace {
+constexpr int kAttBwd2Threads = 320;  // TMA warp, MMA warp, 8 softmax-gradient warps
 struct AttBwd2Cfg {
   static constexpr int KV = 32768;  // 128 keys x 128 hd
   static constexpr int QT = 16384;  // 64 queries x 128 hd
+  static constexpr int NQ = 3;      // Q / dO stages
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV;
-  static constexpr int OFF_Q = 2 * KV;           // 2 buffers
-  static constexpr int OFF_DO = OFF_Q + 2 * QT;  // 2 buffers
-  static constexpr int OFF_PT = OFF_DO + 2 * QT;  // 128 keys x 64 queries
+  static constexpr int OFF_Q = 2 * KV;
+  static constexpr int OFF_DO = OFF_Q + NQ * QT;
+  static constexpr int OFF_PT = OFF_DO + NQ * QT;  // 128 keys x 64 queries
   static constexpr int OFF_DST = OFF_PT + 16384;
-  static constexpr int OFF_LD = OFF_DST + 16384;  // [2][lse 64 | D 64]
+  static constexpr int OFF_DQS = OFF_DST + 16384;  // dQ staging: 8 warps x [32 q][32 d] fp32
+  static constexpr int OFF_LD = OFF_DQS + 8 * 4096;  // [2][lse 64 | D 64]
   static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
-  static constexpr int NBAR = 14;
+  static constexpr int NBAR = 19;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 }  // namespace
 
-__global__ void __launch_bounds__(kAttThreads, 1)
+template <bool DET>
+__global__ void __launch_bounds__(kAttBwd2Threads, 1)
     attn_bwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_kv,
                         const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
-                        const float* __restrict__ delta, float* __restrict__ dq_acc,
+                        const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+                        const float* __restrict__ delta,
                         __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ cs, int S,
                         int Hq, int Hkv, float scale, float scale_log2, int* err) {
   using C = AttBwd2Cfg;
@@ -697,21 +731,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q, sDO = s0 + C::OFF_DO;
-  const uint32_t sPt = s0 + C::OFF_PT, sDSt = s0 + C::OFF_DST;
+  const uint32_t sPt = s0 + C::OFF_PT, sDSt = s0 + C::OFF_DST, sDQS = s0 + C::OFF_DQS;
   float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
   const uint32_t kv_full = b0;
   auto qdo_full = [&](int i) { return b0 + 8u * (1 + i); };
-  auto qdo_empty = [&](int i) { return b0 + 8u * (3 + i); };
-  const uint32_t sp_full = b0 + 40, ps_full = b0 + 48, pds_free = b0 + 56, dq_full = b0 + 64,
-                 dq_free = b0 + 72, acc_done = b0 + 80, drain = b0 + 88;
-  auto ld_full = [&](int i) { return b0 + 8u * (12 + i); };
+  auto qdo_empty = [&](int i) { return b0 + 8u * (4 + i); };
+  const uint32_t sp_full = b0 + 56, s_free = b0 + 64, ps_full = b0 + 72, pds_free = b0 + 80;
+  auto dq_full = [&](int i) { return b0 + 88u + 8u * i; };
+  auto dq_free = [&](int i) { return b0 + 104u + 8u * i; };
+  const uint32_t acc_done = b0 + 120, drain = b0 + 128;
+  auto ld_full = [&](int i) { return b0 + 136u + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  int j, g, b;
+  grid_rank_first(j, g, b);  // key block 0 sees the most query blocks
   const int grp = Hq / Hkv;
   const int k0 = j * 128;
   const int nqb = (S + 63) / 64;
@@ -721,24 +758,27 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NQ; ++i) {
       mbar_init(qdo_full(i), 1);
       mbar_init(qdo_empty(i), 1);
     }
     mbar_init(sp_full, 1);
-    mbar_init(ps_full, 128);
+    mbar_init(s_free, 256);
+    mbar_init(ps_full, 256);
     mbar_init(pds_free, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(dq_full(i), 1);
+      mbar_init(dq_free(i), 256);
+      mbar_init(ld_full(i), 64);
+    }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(ld_full(0), 64);
-    mbar_init(ld_full(1), 64);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_kv);
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -760,15 +800,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     bool ok = true;
     int issued = 0;
     for (int it = 0; it < n_it; ++it) {
-      const int bi = it & 1;
+      const int bq = it % C::NQ;
       const int h = g * grp + it / per_head;
       const int q0 = (first + it % per_head) * 64;
-      if (!mbar_wait(qdo_empty(bi), ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-      mbar_arrive_expect_tx(qdo_full(bi), 2 * C::QT);
+      if (!mbar_wait(qdo_empty(bq), ((it / C::NQ) & 1) ^ 1, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(qdo_full(bq), 2 * C::QT);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        tma_load_3d(sQ + bi * C::QT + c * 8192, &tm_q, qdo_full(bi), h * HD + 64 * c, q0, b);
-        tma_load_3d(sDO + bi * C::QT + c * 8192, &tm_do, qdo_full(bi), h * HD + 64 * c, q0, b);
+        tma_load_3d(sQ + bq * C::QT + c * 8192, &tm_q, qdo_full(bq), h * HD + 64 * c, q0, b);
+        tma_load_3d(sDO + bq * C::QT + c * 8192, &tm_do, qdo_full(bq), h * HD + 64 * c, q0, b);
       }
       issued = it + 1;
     }
@@ -776,48 +816,48 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       mbar_wait(kv_full, 0, nullptr);
-      for (int it = issued - 1; it >= 0 && it >= issued - 2; --it)
-        mbar_wait(qdo_full(it & 1), (it >> 1) & 1, nullptr);
+      for (int it = issued - 1; it >= 0 && it >= issued - C::NQ; --it)
+        mbar_wait(qdo_full(it % C::NQ), (it / C::NQ) & 1, nullptr);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     bool ok = mbar_wait(kv_full, 0, abort_flag);
     for (int it = 0; ok && it <= n_it; ++it) {
-      if (it < n_it) {  // S^T and dP^T of block it
-        const int bi = it & 1;
-        if (!mbar_wait(qdo_full(bi), (it >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (it >= 1 && !mbar_wait(ps_full, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      if (it < n_it) {  // S^T and dP^T of block it, once the threads hold block it - 1's
+        const int bq = it % C::NQ;
+        if (!mbar_wait(qdo_full(bq), (it / C::NQ) & 1, abort_flag)) { ok = false; break; }
+        if (it >= 1 && !mbar_wait(s_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;   // K / V: 128-row boxes
           const uint32_t qa = (kk >> 2) * 8192 + (kk & 3) * 32;    // Q / dO: 64-row boxes
           umma_bf16(tmem_base, smem_desc_sw128(sK + ka, 16, 1024),
-                    smem_desc_sw128(sQ + bi * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
+                    smem_desc_sw128(sQ + bq * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
           umma_bf16(tmem_base + COL_DP, smem_desc_sw128(sV + ka, 16, 1024),
-                    smem_desc_sw128(sDO + bi * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
+                    smem_desc_sw128(sDO + bq * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
         }
         umma_commit(sp_full);
       }
-      if (it >= 1) {  // dV, dK, dQ^T of block it - 1
-        const int ip = it - 1, bi = ip & 1;
-        if (it == n_it && !mbar_wait(ps_full, ip & 1, abort_flag)) { ok = false; break; }
-        if (ip >= 1 && !mbar_wait(dq_free, (ip - 1) & 1, abort_flag)) { ok = false; break; }
+      if (it >= 1) {  // dV, dK, dQ^T of block it - 1, once its P^T and dS^T are in shared memory
+        const int ip = it - 1, bq = ip % C::NQ, bd = ip & 1;
+        if (!mbar_wait(ps_full, ip & 1, abort_flag)) { ok = false; break; }
+        if (ip >= 2 && !mbar_wait(dq_free(bd), ((ip >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // over the 64 queries
           const uint32_t acc = (ip > 0 || kk > 0) ? 1u : 0u;
           umma_bf16(tmem_base + COL_DV, smem_desc_sw128(sPt + kk * 32, 16, 1024),
-                    smem_desc_sw128(sDO + bi * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
+                    smem_desc_sw128(sDO + bq * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
           umma_bf16(tmem_base + COL_DK, smem_desc_sw128(sDSt + kk * 32, 16, 1024),
-                    smem_desc_sw128(sQ + bi * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
+                    smem_desc_sw128(sQ + bq * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // over the 128 keys
-          umma_bf16(tmem_base + COL_DQ, smem_desc_sw128(sK + kk * 2048, 16384, 1024),
+          umma_bf16(tmem_base + COL_DQ + 64 * bd, smem_desc_sw128(sK + kk * 2048, 16384, 1024),
                     smem_desc_sw128(sDSt + kk * 2048, 16384, 1024), ID_Q, kk > 0 ? 1u : 0u);
-        umma_commit(dq_full);
-        umma_commit(qdo_empty(bi));
+        umma_commit(dq_full(bd));
+        umma_commit(qdo_empty(bq));
         umma_commit(pds_free);
       }
     }
@@ -831,7 +871,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- threads
+    // Eight warps: two per TMEM lane quarter, each taking one half (32) of the
+    // block's 64 query columns, so every scheduler has two warps to switch
+    // between and each thread handles 32 elements of a block.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // key row of S^T / dP^T; head-dim lane of dQ^T
     const int key = k0 + r;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
@@ -850,31 +894,51 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         dv = delta[o];
       }
     };
-    // dQ^T of block it_ (queries of head h_ from q0_): thread = head-dim lane r
-    auto emit_dq = [&](int it_) {
-      const int h_ = g * grp + it_ / per_head;
-      const int q0_ = (first + it_ % per_head) * 64;
-      float* col = dq_acc + ((int64_t)b * S + q0_) * ldo + (int64_t)h_ * HD + r;
+    // dQ^T of block it_ (this warp's 32 queries, head-dim lanes of its
+    // quarter) from registers into the warp's staging tile, then one TMA
+    // reduce-add into the fp32 dQ buffer.  The tile is rewritten only after
+    // the previous reduce has finished reading it.
+    const uint32_t stage = sDQS + (uint32_t)(warp - 2) * 4096u;
+    auto stage_dq = [&](int it_, const uint32_t (&v)[32]) {
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(lane_base + COL_DQ + 32 * c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (q0_ + 32 * c + e < S) atomicAdd(col + (int64_t)(32 * c + e) * ldo, __uint_as_float(v[e]));
+      for (int e = 0; e < 32; ++e)
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(stage + (uint32_t)e * 128u + (uint32_t)lane * 4u),
+                     "r"(v[e])
+                     : "memory");
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int h_ = g * grp + it_ / per_head;
+        const int qb_ = (first + it_ % per_head) * 64 + 32 * half;
+        if (DET)  // this key block's own slot of the dQ buffer
+          tma_store_3d(&tm_dq, stage, h_ * HD + 32 * quarter, qb_, j * (int)gridDim.z + b);
+        else
+          tma_reduce_add_3d(&tm_dq, stage, h_ * HD + 32 * quarter, qb_, b);
+        bulk_commit_group();
       }
+    };
+    auto emit_dq = [&](int it_) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full(it_ & 1), (it_ >> 1) & 1, abort_flag))) return false;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_base + COL_DQ + 64 * (it_ & 1) + 32 * half, v);
+      tmem_ld_wait();
+      stage_dq(it_, v);
+      return true;
     };
     float next_l, next_d;
     fetch(0, next_l, next_d);
     const uint32_t rowoff = (uint32_t)r * 128u;
     for (int it = 0; it < n_it; ++it) {
       const int q0 = (first + it % per_head) * 64;
+      const int qb = q0 + 32 * half;  // first query of this thread's columns
       float* bL = sLD + (it & 1) * 128;
       float* bD = bL + 64;
-      // The buffer written here was last read for block it - 2, and every
-      // thread finished that before the MMA warp could issue block it - 1,
-      // whose S^T this thread has already waited for.
+      // The buffer written here was last read for block it - 2; this thread
+      // has since waited for that block's P^T / dS^T to be consumed, which
+      // needed every thread to have finished computing it.
       if (tid < 64) {
         bL[tid] = next_l;
         bD[tid] = next_d;
@@ -883,69 +947,82 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       fetch(it + 1, next_l, next_d);
       ok = __all_sync(0xffffffffu, mbar_wait(ld_full(it & 1), (it >> 1) & 1, abort_flag));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sp_full, it & 1, abort_flag));
+      // dQ^T of block it - 2 (its buffer is the one block it will use) is
+      // read together with this block's S^T and dP^T
+      if (ok && it >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full(it & 1), ((it - 2) >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(lane_base + 32 * c, sr);
-        tmem_ld_32x32b_x32(lane_base + COL_DP + 32 * c, dr);
-        tmem_ld_wait();
-        float p[32], ds[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qq = 32 * c + e;
-          const int q = q0 + qq;
-          float pv = 0.f;
-          if (q < S && key <= q) pv = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -bL[qq]));
-          p[e] = pv;
-          ds[e] = pv * (__uint_as_float(dr[e]) - bD[qq]);
-        }
-        if (c == 0 && it >= 1) {  // P^T, dS^T of the previous block consumed
-          ok = __all_sync(0xffffffffu, mbar_wait(pds_free, (it - 1) & 1, abort_flag));
-          if (!ok) break;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int jj = c * 4 + k;
-          const uint32_t off = rowoff + (uint32_t)((jj ^ (r & 7)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sPt + off),
-                       "r"(pack2_bf16(p[8 * k], p[8 * k + 1])), "r"(pack2_bf16(p[8 * k + 2], p[8 * k + 3])),
-                       "r"(pack2_bf16(p[8 * k + 4], p[8 * k + 5])), "r"(pack2_bf16(p[8 * k + 6], p[8 * k + 7]))
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDSt + off),
-                       "r"(pack2_bf16(ds[8 * k], ds[8 * k + 1])), "r"(pack2_bf16(ds[8 * k + 2], ds[8 * k + 3])),
-                       "r"(pack2_bf16(ds[8 * k + 4], ds[8 * k + 5])), "r"(pack2_bf16(ds[8 * k + 6], ds[8 * k + 7]))
-                       : "memory");
-        }
+      uint32_t sr[32], dr[32], qv[32];
+      tmem_ld_32x32b_x32(lane_base + 32 * half, sr);
+      tmem_ld_32x32b_x32(lane_base + COL_DP + 32 * half, dr);
+      if (it >= 2) tmem_ld_32x32b_x32(lane_base + COL_DQ + 64 * (it & 1) + 32 * half, qv);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_free);  // S^T / dP^T are in registers: the next block may overwrite them
+      if (it >= 2) {
+        mbar_arrive(dq_free(it & 1));
+        stage_dq(it - 2, qv);
       }
-      if (!ok) break;
+      const float4* L4 = reinterpret_cast<const float4*>(bL + 32 * half);
+      const float4* D4 = reinterpret_cast<const float4*>(bD + 32 * half);
+      uint32_t pp[16], dd[16];
+      auto grad_tile = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 l4 = L4[k], d4 = D4[k];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], sv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = 4 * k + i;
+            float x = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -lv[i]));
+            if (kMask && !(qb + e < S && key <= qb + e)) x = 0.f;
+            pv[i] = x;
+            sv[i] = x * (__uint_as_float(dr[e]) - dv[i]);
+          }
+          pp[2 * k] = pack2_bf16(pv[0], pv[1]);
+          pp[2 * k + 1] = pack2_bf16(pv[2], pv[3]);
+          dd[2 * k] = pack2_bf16(sv[0], sv[1]);
+          dd[2 * k + 1] = pack2_bf16(sv[2], sv[3]);
+        }
+      };
+      // Only blocks that touch the diagonal or the sequence end need the mask.
+      if (qb < k0 + 128 || qb + 32 > S)
+        grad_tile(std::true_type{});
+      else
+        grad_tile(std::false_type{});
+      if (it >= 1) {  // P^T, dS^T of the previous block consumed
+        ok = __all_sync(0xffffffffu, mbar_wait(pds_free, (it - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int jj = half * 4 + k;  // 16-byte chunk of the 128-byte row
+        const uint32_t off = rowoff + (uint32_t)((jj ^ (r & 7)) * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sPt + off), "r"(pp[4 * k]),
+                     "r"(pp[4 * k + 1]), "r"(pp[4 * k + 2]), "r"(pp[4 * k + 3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sDSt + off), "r"(dd[4 * k]),
+                     "r"(dd[4 * k + 1]), "r"(dd[4 * k + 2]), "r"(dd[4 * k + 3])
+                     : "memory");
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ps_full);
-      if (it >= 1) {  // dQ of the previous block, then its TMEM columns are free
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        emit_dq(it - 1);
-        tc_fence_before();
-        mbar_arrive(dq_free);
-      }
     }
-    if (ok && n_it > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (n_it - 1) & 1, abort_flag));
-      if (ok) {
-        tc_fence_after();
-        emit_dq(n_it - 1);
-      }
-    }
+    // the last two blocks' dQ
+    for (int ip = n_it >= 2 ? n_it - 2 : 0; ok && ip < n_it; ++ip) ok = emit_dq(ip);
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (ok) {
       tc_fence_after();
       const int64_t ld = (int64_t)(Hq + 2 * Hkv) * HD;
-      // dK: pairs (d, d + HD/2) get the inverse rotation of the key's position
-#pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
+      // dK: pairs (d, d + HD/2) get the inverse rotation of the key's position;
+      // this warp takes d in [32 half, 32 half + 32) and its partners
+      {
+        const int c = half;
         uint32_t x1[32], x2[32];
         tmem_ld_32x32b_x32(lane_base + COL_DK + 32 * c, x1);
         tmem_ld_32x32b_x32(lane_base + COL_DK + HD / 2 + 32 * c, x2);
@@ -974,8 +1051,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
         }
       }
+      // dV: this warp takes columns [64 half, 64 half + 64)
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
         uint32_t v[32];
         tmem_ld_32x32b_x32(lane_base + COL_DV + 32 * c, v);
         tmem_ld_wait();
@@ -996,6 +1075,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's dQ reduces are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -1051,7 +1131,7 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-template <int HD>
+template <int HD, bool DET>
 int bwd_tc(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
            const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq,
            int Hkv, const float2* cs, int* err, cudaStream_t st) {
@@ -1075,22 +1155,24 @@ int bwd_tc(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16
     return -3;
   static bool set = false;
   if (!set) {
-    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<HD, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM) != cudaSuccess)
       return -3;
     set = true;
   }
   const int64_t T = (int64_t)B * S;
-  if (cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess) return -3;
+  if (!DET && cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess)
+    return -3;
   attn_delta(o, dout, delta, B, S, Hq, HD, st);
   const float scale = 1.f / sqrtf((float)HD);
   dim3 grid((S + 127) / 128, Hkv, B);
-  attn_bwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(
+  attn_bwd_tc_kernel<HD, DET><<<grid, kAttThreads, C::SMEM, st>>>(
       tq, td, lse, delta, dq_acc, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
-  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, st);
+  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, DET ? (S + 127) / 128 : 0, st);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
+template <bool DET>
 int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
             const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq,
             int Hkv, const float2* cs, int* err, cudaStream_t st) {
@@ -1099,8 +1181,8 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
   auto fn = encode_fn_att();
   if (!fn) return -3;
   const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
-  CUtensorMap tkv, tq, td;
-  cuuint32_t box_kv[3] = {64, 128, 1}, box_q[3] = {64, 64, 1};
+  CUtensorMap tkv, tq, td, tdq;
+  cuuint32_t box_kv[3] = {64, 128, 1}, box_q[3] = {64, 64, 1}, box_dq[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   cuuint64_t dq[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t sq[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(S * W * 2)};
@@ -1112,24 +1194,31 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
+  cuuint64_t sdq[2] = {(cuuint64_t)(WO * 4), (cuuint64_t)(S * WO * 4)};
+  const int nkb = (S + 127) / 128;
+  cuuint64_t ddq[3] = {(cuuint64_t)WO, (cuuint64_t)S, (cuuint64_t)(DET ? B * nkb : B)};
   if (!enc(&tkv, qkv, dq, sq, box_kv) || !enc(&tq, qkv, dq, sq, box_q) ||
-      !enc(&td, dout, dd, sd, box_q))
+      !enc(&td, dout, dd, sd, box_q) ||
+      fn(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, ddq, sdq, box_dq, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
   static bool set = false;
   if (!set) {
-    if (cudaFuncSetAttribute(attn_bwd_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_bwd_tc2_kernel<DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM) != cudaSuccess)
       return -3;
     set = true;
   }
   const int64_t T = (int64_t)B * S;
-  if (cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess) return -3;
+  if (!DET && cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess)
+    return -3;
   attn_delta(o, dout, delta, B, S, Hq, HD, st);
   const float scale = 1.f / sqrtf((float)HD);
   dim3 grid((S + 127) / 128, Hkv, B);
-  attn_bwd_tc2_kernel<<<grid, kAttThreads, C::SMEM, st>>>(
-      tkv, tq, td, lse, delta, dq_acc, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
-  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, st);
+  attn_bwd_tc2_kernel<DET><<<grid, kAttBwd2Threads, C::SMEM, st>>>(
+      tkv, tq, td, tdq, lse, delta, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
+  attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, DET ? nkb : 0, st);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1137,11 +1226,18 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
 
 int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
              const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S,
-             int Hq, int Hkv, int hd, const float2* cs, int* err, cudaStream_t st) {
+             int Hq, int Hkv, int hd, const float2* cs, bool deterministic, int* err,
+             cudaStream_t st) {
   if (B <= 0 || S <= 0) return 0;
   if (Hkv <= 0 || Hq % Hkv) return -1;
-  if (hd == 64) return bwd_tc<64>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
-  if (hd == 128) return bwd_tc2(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
+  if (hd == 64)
+    return deterministic
+               ? bwd_tc<64, true>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st)
+               : bwd_tc<64, false>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
+  if (hd == 128)
+    return deterministic
+               ? bwd_tc2<true>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st)
+               : bwd_tc2<false>(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, cs, err, st);
   return -1;
 }
 

@@ -772,7 +772,7 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   {
     Timed t(c, 1, 2.5 * attn_fwd_flops(B, S, Hq, hd));
     if (sf::attn_bwd(c->qkv, c->o, c->dob, c->lse, c->delta, c->dq_acc, c->dqkv, B, S, Hq, Hkv,
-                     hd, c->rope_cs, c->dev_err, c->sC) != 0) {
+                     hd, c->rope_cs, c->cfg.deterministic != 0, c->dev_err, c->sC) != 0) {
       ctx->set_err("attention backward launch failed");
       return SF_ECUDA;
     }
@@ -905,7 +905,8 @@ int init(sf_ctx* ctx) {
        dalloc(ctx, &ctx->lse, T * cf.n_heads) && dalloc(ctx, &ctx->h, T * d);
   ok = ok && dalloc(ctx, &ctx->dX, T * d) && dalloc(ctx, &ctx->dw2, T * d) &&
        dalloc(ctx, &ctx->dh, T * d) && dalloc(ctx, &ctx->du, T * d) &&
-       dalloc(ctx, &ctx->dq_acc, T * ctx->qdim) && dalloc(ctx, &ctx->delta, T * cf.n_heads) &&
+       dalloc(ctx, &ctx->dq_acc, (cf.deterministic ? (ctx->Smax + 127) / 128 : 1) * T * ctx->qdim) &&
+       dalloc(ctx, &ctx->delta, T * cf.n_heads) &&
        dalloc(ctx, &ctx->dg_part, (int64_t)ctx->dg_parts * d) && dalloc(ctx, &ctx->dXb, T * d) &&
        dalloc(ctx, &ctx->dm, T * F) && dalloc(ctx, &ctx->dab, T * 2 * F) &&
        dalloc(ctx, &ctx->dhb, T * d) && dalloc(ctx, &ctx->dob, T * ctx->qdim) &&

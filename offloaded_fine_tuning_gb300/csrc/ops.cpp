@@ -133,7 +133,7 @@ int sf_op_attn_fwd(const uint16_t* qkv, uint16_t* o, float* lse, int32_t B, int3
 int sf_op_attn_bwd(const uint16_t* qkv, const uint16_t* o, const uint16_t* dout,
                    const float* lse, float* delta, float* dq_acc, uint16_t* dqkv, int32_t B,
                    int32_t S_, int32_t Hq, int32_t Hkv, int32_t hd, const float* table,
-                   void* stream) {
+                   int32_t deterministic, void* stream) {
   if (B < 0 || S_ < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || (hd != 64 && hd != 128)) return SF_EINVAL;
   if (B == 0 || S_ == 0) return SF_OK;
   if (!qkv || !o || !dout || !lse || !delta || !dq_acc || !dqkv) return SF_EINVAL;
@@ -143,7 +143,7 @@ int sf_op_attn_bwd(const uint16_t* qkv, const uint16_t* o, const uint16_t* dout,
   if (sf::attn_bwd(reinterpret_cast<const bf16*>(qkv), reinterpret_cast<const bf16*>(o),
                    reinterpret_cast<const bf16*>(dout), lse, delta, dq_acc,
                    reinterpret_cast<bf16*>(dqkv), B, S_, Hq, Hkv, hd,
-                   reinterpret_cast<const float2*>(table), err, S(stream)) != 0)
+                   reinterpret_cast<const float2*>(table), deterministic != 0, err, S(stream)) != 0)
     return SF_ECUDA;
   return SF_OK;
 }

@@ -60,18 +60,22 @@ void cast_bf16_f32(const __nv_bfloat16* x, float* y, int64_t n, cudaStream_t st)
 // kDevAttnTimeout to *err.
 int attn_fwd(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq,
              int Hkv, int hd, int* err, cudaStream_t st);
-// Backward on tcgen05 (attention_tc.cu).  dq_acc: fp32 scratch [T, Hq*hd]
-// (zeroed inside); delta: fp32 scratch [B, Hq, S].  Writes dQ and dK (inverse
-// RoPE applied when cs != null) and dV into dqkv.
+// Backward on tcgen05 (attention_tc.cu).  delta: fp32 scratch [B, Hq, S].
+// dq_acc: fp32 scratch, [T, Hq*hd] (zeroed inside, partials added in the
+// order they arrive) or, when deterministic, [ceil(S/128)][T, Hq*hd] (one slot
+// per 128-key block, summed in key order: bit-reproducible).  Writes dQ and dK
+// (inverse RoPE applied when cs != null) and dV into dqkv.
 int attn_bwd(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dout,
              const float* lse, float* delta, float* dq_acc, __nv_bfloat16* dqkv, int B, int S,
-             int Hq, int Hkv, int hd, const float2* cs, int* err, cudaStream_t st);
+             int Hq, int Hkv, int hd, const float2* cs, bool deterministic, int* err,
+             cudaStream_t st);
 // delta[b, h, s] = sum_j dO * O over one head's row (attention.cu)
 void attn_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta, int B, int S,
                 int Hq, int hd, cudaStream_t st);
-// dQ = scale * dq_acc, inverse RoPE, into the query columns of dqkv (attention.cu)
+// dQ = scale * (accumulated or slot-summed dq_acc), inverse RoPE, into the
+// query columns of dqkv (attention.cu); slots = 0 for one accumulated buffer.
 void attn_dq_finalize(const float* dq_acc, __nv_bfloat16* dqkv, int B, int S, int Hq, int Hkv,
-                      int hd, float scale, const float2* cs, cudaStream_t st);
+                      int hd, float scale, const float2* cs, int slots, cudaStream_t st);
 
 int num_sms();
 

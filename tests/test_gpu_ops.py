@@ -216,8 +216,9 @@ def split_qkv(qkv, B, S, Hq, Hkv, hd):
     return q, k, v
 
 
+@pytest.mark.parametrize("det", [0, 1])
 @pytest.mark.parametrize("B,S,Hq,Hkv,hd", ATTN_CASES)
-def test_attention_fwd_bwd(B, S, Hq, Hkv, hd):
+def test_attention_fwd_bwd(B, S, Hq, Hkv, hd, det):
     qkv, do = attn_inputs(B, S, Hq, Hkv, hd)
     q, k, v = (a.astype(np.float64) for a in split_qkv(qkv, B, S, Hq, Hkv, hd))
     o_ref, lse_ref = oracle.attention_fwd(q, k, v)
@@ -231,16 +232,24 @@ def test_attention_fwd_bwd(B, S, Hq, Hkv, hd):
     # backward from the kernel's own O and LSE (as in the step), without RoPE
     dq_ref, dk_ref, dv_ref = oracle.attention_bwd(do.reshape(B, S, Hq, hd).astype(np.float64), q, k, v)
     DO = cuda(do, torch.bfloat16)
-    DQKV = torch.zeros_like(QKV)
     DEL = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
-    DQA = torch.empty((B * S, Hq * hd), dtype=torch.float32, device="cuda")
-    assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(), DEL.data_ptr(),
-                          DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0, stream()) == 0
-    sync()
-    gq, gk, gv = split_qkv(host(DQKV), B, S, Hq, Hkv, hd)
+    # garbage in the scratch: the deterministic slots must not need zeroing
+    DQA = torch.full((sf.attn_dq_scratch_floats(B, S, Hq, hd, det),), float("nan"),
+                     dtype=torch.float32, device="cuda")
+    runs = []
+    for _ in range(2 if det else 1):
+        DQKV = torch.zeros_like(QKV)
+        assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(),
+                              DEL.data_ptr(), DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0,
+                              stream(), deterministic=det) == 0
+        sync()
+        runs.append(host(DQKV))
+    gq, gk, gv = split_qkv(runs[0], B, S, Hq, Hkv, hd)
     assert rel_l2(gq, dq_ref) < 1e-2
     assert rel_l2(gk, dk_ref) < 1e-2
     assert rel_l2(gv, dv_ref) < 1e-2
+    if det:  # bit-reproducible
+        assert np.array_equal(runs[0].view(np.uint16), runs[1].view(np.uint16))
 
 
 def test_attention_bwd_with_inverse_rope():
@@ -268,7 +277,8 @@ def test_attention_bwd_with_inverse_rope():
     assert rel_l2(gv, dv) < 1e-2
 
 
-def test_attention_full_size_sampled_heads():
+@pytest.mark.parametrize("det", [0, 1])
+def test_attention_full_size_sampled_heads(det):
     """8B shape: B=8, S=2048, 32 query / 8 kv heads of 128.  Forward output of
     sampled (batch, head) pairs and the backward of one whole kv group."""
     B, S, Hq, Hkv, hd = 8, 2048, 32, 8, 128
@@ -279,10 +289,12 @@ def test_attention_full_size_sampled_heads():
     assert sf.op_attn_fwd(QKV.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, S, Hq, Hkv, hd, stream()) == 0
     DQKV = torch.zeros_like(QKV)
     DEL = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
-    DQA = torch.empty((B * S, Hq * hd), dtype=torch.float32, device="cuda")
+    DQA = torch.empty((sf.attn_dq_scratch_floats(B, S, Hq, hd, det),), dtype=torch.float32,
+                      device="cuda")
     DO = cuda(do, torch.bfloat16)
     assert sf.op_attn_bwd(QKV.data_ptr(), O.data_ptr(), DO.data_ptr(), LSE.data_ptr(),
-                          DEL.data_ptr(), DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0, stream()) == 0
+                          DEL.data_ptr(), DQA.data_ptr(), DQKV.data_ptr(), B, S, Hq, Hkv, hd, 0,
+                          stream(), deterministic=det) == 0
     sync()
     o_all, dqkv_all = host(O), host(DQKV)
     b, g = 5, 6  # one batch row, one kv group (query heads 24..27)

@@ -17,7 +17,10 @@ sf = pytest.importorskip("offloaded_fine_tuning_gb300")
 
 
 def make_model(cfg, mast, **kw):
+    """An engine with the unit masters loaded.  Deterministic by default: the
+    bitwise comparisons below need bit-reproducible attention backward sums."""
     kw.setdefault("retain_grads", 1)
+    kw.setdefault("deterministic", 1)
     m = sf.Model(sf.make_config(cfg, **kw))
     for u, a in mast.items():
         m.load(u, a)
@@ -41,20 +44,21 @@ def compare(cfg, m, loss_ref, g_ref, tol=GRAD_RL2):
     return errs
 
 
+@pytest.mark.parametrize("det", [1, 0])
 @pytest.mark.parametrize("name", ["tiny", "small-gqa", "small-hd128"])
-def test_step_matches_oracle(name):
+def test_step_matches_oracle(name, det):
     cfg = CONFIGS.get(name) or TEST_CONFIGS[name]
     sf.lib(build_if_needed=True)
     mast = masters(cfg)
     tok, lab = inputs.tokens_and_labels(cfg)
     loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
-    with make_model(cfg, mast) as m:
+    with make_model(cfg, mast, deterministic=det) as m:
         assert m.train_step(tok, lab) == sf.SF_OK, m.error()
         compare(cfg, m, loss_ref, g_ref)
-        # a second identical step gives bit-identical results (no state leaks between steps)
-        g0, l0 = m.grads(0), m.loss()
-        assert m.train_step(tok, lab) == sf.SF_OK
-        assert m.loss() == l0 and np.array_equal(m.grads(0), g0)
+        if det:  # a second identical step is bit-identical (no state leaks between steps)
+            g0, l0 = m.grads(0), m.loss()
+            assert m.train_step(tok, lab) == sf.SF_OK
+            assert m.loss() == l0 and np.array_equal(m.grads(0), g0)
 
 
 def test_ring_size_invariance_is_bitwise():

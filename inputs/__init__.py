@@ -17,7 +17,7 @@ import threading
 import numpy as np
 
 from .configs import (ModelConfig, LceConfig, CONFIGS, LCE_STRESS, TEST_CONFIGS,
-                      IGNORE_INDEX, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD,
+                      VARIANT_CONFIGS, IGNORE_INDEX, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD,
                       layer_tensor_shapes, unit_numel)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -133,7 +133,8 @@ def _stream(unit: int, tensor_idx: int) -> int:
 
 def layer_master(cfg: ModelConfig, layer: int, seed: int = SEED_WEIGHTS) -> np.ndarray:
     """fp32 master weights of decoder layer ``layer`` as one flat array, in the
-    unit order g1, Wq, Wk, Wv, Wo, g2, Wg, Wu, Wd (matrices N(0, 0.02), gains 1)."""
+    unit order g1, Wq, Wk, Wv, [bq, bk, bv,] Wo, g2, Wg, Wu, Wd (matrices and
+    biases N(0, 0.02), gains 1)."""
     out = np.empty(unit_numel(cfg, layer), dtype=np.float32)
     off = 0
     for idx, (name, shape) in enumerate(layer_tensor_shapes(cfg)):
@@ -151,6 +152,8 @@ def unit_master(cfg: ModelConfig, unit: int, seed: int = SEED_WEIGHTS) -> np.nda
     if unit >= 0:
         return layer_master(cfg, unit, seed)
     n = unit_numel(cfg, unit)
+    if n == 0:
+        raise ValueError("unit %d has no tensor in this model" % unit)
     if unit == UNIT_FINAL_NORM:
         return np.ones(n, dtype=np.float32)
     return normal(seed, _stream(unit, 0), n, 0.0, 0.02)

@@ -24,6 +24,8 @@ class ModelConfig:
     rms_eps: float = 1e-5
     rope_base: float = 10000.0
     ring_slots: int = 2
+    qkv_bias: bool = False        # Qwen-style biases on the Q, K and V projections
+    tie_embeddings: bool = False  # the LM head is the embedding matrix
 
     @property
     def tokens(self) -> int:
@@ -44,10 +46,13 @@ class LceConfig:
 
 
 def layer_tensor_shapes(c: ModelConfig):
-    """(name, shape) of one decoder layer's tensors in unit order."""
+    """(name, shape) of one decoder layer's tensors in unit order (the Q, K, V
+    biases follow W_v when the model has them)."""
     q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    bias = [("bq", (q,)), ("bk", (kv,)), ("bv", (kv,))] if c.qkv_bias else []
     return [("g1", (c.hidden,)), ("wq", (q, c.hidden)), ("wk", (kv, c.hidden)),
-            ("wv", (kv, c.hidden)), ("wo", (c.hidden, q)), ("g2", (c.hidden,)),
+            ("wv", (kv, c.hidden))] + bias + [
+            ("wo", (c.hidden, q)), ("g2", (c.hidden,)),
             ("wg", (c.ffn, c.hidden)), ("wu", (c.ffn, c.hidden)), ("wd", (c.hidden, c.ffn))]
 
 
@@ -60,6 +65,8 @@ def unit_numel(c: ModelConfig, unit: int) -> int:
                 k *= x
             n += k
         return n
+    if unit == UNIT_LM_HEAD and c.tie_embeddings:
+        return 0  # no separate tensor
     if unit in (UNIT_EMBED, UNIT_LM_HEAD):
         return c.vocab * c.hidden
     if unit == UNIT_FINAL_NORM:
@@ -88,4 +95,17 @@ TEST_CONFIGS = {
                                rope_base=500000.0, ring_slots=2),
     "micro": ModelConfig("micro-2L-d64", 2, 64, 2, 1, 32, 96, 50, 2, 8,
                          rope_base=10000.0, ring_slots=2),
+    # Qwen-style: Q/K/V biases and an LM head tied to the embedding
+    "small-qwen": ModelConfig("small-qwen-3L-d384", 3, 384, 6, 2, 64, 1000, 3000, 2, 200,
+                              rope_base=1000000.0, ring_slots=2, qkv_bias=True,
+                              tie_embeddings=True),
+}
+
+# A full-size model of that family: the Qwen2.5-3B shape (36 layers, hidden
+# 2048, 16 query / 2 kv heads of 128, FFN 11008, vocab 151936, biases on
+# Q/K/V, tied embeddings).
+VARIANT_CONFIGS = {
+    "qwen-3b": ModelConfig("qwen-3b-36L-d2048-gqa-tied", 36, 2048, 16, 2, 128, 11008, 151936,
+                           8, 2048, rms_eps=1e-6, rope_base=1000000.0, ring_slots=3,
+                           qkv_bias=True, tie_embeddings=True),
 }

@@ -20,7 +20,10 @@ Readings taken where the pages are silent:
   * GQA: query head h reads kv head floor(h / (Hq / Hkv)) (contiguous groups).
   * Loss: mean of (logsumexp(z_t) - z_t[y_t]) over the whole batch's rows whose
     label is not IGNORE_INDEX; with no valid row the loss and all gradients are 0.
-  * Embedding and LM head are separate (untied) tensors.
+  * Embedding and LM head are separate tensors, unless the model ties them
+    (then the LM head is the embedding matrix and its gradient is the sum of
+    the two uses).
+  * Qwen-family models add a bias to the Q, K and V projections, before RoPE.
   * Adam: bias-corrected, decoupled weight decay (AdamW form), no clipping.
 """
 from __future__ import annotations
@@ -184,9 +187,12 @@ def layer_fwd(x, p, cfg, cos, sin):
     Hq, Hkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     xf = x.reshape(T, d)
     u, c1 = rmsnorm_fwd(xf, p["g1"], cfg.rms_eps)
-    q = rope_fwd((u @ p["wq"].T).reshape(B, S, Hq, hd), cos, sin)
-    k = rope_fwd((u @ p["wk"].T).reshape(B, S, Hkv, hd), cos, sin)
-    v = (u @ p["wv"].T).reshape(B, S, Hkv, hd)
+    q, k, v = u @ p["wq"].T, u @ p["wk"].T, u @ p["wv"].T
+    if "bq" in p:  # projection biases, added before the rotation
+        q, k, v = q + p["bq"], k + p["bk"], v + p["bv"]
+    q = rope_fwd(q.reshape(B, S, Hq, hd), cos, sin)
+    k = rope_fwd(k.reshape(B, S, Hkv, hd), cos, sin)
+    v = v.reshape(B, S, Hkv, hd)
     o, _ = attention_fwd(q, k, v)
     of = o.reshape(T, Hq * hd)
     h = xf + of @ p["wo"].T
@@ -222,6 +228,8 @@ def layer_bwd(dout, p, cache, cfg, cos, sin):
     dv = dv.reshape(T, Hkv * hd)
     u = cache["u"]
     gr["wq"], gr["wk"], gr["wv"] = dq.T @ u, dk.T @ u, dv.T @ u
+    if "bq" in p:
+        gr["bq"], gr["bk"], gr["bv"] = dq.sum(axis=0), dk.sum(axis=0), dv.sum(axis=0)
     du = dq @ p["wq"] + dk @ p["wk"] + dv @ p["wv"]
     dxn, gr["g1"] = rmsnorm_bwd(du, p["g1"], cache["c1"])
     return dh + dxn, gr
@@ -232,7 +240,8 @@ def layer_bwd(dout, p, cache, cfg, cos, sin):
 class ModelWeights:
     """Weights the step computes with (already rounded to bf16 by the caller
     where the compared path uses bf16).  layers[i] maps g1, wq, wk, wv, wo, g2,
-    wg, wu, wd to arrays in nn.Linear [out, in] layout."""
+    wg, wu, wd (and bq, bk, bv when the model has projection biases) to arrays
+    in nn.Linear [out, in] layout.  lm_head None: tied to the embedding."""
     layers: list
     embed: np.ndarray
     final_norm: np.ndarray
@@ -243,14 +252,18 @@ class ModelWeights:
 def step(w: ModelWeights, tokens, labels, cfg, dtype=np.float64, return_hidden=False):
     """Forward and backward of the whole stack plus mean token cross-entropy.
     tokens, labels: int [B, S].  Returns (loss, grads) with grads = dict(
-    layers=[{name: array}], embed, final_norm, lm_head).  With return_hidden the
-    per-layer inputs X_l, the final hidden states and the logits are returned too."""
+    layers=[{name: array}], embed, final_norm, lm_head).  With a tied LM head
+    (w.lm_head None) grads["lm_head"] is None and grads["embed"] holds both
+    uses of the embedding.  With return_hidden the per-layer inputs X_l, the
+    final hidden states and the logits are returned too."""
     tokens = np.asarray(tokens)
     B, S = tokens.shape
     T, d = B * S, cfg.hidden
     cast = lambda a: np.asarray(a, dtype=dtype)
     layers = [{k: cast(v) for k, v in lp.items()} for lp in w.layers]
-    E, gf, Wlm = cast(w.embed), cast(w.final_norm), cast(w.lm_head)
+    E, gf = cast(w.embed), cast(w.final_norm)
+    tied = w.lm_head is None
+    Wlm = E if tied else cast(w.lm_head)
     cos, sin = rope_tables(S, cfg.head_dim, cfg.rope_base, dtype)
 
     x = E[tokens]                                  # [B, S, d]
@@ -270,6 +283,8 @@ def step(w: ModelWeights, tokens, labels, cfg, dtype=np.float64, return_hidden=F
         dx, g_layers[i] = layer_bwd(dx, layers[i], caches[i], cfg, cos, sin)
     g_E = np.zeros_like(E)
     np.add.at(g_E, tokens.reshape(T), dx)
+    if tied:  # one tensor used twice: its gradient is the sum of both uses
+        g_E, g_lm = g_E + g_lm, None
     grads = dict(layers=g_layers, embed=g_E, final_norm=g_gf, lm_head=g_lm, dx0=dx)
     if return_hidden:
         return loss, grads, dict(xs=xs, x_final=x.reshape(T, d), logits=z, hf=hf)

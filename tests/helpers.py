@@ -24,10 +24,12 @@ def rel_l2(a, b) -> float:
 
 
 def masters(cfg):
-    """fp32 master arrays per unit, as the library receives them."""
+    """fp32 master arrays per unit, as the library receives them (no LM-head
+    unit when it is tied to the embedding)."""
     m = {l: inputs.unit_master(cfg, l) for l in range(cfg.n_layers)}
     for u in (UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD):
-        m[u] = inputs.unit_master(cfg, u)
+        if inputs.unit_numel(cfg, u):
+            m[u] = inputs.unit_master(cfg, u)
     return m
 
 
@@ -43,7 +45,7 @@ def oracle_weights(cfg, mast=None, round_bf16=True) -> ModelWeights:
     return ModelWeights(layers=layers,
                         embed=r(mast[UNIT_EMBED]).reshape(V, d),
                         final_norm=r(mast[UNIT_FINAL_NORM]),
-                        lm_head=r(mast[UNIT_LM_HEAD]).reshape(V, d))
+                        lm_head=None if cfg.tie_embeddings else r(mast[UNIT_LM_HEAD]).reshape(V, d))
 
 
 def flat_layer_grads(cfg, g: dict) -> np.ndarray:

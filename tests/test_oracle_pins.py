@@ -268,16 +268,17 @@ def torch_model_loss(w, tok, lab, cfg):
     for i, lp in enumerate(w.layers):
         p = {k: P(f"{i}.{k}", v) for k, v in lp.items()}
         u = F.rms_norm(x, (cfg.hidden,), weight=p["g1"], eps=cfg.rms_eps)
-        q = F.linear(u, p["wq"]).view(B, S, cfg.n_heads, cfg.head_dim)
-        k = F.linear(u, p["wk"]).view(B, S, cfg.n_kv_heads, cfg.head_dim)
-        v = F.linear(u, p["wv"]).view(B, S, cfg.n_kv_heads, cfg.head_dim)
+        q = F.linear(u, p["wq"], p.get("bq")).view(B, S, cfg.n_heads, cfg.head_dim)
+        k = F.linear(u, p["wk"], p.get("bk")).view(B, S, cfg.n_kv_heads, cfg.head_dim)
+        v = F.linear(u, p["wv"], p.get("bv")).view(B, S, cfg.n_kv_heads, cfg.head_dim)
         q, k = rope_complex_torch(q, cfg.rope_base), rope_complex_torch(k, cfg.rope_base)
         o = torch_causal_attention(q, k, v).reshape(B, S, -1)
         h = x + F.linear(o, p["wo"])
         w2 = F.rms_norm(h, (cfg.hidden,), weight=p["g2"], eps=cfg.rms_eps)
         x = h + F.linear(F.silu(F.linear(w2, p["wg"])) * F.linear(w2, p["wu"]), p["wd"])
     hf = F.rms_norm(x, (cfg.hidden,), weight=P("final_norm", w.final_norm), eps=cfg.rms_eps)
-    z = F.linear(hf, P("lm_head", w.lm_head)).reshape(B * S, -1)
+    # a tied head is the same leaf tensor as the embedding: autograd sums both uses
+    z = F.linear(hf, E if w.lm_head is None else P("lm_head", w.lm_head)).reshape(B * S, -1)
     loss = F.cross_entropy(z, torch.tensor(lab.reshape(-1), dtype=torch.long),
                            ignore_index=IGNORE_INDEX)
     loss.backward()
@@ -292,7 +293,11 @@ def step_vs_torch_error(cfg):
     errs = [abs(loss - lt) / lt]
     for i, lg in enumerate(g["layers"]):
         errs += [rel_l2(v, gt[f"{i}.{k}"]) for k, v in lg.items()]
-    errs += [rel_l2(g[k], gt[k]) for k in ("embed", "final_norm", "lm_head")]
+    errs += [rel_l2(g[k], gt[k]) for k in ("embed", "final_norm")]
+    if w.lm_head is None:
+        assert g["lm_head"] is None and "lm_head" not in gt
+    else:
+        errs.append(rel_l2(g["lm_head"], gt["lm_head"]))
     return max(errs)
 
 
@@ -300,6 +305,63 @@ def step_vs_torch_error(cfg):
 def test_step_matches_torch_autograd(name):
     cfg = CONFIGS.get(name) or TEST_CONFIGS[name]
     assert step_vs_torch_error(cfg) < 1e-10
+
+
+@pytest.mark.parametrize("bias,tied", [(True, False), (False, True), (True, True)])
+def test_variant_step_matches_torch_autograd(bias, tied):
+    """Projection biases and a tied LM head: the oracle against torch autograd
+    on the model assembled from library ops (F.linear with its bias argument;
+    the embedding leaf reused as the head)."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, qkv_bias=bias, tie_embeddings=tied)
+    assert step_vs_torch_error(cfg) < 1e-10
+
+
+def test_zero_biases_and_tying_reduce_to_the_plain_model():
+    """Zero projection biases change nothing; a tied model equals the untied
+    one whose head is a copy of the embedding, with the two gradients summed."""
+    base = TEST_CONFIGS["micro"]
+    w = oracle_weights(base)
+    tok, lab = inputs.tokens_and_labels(base)
+    loss0, g0 = oracle.step(w, tok, lab, base)
+    wb = oracle_weights(base)
+    for lp in wb.layers:
+        lp["bq"] = np.zeros(base.n_heads * base.head_dim)
+        lp["bk"] = np.zeros(base.n_kv_heads * base.head_dim)
+        lp["bv"] = np.zeros(base.n_kv_heads * base.head_dim)
+    loss1, g1 = oracle.step(wb, tok, lab, base.with_(qkv_bias=True))
+    assert loss1 == loss0
+    assert all(np.array_equal(a[k], b[k]) for a, b in zip(g0["layers"], g1["layers"]) for k in a)
+    wu = oracle_weights(base)
+    wu.lm_head = wu.embed.copy()
+    lu, gu = oracle.step(wu, tok, lab, base)
+    wt = oracle_weights(base)
+    wt.lm_head = None
+    lt, gt = oracle.step(wt, tok, lab, base.with_(tie_embeddings=True))
+    assert lt == lu
+    assert rel_l2(gt["embed"], gu["embed"] + gu["lm_head"]) < 1e-14
+
+
+def test_gradient_accumulation_identity():
+    """Accumulating micro-batches: the full-batch gradient equals the sum of
+    the micro-batch gradients each weighted by its share of the valid labels
+    (the global-mean loss), the reading the engine's accumulation follows."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, batch=3)
+    w = oracle_weights(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lab = lab.copy()
+    lab[1, :50] = IGNORE_INDEX  # unequal valid counts per micro-batch
+    loss, g = oracle.step(w, tok, lab, cfg)
+    n_all = int(np.sum(lab != IGNORE_INDEX))
+    parts = []
+    for b in range(cfg.batch):
+        n_b = int(np.sum(lab[b] != IGNORE_INDEX))
+        lb, gb = oracle.step(w, tok[b:b + 1], lab[b:b + 1], cfg.with_(batch=1))
+        parts.append((n_b / n_all, lb, gb))
+    assert abs(sum(f * l for f, l, _ in parts) - loss) < 1e-12
+    for k in g["layers"][0]:
+        acc = sum(f * gb["layers"][0][k] for f, _, gb in parts)
+        assert rel_l2(acc, g["layers"][0][k]) < 1e-12, k
+    assert rel_l2(sum(f * gb["embed"] for f, _, gb in parts), g["embed"]) < 1e-12
 
 
 def test_fp32_oracle_close_to_fp64():
@@ -326,7 +388,9 @@ def fd_max_error(cfg, n_coords=3, seed=5):
         lp["g2"] = lp["g2"] + 0.1 * rng.standard_normal(lp["g2"].shape)
     w.final_norm = w.final_norm + 0.1 * rng.standard_normal(w.final_norm.shape)
     w.layers = [{k: v.astype(np.float64) for k, v in lp.items()} for lp in w.layers]
-    w.embed, w.final_norm, w.lm_head = (a.astype(np.float64) for a in (w.embed, w.final_norm, w.lm_head))
+    w.embed, w.final_norm = w.embed.astype(np.float64), w.final_norm.astype(np.float64)
+    if w.lm_head is not None:
+        w.lm_head = w.lm_head.astype(np.float64)
     _, g = oracle.step(w, tok, lab, cfg)
 
     def tensors():
@@ -334,7 +398,8 @@ def fd_max_error(cfg, n_coords=3, seed=5):
             for k in lp:
                 yield lp, k, g["layers"][i][k]
         yield w.__dict__, "final_norm", g["final_norm"]
-        yield w.__dict__, "lm_head", g["lm_head"]
+        if w.lm_head is not None:
+            yield w.__dict__, "lm_head", g["lm_head"]
         yield w.__dict__, "embed", g["embed"]
 
     worst = 0.0
@@ -361,6 +426,11 @@ def fd_max_error(cfg, n_coords=3, seed=5):
 
 def test_finite_differences_fp64():
     assert fd_max_error(TEST_CONFIGS["micro"]) < 1e-6
+
+
+def test_finite_differences_fp64_biases_and_tied_head():
+    cfg = TEST_CONFIGS["micro"].with_(qkv_bias=True, tie_embeddings=True)
+    assert fd_max_error(cfg) < 1e-6
 
 
 # ------------------------------------------------------------------ Adam
@@ -448,6 +518,20 @@ def test_planted_mistake_is_caught(monkeypatch, target, mutant, pin):
     assert pin() < 1e-10
     monkeypatch.setattr(ls, target, mutant)
     assert pin() > 1e-3
+
+
+def test_planted_bias_gradient_mistake_is_caught(monkeypatch):
+    """Dropping the K-bias gradient in the oracle fails the autograd pin."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, qkv_bias=True)
+    assert step_vs_torch_error(cfg) < 1e-10
+    orig = ls.layer_bwd
+
+    def mutant(*args, **kw):
+        dx, gr = orig(*args, **kw)
+        gr["bk"] = np.zeros_like(gr["bk"])
+        return dx, gr
+    monkeypatch.setattr(ls, "layer_bwd", mutant)
+    assert step_vs_torch_error(cfg) > 1e-3
 
 
 def test_planted_backward_mistake_is_caught_by_finite_differences(monkeypatch):

@@ -94,7 +94,13 @@ typedef struct sf_ctx sf_ctx;
  *     the last bits of a gradient can differ between two identical steps;
  *     1 = every key block writes its own slot and the slots are summed in key
  *     order (bit-reproducible steps, ~ceil(max_seq/128) x more dQ scratch in
- *     device memory and one extra pass over it). */
+ *     device memory and one extra pass over it).
+ *   qkv_bias: 1 = the Q, K and V projections have biases (Qwen family); a
+ *     layer unit then holds bq [Hq*hd], bk [Hkv*hd], bv [Hkv*hd] right after
+ *     W_v, and the biases are added before the rotary embedding.
+ *   tie_embeddings: 1 = the LM head is the embedding matrix; there is no
+ *     SF_UNIT_LM_HEAD unit (its numel is 0) and the embedding's gradient is
+ *     the sum of both uses. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -108,6 +114,8 @@ typedef struct {
   int32_t async_update;
   int32_t offload_activations;
   int32_t deterministic;
+  int32_t qkv_bias;
+  int32_t tie_embeddings;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -175,6 +183,19 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* fp32_master, s
  * SF_ESTATE. */
 int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
                   int32_t seq, const sf_adam* adam);
+
+/* Gradient accumulation: one optimizer step over n_micro micro-batches of
+ * batch x seq tokens each (tokens, labels: [n_micro, batch, seq] int32).  The
+ * micro-batches run through the ring one after another; each one's gradients
+ * are added into fp32 sums on the host (allocated on the first call with
+ * n_micro > 1: 4 bytes per parameter), and the host update, overlapped with
+ * the last micro-batch's backward as in sf_train_step, uses the sums.  The
+ * result equals one sf_train_step over the n_micro * batch sequences: the
+ * loss is the mean over every valid label of the step, and sf_get_grads
+ * returns the summed gradients.  Same errors as sf_train_step; every
+ * micro-batch is checked before the first one runs. */
+int sf_train_step_accum(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels,
+                        int32_t n_micro, int32_t batch, int32_t seq, const sf_adam* adam);
 
 /* Gradient of the last step for `unit`, in sf_unit_numel order, upcast from
  * the bf16 values that were streamed to the host (the embedding gradient is
@@ -245,6 +266,22 @@ int sf_debug_inject(sf_ctx* ctx, int32_t what, int32_t arg);
 int sf_op_gemm(int32_t layout, int32_t epi, int64_t M, int64_t N, int64_t K, const void* A,
                int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R,
                int64_t ldr, float alpha, void* stream);
+
+/* C[M,N] bf16 = alpha * A[M,K] * B[N,K]^T + bias[N]: a projection forward with
+ * a bias (the Q, K, V projections of Qwen-family models), the bias added to
+ * the fp32 accumulator before the rounding.  bias bf16 [N], 64-byte aligned;
+ * the other arguments as for sf_op_gemm with layout 0. */
+int sf_op_gemm_bias(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, void* C, int64_t ldc, const uint16_t* bias, float alpha,
+                    void* stream);
+
+/* Gradient of a bias: db[c] = sum over the rows r of dy[r, c], dy bf16 [rows,
+ * cols] with row stride ld (cols even, ld even, 4-byte aligned), db bf16
+ * [cols]; fp32 accumulation in a fixed order (bit-reproducible).  part: fp32
+ * scratch of sf_op_bias_grad_scratch(rows, cols) floats. */
+int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, float* part,
+                    uint16_t* db, void* stream);
+int64_t sf_op_bias_grad_scratch(int64_t rows, int32_t cols);
 
 /* y[r] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)), rstd[r] = 1/sqrt(...);
  * x fp32 [rows, d], g bf16 [d], y bf16 [rows, d], rstd fp32 [rows]. */

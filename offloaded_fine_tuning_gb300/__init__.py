@@ -42,7 +42,8 @@ class Config(ctypes.Structure):
                [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
                 ("device", ctypes.c_int32), ("adam_threads", ctypes.c_int32),
                 ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32),
-                ("offload_activations", ctypes.c_int32), ("deterministic", ctypes.c_int32)]
+                ("offload_activations", ctypes.c_int32), ("deterministic", ctypes.c_int32),
+                ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32)]
 
 
 class Adam(ctypes.Structure):
@@ -79,6 +80,7 @@ _SIGS = {
     "sf_last_error": (ctypes.c_char_p, [_VP]),
     "sf_load_layer_weights": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_train_step": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, ctypes.POINTER(Adam)]),
+    "sf_train_step_accum": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, ctypes.POINTER(Adam)]),
     "sf_get_grads": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_get_weights": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_loss": (ctypes.c_int, [_VP, ctypes.POINTER(_F32)]),
@@ -96,6 +98,10 @@ _SIGS = {
     "sf_op_rmsnorm_bwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_rope_table": (ctypes.c_int, [_I32, _I32, _F32, _VP]),
     "sf_op_rope": (ctypes.c_int, [_VP, _I64, _I64, _I32, _I32, _I32, _VP, _I32, _VP]),
+    "sf_op_gemm_bias": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _VP,
+                                       ctypes.c_float, _VP]),
+    "sf_op_bias_grad": (ctypes.c_int, [_VP, _I64, _I64, _I32, _VP, _VP, _VP]),
+    "sf_op_bias_grad_scratch": (ctypes.c_int64, [_I64, _I32]),
     "sf_op_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
     "sf_op_attn_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                       _I32, _VP, _I32, _VP]),
@@ -148,7 +154,9 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   retain_grads=retain_grads, rms_eps=shape.rms_eps, rope_base=shape.rope_base,
                   device=device, adam_threads=adam_threads, wait_timeout_ms=wait_timeout_ms,
                   async_update=async_update, offload_activations=offload_activations,
-                  deterministic=deterministic)
+                  deterministic=deterministic,
+                  qkv_bias=int(getattr(shape, "qkv_bias", False)),
+                  tie_embeddings=int(getattr(shape, "tie_embeddings", False)))
 
 
 def unit_numel(cfg: Config, unit: int) -> int:
@@ -205,6 +213,21 @@ class Model:
 
     def step(self, tokens, labels, adam: Adam | None = None) -> float:
         _check(self.train_step(tokens, labels, adam), self.h, "sf_train_step")
+        return self.loss()
+
+    def train_step_accum(self, tokens: np.ndarray, labels: np.ndarray,
+                         adam: Adam | None = None) -> int:
+        """One optimizer step over micro-batches: tokens, labels [n_micro, batch, seq].
+        Returns the status."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        y = np.ascontiguousarray(labels, dtype=np.int32)
+        assert t.shape == y.shape and t.ndim == 3
+        return lib().sf_train_step_accum(self.h, t.ctypes.data, y.ctypes.data, t.shape[0],
+                                         t.shape[1], t.shape[2],
+                                         ctypes.byref(adam) if adam is not None else None)
+
+    def step_accum(self, tokens, labels, adam: Adam | None = None) -> float:
+        _check(self.train_step_accum(tokens, labels, adam), self.h, "sf_train_step_accum")
         return self.loss()
 
     def loss(self) -> float:
@@ -286,6 +309,18 @@ def op_rope(x, ld, tokens, seq, heads, head_dim, table, inverse=0, stream=0) -> 
 
 def op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, stream=0) -> int:
     return lib().sf_op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, _s(stream))
+
+
+def op_gemm_bias(M, N, K, A, lda, B, ldb, C, ldc, bias, alpha=1.0, stream=0) -> int:
+    return lib().sf_op_gemm_bias(M, N, K, A, lda, B, ldb, C, ldc, bias, alpha, _s(stream))
+
+
+def op_bias_grad(dy, ld, rows, cols, part, db, stream=0) -> int:
+    return lib().sf_op_bias_grad(dy, ld, rows, cols, part, db, _s(stream))
+
+
+def bias_grad_scratch_floats(rows, cols) -> int:
+    return int(lib().sf_op_bias_grad_scratch(rows, cols))
 
 
 def op_attn_bwd(qkv, o, dout, lse, delta, dq_acc, dqkv, B, S, Hq, Hkv, hd, table=0, stream=0,

@@ -204,6 +204,33 @@ void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, 
   reduce_parts_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d, out);
 }
 
+// Column sums of x [rows, cols] bf16 (row stride ld) as fp32 partials:
+// part[p][c] sums the rows [rows*p/parts, rows*(p+1)/parts).  Two columns per
+// thread, so a warp reads 128 contiguous bytes of a row.
+__global__ void colsum_parts_kernel(const __nv_bfloat16* __restrict__ x, int64_t ld, int64_t rows,
+                                    int cols, float* __restrict__ part, int parts) {
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  const int p = blockIdx.y;
+  if (c >= cols) return;
+  const int64_t r0 = rows * p / parts, r1 = rows * (p + 1) / parts;
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+  for (int64_t r = r0; r < r1; ++r) {
+    const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + r * ld + c));
+    s0 += v.x;
+    s1 += v.y;
+  }
+  part[(int64_t)p * cols + c] = s0;
+  part[(int64_t)p * cols + c + 1] = s1;
+}
+
+void bias_grad(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float* part, int parts,
+               __nv_bfloat16* out, cudaStream_t st) {
+  dim3 grid((unsigned)((cols / 2 + 127) / 128), (unsigned)parts);
+  colsum_parts_kernel<<<grid, 128, 0, st>>>(x, ld, rows, cols, part, parts);
+  reduce_parts_bf16(part, parts, cols, out, st);
+}
+
 // ------------------------------------------------------------------ RoPE
 // In place on the first `heads` heads of each token row of qkv.  cs[s*hd/2 + j]
 // = (cos, sin) of s * base^(-2j/hd).  inverse = 1 rotates by the opposite angle

@@ -133,7 +133,13 @@ struct HostUnit {
   uint16_t* pack = nullptr;   // pinned
   std::unique_ptr<float[]> master, m, v;
   std::vector<uint16_t> retained;  // last step's gradients (retain_grads)
+  std::unique_ptr<float[]> acc;    // gradient sum over the micro-batches of a step
+  std::vector<float> retained_acc; // last accumulated step's summed gradients
 };
+
+// Where a micro-batch stands in a step: the only one, or the first, a middle
+// or the last of several whose gradients are summed before the update.
+enum Phase : int { kOnly = 0, kFirst = 1, kMid = 2, kLast = 3 };
 
 // Adam constants of one step (bias corrections folded in by adam_consts).
 struct AdamK {
@@ -153,7 +159,9 @@ struct sf_ctx {
   bool poisoned = false;
   int L = 0, R = 0;
   int64_t d = 0, qdim = 0, kvdim = 0, qkvdim = 0, F = 0, V = 0, Tmax = 0, Smax = 0;
-  int64_t off_g1 = 0, off_qkv = 0, off_o = 0, off_g2 = 0, off_gu = 0, off_d = 0, pack_elems = 0;
+  int64_t off_g1 = 0, off_qkv = 0, off_bqkv = 0, off_o = 0, off_g2 = 0, off_gu = 0, off_d = 0,
+          pack_elems = 0;
+  bool bias = false, tied = false;  // Q/K/V projection biases; LM head = embedding
   std::vector<Seg> segs;
   int64_t chunk_rows = 0;
   int dg_parts = 0;
@@ -218,6 +226,7 @@ struct sf_ctx {
     sf_adam adam;
     int64_t t;
     int arg;        // row range of a deferred embedding-update task
+    int phase;      // micro-batch phase (Phase)
   };
   std::deque<Task> aq;
   int aq_pending = 0;
@@ -237,6 +246,8 @@ struct sf_ctx {
   std::string aq_err;
   bool aq_stop = false;
   const sf_adam* cur_adam = nullptr;
+  int phase = kOnly;          // of the micro-batch being run; copied into its tasks
+  bool last_accum = false;    // the last step summed several micro-batches
   double upd_layer_ms = 0.0;  // host Adam time of layer tasks since the last stats
   int64_t upd_layer_n = 0;
   sf_adam adam_copy{};
@@ -380,6 +391,33 @@ void refresh_bf16_span(uint16_t* __restrict p, const float* __restrict w, int64_
   for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
 }
 
+// A micro-batch's gradient (bf16 in the pack) into the fp32 sum, then the
+// unchanged weights back into the pack for the next micro-batch's copy.
+void accum_span(uint16_t* __restrict p, float* __restrict acc, const float* __restrict w,
+                int64_t b, int64_t e, bool first) {
+  for (int64_t i = b; i < e; ++i) {
+    const float g = bf2f(p[i]);
+    acc[i] = first ? g : acc[i] + g;
+    p[i] = f2bf(w[i]);
+  }
+}
+
+// Adam on the summed gradient (fp32 sum + the last micro-batch's bf16 part).
+void adam_acc_span(uint16_t* __restrict p, const float* __restrict acc, float* __restrict w,
+                   float* __restrict m, float* __restrict v, int64_t b, int64_t e, const AdamK k) {
+  for (int64_t i = b; i < e; ++i) {
+    const float g = acc[i] + bf2f(p[i]);
+    const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
+    const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
+    float th = w[i];
+    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    m[i] = mi;
+    v[i] = vi;
+    w[i] = th;
+    p[i] = f2bf(th);
+  }
+}
+
 AdamK adam_consts(const sf_adam& a, int64_t step_t) {
   return {a.beta1, a.beta2, a.lr, a.eps, a.weight_decay, 1.f - std::pow(a.beta1, (float)step_t),
           1.f - std::pow(a.beta2, (float)step_t)};
@@ -387,9 +425,42 @@ AdamK adam_consts(const sf_adam& a, int64_t step_t) {
 
 // One unit: optional copy of the gradients, then either the Adam update of the
 // fp32 master (refreshing the bf16 pack in place) or, without an optimizer, a
-// refresh of the pack from the unchanged master.
+// refresh of the pack from the unchanged master.  Micro-batches before the
+// last only add their gradient into the unit's fp32 sum; the last one updates
+// with the whole sum.
 void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_adam& a,
-                 int64_t step_t) {
+                 int64_t step_t, int phase) {
+  uint16_t* p = hu.pack;
+  float* w = hu.master.get();
+  float* acc = hu.acc.get();
+  if (phase == kFirst || phase == kMid) {
+    const bool first = phase == kFirst;
+    ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, first](int64_t b, int64_t e) {
+      accum_span(p, acc, w, b, e, first);
+    });
+    return;
+  }
+  if (phase == kLast) {
+    if (retain) {
+      hu.retained_acc.resize((size_t)hu.elems);
+      float* dst = hu.retained_acc.data();
+      ctx->pool->parallel_for(hu.elems, 1 << 16, [dst, p, acc](int64_t b, int64_t e) {
+        for (int64_t i = b; i < e; ++i) dst[i] = acc[i] + bf2f(p[i]);
+      });
+    }
+    if (!adam_on) {
+      ctx->pool->parallel_for(hu.elems, 1 << 16,
+                              [p, w](int64_t b, int64_t e) { refresh_bf16_span(p, w, b, e); });
+      return;
+    }
+    const AdamK k = adam_consts(a, step_t);
+    float* m = hu.m.get();
+    float* v = hu.v.get();
+    ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, m, v, k](int64_t b, int64_t e) {
+      adam_acc_span(p, acc, w, m, v, b, e, k);
+    });
+    return;
+  }
   if (retain) {
     hu.retained.resize((size_t)hu.elems);
     uint16_t* dst = hu.retained.data();
@@ -398,8 +469,6 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_
       std::memcpy(dst + b, src + b, (size_t)(e - b) * 2);
     });
   }
-  uint16_t* p = hu.pack;
-  float* w = hu.master.get();
   if (!adam_on) {
     ctx->pool->parallel_for(hu.elems, 1 << 16,
                             [p, w](int64_t b, int64_t e) { refresh_bf16_span(p, w, b, e); });
@@ -431,6 +500,7 @@ void e_update_row(sf_ctx* ctx, int64_t r) {
     const int64_t d = ctx->d, o = r * d;
     adam_f32_span(ctx->dE.get() + o, ctx->E.get() + o, ctx->Em.get() + o, ctx->Ev.get() + o, 0, d,
                   ctx->e_k);
+    if (ctx->tied) refresh_bf16_span(ctx->lm.pack + o, ctx->E.get() + o, 0, d);  // the head's copy
     st.store(2, std::memory_order_release);
   } else {
     while (st.load(std::memory_order_acquire) != 2) std::this_thread::yield();
@@ -450,16 +520,27 @@ void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg = 0);
 // update of the embedding is then deferred: the next step's gather updates the
 // rows its tokens need, and background tasks of the lowest priority update
 // the rest while the update thread would otherwise wait for gradients.
-void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
+// A tied LM head adds its (dense) gradient, which the head's pack holds, to
+// every row, and each row's update refreshes that row of the head's pack.
+// Micro-batches before the last only add into dE (and put the unchanged
+// embedding back into the head's pack for the next micro-batch).
+void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int phase) {
   const int64_t d = ctx->d, V = ctx->V, T = (int64_t)ctx->tok_copy.size();
   if (ctx->e_pending) e_update_rows(ctx, 0, V);  // finish a previous update first
   ctx->e_pending = false;
   float* dE = ctx->dE.get();
-  {
+  const bool first = phase == kOnly || phase == kFirst;
+  if (ctx->tied) {
+    const uint16_t* gh = ctx->lm.pack;
+    ctx->pool->parallel_for(V * d, 1 << 16, [dE, gh, first](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i) dE[i] = (first ? 0.f : dE[i]) + bf2f(gh[i]);
+    });
+  } else if (first) {
     const int32_t* rows = ctx->e_rows.data();
     ctx->pool->parallel_for((int64_t)ctx->e_rows.size(), 64, [rows, dE, d](int64_t b, int64_t e) {
       for (int64_t i = b; i < e; ++i) std::memset(dE + (int64_t)rows[i] * d, 0, (size_t)d * 4);
     });
+    ctx->e_rows.clear();
   }
   const int32_t* tokens = ctx->tok_copy.data();
   const uint16_t* g = ctx->x0_pin;
@@ -470,10 +551,20 @@ void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t) {
       for (int64_t j = c0; j < c1; ++j) row[j] += bf2f(gr[j]);
     }
   });
-  ctx->e_rows.assign(ctx->tok_copy.begin(), ctx->tok_copy.end());
-  std::sort(ctx->e_rows.begin(), ctx->e_rows.end());
-  ctx->e_rows.erase(std::unique(ctx->e_rows.begin(), ctx->e_rows.end()), ctx->e_rows.end());
-  if (!adam_on) return;
+  if (!ctx->tied) {  // rows holding gradient, zeroed before the next step's scatter
+    ctx->e_rows.insert(ctx->e_rows.end(), ctx->tok_copy.begin(), ctx->tok_copy.end());
+    std::sort(ctx->e_rows.begin(), ctx->e_rows.end());
+    ctx->e_rows.erase(std::unique(ctx->e_rows.begin(), ctx->e_rows.end()), ctx->e_rows.end());
+  }
+  const bool last = phase == kOnly || phase == kLast;
+  if (!last || !adam_on) {
+    if (ctx->tied) {  // the head's pack holds gradients: put the weights back
+      uint16_t* p = ctx->lm.pack;
+      const float* E = ctx->E.get();
+      ctx->pool->parallel_for(V * d, 1 << 16, [p, E](int64_t b, int64_t e) { refresh_bf16_span(p, E, b, e); });
+    }
+    return;
+  }
   ctx->e_k = adam_consts(a, step_t);
   for (int64_t r = 0; r < V; ++r) ctx->e_state[r].store(0, std::memory_order_relaxed);
   std::atomic_thread_fence(std::memory_order_release);
@@ -500,10 +591,10 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED && t.unit != kUnitEmbedRest) {
     // the gradients are dropped: put the unchanged weights back into the pack
     if (t.unit >= 0) {
-      host_update(ctx, ctx->layers[t.unit], false, false, t.adam, t.t);
+      host_update(ctx, ctx->layers[t.unit], false, false, t.adam, t.t, kOnly);
     } else {
-      host_update(ctx, ctx->lm, false, false, t.adam, t.t);
-      host_update(ctx, ctx->fn, false, false, t.adam, t.t);
+      if (!ctx->tied) host_update(ctx, ctx->lm, false, false, t.adam, t.t, kOnly);
+      host_update(ctx, ctx->fn, false, false, t.adam, t.t, kOnly);
     }
     finish_task(ctx, t, SF_ESTATE, "injected Adam worker failure on unit " + std::to_string(t.unit));
     return;
@@ -512,15 +603,15 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   trace(ctx, 5, t.unit);
   const bool retain = ctx->cfg.retain_grads != 0;
   if (t.unit >= 0) {
-    host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t);
+    host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t, t.phase);
   } else if (t.unit == SF_UNIT_EMBED) {
-    embed_grad(ctx, t.adam_on, t.adam, t.t);
+    embed_grad(ctx, t.adam_on, t.adam, t.t, t.phase);
   } else if (t.unit == kUnitEmbedRest) {
     const int64_t V = ctx->V;
     e_update_rows(ctx, V * t.arg / kEmbedRestTasks, V * (t.arg + 1) / kEmbedRestTasks);
-  } else {  // LM head and final norm
-    host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t);
-    host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t);
+  } else {  // LM head (unless tied: the embedding task takes its gradient) and final norm
+    if (!ctx->tied) host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t, t.phase);
+    host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t, t.phase);
   }
   const double ms = std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
   ctx->adam_ms += ms;
@@ -586,7 +677,7 @@ void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg) {
                      : unit == kUnitEmbedRest ? ctx->L + 1
                      : (unit >= 0 ? unit : ctx->L);
     ctx->aq.push_back({unit, ev, prio, Clock::now() + std::chrono::milliseconds(ctx->wait_ms),
-                       ctx->adam_on, ctx->adam_copy, ctx->adam_t, arg});
+                       ctx->adam_on, ctx->adam_copy, ctx->adam_t, arg, ctx->phase});
     ++ctx->unit_pending[unit_slot(ctx, unit)];
     ++ctx->aq_pending;
   }
@@ -665,11 +756,12 @@ struct Timed {
 
 int gemm(sf_ctx* ctx, int layout, int epi, int64_t M, int64_t N, int64_t K, const void* A,
          int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R = nullptr,
-         int64_t ldr = 0, float alpha = 1.f) {
+         int64_t ldr = 0, float alpha = 1.f, const void* bias = nullptr) {
   sf::GemmArgs g;
   g.layout = layout; g.epi = epi; g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.R = R; g.ldr = ldr;
   g.alpha = alpha;
+  g.bias = bias;
   int st;
   char why[128] = {0};
   {
@@ -707,18 +799,20 @@ float* xck(sf_ctx* c, int l, int64_t T) {
 
 // ------------------------------------------------------------------ layer compute
 struct LayerW {
-  const bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+  const bf16 *g1, *wqkv, *bqkv, *wo, *g2, *wgu, *wd;  // bqkv null without projection biases
 };
 struct LayerG {
-  bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+  bf16 *g1, *wqkv, *bqkv, *wo, *g2, *wgu, *wd;
 };
 LayerW slot_w(sf_ctx* c, int s) {
   const bf16* b = c->ring[s];
-  return {b + c->off_g1, b + c->off_qkv, b + c->off_o, b + c->off_g2, b + c->off_gu, b + c->off_d};
+  return {b + c->off_g1, b + c->off_qkv, c->bias ? b + c->off_bqkv : nullptr, b + c->off_o,
+          b + c->off_g2, b + c->off_gu, b + c->off_d};
 }
 LayerG slot_g(sf_ctx* c, int s) {
   bf16* b = c->ring[s] + c->pack_elems;
-  return {b + c->off_g1, b + c->off_qkv, b + c->off_o, b + c->off_g2, b + c->off_gu, b + c->off_d};
+  return {b + c->off_g1, b + c->off_qkv, c->bias ? b + c->off_bqkv : nullptr, b + c->off_o,
+          b + c->off_g2, b + c->off_gu, b + c->off_d};
 }
 
 // Forward of one layer from X_l (fp32) to X_{l+1}; with `full == false` the
@@ -730,7 +824,11 @@ int layer_forward(sf_ctx* c, const LayerW& w, const float* Xin, float* Xout, int
   const int64_t T = (int64_t)B * S, d = c->d, F = c->F;
   const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
   sf::rmsnorm_fwd(Xin, w.g1, c->u, c->rstd1, T, (int)d, c->cfg.rms_eps, c->sC);
-  RET(gemm(c, sf::kNT, sf::kEpiBF16, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim));
+  if (w.bqkv)  // projection biases, added to the fp32 accumulator before RoPE
+    RET(gemm(c, sf::kNT, sf::kEpiBF16Bias, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim,
+             nullptr, 0, 1.f, w.bqkv));
+  else
+    RET(gemm(c, sf::kNT, sf::kEpiBF16, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim));
   sf::rope_inplace(c->qkv, c->qkvdim, T, S, Hq + Hkv, hd, c->rope_cs, 0, c->sC);
   {
     Timed t(c, 1, attn_fwd_flops(B, S, Hq, hd));
@@ -777,6 +875,11 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
       return SF_ECUDA;
     }
   }
+  // the biases' gradient: column sums of the pre-rotation dQ, dK, dV
+  if (g.bqkv) {
+    sf::bias_grad(c->dqkv, c->qkvdim, T, (int)c->qkvdim, c->dg_part, c->dg_parts, g.bqkv, c->sC);
+    c->launches += 2;
+  }
   // QKV projection from u = RMSNorm(X_l; g1)
   RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, c->qkvdim, c->dqkv, c->qkvdim, w.wqkv, d, c->du, d));
   RET(gemm(c, sf::kTN, sf::kEpiBF16, c->qkvdim, d, T, c->dqkv, c->qkvdim, c->u, d, g.wqkv, d));
@@ -818,8 +921,9 @@ size_t unit_numel_cfg(const sf_config* c, int32_t unit) {
                 kv = (int64_t)c->n_kv_heads * c->head_dim, F = c->ffn;
   if (unit >= 0) {
     if (unit >= c->n_layers) return 0;
-    return (size_t)(2 * d + q * d + 2 * kv * d + d * q + 3 * F * d);
+    return (size_t)(2 * d + q * d + 2 * kv * d + d * q + 3 * F * d + (c->qkv_bias ? q + 2 * kv : 0));
   }
+  if (unit == SF_UNIT_LM_HEAD && c->tie_embeddings) return 0;  // the head is the embedding
   if (unit == SF_UNIT_EMBED || unit == SF_UNIT_LM_HEAD) return (size_t)c->vocab * (size_t)d;
   if (unit == SF_UNIT_FINAL_NORM) return (size_t)d;
   return 0;
@@ -838,6 +942,9 @@ const char* validate(const sf_config* c) {
   if (c->ring_slots < 2 || c->ring_slots > std::max(2, c->n_layers)) return "ring_slots must be in [2, max(2, n_layers)]";
   if (c->lce_chunk_rows < 0) return "lce_chunk_rows must be >= 0";
   if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.f)) return "rms_eps must be > 0 and rope_base > 1";
+  if (c->qkv_bias < 0 || c->qkv_bias > 1 || c->tie_embeddings < 0 || c->tie_embeddings > 1 ||
+      c->deterministic < 0 || c->deterministic > 1)
+    return "qkv_bias, tie_embeddings and deterministic must be 0 or 1";
   return nullptr;
 }
 
@@ -857,9 +964,12 @@ int init(sf_ctx* ctx) {
   const int64_t d = ctx->d, T = ctx->Tmax, F = ctx->F, V = ctx->V, L = ctx->L;
   // padded pack: each group starts on a 256-byte boundary
   constexpr int64_t A = 128;
+  ctx->bias = cf.qkv_bias != 0;
+  ctx->tied = cf.tie_embeddings != 0;
   ctx->off_g1 = 0;
   ctx->off_qkv = round_up(d, A);
-  ctx->off_o = round_up(ctx->off_qkv + ctx->qkvdim * d, A);
+  ctx->off_bqkv = round_up(ctx->off_qkv + ctx->qkvdim * d, A);  // only when biased
+  ctx->off_o = ctx->bias ? round_up(ctx->off_bqkv + ctx->qkvdim, A) : ctx->off_bqkv;
   ctx->off_g2 = round_up(ctx->off_o + d * ctx->qdim, A);
   ctx->off_gu = round_up(ctx->off_g2 + d, A);
   ctx->off_d = round_up(ctx->off_gu + 2 * F * d, A);
@@ -871,6 +981,7 @@ int init(sf_ctx* ctx) {
   };
   seg(ctx->off_g1, d);
   seg(ctx->off_qkv, ctx->qkvdim * d);
+  if (ctx->bias) seg(ctx->off_bqkv, ctx->qkvdim);
   seg(ctx->off_o, d * ctx->qdim);
   seg(ctx->off_g2, d);
   seg(ctx->off_gu, 2 * F * d);
@@ -907,7 +1018,8 @@ int init(sf_ctx* ctx) {
        dalloc(ctx, &ctx->dh, T * d) && dalloc(ctx, &ctx->du, T * d) &&
        dalloc(ctx, &ctx->dq_acc, (cf.deterministic ? (ctx->Smax + 127) / 128 : 1) * T * ctx->qdim) &&
        dalloc(ctx, &ctx->delta, T * cf.n_heads) &&
-       dalloc(ctx, &ctx->dg_part, (int64_t)ctx->dg_parts * d) && dalloc(ctx, &ctx->dXb, T * d) &&
+       dalloc(ctx, &ctx->dg_part, (int64_t)ctx->dg_parts * std::max(d, ctx->qkvdim)) &&
+       dalloc(ctx, &ctx->dXb, T * d) &&
        dalloc(ctx, &ctx->dm, T * F) && dalloc(ctx, &ctx->dab, T * 2 * F) &&
        dalloc(ctx, &ctx->dhb, T * d) && dalloc(ctx, &ctx->dob, T * ctx->qdim) &&
        dalloc(ctx, &ctx->dqkv, T * ctx->qkvdim);
@@ -931,16 +1043,23 @@ int init(sf_ctx* ctx) {
 
   // ---- host buffers
   ctx->layers.resize(L);
-  auto host_unit = [&](HostUnit& hu, int64_t elems) -> bool {
+  // pack_only: the tied LM head, whose weights and state are the embedding's
+  auto host_unit = [&](HostUnit& hu, int64_t elems, bool pack_only = false) -> bool {
     hu.elems = elems;
     if (!halloc(ctx, &hu.pack, elems)) return false;
+    uint16_t* p = hu.pack;
+    if (pack_only) {
+      ctx->pool->parallel_for(elems, 1 << 18, [&](int64_t s, int64_t e) {
+        std::memset(p + s, 0, (size_t)(e - s) * 2);
+      });
+      return true;
+    }
     if (!new_floats(ctx, hu.master, elems) || !new_floats(ctx, hu.m, elems) ||
         !new_floats(ctx, hu.v, elems))
       return false;
     float* a = hu.master.get();
     float* b = hu.m.get();
     float* c = hu.v.get();
-    uint16_t* p = hu.pack;
     ctx->pool->parallel_for(elems, 1 << 18, [&](int64_t s, int64_t e) {
       std::memset(a + s, 0, (size_t)(e - s) * 4);
       std::memset(b + s, 0, (size_t)(e - s) * 4);
@@ -950,7 +1069,7 @@ int init(sf_ctx* ctx) {
     return true;
   };
   for (int l = 0; l < L && ok; ++l) ok = host_unit(ctx->layers[l], ctx->pack_elems);
-  ok = ok && host_unit(ctx->lm, V * d) && host_unit(ctx->fn, round_up(d, A));
+  ok = ok && host_unit(ctx->lm, V * d, ctx->tied) && host_unit(ctx->fn, round_up(d, A));
   ok = ok && new_floats(ctx, ctx->E, V * d) && new_floats(ctx, ctx->Em, V * d) &&
        new_floats(ctx, ctx->Ev, V * d) && new_floats(ctx, ctx->dE, V * d);
   if (ok && ctx->xoff) ok = halloc(ctx, &ctx->x_pin, L * T * d);
@@ -1043,14 +1162,11 @@ void scatter_unit(sf_ctx* ctx, const float* in, float* master) {
   }
 }
 
-int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S,
-         const sf_adam* adam) {
-  const int64_t T = (int64_t)B * S, d = ctx->d, V = ctx->V;
-  const int L = ctx->L, R = ctx->R;
-  const auto t_host0 = Clock::now();
-  trace(ctx, 1, -9);
-  // ---- validate on the host, count valid labels
-  int64_t n_valid = 0;
+// Host-side check of a step's tokens and labels; counts the valid labels.
+int check_batch(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int64_t T,
+                int64_t* n_valid) {
+  const int64_t V = ctx->V;
+  int64_t n = 0;
   for (int64_t t = 0; t < T; ++t) {
     if (tokens[t] < 0 || tokens[t] >= V) {
       ctx->set_err("token %d at position %lld outside [0, %lld)", tokens[t], (long long)t, (long long)V);
@@ -1062,8 +1178,22 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
       ctx->set_err("label %d at position %lld outside [0, %lld) and not ignore_index", y, (long long)t, (long long)V);
       return SF_EINVAL;
     }
-    ++n_valid;
+    ++n;
   }
+  *n_valid = n;
+  return SF_OK;
+}
+
+// One micro-batch through the whole stack (its tokens and labels already
+// checked).  n_valid_total: valid labels of the whole step (all its
+// micro-batches), which normalises the loss; phase: where this micro-batch
+// stands (the host tasks it posts sum or update).
+int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S,
+         const sf_adam* adam, int phase, int64_t n_valid_total) {
+  const int64_t T = (int64_t)B * S, d = ctx->d, V = ctx->V;
+  const int L = ctx->L, R = ctx->R;
+  const auto t_host0 = Clock::now();
+  trace(ctx, 1, -9);
   // The embedding update of the previous step reads its tokens and the pinned
   // input-gradient buffer, which this step is about to overwrite.  Without
   // async_update every update of the previous step is finished here (also the
@@ -1071,8 +1201,10 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   if (ctx->async) RET(wait_unit(ctx, SF_UNIT_EMBED));
   else RET(wait_tasks(ctx));
   ctx->tok_copy.assign(tokens, tokens + T);
-  ctx->adam_on = adam != nullptr;
-  if (adam) {
+  ctx->phase = phase;
+  const bool updates = phase == kOnly || phase == kLast;  // this micro-batch's tasks update
+  ctx->adam_on = adam != nullptr && updates;
+  if (ctx->adam_on) {
     ctx->adam_copy = *adam;
     ++ctx->adam_t;
   }
@@ -1131,6 +1263,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     RET(h2d_layer(l));
     if (l == L - 1) {  // the LM head and final norm follow the last layer on the copy stream
       if (ctx->async) RET(wait_unit(ctx, SF_UNIT_LM_HEAD));
+      if (ctx->async && ctx->tied) RET(wait_unit(ctx, kUnitEmbedRest));  // every row refreshed
       CK(cudaMemcpyAsync(ctx->Wlm, ctx->lm.pack, (size_t)V * d * 2, cudaMemcpyHostToDevice, ctx->sU));
       CK(cudaMemcpyAsync(ctx->gf, ctx->fn.pack, (size_t)ctx->fn.elems * 2, cudaMemcpyHostToDevice, ctx->sU));
       CK(cudaEventRecord(ctx->ev_lm, ctx->sU));
@@ -1158,7 +1291,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
 
   // ---- A10: fused LM head + cross-entropy, forward and backward
   CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_lm, 0));
-  RET(head_fwd_bwd(ctx, T, n_valid));
+  RET(head_fwd_bwd(ctx, T, n_valid_total));
   CK(cudaEventRecord(ctx->ev_head, ctx->sC));
   // sliding: bring checkpoint l back into slot l % 4 once that slot's last user
   // is done (the head for the slot of X_L, else the backward of layer l + 4)
@@ -1371,6 +1504,11 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t nume
     ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
       std::memcpy(master + b, w + b, (size_t)(e - b) * 4);
     });
+    if (ctx->tied) {  // the LM head streams the embedding's bf16 copy
+      uint16_t* p = ctx->lm.pack;
+      const float* E = master;
+      ctx->pool->parallel_for(n, 1 << 16, [p, E](int64_t b, int64_t e) { refresh_bf16_span(p, E, b, e); });
+    }
   }
   ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
     std::memset(m + b, 0, (size_t)(e - b) * 4);
@@ -1379,36 +1517,66 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t nume
   return SF_OK;
 }
 
-int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
-                  int32_t seq, const sf_adam* adam) {
+}  // extern "C"
+
+namespace {
+
+// One optimizer step over n_micro micro-batches of batch x seq tokens each:
+// the micro-batches run one after another through the ring, their gradients
+// are summed on the host, and the update uses the sum (the loss is the mean
+// over every valid label of the step).
+int train(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t n_micro,
+          int32_t batch, int32_t seq, const sf_adam* adam, const char* fn) {
   if (!ctx) return SF_EINVAL;
   if (ctx->poisoned) {
     ctx->set_err("context is poisoned by an earlier CUDA error");
     return SF_ESTATE;
   }
-  if (!tokens || !labels || batch < 1 || seq < 1 || seq > ctx->Smax ||
+  if (!tokens || !labels || n_micro < 1 || batch < 1 || seq < 1 || seq > ctx->Smax ||
       (int64_t)batch * seq > ctx->Tmax) {
-    ctx->set_err("sf_train_step: bad arguments (batch %d, seq %d)", batch, seq);
+    ctx->set_err("%s: bad arguments (micro-batches %d, batch %d, seq %d)", fn, n_micro, batch, seq);
     return SF_EINVAL;
   }
   if (adam && !(adam->lr >= 0.f && adam->beta1 >= 0.f && adam->beta1 < 1.f &&
                 adam->beta2 >= 0.f && adam->beta2 < 1.f && adam->eps > 0.f)) {
-    ctx->set_err("sf_train_step: bad Adam hyper-parameters");
+    ctx->set_err("%s: bad Adam hyper-parameters", fn);
     return SF_EINVAL;
+  }
+  const int64_t T = (int64_t)batch * seq;
+  int64_t n_valid_total = 0;
+  for (int i = 0; i < n_micro; ++i) {
+    int64_t n = 0;
+    RET(check_batch(ctx, tokens + i * T, labels + i * T, T, &n));
+    n_valid_total += n;
   }
   if (cudaSetDevice(ctx->cfg.device) != cudaSuccess) {
     ctx->set_err("cudaSetDevice failed");
     return SF_ECUDA;
   }
-  int st;
+  if (n_micro > 1) {  // fp32 gradient sums, allocated once
+    auto need = [&](HostUnit& hu) { return hu.master && !hu.acc && !new_floats(ctx, hu.acc, hu.elems); };
+    bool fail = false;
+    for (HostUnit& hu : ctx->layers) fail = fail || need(hu);
+    fail = fail || need(ctx->lm) || need(ctx->fn);
+    if (fail) return SF_ENOMEM;
+  }
+  int st = SF_OK;
+  double loss = 0.0;
   try {
-    st = step(ctx, tokens, labels, batch, seq, adam);
+    for (int i = 0; i < n_micro && st == SF_OK; ++i) {
+      const int phase = n_micro == 1 ? kOnly : i == 0 ? kFirst : i == n_micro - 1 ? kLast : kMid;
+      st = step(ctx, tokens + i * T, labels + i * T, batch, seq, adam, phase, n_valid_total);
+      loss += ctx->loss;
+    }
   } catch (...) {
     ctx->set_err("host exception in the step");
     ctx->poisoned = true;
     st = SF_ESTATE;
   }
-  if (st != SF_OK && st != SF_EINVAL) {
+  if (st == SF_OK) {
+    ctx->loss = (float)loss;
+    ctx->last_accum = n_micro > 1;
+  } else if (st != SF_EINVAL) {
     // leave no copy, kernel or host update of this step in flight
     const std::string why = ctx->err;
     cudaStreamSynchronize(ctx->sC);
@@ -1419,6 +1587,20 @@ int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int
     if (st == SF_ECUDA || st == SF_EDEVICE) ctx->poisoned = true;
   }
   return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sf_train_step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t batch,
+                  int32_t seq, const sf_adam* adam) {
+  return train(ctx, tokens, labels, 1, batch, seq, adam, "sf_train_step");
+}
+
+int sf_train_step_accum(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels,
+                        int32_t n_micro, int32_t batch, int32_t seq, const sf_adam* adam) {
+  return train(ctx, tokens, labels, n_micro, batch, seq, adam, "sf_train_step_accum");
 }
 
 int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
@@ -1436,6 +1618,15 @@ int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
     return SF_OK;
   }
   const HostUnit& hu = unit >= 0 ? ctx->layers[unit] : (unit == SF_UNIT_LM_HEAD ? ctx->lm : ctx->fn);
+  if (ctx->last_accum) {  // the fp32 sum over the step's micro-batches
+    const float* g = hu.retained_acc.data();
+    if (unit >= 0) {
+      for (const Seg& s : ctx->segs) std::memcpy(out + s.src, g + s.dst, (size_t)s.n * 4);
+    } else {
+      std::memcpy(out, g, numel * 4);
+    }
+    return SF_OK;
+  }
   const uint16_t* g = hu.retained.data();
   if (unit >= 0) {
     for (const Seg& s : ctx->segs)

@@ -34,6 +34,7 @@ struct GemmParams {
   int64_t ldr;
   float alpha;
   int* err;
+  const __nv_bfloat16* bias;  // kEpiBF16Bias: one value per output column
 };
 
 constexpr int kBM = 128;
@@ -72,22 +73,48 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
                                           const uint32_t (&r)[32]) {
   const float a = p.alpha;
   const bool full = (col + 32 <= p.N);
-  if constexpr (EPI == kEpiBF16) {
+  if constexpr (EPI == kEpiBF16 || EPI == kEpiBF16Bias) {
     __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
+    float bv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bv[j] = 0.f;
+    if constexpr (EPI == kEpiBF16Bias) {
+      if (full) {
+        const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col);  // 64-byte aligned: col % 32 == 0
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = b4[q];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            bv[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+            bv[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col + j < p.N) bv[j] = __bfloat162float(p.bias[col + j]);
+      }
+    }
     if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * a, __uint_as_float(r[8 * q + 1]) * a);
-        v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * a, __uint_as_float(r[8 * q + 3]) * a);
-        v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * a, __uint_as_float(r[8 * q + 5]) * a);
-        v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * a, __uint_as_float(r[8 * q + 7]) * a);
+        v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * a + bv[8 * q + 0],
+                          __uint_as_float(r[8 * q + 1]) * a + bv[8 * q + 1]);
+        v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * a + bv[8 * q + 2],
+                          __uint_as_float(r[8 * q + 3]) * a + bv[8 * q + 3]);
+        v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * a + bv[8 * q + 4],
+                          __uint_as_float(r[8 * q + 5]) * a + bv[8 * q + 5]);
+        v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * a + bv[8 * q + 6],
+                          __uint_as_float(r[8 * q + 7]) * a + bv[8 * q + 7]);
         reinterpret_cast<uint4*>(c)[q] = v;
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (col + j < p.N) c[j] = __float2bfloat16_rn(__uint_as_float(r[j]) * a);
+        if (col + j < p.N) c[j] = __float2bfloat16_rn(__uint_as_float(r[j]) * a + bv[j]);
     }
   } else {
     float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
@@ -367,6 +394,9 @@ static int launch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, con
     case kEpiF32: return launch_t<A_MN, B_MN, BN, kEpiF32>(ta, tb, p, st, why);
     case kEpiF32Add: return launch_t<A_MN, B_MN, BN, kEpiF32Add>(ta, tb, p, st, why);
     case kEpiF32Acc: return launch_t<A_MN, B_MN, BN, kEpiF32Acc>(ta, tb, p, st, why);
+    case kEpiBF16Bias:  // forward projections only (Y = X W^T + b)
+      if constexpr (!A_MN && !B_MN) return launch_t<A_MN, B_MN, BN, kEpiBF16Bias>(ta, tb, p, st, why);
+      break;
   }
   snprintf(why, 64, "gemm: bad epilogue %d", epi);
   return -1;
@@ -378,12 +408,17 @@ int gemm_check(const GemmArgs& a, char* why) {
     snprintf(why, 64, "gemm: bad sizes");
     return -1;
   }
-  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiF32Acc) {
+  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiBF16Bias ||
+      (a.epi == kEpiBF16Bias && a.layout != kNT)) {
     snprintf(why, 64, "gemm: bad layout %d or epilogue %d", a.layout, a.epi);
     return -1;
   }
-  if (!a.A || !a.B || !a.C || (a.epi == kEpiF32Add && !a.R)) {
+  if (!a.A || !a.B || !a.C || (a.epi == kEpiF32Add && !a.R) || (a.epi == kEpiBF16Bias && !a.bias)) {
     snprintf(why, 64, "gemm: null operand");
+    return -1;
+  }
+  if (a.epi == kEpiBF16Bias && (reinterpret_cast<uintptr_t>(a.bias) & 63)) {
+    snprintf(why, 64, "gemm: bias must be 64-byte aligned");
     return -1;
   }
   // TMA: 16-byte aligned bases and row strides.
@@ -418,7 +453,8 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
     snprintf(why, 64, "gemm: tensor map encode failed");
     return -3;
   }
-  GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err};
+  GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err,
+               reinterpret_cast<const __nv_bfloat16*>(a.bias)};
   if (BN == 256) {
     if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, p, st, why);
     if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, p, st, why);

@@ -61,6 +61,39 @@ int sf_op_gemm(int32_t layout, int32_t epi, int64_t M, int64_t N, int64_t K, con
   return SF_OK;
 }
 
+int sf_op_gemm_bias(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, void* C, int64_t ldc, const uint16_t* bias, float alpha,
+                    void* stream) {
+  sf::GemmArgs g;
+  g.layout = sf::kNT; g.epi = sf::kEpiBF16Bias; g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.alpha = alpha;
+  g.bias = bias;
+  char why[128];
+  if (sf::gemm_check(g, why) != 0) return SF_EINVAL;
+  if (M == 0 || N == 0) return SF_OK;
+  int* err = dev_err_word();
+  if (!err) return SF_ECUDA;
+  const int st = sf::gemm(g, err, S(stream), why);
+  if (st == -1) return SF_EINVAL;
+  if (st != 0) return SF_ECUDA;
+  return SF_OK;
+}
+
+int64_t sf_op_bias_grad_scratch(int64_t rows, int32_t cols) {
+  if (rows < 0 || cols < 0) return -1;
+  return (int64_t)sf::rmsnorm_bwd_parts(rows) * cols;
+}
+
+int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, float* part,
+                    uint16_t* db, void* stream) {
+  if (rows < 0 || cols < 2 || cols % 2 || ld < cols || ld % 2) return SF_EINVAL;
+  if (!dy || !part || !db || (reinterpret_cast<uintptr_t>(dy) & 3)) return SF_EINVAL;
+  if (rows == 0) return SF_EINVAL;
+  sf::bias_grad(reinterpret_cast<const bf16*>(dy), ld, rows, cols, part,
+                sf::rmsnorm_bwd_parts(rows), reinterpret_cast<bf16*>(db), S(stream));
+  return cudaGetLastError() == cudaSuccess ? SF_OK : SF_ECUDA;
+}
+
 int sf_op_rmsnorm_fwd(const float* x, const uint16_t* g, uint16_t* y, float* rstd, int64_t rows,
                       int32_t d, float eps, void* stream) {
   if (rows < 0 || d < 8 || d % 8 || !(eps > 0.f)) return SF_EINVAL;

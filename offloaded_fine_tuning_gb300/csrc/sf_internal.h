@@ -13,7 +13,8 @@ namespace sf {
 //   kTN: A [K,M] (M contiguous), B [K,N] (N contiguous)   -> dW = dY^T X
 enum GemmLayout : int { kNT = 0, kNN = 1, kTN = 2 };
 // Epilogues: C bf16 = alpha*acc | C f32 = alpha*acc | C f32 = R + alpha*acc | C f32 += alpha*acc
-enum GemmEpi : int { kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3 };
+// | C bf16 = alpha*acc + bias[col] (bias bf16 [N], 64-byte aligned; layout kNT only)
+enum GemmEpi : int { kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3, kEpiBF16Bias = 4 };
 
 struct GemmArgs {
   int layout = kNT, epi = kEpiBF16;
@@ -27,6 +28,7 @@ struct GemmArgs {
   const float* R = nullptr;
   int64_t ldr = 0;
   float alpha = 1.f;
+  const void* bias = nullptr;  // kEpiBF16Bias
 };
 
 // Returns 0, or a negative status with a message in `why` (64 chars at least).
@@ -43,6 +45,10 @@ void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, cons
                  int64_t rows, int d, cudaStream_t st);
 int rmsnorm_bwd_parts(int64_t rows);
 void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st);
+// out[c] = bf16(sum over rows of x[r, c]) for x bf16 [rows, cols] (cols even, row
+// stride ld, 4-byte aligned rows); part: fp32 scratch [parts, cols]
+void bias_grad(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float* part, int parts,
+               __nv_bfloat16* out, cudaStream_t st);
 void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
                   int head_dim, const float2* cs, int inverse, cudaStream_t st);
 void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn,

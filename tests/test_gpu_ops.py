@@ -197,6 +197,49 @@ def test_swiglu_fwd_bwd():
     assert rel_l2(got[:, :F], da) < BF16_RL2 and rel_l2(got[:, F:], db) < BF16_RL2
 
 
+# ------------------------------------------------------------------ projection bias
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (5, 72, 8), (640, 1152, 384)])
+def test_gemm_bias_epilogue(M, N, K):
+    """Y = X W^T + b with the bias added to the fp32 accumulator (bf16 out)."""
+    x = bf16_values(rnd(11, (M, K)))
+    w = bf16_values(rnd(12, (N, K), 0.05))
+    bias = bf16_values(rnd(13, (N,), 0.5))
+    X, W, Bv = cuda(x, torch.bfloat16), cuda(w, torch.bfloat16), cuda(bias, torch.bfloat16)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert sf.op_gemm_bias(M, N, K, X.data_ptr(), K, W.data_ptr(), K, Y.data_ptr(), N,
+                           Bv.data_ptr(), 1.0, stream()) == 0
+    sync()
+    ref = x.astype(np.float64) @ w.astype(np.float64).T + bias.astype(np.float64)
+    assert rel_l2(host(Y), ref) < BF16_RL2
+
+
+def test_gemm_bias_rejects_bad_arguments():
+    X = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((64, 64), dtype=torch.bfloat16, device="cuda")
+    Bv = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+    assert sf.op_gemm_bias(64, 64, 64, X.data_ptr(), 64, X.data_ptr(), 64, Y.data_ptr(), 64, 0,
+                           1.0, stream()) == sf.SF_EINVAL
+    assert sf.op_gemm_bias(64, 64, 64, X.data_ptr(), 64, X.data_ptr(), 64, Y.data_ptr(), 64,
+                           Bv.data_ptr() + 2, 1.0, stream()) == sf.SF_EINVAL
+
+
+@pytest.mark.parametrize("rows,cols,ld", [(1, 8, 8), (300, 640, 640), (4000, 1000, 1024)])
+def test_bias_grad_is_the_column_sum(rows, cols, ld):
+    dy = bf16_values(rnd(21, (rows, ld)))
+    DY = cuda(dy, torch.bfloat16)
+    part = torch.empty(sf.bias_grad_scratch_floats(rows, cols), dtype=torch.float32, device="cuda")
+    DB = torch.empty(cols, dtype=torch.bfloat16, device="cuda")
+    outs = []
+    for _ in range(2):
+        assert sf.op_bias_grad(DY.data_ptr(), ld, rows, cols, part.data_ptr(), DB.data_ptr(),
+                               stream()) == 0
+        sync()
+        outs.append(host(DB))
+    ref = dy[:, :cols].astype(np.float64).sum(axis=0)
+    assert rel_l2(outs[0], ref) < BF16_RL2
+    assert np.array_equal(outs[0], outs[1])
+
+
 # ------------------------------------------------------------------ attention
 ATTN_CASES = [(2, 200, 6, 2, 64), (1, 130, 4, 1, 128), (1, 64, 2, 2, 64), (2, 1, 4, 2, 128),
               (1, 300, 12, 1, 128), (1, 64, 2, 2, 128), (3, 257, 8, 2, 128), (1, 40, 4, 4, 128)]

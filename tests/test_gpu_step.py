@@ -38,7 +38,10 @@ def compare(cfg, m, loss_ref, g_ref, tol=GRAD_RL2):
             off += n
     errs["embed"] = rel_l2(m.grads(UNIT_EMBED).reshape(cfg.vocab, cfg.hidden), g_ref["embed"])
     errs["final_norm"] = rel_l2(m.grads(UNIT_FINAL_NORM), g_ref["final_norm"])
-    errs["lm_head"] = rel_l2(m.grads(UNIT_LM_HEAD).reshape(cfg.vocab, cfg.hidden), g_ref["lm_head"])
+    if g_ref["lm_head"] is not None:
+        errs["lm_head"] = rel_l2(m.grads(UNIT_LM_HEAD).reshape(cfg.vocab, cfg.hidden), g_ref["lm_head"])
+    else:  # tied: no separate unit
+        assert m.numel(UNIT_LM_HEAD) == 0
     bad = {k: v for k, v in errs.items() if v > (LOSS_RTOL if k == "loss" else tol)}
     assert not bad, f"outside tolerance: {bad}"
     return errs
@@ -59,6 +62,105 @@ def test_step_matches_oracle(name, det):
             g0, l0 = m.grads(0), m.loss()
             assert m.train_step(tok, lab) == sf.SF_OK
             assert m.loss() == l0 and np.array_equal(m.grads(0), g0)
+
+
+# ------------------------------------------------------------------ model variants
+@pytest.mark.parametrize("bias,tied", [(True, True), (True, False), (False, True)])
+def test_variant_step_matches_oracle(bias, tied):
+    """Qwen-style Q/K/V biases and a tied LM head against the oracle."""
+    cfg = TEST_CONFIGS["small-qwen"].with_(qkv_bias=bias, tie_embeddings=tied)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
+    with make_model(cfg, mast) as m:
+        assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+        compare(cfg, m, loss_ref, g_ref)
+
+
+def test_tied_variant_adam_tracks_oracle():
+    """Two Adam steps of the biased, tied model: the embedding (also the LM
+    head) and a layer's weights follow the oracle's updates."""
+    cfg = TEST_CONFIGS["small-qwen"].with_(n_layers=2)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lr = 1e-4  # as in the multi-step test above: updates well above the bf16 noise of a step
+    adam = sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    theta = {u: a.astype(np.float32).copy() for u, a in mast.items()}
+    mom = {u: (np.zeros_like(a), np.zeros_like(a)) for u, a in theta.items()}
+    for asyn in (0, 1):
+        th_ = {u: a.copy() for u, a in theta.items()}
+        mo_ = {u: (a.copy(), b.copy()) for u, (a, b) in mom.items()}
+        with make_model(cfg, mast, async_update=asyn) as m:
+            for t in range(1, 3):
+                loss_ref, g = oracle.step(oracle_weights(cfg, th_), tok, lab, cfg)
+                assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+                assert abs(m.loss() - loss_ref) / loss_ref < LOSS_RTOL
+                for u in th_:
+                    gu = (np.concatenate([g["layers"][u][n].reshape(-1) for n, _ in layer_tensor_shapes(cfg)])
+                          if u >= 0 else {UNIT_EMBED: g["embed"], UNIT_FINAL_NORM: g["final_norm"]}[u].reshape(-1))
+                    th, mm, vv = oracle.adam_update(th_[u], gu.astype(np.float32), *mo_[u], t, lr)
+                    th_[u], mo_[u] = th.astype(np.float32), (mm.astype(np.float32), vv.astype(np.float32))
+            m.sync()
+            for u in (0, UNIT_EMBED, UNIT_FINAL_NORM):
+                w = m.weights(u)
+                assert rel_l2(w - mast[u], th_[u] - mast[u]) < 0.1, u
+                assert rel_l2(w, th_[u]) < 1e-3, u
+
+
+@pytest.mark.parametrize("name,n_micro", [("small-gqa", 2), ("small-qwen", 3)])
+def test_gradient_accumulation_matches_the_full_batch(name, n_micro):
+    """n_micro micro-batches summed on the host equal the oracle's step on the
+    whole batch (global-mean loss over every valid label)."""
+    cfg = TEST_CONFIGS[name].with_(batch=n_micro)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lab = lab.copy()
+    lab[0, :37] = IGNORE_INDEX  # micro-batches with different valid counts
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
+    micro = cfg.with_(batch=1)
+    with make_model(micro, mast) as m:
+        assert m.train_step_accum(tok[:, None, :], lab[:, None, :]) == sf.SF_OK, m.error()
+        compare(cfg, m, loss_ref, g_ref)
+        # a plain step afterwards reports its own (bf16) gradients again
+        assert m.train_step(tok[:1], lab[:1]) == sf.SF_OK
+        _, g1 = oracle.step(oracle_weights(cfg, mast), tok[:1], lab[:1], micro)
+        assert rel_l2(m.grads(0)[:cfg.hidden], g1["layers"][0]["g1"]) < GRAD_RL2
+
+
+def test_gradient_accumulation_adam_uses_the_summed_gradient():
+    """An accumulated Adam step (updates overlapping the last micro-batch)
+    applies Adam to the summed gradient that sf_get_grads reports, and its
+    loss is the full batch's."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, batch=2)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lr, wd = 1e-3, 0.01
+    adam = sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=wd)
+    with make_model(cfg, mast) as full:
+        assert full.train_step(tok, lab) == sf.SF_OK
+        lref = full.loss()
+    with make_model(cfg.with_(batch=1), mast, async_update=1) as acc:
+        assert acc.train_step_accum(tok[:, None, :], lab[:, None, :], adam) == sf.SF_OK
+        assert abs(acc.loss() - lref) <= 1e-5 * lref
+        acc.sync()
+        for u in (0, 1, UNIT_EMBED, UNIT_LM_HEAD, UNIT_FINAL_NORM):
+            g = acc.grads(u)
+            z = np.zeros_like(g)
+            want, _, _ = oracle.adam_update(mast[u], g, z, z, 1, lr, weight_decay=wd)
+            got = acc.weights(u)
+            assert rel_l2(got - mast[u], want.astype(np.float32) - mast[u]) < 1e-4, u
+
+
+def test_gradient_accumulation_rejects_a_bad_micro_batch_before_running():
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2, batch=1)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg.with_(batch=3))
+    tok = tok.copy()
+    tok[2, 5] = cfg.vocab  # only the last micro-batch is bad
+    with make_model(cfg, mast) as m:
+        assert m.train_step_accum(tok[:, None, :], lab[:, None, :]) == sf.SF_EINVAL
+        assert "token" in m.error()
+        assert m.train_step(tok[:1], lab[:1]) == sf.SF_OK
 
 
 def test_ring_size_invariance_is_bitwise():

@@ -30,7 +30,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import inputs  # noqa: E402
-from inputs import CONFIGS, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD  # noqa: E402
+from inputs import CONFIGS, VARIANT_CONFIGS, UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD  # noqa: E402
+
+ALL_CONFIGS = {**CONFIGS, **VARIANT_CONFIGS}
 
 METRIC = "fine-tune tokens/sec at 1 GB300; % of step roofline (tensor peak vs host-link)"
 UNIT = "tokens/s"
@@ -231,8 +233,23 @@ def load_model(sf, c, ring, async_update, offload_activations=0):
     for l in range(c.n_layers):
         m.load(l, inputs.layer_master(c, l))
     for u in (UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD):
-        m.load(u, inputs.unit_master(c, u))
+        if inputs.unit_numel(c, u):  # no LM-head unit when it is tied
+            m.load(u, inputs.unit_master(c, u))
     return m
+
+
+def host_adam_bytes(c, micro=1):
+    """Host memory traffic of one step's updates.  Layers, final norm and an
+    untied LM head: 28 B per parameter (bf16 gradient in, fp32 master, m, v
+    read and written, bf16 pack out).  Embedding: 24 B (fp32 gradient, state)
+    plus, when it is the tied head, 6 B to fold the head's bf16 gradient into
+    it.  Each extra micro-batch adds 12 B per packed parameter (bf16 gradient
+    in, fp32 sum read and written, bf16 weights back)."""
+    P_l = inputs.unit_numel(c, 0)
+    packed = c.n_layers * P_l + c.hidden + inputs.unit_numel(c, UNIT_LM_HEAD)
+    emb = c.vocab * c.hidden
+    b = 28.0 * packed + 24.0 * emb + (6.0 * emb if c.tie_embeddings else 0.0)
+    return b + (micro - 1) * 12.0 * (packed + (emb if c.tie_embeddings else 0))
 
 
 def run_ours(args, c):
@@ -254,12 +271,26 @@ def run_ours(args, c):
     m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1,
                    1 if args.offload_activations else 0)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
-    # a fresh batch each step (rank-specific seeds for replicas)
+    # a fresh batch each step (rank-specific seeds for replicas); with --micro N
+    # a step is N micro-batches of the workload's batch, summed before the update
+    n_micro = max(1, args.micro)
     n_batches = args.warmup + 2 * args.steps
-    batches = [inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + 1000 * rank + i) for i in range(n_batches)]
-    T = c.batch * c.seq
+
+    def make_batch(i):
+        parts = [inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + 1000 * rank + n_micro * i + j)
+                 for j in range(n_micro)]
+        if n_micro == 1:
+            return parts[0]
+        return np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts])
+
+    batches = [make_batch(i) for i in range(n_batches)]
+    T = n_micro * c.batch * c.seq
+
+    def train(tok, lab):
+        return m.train_step(tok, lab, adam) if n_micro == 1 else m.train_step_accum(tok, lab, adam)
+
     for i in range(args.warmup):
-        assert m.train_step(*batches[i], adam) == sf.SF_OK, m.error()
+        assert train(*batches[i]) == sf.SF_OK, m.error()
 
     m.sync()  # no warm-up update runs into the timed region
     m.trace()  # start the host timeline at the timed region
@@ -274,7 +305,7 @@ def run_ours(args, c):
     e0.record()
     stats = []
     for i in range(args.steps):
-        st = m.train_step(*batches[args.warmup + i], adam)
+        st = train(*batches[args.warmup + i])
         assert st == sf.SF_OK, m.error()
         stats.append(m.stats())
     m.sync()  # the last step's host updates belong to the timed work
@@ -289,15 +320,16 @@ def run_ours(args, c):
 
     # ---- end to end through the public call: stage the batch from pinned host
     # memory each step, run the step, read the loss back
-    pin_tok = torch.empty((c.batch, c.seq), dtype=torch.int32, pin_memory=True)
-    pin_lab = torch.empty((c.batch, c.seq), dtype=torch.int32, pin_memory=True)
+    shape = (c.batch, c.seq) if n_micro == 1 else (n_micro, c.batch, c.seq)
+    pin_tok = torch.empty(shape, dtype=torch.int32, pin_memory=True)
+    pin_lab = torch.empty(shape, dtype=torch.int32, pin_memory=True)
     t0 = time.perf_counter()
     losses = []
     for i in range(args.steps):
         tok, lab = batches[args.warmup + args.steps + i]
         pin_tok.numpy()[...] = tok
         pin_lab.numpy()[...] = lab
-        assert m.train_step(pin_tok.numpy(), pin_lab.numpy(), adam) == sf.SF_OK, m.error()
+        assert train(pin_tok.numpy(), pin_lab.numpy()) == sf.SF_OK, m.error()
         losses.append(m.loss())
     m.sync()
     e2e_s = time.perf_counter() - t0
@@ -312,19 +344,19 @@ def run_ours(args, c):
     gemm_n = sum(s["gemm_launches"] for s in stats)
     attn_ms = sum(s["attn_ms"] for s in stats)
     attn_fl = sum(s["attn_flops"] for s in stats)
-    h2d = statistics.mean(s["h2d_bytes"] for s in stats)
-    d2h = statistics.mean(s["d2h_bytes"] for s in stats)
-    gpu_step = statistics.mean(s["step_ms"] for s in stats)
+    # the engine's counters cover the last micro-batch of a step
+    h2d = n_micro * statistics.mean(s["h2d_bytes"] for s in stats)
+    d2h = n_micro * statistics.mean(s["d2h_bytes"] for s in stats)
+    gpu_step = n_micro * statistics.mean(s["step_ms"] for s in stats)
     achieved = gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
-    F_exec = step_flops(c, executed=True)
+    F_exec = n_micro * step_flops(c, executed=True)
     t_tensor = F_exec / (bf16_sust * 1e12)
     t_link = (h2d + d2h) / (link["bidir"] * 1e9)
     t_roof = max(t_tensor, t_link)
     # host memory: the Adam update of every unit (28 B per layer / LM-head
     # parameter: bf16 grad in, fp32 master, m, v read and written, bf16 out;
     # 24 B per embedding parameter, whose gradient is fp32) plus the DMA copies
-    P_l = inputs.unit_numel(c, 0)
-    adam_bytes = 28.0 * (c.n_layers * P_l + c.vocab * c.hidden + c.hidden) + 24.0 * c.vocab * c.hidden
+    adam_bytes = host_adam_bytes(c, n_micro)
     host_bytes = adam_bytes + h2d + d2h
     t_host = host_bytes / (host_gbs * 1e9)
     if args.trace:
@@ -340,7 +372,8 @@ def run_ours(args, c):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": c.name, "global_batch": c.batch * world, "seq_len": c.seq,
+        "config": {"workload": c.name, "global_batch": n_micro * c.batch * world, "seq_len": c.seq,
+                   "micro_batches": n_micro,
                    "layers": c.n_layers, "ring_slots": args.ring or c.ring_slots,
                    "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
                    "host_updates": "synchronous" if args.sync_updates else "overlap next step",
@@ -348,12 +381,12 @@ def run_ours(args, c):
                    "l2": "inputs larger than L2 (each step streams every layer's weights and gradients)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": int(sum(s["kernel_launches"] for s in stats)),
+        "gpu_launches": int(n_micro * sum(s["kernel_launches"] for s in stats)),
         "roofline": {"kernel": "gemm_tcgen05", "bound": "tensor", "achieved": achieved,
                      "peak": bf16_sust, "unit": "TFLOP/s",
                      "frac": achieved / bf16_sust if achieved else None, "traffic": None,
                      "peak_source": f"{peak_src} bf16 sustained (cuBLAS, long loop)",
-                     "launches": gemm_n, "gemm_ms_per_step": gemm_ms / args.steps},
+                     "launches": n_micro * gemm_n, "gemm_ms_per_step": n_micro * gemm_ms / args.steps},
         "step_roofline": {"flops": F_exec, "t_tensor_ms": t_tensor * 1e3, "h2d_bytes": h2d,
                           "d2h_bytes": d2h, "link_gbs": link, "t_link_ms": t_link * 1e3,
                           "t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
@@ -491,7 +524,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="8b", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="8b", choices=sorted(ALL_CONFIGS))
+    ap.add_argument("--micro", type=int, default=1,
+                    help="gradient accumulation: micro-batches (of the workload's batch) per step")
     ap.add_argument("--ring", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -507,7 +542,7 @@ def main():
     ap.add_argument("--shape", default="16384,6144,4096", help="M,N,K for --op gemm")
     ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])
     args = ap.parse_args()
-    c = CONFIGS[args.config]
+    c = ALL_CONFIGS[args.config]
     if args.sweep_batch:
         run_sweep(args, c)
     elif args.op:

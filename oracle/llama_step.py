@@ -303,3 +303,69 @@ def adam_update(theta, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_
     vhat = v / (1.0 - beta2 ** t)
     theta = theta - lr * weight_decay * theta - lr * mhat / (np.sqrt(vhat) + eps)
     return theta, m, v
+
+
+# ---------------------------------------------------------------- Adam with 16-bit moments
+# Optimizer-state compression: the moments are stored as bfloat16, rounded
+# stochastically so that increments far below a bf16 step (v moves by
+# (1 - beta2) = 0.1% of itself per step) survive in expectation.  The random
+# bits are a counter-based hash of (step, unit, moment, element index), so
+# both implementations draw the same bits.
+_U32 = np.uint32
+
+
+def lowbias32(x):
+    """32-bit integer hash (Wellons' "lowbias32": xorshift-multiply rounds with
+    the constants 0x7feb352d and 0x846ca68b), elementwise on uint32."""
+    x = np.asarray(x, dtype=_U32)
+    with np.errstate(over="ignore"):
+        x = x ^ (x >> _U32(16))
+        x = x * _U32(0x7FEB352D)
+        x = x ^ (x >> _U32(15))
+        x = x * _U32(0x846CA68B)
+        x = x ^ (x >> _U32(16))
+    return x
+
+
+def sr_key(t, unit, which):
+    """Stream key of step t >= 1, unit (layer index, or -1 embedding, -2 final
+    norm, -3 LM head) and moment (1 = first, 2 = second)."""
+    with np.errstate(over="ignore"):
+        mixed = lowbias32(_U32(t & 0xFFFFFFFF)) ^ (_U32(unit + 3) * _U32(0x9E3779B9)) ^ _U32(which)
+    return lowbias32(mixed)
+
+
+def sr_bits(key, index):
+    """The random word of element `index` (its position in the unit's tensors,
+    concatenated in unit order) in the stream `key`."""
+    return lowbias32(np.asarray(index, dtype=np.uint64).astype(_U32) ^ _U32(key))
+
+
+def bf16_round_stochastic(x, r):
+    """Round float32 x to bfloat16 upwards (in magnitude) with probability
+    (low 16 bits of x) / 2^16: add the low 16 bits of r to x's bits, then
+    truncate.  E[result] = x for finite x.  Result as float32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(_U32).astype(np.uint64)
+    u = (u + (np.asarray(r, dtype=np.uint64) & np.uint64(0xFFFF))) & np.uint64(0xFFFF0000)
+    return u.astype(_U32).view(np.float32).reshape(np.shape(x))
+
+
+def adam_update_bf16_states(theta, g, m, v, t, lr, unit, beta1=0.9, beta2=0.999, eps=1e-8,
+                            weight_decay=0.0, index0=0):
+    """adam_update in float32 arithmetic with the moments m, v stored as
+    bfloat16 (float32 arrays holding bf16 values): the new moments are
+    computed in float32, used unrounded for this step's parameter update,
+    then stored with bf16_round_stochastic (element i of the unit draws
+    sr_bits(sr_key(t, unit, 1 or 2), index0 + i)).  Returns (theta, m, v)."""
+    f = np.float32
+    theta, g, m, v = (np.asarray(a, dtype=np.float32) for a in (theta, g, m, v))
+    b1, b2, lr_, eps_, wd = f(beta1), f(beta2), f(lr), f(eps), f(weight_decay)
+    bc1 = f(1.0) - f(np.power(b1, f(t)))
+    bc2 = f(1.0) - f(np.power(b2, f(t)))
+    m1 = b1 * m + (f(1.0) - b1) * g
+    v1 = b2 * v + (f(1.0) - b2) * g * g
+    th = theta - lr_ * wd * theta - lr_ * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps_)
+    idx = index0 + np.arange(theta.size, dtype=np.uint64)
+    mq = bf16_round_stochastic(m1, sr_bits(sr_key(t, unit, 1), idx).reshape(theta.shape))
+    vq = bf16_round_stochastic(v1, sr_bits(sr_key(t, unit, 2), idx).reshape(theta.shape))
+    return th.astype(np.float32), mq, vq

@@ -453,6 +453,71 @@ def test_adam_matches_torch_adamw_and_first_step_closed_form():
     assert rel_l2(th - theta, tt.detach().numpy() - theta) < 1e-9
 
 
+# ------------------------------------------------------------------ 16-bit Adam moments
+def test_stochastic_rounding_is_exact_in_the_mean_and_keeps_bf16_values():
+    """Over all 2^16 values of the random low half-word the rounded results
+    average to x exactly; values already in bf16 are never moved."""
+    x = RNG.standard_normal(64).astype(np.float32) * np.float32(10.0) ** RNG.integers(-6, 3, 64).astype(np.float32)
+    r = np.arange(65536, dtype=np.uint32)
+    for xi in x:
+        q = ls.bf16_round_stochastic(np.full(65536, xi, np.float32), r).astype(np.float64)
+        assert q.mean() == pytest.approx(float(xi), rel=1e-12, abs=0)
+        lo, hi = q.min(), q.max()
+        assert lo <= xi <= hi and np.unique(q).size <= 2
+    b = oracle.bf16_round(x)
+    assert np.array_equal(ls.bf16_round_stochastic(b, RNG.integers(0, 2**32, 64, dtype=np.uint64)), b)
+
+
+def test_stochastic_rounding_bits_are_uniform():
+    """The hashed words of one stream look uniform: the rounding-up rate of a
+    value a quarter of the way between two bf16 neighbours is 1/4."""
+    n = 1 << 20
+    r = ls.sr_bits(ls.sr_key(7, 3, 2), np.arange(n))
+    lo16 = (r & np.uint32(0xFFFF)).astype(np.float64)
+    assert abs(lo16.mean() / 65536 - 0.5) < 3e-3
+    x = np.float32(1.0) + np.float32(2.0 ** -7) / np.float32(4.0)  # 1 + ulp/4
+    up = ls.bf16_round_stochastic(np.full(n, x, np.float32), r) > 1.0
+    assert abs(up.mean() - 0.25) < 3e-3
+    # different steps, units and moments give different streams
+    keys = {int(ls.sr_key(t, u, w)) for t in (1, 2) for u in (-3, -1, 0, 5) for w in (1, 2)}
+    assert len(keys) == 16
+
+
+def test_bf16_moments_track_float32_adam_where_nearest_rounding_stalls():
+    """3000 Adam steps on noisy gradients: with stochastically rounded bf16
+    moments the second moment stays with the float32 one; rounding to nearest
+    loses the 0.1%-per-step increments once v is large (it stalls)."""
+    n, steps = 2000, 3000
+    rng = np.random.default_rng(3)
+    th32 = thsr = thrn = np.zeros(n, np.float32)
+    m32 = v32 = msr = vsr = mrn = vrn = np.zeros(n, np.float32)
+    for t in range(1, steps + 1):
+        g = rng.standard_normal(n).astype(np.float32) * np.float32(1e-3)
+        th32, m32, v32 = (a.astype(np.float32) for a in ls.adam_update(th32, g, m32, v32, t, 1e-4))
+        thsr, msr, vsr = ls.adam_update_bf16_states(thsr, g, msr, vsr, t, 1e-4, unit=0)
+        thrn, mrn, vrn = ls.adam_update(thrn, g, mrn, vrn, t, 1e-4)
+        mrn, vrn = oracle.bf16_round(mrn.astype(np.float32)), oracle.bf16_round(vrn.astype(np.float32))
+    assert abs(vsr.mean() / v32.mean() - 1.0) < 0.02
+    assert abs(vrn.mean() / v32.mean() - 1.0) > 0.1
+    assert rel_l2(thsr, th32) < 0.05
+
+
+def test_bf16_moment_adam_first_step_closed_form():
+    """Step 1 from zero moments: the parameter update is float32 Adam's, and
+    the stored moments are the bf16 neighbours of (1-b1) g and (1-b2) g^2."""
+    n = 500
+    th = RNG.standard_normal(n).astype(np.float32)
+    g = RNG.standard_normal(n).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    t1, m1, v1 = ls.adam_update_bf16_states(th, g, z, z, 1, 1e-3, unit=4, weight_decay=0.01)
+    want = th - np.float32(1e-3 * 0.01) * th - np.float32(1e-3) * g / (np.abs(g) + np.float32(1e-8))
+    assert rel_l2(t1 - th, want - th) < 1e-5
+    for q, exact in ((m1, np.float32(0.1) * g), (v1, np.float32(0.001) * g * g)):
+        dn = oracle.bf16_round(exact)  # nearest; the result is it or its neighbour
+        assert np.all(np.abs(q - exact) <= np.abs(exact) * 2.0 ** -7 + 1e-30)
+        assert np.mean(q == dn) > 0.4
+
+
 # ------------------------------------------------------------------ planted mistakes
 def _mut_rope_sign(x, cos, sin):
     half = x.shape[-1] // 2

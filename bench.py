@@ -226,9 +226,9 @@ def run_reference(args, c):
 
 
 # ------------------------------------------------------------------ our arm
-def load_model(sf, c, ring, async_update, offload_activations=0):
+def load_model(sf, c, ring, async_update, offload_activations=0, bf16_adam_state=0):
     cfg = sf.make_config(c, ring_slots=ring, retain_grads=0, async_update=async_update,
-                         offload_activations=offload_activations)
+                         offload_activations=offload_activations, bf16_adam_state=bf16_adam_state)
     m = sf.Model(cfg)
     for l in range(c.n_layers):
         m.load(l, inputs.layer_master(c, l))
@@ -238,7 +238,7 @@ def load_model(sf, c, ring, async_update, offload_activations=0):
     return m
 
 
-def host_adam_bytes(c, micro=1):
+def host_adam_bytes(c, micro=1, bf16_state=False):
     """Host memory traffic of one step's updates.  Layers, final norm and an
     untied LM head: 28 B per parameter (bf16 gradient in, fp32 master, m, v
     read and written, bf16 pack out).  Embedding: 24 B (fp32 gradient, state)
@@ -248,7 +248,8 @@ def host_adam_bytes(c, micro=1):
     P_l = inputs.unit_numel(c, 0)
     packed = c.n_layers * P_l + c.hidden + inputs.unit_numel(c, UNIT_LM_HEAD)
     emb = c.vocab * c.hidden
-    b = 28.0 * packed + 24.0 * emb + (6.0 * emb if c.tie_embeddings else 0.0)
+    s = 8.0 if bf16_state else 0.0  # bf16 moments: 2 + 2 bytes read and written instead of 4 + 4
+    b = (28.0 - s) * packed + (24.0 - s) * emb + (6.0 * emb if c.tie_embeddings else 0.0)
     return b + (micro - 1) * 12.0 * (packed + (emb if c.tie_embeddings else 0))
 
 
@@ -269,7 +270,7 @@ def run_ours(args, c):
     host_gbs = sf.probe_host_bandwidth(0, 8 << 30)
 
     m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1,
-                   1 if args.offload_activations else 0)
+                   1 if args.offload_activations else 0, 1 if args.bf16_adam_state else 0)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
     # a fresh batch each step (rank-specific seeds for replicas); with --micro N
     # a step is N micro-batches of the workload's batch, summed before the update
@@ -356,7 +357,7 @@ def run_ours(args, c):
     # host memory: the Adam update of every unit (28 B per layer / LM-head
     # parameter: bf16 grad in, fp32 master, m, v read and written, bf16 out;
     # 24 B per embedding parameter, whose gradient is fp32) plus the DMA copies
-    adam_bytes = host_adam_bytes(c, n_micro)
+    adam_bytes = host_adam_bytes(c, n_micro, args.bf16_adam_state)
     host_bytes = adam_bytes + h2d + d2h
     t_host = host_bytes / (host_gbs * 1e9)
     if args.trace:
@@ -378,6 +379,7 @@ def run_ours(args, c):
                    "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
                    "host_updates": "synchronous" if args.sync_updates else "overlap next step",
                    "activations": "sliding (host)" if args.offload_activations else "resident",
+                   "adam_state": "bf16, stochastic rounding" if args.bf16_adam_state else "fp32",
                    "l2": "inputs larger than L2 (each step streams every layer's weights and gradients)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps},
@@ -532,6 +534,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--offload-activations", action="store_true",
                     help="sliding activations: layer checkpoints go to pinned host memory")
+    ap.add_argument("--bf16-adam-state", action="store_true",
+                    help="host Adam moments stored as bf16 with stochastic rounding")
     ap.add_argument("--sync-updates", action="store_true",
                     help="finish every host update before a step returns (no cross-step overlap)")
     ap.add_argument("--sweep-batch", default="",

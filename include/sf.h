@@ -100,7 +100,14 @@ typedef struct sf_ctx sf_ctx;
  *     W_v, and the biases are added before the rotary embedding.
  *   tie_embeddings: 1 = the LM head is the embedding matrix; there is no
  *     SF_UNIT_LM_HEAD unit (its numel is 0) and the embedding's gradient is
- *     the sum of both uses. */
+ *     the sum of both uses.
+ *   bf16_adam_state: 0 = the host keeps Adam's moments in fp32 (28 bytes of
+ *     host memory traffic per parameter and step); 1 = it keeps them as
+ *     bf16, rounded stochastically (random bits: the lowbias32 hash of the
+ *     element's index in its unit, keyed by step and unit; the low half-word
+ *     rounds the first moment, the high half-word the second), which
+ *     cuts that traffic to 20 bytes and the host state from 14 to 10 bytes
+ *     per parameter.  The update arithmetic stays fp32. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -116,6 +123,7 @@ typedef struct {
   int32_t deterministic;
   int32_t qkv_bias;
   int32_t tie_embeddings;
+  int32_t bf16_adam_state;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -204,6 +212,21 @@ int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
 
 /* Current fp32 master weights of `unit`.  Errors: SF_EINVAL. */
 int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
+
+/* Checkpointing of the optimizer.  sf_get_adam_state copies a unit's Adam
+ * moments (first into m, second into v; fp32, the caller's order, numel =
+ * sf_unit_numel) after waiting for pending updates; sf_set_adam_state
+ * restores them (with bf16_adam_state they are rounded to nearest bf16).
+ * sf_get_adam_step / sf_set_adam_step read and set the step count t of the
+ * bias corrections (the next update uses t + 1).  Together with
+ * sf_get_weights / sf_load_layer_weights (which zeroes the moments, so load
+ * the weights first) they save and resume training exactly.  Errors:
+ * SF_EINVAL (bad unit, numel or pointer), SF_ETIMEOUT / SF_ESTATE from the
+ * wait for pending updates. */
+int sf_get_adam_state(sf_ctx* ctx, int32_t unit, float* m, float* v, size_t numel);
+int sf_set_adam_state(sf_ctx* ctx, int32_t unit, const float* m, const float* v, size_t numel);
+int sf_get_adam_step(sf_ctx* ctx, int64_t* t);
+int sf_set_adam_step(sf_ctx* ctx, int64_t t);
 
 /* Wait (bounded by wait_timeout_ms) until every host update posted by the
  * steps so far is done; returns the first error a pending update reported.

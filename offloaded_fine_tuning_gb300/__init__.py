@@ -43,7 +43,8 @@ class Config(ctypes.Structure):
                 ("device", ctypes.c_int32), ("adam_threads", ctypes.c_int32),
                 ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32),
                 ("offload_activations", ctypes.c_int32), ("deterministic", ctypes.c_int32),
-                ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32)]
+                ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32),
+                ("bf16_adam_state", ctypes.c_int32)]
 
 
 class Adam(ctypes.Structure):
@@ -83,6 +84,10 @@ _SIGS = {
     "sf_train_step_accum": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, ctypes.POINTER(Adam)]),
     "sf_get_grads": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
     "sf_get_weights": (ctypes.c_int, [_VP, _I32, _VP, _SZ]),
+    "sf_get_adam_state": (ctypes.c_int, [_VP, _I32, _VP, _VP, _SZ]),
+    "sf_set_adam_state": (ctypes.c_int, [_VP, _I32, _VP, _VP, _SZ]),
+    "sf_get_adam_step": (ctypes.c_int, [_VP, ctypes.POINTER(_I64)]),
+    "sf_set_adam_step": (ctypes.c_int, [_VP, _I64]),
     "sf_loss": (ctypes.c_int, [_VP, ctypes.POINTER(_F32)]),
     "sf_sync": (ctypes.c_int, [_VP]),
     "sf_set_timing": (ctypes.c_int, [_VP, _I32]),
@@ -144,7 +149,8 @@ def _check(st: int, ctx=None, what=""):
 
 def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_grads=1,
                 lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0,
-                async_update=0, offload_activations=0, deterministic=0) -> Config:
+                async_update=0, offload_activations=0, deterministic=0,
+                bf16_adam_state=0) -> Config:
     """sf_config from a shape object with the fields of inputs.ModelConfig."""
     return Config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
                   n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, ffn=shape.ffn,
@@ -156,7 +162,8 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   async_update=async_update, offload_activations=offload_activations,
                   deterministic=deterministic,
                   qkv_bias=int(getattr(shape, "qkv_bias", False)),
-                  tie_embeddings=int(getattr(shape, "tie_embeddings", False)))
+                  tie_embeddings=int(getattr(shape, "tie_embeddings", False)),
+                  bf16_adam_state=bf16_adam_state)
 
 
 def unit_numel(cfg: Config, unit: int) -> int:
@@ -234,6 +241,30 @@ class Model:
         out = _F32()
         _check(lib().sf_loss(self.h, ctypes.byref(out)), self.h, "sf_loss")
         return float(out.value)
+
+    def adam_state(self, unit: int):
+        """(m, v) of a unit as fp32 arrays in the caller's order."""
+        m = np.empty(self.numel(unit), dtype=np.float32)
+        v = np.empty_like(m)
+        _check(lib().sf_get_adam_state(self.h, unit, m.ctypes.data, v.ctypes.data, m.size),
+               self.h, "sf_get_adam_state")
+        return m, v
+
+    def set_adam_state(self, unit: int, m: np.ndarray, v: np.ndarray) -> None:
+        m = np.ascontiguousarray(m, dtype=np.float32).reshape(-1)
+        v = np.ascontiguousarray(v, dtype=np.float32).reshape(-1)
+        _check(lib().sf_set_adam_state(self.h, unit, m.ctypes.data, v.ctypes.data, m.size),
+               self.h, "sf_set_adam_state")
+
+    @property
+    def adam_step(self) -> int:
+        t = _I64()
+        _check(lib().sf_get_adam_step(self.h, ctypes.byref(t)), self.h, "sf_get_adam_step")
+        return int(t.value)
+
+    @adam_step.setter
+    def adam_step(self, t: int) -> None:
+        _check(lib().sf_set_adam_step(self.h, t), self.h, "sf_set_adam_step")
 
     def grads(self, unit: int) -> np.ndarray:
         out = np.empty(self.numel(unit), dtype=np.float32)

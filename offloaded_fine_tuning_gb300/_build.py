@@ -42,7 +42,10 @@ def up_to_date() -> bool:
 
 def _compile(src: str, verbose: bool, extra: list[str]) -> str:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3,-fno-math-errno",
+    # host code without contraction into fused multiply-adds: the host Adam then
+    # rounds exactly like a plain float32 statement of it, on x86 and Arm alike
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17",
+           "-Xcompiler", "-fPIC,-O3,-fno-math-errno,-ffp-contract=off",
            "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj, *extra]
     if verbose:
         print(" ".join(cmd), flush=True)

@@ -132,6 +132,7 @@ struct HostUnit {
   int64_t elems = 0;          // padded pack length
   uint16_t* pack = nullptr;   // pinned
   std::unique_ptr<float[]> master, m, v;
+  std::unique_ptr<uint16_t[]> m16, v16;  // the moments as bf16 (compressed optimizer state)
   std::vector<uint16_t> retained;  // last step's gradients (retain_grads)
   std::unique_ptr<float[]> acc;    // gradient sum over the micro-batches of a step
   std::vector<float> retained_acc; // last accumulated step's summed gradients
@@ -142,8 +143,12 @@ struct HostUnit {
 enum Phase : int { kOnly = 0, kFirst = 1, kMid = 2, kLast = 3 };
 
 // Adam constants of one step (bias corrections folded in by adam_consts).
+// Adam constants of one step, with the bias corrections folded in:
+// lr (m/bc1) / (sqrt(v/bc2) + eps) = alpha m / (sqrt(v) + eps2) with
+// alpha = lr sqrt(bc2) / bc1 and eps2 = eps sqrt(bc2): one square root and
+// one division per element (the divider is the bottleneck of a host core).
 struct AdamK {
-  float b1, b2, lr, eps, wd, bc1, bc2;
+  float b1, b2, lrwd, alpha, eps2;
 };
 
 // (offset in the caller's unpadded order, offset in the padded pack, count)
@@ -190,6 +195,9 @@ struct sf_ctx {
   std::vector<HostUnit> layers;
   HostUnit lm, fn;  // LM head [V*d], final norm [d]
   std::unique_ptr<float[]> E, Em, Ev, dE;
+  std::unique_ptr<uint16_t[]> Em16, Ev16;  // compressed embedding moments
+  bool cstate = false;                     // bf16 Adam moments, stochastically rounded
+  uint32_t e_key = 0;                      // their random stream for a pending embedding update
   uint16_t* x0_pin = nullptr;    // gathered embeddings, later the input gradient dX0
   int32_t* lab_pin = nullptr;
   float* loss_pin = nullptr;
@@ -334,6 +342,21 @@ bool new_floats(sf_ctx* ctx, std::unique_ptr<float[]>& p, int64_t n) {
   if (!p) ctx->set_err("host allocation of %lld floats failed", (long long)n);
   return (bool)p;
 }
+bool new_halves(sf_ctx* ctx, std::unique_ptr<uint16_t[]>& p, int64_t n) {
+  p.reset(new (std::nothrow) uint16_t[std::max<int64_t>(n, 1)]);
+  if (!p) ctx->set_err("host allocation of %lld 16-bit values failed", (long long)n);
+  return (bool)p;
+}
+// Zero elements [b, e) of a unit's moments, whichever storage it uses.
+void zero_moments(sf_ctx* ctx, float* m, float* v, uint16_t* m16, uint16_t* v16, int64_t b,
+                  int64_t e) {
+  ctx->pool->parallel_for(e - b, 1 << 18, [=](int64_t x, int64_t y) {
+    if (m) std::memset(m + b + x, 0, (size_t)(y - x) * 4);
+    if (v) std::memset(v + b + x, 0, (size_t)(y - x) * 4);
+    if (m16) std::memset(m16 + b + x, 0, (size_t)(y - x) * 2);
+    if (v16) std::memset(v16 + b + x, 0, (size_t)(y - x) * 2);
+  });
+}
 
 // Bounded host wait on an event.
 int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
@@ -365,7 +388,7 @@ void adam_bf16_span(uint16_t* __restrict p, float* __restrict w, float* __restri
     const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
     const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
     float th = w[i];
-    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    th = th - k.lrwd * th - k.alpha * mi / (std::sqrt(vi) + k.eps2);
     m[i] = mi;
     v[i] = vi;
     w[i] = th;
@@ -380,7 +403,7 @@ void adam_f32_span(const float* __restrict g, float* __restrict w, float* __rest
     const float mi = k.b1 * m[i] + (1.f - k.b1) * gi;
     const float vi = k.b2 * v[i] + (1.f - k.b2) * gi * gi;
     float th = w[i];
-    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    th = th - k.lrwd * th - k.alpha * mi / (std::sqrt(vi) + k.eps2);
     m[i] = mi;
     v[i] = vi;
     w[i] = th;
@@ -410,7 +433,7 @@ void adam_acc_span(uint16_t* __restrict p, const float* __restrict acc, float* _
     const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
     const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
     float th = w[i];
-    th = th - k.lr * k.wd * th - k.lr * (mi / k.bc1) / (std::sqrt(vi / k.bc2) + k.eps);
+    th = th - k.lrwd * th - k.alpha * mi / (std::sqrt(vi) + k.eps2);
     m[i] = mi;
     v[i] = vi;
     w[i] = th;
@@ -419,8 +442,81 @@ void adam_acc_span(uint16_t* __restrict p, const float* __restrict acc, float* _
 }
 
 AdamK adam_consts(const sf_adam& a, int64_t step_t) {
-  return {a.beta1, a.beta2, a.lr, a.eps, a.weight_decay, 1.f - std::pow(a.beta1, (float)step_t),
-          1.f - std::pow(a.beta2, (float)step_t)};
+  const double bc1 = 1.0 - std::pow((double)a.beta1, (double)step_t);
+  const double sbc2 = std::sqrt(1.0 - std::pow((double)a.beta2, (double)step_t));
+  return {a.beta1, a.beta2, a.lr * a.weight_decay, (float)(a.lr * sbc2 / bc1),
+          (float)(a.eps * sbc2)};
+}
+
+// ---- compressed optimizer state: bf16 moments, rounded stochastically.
+// Random bits: a counter-based hash (lowbias32, C. Wellons' xorshift-multiply
+// hash) of the element's index in its unit, keyed by step and unit; its low
+// half-word rounds the first moment, its high half-word the second.
+inline uint32_t lowbias32(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352dU;
+  x ^= x >> 15;
+  x *= 0x846ca68bU;
+  x ^= x >> 16;
+  return x;
+}
+inline uint32_t sr_key(int64_t t, int unit) {
+  return lowbias32(lowbias32((uint32_t)t) ^ ((uint32_t)(unit + 3) * 0x9E3779B9U));
+}
+// x to bf16, rounded up in magnitude with probability (low 16 bits of x) / 2^16
+inline uint16_t bf16_sr(float x, uint32_t r) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  return (uint16_t)((u + (r & 0xFFFFu)) >> 16);
+}
+
+// Adam on [b, e) with bf16 moments.  G: 0 = bf16 gradient in the pack, 1 =
+// fp32 sum acc + the pack's bf16 part, 2 = fp32 gradient acc (the pack, if
+// any, only receives the new bf16 weights).  idx_off: the caller's index of
+// element 0 (selects the random words).
+template <int G>
+void adam_c_span(uint16_t* __restrict p, const float* __restrict acc, float* __restrict w,
+                 uint16_t* __restrict m, uint16_t* __restrict v, int64_t b, int64_t e,
+                 const AdamK k, uint32_t key, int64_t idx_off) {
+  for (int64_t i = b; i < e; ++i) {
+    const float g = G == 0 ? bf2f(p[i]) : G == 1 ? acc[i] + bf2f(p[i]) : acc[i];
+    const float mi = k.b1 * bf2f(m[i]) + (1.f - k.b1) * g;
+    const float vi = k.b2 * bf2f(v[i]) + (1.f - k.b2) * g * g;
+    float th = w[i];
+    th = th - k.lrwd * th - k.alpha * mi / (std::sqrt(vi) + k.eps2);
+    w[i] = th;
+    if (G != 2 || p) p[i] = f2bf(th);
+    const uint32_t r = lowbias32((uint32_t)(i + idx_off) ^ key);
+    m[i] = bf16_sr(mi, r);
+    v[i] = bf16_sr(vi, r >> 16);
+  }
+}
+
+// The compressed-state update of a packed unit, segment by segment so that
+// every element draws the random words of its index in the caller's order.
+void adam_compressed(sf_ctx* ctx, HostUnit& hu, int unit, const AdamK k, int64_t step_t,
+                     bool with_acc) {
+  const uint32_t key = sr_key(step_t, unit);
+  std::vector<Seg> one;
+  const std::vector<Seg>* segs = &ctx->segs;
+  if (unit < 0) {  // LM head or final norm: one unpadded range
+    one.push_back({0, 0, unit == SF_UNIT_FINAL_NORM ? ctx->d : ctx->V * ctx->d});
+    segs = &one;
+  }
+  for (const Seg& s : *segs) {
+    uint16_t* p = hu.pack + s.dst;
+    const float* acc = with_acc ? hu.acc.get() + s.dst : nullptr;
+    float* w = hu.master.get() + s.dst;
+    uint16_t* m = hu.m16.get() + s.dst;
+    uint16_t* v = hu.v16.get() + s.dst;
+    const int64_t off = s.src;
+    ctx->pool->parallel_for(s.n, 1 << 16, [=](int64_t b, int64_t e) {
+      if (with_acc)
+        adam_c_span<1>(p, acc, w, m, v, b, e, k, key, off);
+      else
+        adam_c_span<0>(p, nullptr, w, m, v, b, e, k, key, off);
+    });
+  }
 }
 
 // One unit: optional copy of the gradients, then either the Adam update of the
@@ -428,8 +524,8 @@ AdamK adam_consts(const sf_adam& a, int64_t step_t) {
 // refresh of the pack from the unchanged master.  Micro-batches before the
 // last only add their gradient into the unit's fp32 sum; the last one updates
 // with the whole sum.
-void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_adam& a,
-                 int64_t step_t, int phase) {
+void host_update(sf_ctx* ctx, HostUnit& hu, int unit, bool retain, bool adam_on,
+                 const sf_adam& a, int64_t step_t, int phase) {
   uint16_t* p = hu.pack;
   float* w = hu.master.get();
   float* acc = hu.acc.get();
@@ -454,6 +550,10 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_
       return;
     }
     const AdamK k = adam_consts(a, step_t);
+    if (ctx->cstate) {
+      adam_compressed(ctx, hu, unit, k, step_t, true);
+      return;
+    }
     float* m = hu.m.get();
     float* v = hu.v.get();
     ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, m, v, k](int64_t b, int64_t e) {
@@ -475,6 +575,10 @@ void host_update(sf_ctx* ctx, HostUnit& hu, bool retain, bool adam_on, const sf_
     return;
   }
   const AdamK k = adam_consts(a, step_t);
+  if (ctx->cstate) {
+    adam_compressed(ctx, hu, unit, k, step_t, false);
+    return;
+  }
   float* m = hu.m.get();
   float* v = hu.v.get();
   ctx->pool->parallel_for(hu.elems, 1 << 16, [p, w, m, v, k](int64_t b, int64_t e) {
@@ -498,9 +602,14 @@ void e_update_row(sf_ctx* ctx, int64_t r) {
   uint8_t expect = 0;
   if (st.compare_exchange_strong(expect, 1, std::memory_order_acq_rel)) {
     const int64_t d = ctx->d, o = r * d;
-    adam_f32_span(ctx->dE.get() + o, ctx->E.get() + o, ctx->Em.get() + o, ctx->Ev.get() + o, 0, d,
-                  ctx->e_k);
-    if (ctx->tied) refresh_bf16_span(ctx->lm.pack + o, ctx->E.get() + o, 0, d);  // the head's copy
+    if (ctx->cstate) {  // the tied head's bf16 row is written by the update itself
+      adam_c_span<2>(ctx->tied ? ctx->lm.pack + o : nullptr, ctx->dE.get() + o, ctx->E.get() + o,
+                     ctx->Em16.get() + o, ctx->Ev16.get() + o, 0, d, ctx->e_k, ctx->e_key, o);
+    } else {
+      adam_f32_span(ctx->dE.get() + o, ctx->E.get() + o, ctx->Em.get() + o, ctx->Ev.get() + o, 0,
+                    d, ctx->e_k);
+      if (ctx->tied) refresh_bf16_span(ctx->lm.pack + o, ctx->E.get() + o, 0, d);  // the head's copy
+    }
     st.store(2, std::memory_order_release);
   } else {
     while (st.load(std::memory_order_acquire) != 2) std::this_thread::yield();
@@ -566,6 +675,7 @@ void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int
     return;
   }
   ctx->e_k = adam_consts(a, step_t);
+  ctx->e_key = sr_key(step_t, SF_UNIT_EMBED);
   for (int64_t r = 0; r < V; ++r) ctx->e_state[r].store(0, std::memory_order_relaxed);
   std::atomic_thread_fence(std::memory_order_release);
   ctx->e_pending = true;
@@ -591,10 +701,10 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED && t.unit != kUnitEmbedRest) {
     // the gradients are dropped: put the unchanged weights back into the pack
     if (t.unit >= 0) {
-      host_update(ctx, ctx->layers[t.unit], false, false, t.adam, t.t, kOnly);
+      host_update(ctx, ctx->layers[t.unit], t.unit, false, false, t.adam, t.t, kOnly);
     } else {
-      if (!ctx->tied) host_update(ctx, ctx->lm, false, false, t.adam, t.t, kOnly);
-      host_update(ctx, ctx->fn, false, false, t.adam, t.t, kOnly);
+      if (!ctx->tied) host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, false, false, t.adam, t.t, kOnly);
+      host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, false, false, t.adam, t.t, kOnly);
     }
     finish_task(ctx, t, SF_ESTATE, "injected Adam worker failure on unit " + std::to_string(t.unit));
     return;
@@ -603,15 +713,15 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   trace(ctx, 5, t.unit);
   const bool retain = ctx->cfg.retain_grads != 0;
   if (t.unit >= 0) {
-    host_update(ctx, ctx->layers[t.unit], retain, t.adam_on, t.adam, t.t, t.phase);
+    host_update(ctx, ctx->layers[t.unit], t.unit, retain, t.adam_on, t.adam, t.t, t.phase);
   } else if (t.unit == SF_UNIT_EMBED) {
     embed_grad(ctx, t.adam_on, t.adam, t.t, t.phase);
   } else if (t.unit == kUnitEmbedRest) {
     const int64_t V = ctx->V;
     e_update_rows(ctx, V * t.arg / kEmbedRestTasks, V * (t.arg + 1) / kEmbedRestTasks);
   } else {  // LM head (unless tied: the embedding task takes its gradient) and final norm
-    if (!ctx->tied) host_update(ctx, ctx->lm, retain, t.adam_on, t.adam, t.t, t.phase);
-    host_update(ctx, ctx->fn, retain, t.adam_on, t.adam, t.t, t.phase);
+    if (!ctx->tied) host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, retain, t.adam_on, t.adam, t.t, t.phase);
+    host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, retain, t.adam_on, t.adam, t.t, t.phase);
   }
   const double ms = std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
   ctx->adam_ms += ms;
@@ -943,8 +1053,8 @@ const char* validate(const sf_config* c) {
   if (c->lce_chunk_rows < 0) return "lce_chunk_rows must be >= 0";
   if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.f)) return "rms_eps must be > 0 and rope_base > 1";
   if (c->qkv_bias < 0 || c->qkv_bias > 1 || c->tie_embeddings < 0 || c->tie_embeddings > 1 ||
-      c->deterministic < 0 || c->deterministic > 1)
-    return "qkv_bias, tie_embeddings and deterministic must be 0 or 1";
+      c->deterministic < 0 || c->deterministic > 1 || c->bf16_adam_state < 0 || c->bf16_adam_state > 1)
+    return "qkv_bias, tie_embeddings, deterministic and bf16_adam_state must be 0 or 1";
   return nullptr;
 }
 
@@ -966,6 +1076,7 @@ int init(sf_ctx* ctx) {
   constexpr int64_t A = 128;
   ctx->bias = cf.qkv_bias != 0;
   ctx->tied = cf.tie_embeddings != 0;
+  ctx->cstate = cf.bf16_adam_state != 0;
   ctx->off_g1 = 0;
   ctx->off_qkv = round_up(d, A);
   ctx->off_bqkv = round_up(ctx->off_qkv + ctx->qkvdim * d, A);  // only when biased
@@ -1054,39 +1165,35 @@ int init(sf_ctx* ctx) {
       });
       return true;
     }
-    if (!new_floats(ctx, hu.master, elems) || !new_floats(ctx, hu.m, elems) ||
-        !new_floats(ctx, hu.v, elems))
+    if (!new_floats(ctx, hu.master, elems)) return false;
+    if (ctx->cstate ? !new_halves(ctx, hu.m16, elems) || !new_halves(ctx, hu.v16, elems)
+                    : !new_floats(ctx, hu.m, elems) || !new_floats(ctx, hu.v, elems))
       return false;
     float* a = hu.master.get();
-    float* b = hu.m.get();
-    float* c = hu.v.get();
     ctx->pool->parallel_for(elems, 1 << 18, [&](int64_t s, int64_t e) {
       std::memset(a + s, 0, (size_t)(e - s) * 4);
-      std::memset(b + s, 0, (size_t)(e - s) * 4);
-      std::memset(c + s, 0, (size_t)(e - s) * 4);
       std::memset(p + s, 0, (size_t)(e - s) * 2);
     });
+    zero_moments(ctx, hu.m.get(), hu.v.get(), hu.m16.get(), hu.v16.get(), 0, elems);
     return true;
   };
   for (int l = 0; l < L && ok; ++l) ok = host_unit(ctx->layers[l], ctx->pack_elems);
   ok = ok && host_unit(ctx->lm, V * d, ctx->tied) && host_unit(ctx->fn, round_up(d, A));
-  ok = ok && new_floats(ctx, ctx->E, V * d) && new_floats(ctx, ctx->Em, V * d) &&
-       new_floats(ctx, ctx->Ev, V * d) && new_floats(ctx, ctx->dE, V * d);
+  ok = ok && new_floats(ctx, ctx->E, V * d) && new_floats(ctx, ctx->dE, V * d) &&
+       (ctx->cstate ? new_halves(ctx, ctx->Em16, V * d) && new_halves(ctx, ctx->Ev16, V * d)
+                    : new_floats(ctx, ctx->Em, V * d) && new_floats(ctx, ctx->Ev, V * d));
   if (ok && ctx->xoff) ok = halloc(ctx, &ctx->x_pin, L * T * d);
   ok = ok && halloc(ctx, &ctx->x0_pin, T * d) && halloc(ctx, &ctx->lab_pin, T) &&
        halloc(ctx, &ctx->loss_pin, 1) && halloc(ctx, &ctx->err_pin, 1);
   if (!ok) return SF_ENOMEM;
   {
     float* a = ctx->E.get();
-    float* b = ctx->Em.get();
-    float* c = ctx->Ev.get();
     float* e2 = ctx->dE.get();
     ctx->pool->parallel_for(V * d, 1 << 18, [&](int64_t s, int64_t e) {
       std::memset(a + s, 0, (size_t)(e - s) * 4);
-      std::memset(b + s, 0, (size_t)(e - s) * 4);
-      std::memset(c + s, 0, (size_t)(e - s) * 4);
       std::memset(e2 + s, 0, (size_t)(e - s) * 4);
     });
+    zero_moments(ctx, ctx->Em.get(), ctx->Ev.get(), ctx->Em16.get(), ctx->Ev16.get(), 0, V * d);
   }
 
   // ---- streams and events
@@ -1472,35 +1579,9 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t nume
     ctx->set_err("sf_load_layer_weights: bad unit %d or numel %zu", unit, numel);
     return SF_EINVAL;
   }
-  HostUnit* hu = nullptr;
-  float *master = nullptr, *m = nullptr, *v = nullptr;
-  int64_t n = (int64_t)numel;
-  if (unit >= 0) {
-    hu = &ctx->layers[unit];
-    scatter_unit(ctx, w, hu->master.get());
-  } else if (unit == SF_UNIT_EMBED) {
-    master = ctx->E.get();
-    m = ctx->Em.get();
-    v = ctx->Ev.get();
-  } else {
-    hu = unit == SF_UNIT_LM_HEAD ? &ctx->lm : &ctx->fn;
-  }
-  if (hu && unit < 0) {
-    float* dst = hu->master.get();
-    ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
-      std::memcpy(dst + b, w + b, (size_t)(e - b) * 4);
-    });
-  }
-  if (hu) {
-    master = hu->master.get();
-    m = hu->m.get();
-    v = hu->v.get();
-    n = hu->elems;
-    uint16_t* p = hu->pack;
-    ctx->pool->parallel_for(n, 1 << 16, [&](int64_t b, int64_t e) {
-      for (int64_t i = b; i < e; ++i) p[i] = f2bf(master[i]);
-    });
-  } else {
+  const int64_t n = (int64_t)numel;
+  if (unit == SF_UNIT_EMBED) {
+    float* master = ctx->E.get();
     ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
       std::memcpy(master + b, w + b, (size_t)(e - b) * 4);
     });
@@ -1509,11 +1590,96 @@ int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* w, size_t nume
       const float* E = master;
       ctx->pool->parallel_for(n, 1 << 16, [p, E](int64_t b, int64_t e) { refresh_bf16_span(p, E, b, e); });
     }
+    zero_moments(ctx, ctx->Em.get(), ctx->Ev.get(), ctx->Em16.get(), ctx->Ev16.get(), 0, n);
+    return SF_OK;
   }
-  ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
-    std::memset(m + b, 0, (size_t)(e - b) * 4);
-    std::memset(v + b, 0, (size_t)(e - b) * 4);
+  HostUnit* hu = unit >= 0 ? &ctx->layers[unit] : unit == SF_UNIT_LM_HEAD ? &ctx->lm : &ctx->fn;
+  float* master = hu->master.get();
+  if (unit >= 0) {
+    scatter_unit(ctx, w, master);
+  } else {
+    ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
+      std::memcpy(master + b, w + b, (size_t)(e - b) * 4);
+    });
+  }
+  uint16_t* p = hu->pack;
+  ctx->pool->parallel_for(hu->elems, 1 << 16, [p, master](int64_t b, int64_t e) {
+    refresh_bf16_span(p, master, b, e);
   });
+  zero_moments(ctx, hu->m.get(), hu->v.get(), hu->m16.get(), hu->v16.get(), 0, hu->elems);
+  return SF_OK;
+}
+
+// The Adam moments of a unit, as fp32 in the caller's order (checkpointing).
+int sf_get_adam_state(sf_ctx* ctx, int32_t unit, float* m, float* v, size_t numel) {
+  if (!ctx || !m || !v || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
+    if (ctx) ctx->set_err("sf_get_adam_state: bad unit %d or numel %zu", unit, numel);
+    return SF_EINVAL;
+  }
+  if (int st = wait_tasks(ctx)) return st;
+  const float *fm, *fv;
+  const uint16_t *hm, *hv;
+  if (unit == SF_UNIT_EMBED) {
+    fm = ctx->Em.get(); fv = ctx->Ev.get(); hm = ctx->Em16.get(); hv = ctx->Ev16.get();
+  } else {
+    const HostUnit& hu = unit >= 0 ? ctx->layers[unit] : unit == SF_UNIT_LM_HEAD ? ctx->lm : ctx->fn;
+    fm = hu.m.get(); fv = hu.v.get(); hm = hu.m16.get(); hv = hu.v16.get();
+  }
+  auto copy = [&](int64_t src, int64_t dst, int64_t cnt) {
+    for (int64_t i = 0; i < cnt; ++i) {
+      m[src + i] = fm ? fm[dst + i] : bf2f(hm[dst + i]);
+      v[src + i] = fv ? fv[dst + i] : bf2f(hv[dst + i]);
+    }
+  };
+  if (unit >= 0) {
+    for (const Seg& s : ctx->segs) copy(s.src, s.dst, s.n);
+  } else {
+    copy(0, 0, (int64_t)numel);
+  }
+  return SF_OK;
+}
+
+// Restore a unit's Adam moments (bf16 storage rounds them to nearest).
+int sf_set_adam_state(sf_ctx* ctx, int32_t unit, const float* m, const float* v, size_t numel) {
+  if (!ctx || !m || !v || unit_numel_cfg(&ctx->cfg, unit) == 0 || numel != unit_numel_cfg(&ctx->cfg, unit)) {
+    if (ctx) ctx->set_err("sf_set_adam_state: bad unit %d or numel %zu", unit, numel);
+    return SF_EINVAL;
+  }
+  if (ctx->poisoned) return SF_ESTATE;
+  if (int st = wait_tasks(ctx)) return st;
+  float *fm, *fv;
+  uint16_t *hm, *hv;
+  if (unit == SF_UNIT_EMBED) {
+    fm = ctx->Em.get(); fv = ctx->Ev.get(); hm = ctx->Em16.get(); hv = ctx->Ev16.get();
+  } else {
+    HostUnit& hu = unit >= 0 ? ctx->layers[unit] : unit == SF_UNIT_LM_HEAD ? ctx->lm : ctx->fn;
+    fm = hu.m.get(); fv = hu.v.get(); hm = hu.m16.get(); hv = hu.v16.get();
+  }
+  auto copy = [&](int64_t src, int64_t dst, int64_t cnt) {
+    for (int64_t i = 0; i < cnt; ++i) {
+      if (fm) { fm[dst + i] = m[src + i]; fv[dst + i] = v[src + i]; }
+      else { hm[dst + i] = f2bf(m[src + i]); hv[dst + i] = f2bf(v[src + i]); }
+    }
+  };
+  if (unit >= 0) {
+    for (const Seg& s : ctx->segs) copy(s.src, s.dst, s.n);
+  } else {
+    copy(0, 0, (int64_t)numel);
+  }
+  return SF_OK;
+}
+
+int sf_get_adam_step(sf_ctx* ctx, int64_t* t) {
+  if (!ctx || !t) return SF_EINVAL;
+  if (int st = wait_tasks(ctx)) return st;
+  *t = ctx->adam_t;
+  return SF_OK;
+}
+
+int sf_set_adam_step(sf_ctx* ctx, int64_t t) {
+  if (!ctx || t < 0) return SF_EINVAL;
+  if (int st = wait_tasks(ctx)) return st;
+  ctx->adam_t = t;
   return SF_OK;
 }
 

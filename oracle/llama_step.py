@@ -309,8 +309,9 @@ def adam_update(theta, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_
 # Optimizer-state compression: the moments are stored as bfloat16, rounded
 # stochastically so that increments far below a bf16 step (v moves by
 # (1 - beta2) = 0.1% of itself per step) survive in expectation.  The random
-# bits are a counter-based hash of (step, unit, moment, element index), so
-# both implementations draw the same bits.
+# bits are a counter-based hash of (step, unit, element index), so both
+# implementations draw the same bits: one 32-bit word per element, its low
+# half-word rounds the first moment and its high half-word the second.
 _U32 = np.uint32
 
 
@@ -327,11 +328,11 @@ def lowbias32(x):
     return x
 
 
-def sr_key(t, unit, which):
-    """Stream key of step t >= 1, unit (layer index, or -1 embedding, -2 final
-    norm, -3 LM head) and moment (1 = first, 2 = second)."""
+def sr_key(t, unit):
+    """Stream key of step t >= 1 and unit (layer index, or -1 embedding, -2
+    final norm, -3 LM head)."""
     with np.errstate(over="ignore"):
-        mixed = lowbias32(_U32(t & 0xFFFFFFFF)) ^ (_U32(unit + 3) * _U32(0x9E3779B9)) ^ _U32(which)
+        mixed = lowbias32(_U32(t & 0xFFFFFFFF)) ^ (_U32(unit + 3) * _U32(0x9E3779B9))
     return lowbias32(mixed)
 
 
@@ -355,17 +356,20 @@ def adam_update_bf16_states(theta, g, m, v, t, lr, unit, beta1=0.9, beta2=0.999,
     """adam_update in float32 arithmetic with the moments m, v stored as
     bfloat16 (float32 arrays holding bf16 values): the new moments are
     computed in float32, used unrounded for this step's parameter update,
-    then stored with bf16_round_stochastic (element i of the unit draws
-    sr_bits(sr_key(t, unit, 1 or 2), index0 + i)).  Returns (theta, m, v)."""
+    then stored with bf16_round_stochastic: element i of the unit draws
+    r = sr_bits(sr_key(t, unit), index0 + i), the first moment rounds with
+    the low and the second with the high half-word of r.  Returns (theta, m, v)."""
     f = np.float32
     theta, g, m, v = (np.asarray(a, dtype=np.float32) for a in (theta, g, m, v))
     b1, b2, lr_, eps_, wd = f(beta1), f(beta2), f(lr), f(eps), f(weight_decay)
-    bc1 = f(1.0) - f(np.power(b1, f(t)))
-    bc2 = f(1.0) - f(np.power(b2, f(t)))
+    # the scalar bias corrections in float64 (1 - b2^t cancels in float32)
+    bc1 = f(1.0 - float(b1) ** t)
+    bc2 = f(1.0 - float(b2) ** t)
     m1 = b1 * m + (f(1.0) - b1) * g
     v1 = b2 * v + (f(1.0) - b2) * g * g
     th = theta - lr_ * wd * theta - lr_ * (m1 / bc1) / (np.sqrt(v1 / bc2) + eps_)
     idx = index0 + np.arange(theta.size, dtype=np.uint64)
-    mq = bf16_round_stochastic(m1, sr_bits(sr_key(t, unit, 1), idx).reshape(theta.shape))
-    vq = bf16_round_stochastic(v1, sr_bits(sr_key(t, unit, 2), idx).reshape(theta.shape))
+    r = sr_bits(sr_key(t, unit), idx).reshape(theta.shape)
+    mq = bf16_round_stochastic(m1, r)
+    vq = bf16_round_stochastic(v1, r >> _U32(16))
     return th.astype(np.float32), mq, vq

@@ -163,6 +163,84 @@ def test_gradient_accumulation_rejects_a_bad_micro_batch_before_running():
         assert m.train_step(tok[:1], lab[:1]) == sf.SF_OK
 
 
+# ------------------------------------------------------------------ optimizer state
+ALL_UNITS = (0, 1, UNIT_EMBED, UNIT_LM_HEAD, UNIT_FINAL_NORM)
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_bf16_adam_state_matches_oracle_elementwise(tied):
+    """The host update with bf16 moments against the oracle on the same
+    inputs (the engine's own gradients, weights and moments): moments bit for
+    bit (same stochastic-rounding bits), weights to float32 rounding."""
+    cfg = TEST_CONFIGS["small-qwen"].with_(n_layers=2, tie_embeddings=tied)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lr, wd = 1e-3, 0.01
+    adam = sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=wd)
+    units = [u for u in ALL_UNITS if inputs.unit_numel(cfg, u)]
+    with make_model(cfg, mast, bf16_adam_state=1) as m:
+        for t in (1, 2):
+            before = {u: (m.weights(u), *m.adam_state(u)) for u in units}
+            assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+            assert m.adam_step == t
+            for u in units:
+                w0, m0, v0 = before[u]
+                want, mq, vq = oracle.adam_update_bf16_states(w0, m.grads(u), m0, v0, t, lr, unit=u,
+                                                              weight_decay=wd)
+                m1, v1 = m.adam_state(u)
+                assert np.array_equal(m1, mq) and np.array_equal(v1, vq), u
+                # the engine folds the bias corrections into two constants: the
+                # same update up to float32 rounding (a few ulps of the update
+                # term, two of the new weight)
+                w1 = m.weights(u)
+                tol = 2 * np.spacing(np.abs(want)) + 5e-7 * np.abs(want - w0)
+                assert np.all(np.abs(w1 - want) <= tol), u
+
+
+@pytest.mark.parametrize("bf16_state", [0, 1])
+def test_checkpoint_and_resume_is_bitwise(bf16_state):
+    """Weights, moments and step count saved after two steps and loaded into a
+    fresh engine: the third step is bit-identical to the uninterrupted run."""
+    cfg = TEST_CONFIGS["small-qwen"].with_(n_layers=2)
+    mast = masters(cfg)
+    batches = [inputs.tokens_and_labels(cfg, seed=70 + i) for i in range(3)]
+    adam = sf.Adam(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    units = [u for u in ALL_UNITS if inputs.unit_numel(cfg, u)]
+    with make_model(cfg, mast, bf16_adam_state=bf16_state, async_update=1) as a:
+        for tk, lb in batches[:2]:
+            a.step(tk, lb, adam)
+        snap = {u: (a.weights(u), *a.adam_state(u)) for u in units}
+        t = a.adam_step
+        loss_a = a.step(*batches[2], adam)
+        after_a = {u: a.weights(u) for u in units}
+    with make_model(cfg, {u: w for u, (w, _, _) in snap.items()}, bf16_adam_state=bf16_state) as b:
+        for u, (_, mm, vv) in snap.items():
+            b.set_adam_state(u, mm, vv)
+        b.adam_step = t
+        loss_b = b.step(*batches[2], adam)
+        assert loss_b == loss_a
+        for u in units:
+            assert np.array_equal(b.weights(u), after_a[u]), u
+
+
+def test_bf16_adam_state_tracks_fp32_state_training():
+    """Three Adam steps with compressed moments stay with fp32 moments."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2)
+    mast = masters(cfg)
+    batches = [inputs.tokens_and_labels(cfg, seed=80 + i) for i in range(3)]
+    adam = sf.Adam(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    out = []
+    for st in (0, 1):
+        with make_model(cfg, mast, bf16_adam_state=st) as m:
+            losses = [m.step(tk, lb, adam) for tk, lb in batches]
+            out.append((losses, {u: m.weights(u) for u in ALL_UNITS}))
+    for l0, l1 in zip(out[0][0], out[1][0]):
+        assert abs(l0 - l1) / l0 < 1e-4
+    for u in ALL_UNITS:
+        d0, d1 = out[0][1][u] - mast[u], out[1][1][u] - mast[u]
+        assert rel_l2(d1, d0) < 0.05, u
+
+
 def test_ring_size_invariance_is_bitwise():
     cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=4)
     mast = masters(cfg)

@@ -472,15 +472,19 @@ def test_stochastic_rounding_bits_are_uniform():
     """The hashed words of one stream look uniform: the rounding-up rate of a
     value a quarter of the way between two bf16 neighbours is 1/4."""
     n = 1 << 20
-    r = ls.sr_bits(ls.sr_key(7, 3, 2), np.arange(n))
-    lo16 = (r & np.uint32(0xFFFF)).astype(np.float64)
-    assert abs(lo16.mean() / 65536 - 0.5) < 3e-3
+    r = ls.sr_bits(ls.sr_key(7, 3), np.arange(n))
     x = np.float32(1.0) + np.float32(2.0 ** -7) / np.float32(4.0)  # 1 + ulp/4
-    up = ls.bf16_round_stochastic(np.full(n, x, np.float32), r) > 1.0
-    assert abs(up.mean() - 0.25) < 3e-3
-    # different steps, units and moments give different streams
-    keys = {int(ls.sr_key(t, u, w)) for t in (1, 2) for u in (-3, -1, 0, 5) for w in (1, 2)}
-    assert len(keys) == 16
+    for half in (r, r >> np.uint32(16)):  # both half-words (first and second moment)
+        lo16 = (half & np.uint32(0xFFFF)).astype(np.float64)
+        assert abs(lo16.mean() / 65536 - 0.5) < 3e-3
+        up = ls.bf16_round_stochastic(np.full(n, x, np.float32), half) > 1.0
+        assert abs(up.mean() - 0.25) < 3e-3
+    # the two half-words are not correlated
+    a, b = (r & np.uint32(0xFFFF)).astype(np.float64), (r >> np.uint32(16)).astype(np.float64)
+    assert abs(np.corrcoef(a, b)[0, 1]) < 5e-3
+    # different steps and units give different streams
+    keys = {int(ls.sr_key(t, u)) for t in (1, 2, 3) for u in (-3, -1, 0, 5)}
+    assert len(keys) == 12
 
 
 def test_bf16_moments_track_float32_adam_where_nearest_rounding_stalls():

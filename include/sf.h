@@ -107,7 +107,16 @@ typedef struct sf_ctx sf_ctx;
  *     element's index in its unit, keyed by step and unit; the low half-word
  *     rounds the first moment, the high half-word the second), which
  *     cuts that traffic to 20 bytes and the host state from 14 to 10 bytes
- *     per parameter.  The update arithmetic stays fp32. */
+ *     per parameter.  The update arithmetic stays fp32.
+ *   fp16_grads: 0 = weight gradients leave the GPU as bf16; 1 = as fp16
+ *     multiplied by a loss scale (3 more mantissa bits; the scale keeps small
+ *     gradients out of fp16's subnormal range).  The host divides the scale
+ *     out; a unit whose gradients overflowed keeps its weights and moments
+ *     for that step (counted in sf_stats.skipped_updates).  The scale halves
+ *     after a step in which an update was skipped and doubles after 1000
+ *     steps without one (with async_update the count of a step is complete
+ *     one step later).
+ *   loss_scale: the initial scale for fp16_grads (0 = 65536; at most 2^24). */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int32_t max_batch, max_seq;
@@ -124,6 +133,8 @@ typedef struct {
   int32_t qkv_bias;
   int32_t tie_embeddings;
   int32_t bf16_adam_state;
+  int32_t fp16_grads;
+  float loss_scale;
 } sf_config;
 
 /* Adam hyper-parameters (bias-corrected; weight_decay is decoupled, AdamW). */
@@ -151,6 +162,8 @@ typedef struct {
   double bwd_layer_ms;     /* recompute + backward compute (compute stream) */
   double d2h_layer_ms;     /* gradient pack copy to the host (copy stream) */
   double update_layer_ms;  /* host Adam of one layer (wall time, update thread) */
+  double loss_scale;       /* fp16_grads: the scale of this step's gradients; else 0 */
+  int64_t skipped_updates; /* fp16_grads: unit updates skipped for overflow, in total */
 } sf_stats;
 
 /* ---------------------------------------------------------------- model API */

@@ -44,7 +44,8 @@ class Config(ctypes.Structure):
                 ("wait_timeout_ms", ctypes.c_int32), ("async_update", ctypes.c_int32),
                 ("offload_activations", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("qkv_bias", ctypes.c_int32), ("tie_embeddings", ctypes.c_int32),
-                ("bf16_adam_state", ctypes.c_int32)]
+                ("bf16_adam_state", ctypes.c_int32), ("fp16_grads", ctypes.c_int32),
+                ("loss_scale", ctypes.c_float)]
 
 
 class Adam(ctypes.Structure):
@@ -58,7 +59,8 @@ class Stats(ctypes.Structure):
                [("gemm_launches", ctypes.c_int64), ("kernel_launches", ctypes.c_int64),
                 ("timing_enabled", ctypes.c_int32)] + \
                [(n, ctypes.c_double) for n in
-                ("fwd_layer_ms", "bwd_layer_ms", "d2h_layer_ms", "update_layer_ms")]
+                ("fwd_layer_ms", "bwd_layer_ms", "d2h_layer_ms", "update_layer_ms", "loss_scale")] + \
+               [("skipped_updates", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -150,7 +152,7 @@ def _check(st: int, ctx=None, what=""):
 def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_grads=1,
                 lce_chunk_rows=0, device=0, adam_threads=0, wait_timeout_ms=0,
                 async_update=0, offload_activations=0, deterministic=0,
-                bf16_adam_state=0) -> Config:
+                bf16_adam_state=0, fp16_grads=0, loss_scale=0.0) -> Config:
     """sf_config from a shape object with the fields of inputs.ModelConfig."""
     return Config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
                   n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, ffn=shape.ffn,
@@ -163,7 +165,8 @@ def make_config(shape, max_batch=None, max_seq=None, ring_slots=None, retain_gra
                   deterministic=deterministic,
                   qkv_bias=int(getattr(shape, "qkv_bias", False)),
                   tie_embeddings=int(getattr(shape, "tie_embeddings", False)),
-                  bf16_adam_state=bf16_adam_state)
+                  bf16_adam_state=bf16_adam_state, fp16_grads=fp16_grads,
+                  loss_scale=loss_scale)
 
 
 def unit_numel(cfg: Config, unit: int) -> int:

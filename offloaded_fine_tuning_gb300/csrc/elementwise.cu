@@ -3,6 +3,7 @@
 // reductions and casts.  All of them stream rows with 16-byte vector accesses
 // and reduce with warp shuffles; none of them is a contraction.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -204,6 +205,21 @@ void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, 
   reduce_parts_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d, out);
 }
 
+__global__ void reduce_parts_f16_kernel(const float* __restrict__ part, int parts, int d,
+                                        __half* __restrict__ out, float scale) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= d) return;
+  float s = 0.f;
+  for (int p = 0; p < parts; ++p) s += part[(int64_t)p * d + j];
+  out[j] = __float2half_rn(s * scale);
+}
+
+void reduce_parts_f16(const float* part, int parts, int d, uint16_t* out, float scale,
+                      cudaStream_t st) {
+  reduce_parts_f16_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d,
+                                                            reinterpret_cast<__half*>(out), scale);
+}
+
 // Column sums of x [rows, cols] bf16 (row stride ld) as fp32 partials:
 // part[p][c] sums the rows [rows*p/parts, rows*(p+1)/parts).  Two columns per
 // thread, so a warp reads 128 contiguous bytes of a row.
@@ -229,6 +245,13 @@ void bias_grad(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float
   dim3 grid((unsigned)((cols / 2 + 127) / 128), (unsigned)parts);
   colsum_parts_kernel<<<grid, 128, 0, st>>>(x, ld, rows, cols, part, parts);
   reduce_parts_bf16(part, parts, cols, out, st);
+}
+
+void bias_grad_f16(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float* part,
+                   int parts, uint16_t* out, float scale, cudaStream_t st) {
+  dim3 grid((unsigned)((cols / 2 + 127) / 128), (unsigned)parts);
+  colsum_parts_kernel<<<grid, 128, 0, st>>>(x, ld, rows, cols, part, parts);
+  reduce_parts_f16(part, parts, cols, out, scale, st);
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -416,6 +439,30 @@ __global__ void cast_f32_bf16_kernel(const float* __restrict__ x, __nv_bfloat16*
   } else {
     for (int64_t j = i; j < n; ++j) y[j] = __float2bfloat16_rn(x[j]);
   }
+}
+
+__global__ void cast_f32_f16_kernel(const float* __restrict__ x, __half* __restrict__ y, int64_t n,
+                                    float scale) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i + 8 <= n) {
+    const float4 a = reinterpret_cast<const float4*>(x + i)[0], b = reinterpret_cast<const float4*>(x + i)[1];
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 h = __floats2half2_rn(f[2 * k] * scale, f[2 * k + 1] * scale);
+      w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(y + i) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    for (int64_t j = i; j < n; ++j) y[j] = __float2half_rn(x[j] * scale);
+  }
+}
+
+void cast_f32_f16(const float* x, uint16_t* y, int64_t n, float scale, cudaStream_t st) {
+  const int64_t threads = (n + 7) / 8;
+  cast_f32_f16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+      x, reinterpret_cast<__half*>(y), n, scale);
 }
 
 void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st) {

@@ -50,6 +50,26 @@ inline uint16_t f2bf(float f) {
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
+// IEEE binary16 bits to float (the host's native half type)
+inline float h2f(uint16_t h) {
+  _Float16 x;
+  std::memcpy(&x, &h, 2);
+  return (float)x;
+}
+// A gradient element from a pack: bf16, or fp16 scaled by the step's loss scale
+template <bool F16>
+inline float grd(uint16_t x, float inv) {
+  if constexpr (F16) {
+    return h2f(x) * inv;
+  } else {
+    (void)inv;
+    uint32_t u = (uint32_t)x << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+  }
+}
+
 inline float bf2f(uint16_t h) {
   uint32_t u = (uint32_t)h << 16;
   float f;
@@ -135,8 +155,13 @@ struct HostUnit {
   std::unique_ptr<uint16_t[]> m16, v16;  // the moments as bf16 (compressed optimizer state)
   std::vector<uint16_t> retained;  // last step's gradients (retain_grads)
   std::unique_ptr<float[]> acc;    // gradient sum over the micro-batches of a step
+  bool acc_bad = false;            // a micro-batch's fp16 gradients overflowed
   std::vector<float> retained_acc; // last accumulated step's summed gradients
+  float retained_inv = 0.f;        // 1/scale of retained fp16 gradients (0: bf16)
 };
+
+// Steps without an overflow before the fp16 gradient scale doubles.
+constexpr int64_t kScaleWindow = 1000;
 
 // Where a micro-batch stands in a step: the only one, or the first, a middle
 // or the last of several whose gradients are summed before the update.
@@ -197,7 +222,19 @@ struct sf_ctx {
   std::unique_ptr<float[]> E, Em, Ev, dE;
   std::unique_ptr<uint16_t[]> Em16, Ev16;  // compressed embedding moments
   bool cstate = false;                     // bf16 Adam moments, stochastically rounded
+  // fp16 gradients: weight gradients leave the GPU as fp16 times lscale; the
+  // scale halves after a step whose gradients overflowed and doubles after
+  // kScaleWindow steps without one
+  bool f16g = false;
+  float lscale = 1.f;
+  int64_t lgood = 0;
+  std::atomic<int64_t> skipped{0};  // unit updates skipped for overflow (total)
+  int64_t skipped_seen = 0;
+  float cur_inv = 0.f;              // 1/scale of the running step's gradients (0: bf16)
+  int gepi() const { return f16g ? sf::kEpiF16 : sf::kEpiBF16; }
+  float gscale() const { return f16g ? lscale : 1.f; }
   uint32_t e_key = 0;                      // their random stream for a pending embedding update
+  bool e_bad = false;                      // the tied head's fp16 gradient overflowed this step
   uint16_t* x0_pin = nullptr;    // gathered embeddings, later the input gradient dX0
   int32_t* lab_pin = nullptr;
   float* loss_pin = nullptr;
@@ -235,6 +272,7 @@ struct sf_ctx {
     int64_t t;
     int arg;        // row range of a deferred embedding-update task
     int phase;      // micro-batch phase (Phase)
+    float ginv;     // 1/scale of the benchmark's fp16 gradients (0: bf16)
   };
   std::deque<Task> aq;
   int aq_pending = 0;
@@ -381,10 +419,11 @@ int wait_event(sf_ctx* ctx, cudaEvent_t ev, const char* what) {
 // The element loops take restrict-qualified pointers so that the compiler
 // vectorises them (the update is bound by host memory bandwidth).
 
+template <bool F16>
 void adam_bf16_span(uint16_t* __restrict p, float* __restrict w, float* __restrict m,
-                    float* __restrict v, int64_t b, int64_t e, const AdamK k) {
+                    float* __restrict v, int64_t b, int64_t e, const AdamK k, float inv) {
   for (int64_t i = b; i < e; ++i) {
-    const float g = bf2f(p[i]);
+    const float g = grd<F16>(p[i], inv);
     const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
     const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
     float th = w[i];
@@ -414,22 +453,25 @@ void refresh_bf16_span(uint16_t* __restrict p, const float* __restrict w, int64_
   for (int64_t i = b; i < e; ++i) p[i] = f2bf(w[i]);
 }
 
-// A micro-batch's gradient (bf16 in the pack) into the fp32 sum, then the
+// A micro-batch's gradient (in the pack) into the fp32 sum, then the
 // unchanged weights back into the pack for the next micro-batch's copy.
+template <bool F16>
 void accum_span(uint16_t* __restrict p, float* __restrict acc, const float* __restrict w,
-                int64_t b, int64_t e, bool first) {
+                int64_t b, int64_t e, bool first, float inv) {
   for (int64_t i = b; i < e; ++i) {
-    const float g = bf2f(p[i]);
+    const float g = grd<F16>(p[i], inv);
     acc[i] = first ? g : acc[i] + g;
     p[i] = f2bf(w[i]);
   }
 }
 
-// Adam on the summed gradient (fp32 sum + the last micro-batch's bf16 part).
+// Adam on the summed gradient (fp32 sum + the last micro-batch's part).
+template <bool F16>
 void adam_acc_span(uint16_t* __restrict p, const float* __restrict acc, float* __restrict w,
-                   float* __restrict m, float* __restrict v, int64_t b, int64_t e, const AdamK k) {
+                   float* __restrict m, float* __restrict v, int64_t b, int64_t e, const AdamK k,
+                   float inv) {
   for (int64_t i = b; i < e; ++i) {
-    const float g = acc[i] + bf2f(p[i]);
+    const float g = acc[i] + grd<F16>(p[i], inv);
     const float mi = k.b1 * m[i] + (1.f - k.b1) * g;
     const float vi = k.b2 * v[i] + (1.f - k.b2) * g * g;
     float th = w[i];
@@ -474,12 +516,12 @@ inline uint16_t bf16_sr(float x, uint32_t r) {
 // fp32 sum acc + the pack's bf16 part, 2 = fp32 gradient acc (the pack, if
 // any, only receives the new bf16 weights).  idx_off: the caller's index of
 // element 0 (selects the random words).
-template <int G>
+template <int G, bool F16 = false>
 void adam_c_span(uint16_t* __restrict p, const float* __restrict acc, float* __restrict w,
                  uint16_t* __restrict m, uint16_t* __restrict v, int64_t b, int64_t e,
-                 const AdamK k, uint32_t key, int64_t idx_off) {
+                 const AdamK k, uint32_t key, int64_t idx_off, float inv = 1.f) {
   for (int64_t i = b; i < e; ++i) {
-    const float g = G == 0 ? bf2f(p[i]) : G == 1 ? acc[i] + bf2f(p[i]) : acc[i];
+    const float g = G == 0 ? grd<F16>(p[i], inv) : G == 1 ? acc[i] + grd<F16>(p[i], inv) : acc[i];
     const float mi = k.b1 * bf2f(m[i]) + (1.f - k.b1) * g;
     const float vi = k.b2 * bf2f(v[i]) + (1.f - k.b2) * g * g;
     float th = w[i];
@@ -495,7 +537,7 @@ void adam_c_span(uint16_t* __restrict p, const float* __restrict acc, float* __r
 // The compressed-state update of a packed unit, segment by segment so that
 // every element draws the random words of its index in the caller's order.
 void adam_compressed(sf_ctx* ctx, HostUnit& hu, int unit, const AdamK k, int64_t step_t,
-                     bool with_acc) {
+                     bool with_acc, float inv) {
   const uint32_t key = sr_key(step_t, unit);
   std::vector<Seg> one;
   const std::vector<Seg>* segs = &ctx->segs;
@@ -511,78 +553,98 @@ void adam_compressed(sf_ctx* ctx, HostUnit& hu, int unit, const AdamK k, int64_t
     uint16_t* v = hu.v16.get() + s.dst;
     const int64_t off = s.src;
     ctx->pool->parallel_for(s.n, 1 << 16, [=](int64_t b, int64_t e) {
-      if (with_acc)
-        adam_c_span<1>(p, acc, w, m, v, b, e, k, key, off);
-      else
-        adam_c_span<0>(p, nullptr, w, m, v, b, e, k, key, off);
+      if (inv != 0.f) {
+        if (with_acc)
+          adam_c_span<1, true>(p, acc, w, m, v, b, e, k, key, off, inv);
+        else
+          adam_c_span<0, true>(p, nullptr, w, m, v, b, e, k, key, off, inv);
+      } else {
+        if (with_acc)
+          adam_c_span<1>(p, acc, w, m, v, b, e, k, key, off);
+        else
+          adam_c_span<0>(p, nullptr, w, m, v, b, e, k, key, off);
+      }
     });
   }
+}
+
+// Does a pack of scaled fp16 gradients hold an overflow (an infinity or NaN)?
+bool f16_overflow(sf_ctx* ctx, const uint16_t* p, int64_t n) {
+  std::atomic<bool> bad{false};
+  ctx->pool->parallel_for(n, 1 << 18, [&](int64_t b, int64_t e) {
+    uint16_t any = 0;
+    for (int64_t i = b; i < e; ++i) any |= (uint16_t)((p[i] & 0x7C00u) == 0x7C00u);
+    if (any) bad.store(true, std::memory_order_relaxed);
+  });
+  return bad.load();
 }
 
 // One unit: optional copy of the gradients, then either the Adam update of the
 // fp32 master (refreshing the bf16 pack in place) or, without an optimizer, a
 // refresh of the pack from the unchanged master.  Micro-batches before the
 // last only add their gradient into the unit's fp32 sum; the last one updates
-// with the whole sum.
+// with the whole sum.  inv != 0: the pack holds fp16 gradients scaled by
+// 1/inv; a unit whose gradients overflowed skips its update (its weights and
+// moments stay as they are) and counts one skipped update.
 void host_update(sf_ctx* ctx, HostUnit& hu, int unit, bool retain, bool adam_on,
-                 const sf_adam& a, int64_t step_t, int phase) {
+                 const sf_adam& a, int64_t step_t, int phase, float inv) {
   uint16_t* p = hu.pack;
   float* w = hu.master.get();
   float* acc = hu.acc.get();
+  const bool f16 = inv != 0.f;
+  const bool bad = f16 && f16_overflow(ctx, p, hu.elems);
   if (phase == kFirst || phase == kMid) {
     const bool first = phase == kFirst;
-    ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, first](int64_t b, int64_t e) {
-      accum_span(p, acc, w, b, e, first);
+    if (first) hu.acc_bad = false;
+    hu.acc_bad = hu.acc_bad || bad;
+    ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, first, inv, f16](int64_t b, int64_t e) {
+      if (f16)
+        accum_span<true>(p, acc, w, b, e, first, inv);
+      else
+        accum_span<false>(p, acc, w, b, e, first, inv);
     });
     return;
   }
-  if (phase == kLast) {
-    if (retain) {
+  const bool skip = bad || (phase == kLast && hu.acc_bad);
+  if (retain) {
+    hu.retained_inv = inv;
+    if (phase == kLast) {
       hu.retained_acc.resize((size_t)hu.elems);
       float* dst = hu.retained_acc.data();
-      ctx->pool->parallel_for(hu.elems, 1 << 16, [dst, p, acc](int64_t b, int64_t e) {
-        for (int64_t i = b; i < e; ++i) dst[i] = acc[i] + bf2f(p[i]);
+      ctx->pool->parallel_for(hu.elems, 1 << 16, [dst, p, acc, inv, f16](int64_t b, int64_t e) {
+        for (int64_t i = b; i < e; ++i)
+          dst[i] = acc[i] + (f16 ? grd<true>(p[i], inv) : grd<false>(p[i], inv));
+      });
+    } else {
+      hu.retained.resize((size_t)hu.elems);
+      uint16_t* dst = hu.retained.data();
+      ctx->pool->parallel_for(hu.elems, 1 << 18, [&](int64_t b, int64_t e) {
+        std::memcpy(dst + b, p + b, (size_t)(e - b) * 2);
       });
     }
-    if (!adam_on) {
-      ctx->pool->parallel_for(hu.elems, 1 << 16,
-                              [p, w](int64_t b, int64_t e) { refresh_bf16_span(p, w, b, e); });
-      return;
-    }
-    const AdamK k = adam_consts(a, step_t);
-    if (ctx->cstate) {
-      adam_compressed(ctx, hu, unit, k, step_t, true);
-      return;
-    }
-    float* m = hu.m.get();
-    float* v = hu.v.get();
-    ctx->pool->parallel_for(hu.elems, 1 << 16, [p, acc, w, m, v, k](int64_t b, int64_t e) {
-      adam_acc_span(p, acc, w, m, v, b, e, k);
-    });
-    return;
   }
-  if (retain) {
-    hu.retained.resize((size_t)hu.elems);
-    uint16_t* dst = hu.retained.data();
-    const uint16_t* src = hu.pack;
-    ctx->pool->parallel_for(hu.elems, 1 << 18, [&](int64_t b, int64_t e) {
-      std::memcpy(dst + b, src + b, (size_t)(e - b) * 2);
-    });
-  }
-  if (!adam_on) {
+  if (skip) ctx->skipped.fetch_add(1, std::memory_order_relaxed);
+  if (!adam_on || skip) {
     ctx->pool->parallel_for(hu.elems, 1 << 16,
                             [p, w](int64_t b, int64_t e) { refresh_bf16_span(p, w, b, e); });
     return;
   }
   const AdamK k = adam_consts(a, step_t);
+  const bool with_acc = phase == kLast;
   if (ctx->cstate) {
-    adam_compressed(ctx, hu, unit, k, step_t, false);
+    adam_compressed(ctx, hu, unit, k, step_t, with_acc, inv);
     return;
   }
   float* m = hu.m.get();
   float* v = hu.v.get();
-  ctx->pool->parallel_for(hu.elems, 1 << 16, [p, w, m, v, k](int64_t b, int64_t e) {
-    adam_bf16_span(p, w, m, v, b, e, k);
+  ctx->pool->parallel_for(hu.elems, 1 << 16, [=](int64_t b, int64_t e) {
+    if (with_acc) {
+      if (f16) adam_acc_span<true>(p, acc, w, m, v, b, e, k, inv);
+      else adam_acc_span<false>(p, acc, w, m, v, b, e, k, inv);
+    } else {
+      if (f16) adam_bf16_span<true>(p, w, m, v, b, e, k, inv);
+      else adam_bf16_span<false>(p, w, m, v, b, e, k, inv);
+    }
   });
 }
 
@@ -633,7 +695,8 @@ void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg = 0);
 // every row, and each row's update refreshes that row of the head's pack.
 // Micro-batches before the last only add into dE (and put the unchanged
 // embedding back into the head's pack for the next micro-batch).
-void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int phase) {
+void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int phase,
+                float inv) {
   const int64_t d = ctx->d, V = ctx->V, T = (int64_t)ctx->tok_copy.size();
   if (ctx->e_pending) e_update_rows(ctx, 0, V);  // finish a previous update first
   ctx->e_pending = false;
@@ -641,8 +704,12 @@ void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int
   const bool first = phase == kOnly || phase == kFirst;
   if (ctx->tied) {
     const uint16_t* gh = ctx->lm.pack;
-    ctx->pool->parallel_for(V * d, 1 << 16, [dE, gh, first](int64_t b, int64_t e) {
-      for (int64_t i = b; i < e; ++i) dE[i] = (first ? 0.f : dE[i]) + bf2f(gh[i]);
+    const bool f16 = inv != 0.f;
+    const bool bad = f16 && f16_overflow(ctx, gh, V * d);
+    ctx->e_bad = (first ? false : ctx->e_bad) || bad;
+    ctx->pool->parallel_for(V * d, 1 << 16, [dE, gh, first, f16, inv](int64_t b, int64_t e) {
+      for (int64_t i = b; i < e; ++i)
+        dE[i] = (first ? 0.f : dE[i]) + (f16 ? grd<true>(gh[i], inv) : grd<false>(gh[i], inv));
     });
   } else if (first) {
     const int32_t* rows = ctx->e_rows.data();
@@ -666,7 +733,9 @@ void embed_grad(sf_ctx* ctx, bool adam_on, const sf_adam& a, int64_t step_t, int
     ctx->e_rows.erase(std::unique(ctx->e_rows.begin(), ctx->e_rows.end()), ctx->e_rows.end());
   }
   const bool last = phase == kOnly || phase == kLast;
-  if (!last || !adam_on) {
+  const bool skip = last && ctx->tied && ctx->e_bad;  // the tied head's fp16 gradient overflowed
+  if (skip) ctx->skipped.fetch_add(1, std::memory_order_relaxed);
+  if (!last || !adam_on || skip) {
     if (ctx->tied) {  // the head's pack holds gradients: put the weights back
       uint16_t* p = ctx->lm.pack;
       const float* E = ctx->E.get();
@@ -701,10 +770,10 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   if (ctx->inject_fail_unit.load() == t.unit && t.unit != SF_UNIT_EMBED && t.unit != kUnitEmbedRest) {
     // the gradients are dropped: put the unchanged weights back into the pack
     if (t.unit >= 0) {
-      host_update(ctx, ctx->layers[t.unit], t.unit, false, false, t.adam, t.t, kOnly);
+      host_update(ctx, ctx->layers[t.unit], t.unit, false, false, t.adam, t.t, kOnly, 0.f);
     } else {
-      if (!ctx->tied) host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, false, false, t.adam, t.t, kOnly);
-      host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, false, false, t.adam, t.t, kOnly);
+      if (!ctx->tied) host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, false, false, t.adam, t.t, kOnly, 0.f);
+      host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, false, false, t.adam, t.t, kOnly, 0.f);
     }
     finish_task(ctx, t, SF_ESTATE, "injected Adam worker failure on unit " + std::to_string(t.unit));
     return;
@@ -713,15 +782,16 @@ void run_task(sf_ctx* ctx, const sf_ctx::Task& t) {
   trace(ctx, 5, t.unit);
   const bool retain = ctx->cfg.retain_grads != 0;
   if (t.unit >= 0) {
-    host_update(ctx, ctx->layers[t.unit], t.unit, retain, t.adam_on, t.adam, t.t, t.phase);
+    host_update(ctx, ctx->layers[t.unit], t.unit, retain, t.adam_on, t.adam, t.t, t.phase, t.ginv);
   } else if (t.unit == SF_UNIT_EMBED) {
-    embed_grad(ctx, t.adam_on, t.adam, t.t, t.phase);
+    embed_grad(ctx, t.adam_on, t.adam, t.t, t.phase, t.ginv);
   } else if (t.unit == kUnitEmbedRest) {
     const int64_t V = ctx->V;
     e_update_rows(ctx, V * t.arg / kEmbedRestTasks, V * (t.arg + 1) / kEmbedRestTasks);
   } else {  // LM head (unless tied: the embedding task takes its gradient) and final norm
-    if (!ctx->tied) host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, retain, t.adam_on, t.adam, t.t, t.phase);
-    host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, retain, t.adam_on, t.adam, t.t, t.phase);
+    if (!ctx->tied)
+      host_update(ctx, ctx->lm, SF_UNIT_LM_HEAD, retain, t.adam_on, t.adam, t.t, t.phase, t.ginv);
+    host_update(ctx, ctx->fn, SF_UNIT_FINAL_NORM, retain, t.adam_on, t.adam, t.t, t.phase, t.ginv);
   }
   const double ms = std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
   ctx->adam_ms += ms;
@@ -787,7 +857,7 @@ void post_task(sf_ctx* ctx, int unit, cudaEvent_t ev, int arg) {
                      : unit == kUnitEmbedRest ? ctx->L + 1
                      : (unit >= 0 ? unit : ctx->L);
     ctx->aq.push_back({unit, ev, prio, Clock::now() + std::chrono::milliseconds(ctx->wait_ms),
-                       ctx->adam_on, ctx->adam_copy, ctx->adam_t, arg, ctx->phase});
+                       ctx->adam_on, ctx->adam_copy, ctx->adam_t, arg, ctx->phase, ctx->cur_inv});
     ++ctx->unit_pending[unit_slot(ctx, unit)];
     ++ctx->aq_pending;
   }
@@ -925,6 +995,14 @@ LayerG slot_g(sf_ctx* c, int s) {
           b + c->off_g2, b + c->off_gu, b + c->off_d};
 }
 
+// A gain gradient from the per-block partials: bf16, or fp16 times the loss scale.
+void grad_parts(sf_ctx* c, int d, bf16* out) {
+  if (c->f16g)
+    sf::reduce_parts_f16(c->dg_part, c->dg_parts, d, reinterpret_cast<uint16_t*>(out), c->lscale, c->sC);
+  else
+    sf::reduce_parts_bf16(c->dg_part, c->dg_parts, d, out, c->sC);
+}
+
 // Forward of one layer from X_l (fp32) to X_{l+1}; with `full == false` the
 // final down projection is skipped (recompute for the backward needs only the
 // intermediates).
@@ -966,17 +1044,19 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
   // down projection: X_{l+1} = h + m Wd^T
   RET(gemm(c, sf::kNN, sf::kEpiBF16, T, F, d, c->dXb, d, w.wd, F, c->dm, F));
-  RET(gemm(c, sf::kTN, sf::kEpiBF16, d, F, T, c->dXb, d, c->mb, F, g.wd, F));
+  RET(gemm(c, sf::kTN, c->gepi(), d, F, T, c->dXb, d, c->mb, F, g.wd, F, nullptr, 0, c->gscale()));
   sf::swiglu_bwd(c->dm, c->ab, c->dab, T, (int)F, c->sC);
   // gate/up projection from w2 = RMSNorm(h; g2)
   RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, 2 * F, c->dab, 2 * F, w.wgu, d, c->dw2, d));
-  RET(gemm(c, sf::kTN, sf::kEpiBF16, 2 * F, d, T, c->dab, 2 * F, c->w2, d, g.wgu, d));
+  RET(gemm(c, sf::kTN, c->gepi(), 2 * F, d, T, c->dab, 2 * F, c->w2, d, g.wgu, d, nullptr, 0,
+           c->gscale()));
   sf::rmsnorm_bwd(c->h, w.g2, c->rstd2, c->dw2, c->dX, c->dh, c->dhb, c->dg_part, c->dg_parts,
                   T, (int)d, c->sC);
-  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, g.g2, c->sC);
+  grad_parts(c, (int)d, g.g2);
   // output projection: h = X_l + o Wo^T
   RET(gemm(c, sf::kNN, sf::kEpiBF16, T, c->qdim, d, c->dhb, d, w.wo, c->qdim, c->dob, c->qdim));
-  RET(gemm(c, sf::kTN, sf::kEpiBF16, d, c->qdim, T, c->dhb, d, c->o, c->qdim, g.wo, c->qdim));
+  RET(gemm(c, sf::kTN, c->gepi(), d, c->qdim, T, c->dhb, d, c->o, c->qdim, g.wo, c->qdim, nullptr,
+           0, c->gscale()));
   {
     Timed t(c, 1, 2.5 * attn_fwd_flops(B, S, Hq, hd));
     if (sf::attn_bwd(c->qkv, c->o, c->dob, c->lse, c->delta, c->dq_acc, c->dqkv, B, S, Hq, Hkv,
@@ -987,15 +1067,20 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   }
   // the biases' gradient: column sums of the pre-rotation dQ, dK, dV
   if (g.bqkv) {
-    sf::bias_grad(c->dqkv, c->qkvdim, T, (int)c->qkvdim, c->dg_part, c->dg_parts, g.bqkv, c->sC);
+    if (c->f16g)
+      sf::bias_grad_f16(c->dqkv, c->qkvdim, T, (int)c->qkvdim, c->dg_part, c->dg_parts,
+                        reinterpret_cast<uint16_t*>(g.bqkv), c->lscale, c->sC);
+    else
+      sf::bias_grad(c->dqkv, c->qkvdim, T, (int)c->qkvdim, c->dg_part, c->dg_parts, g.bqkv, c->sC);
     c->launches += 2;
   }
   // QKV projection from u = RMSNorm(X_l; g1)
   RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, c->qkvdim, c->dqkv, c->qkvdim, w.wqkv, d, c->du, d));
-  RET(gemm(c, sf::kTN, sf::kEpiBF16, c->qkvdim, d, T, c->dqkv, c->qkvdim, c->u, d, g.wqkv, d));
+  RET(gemm(c, sf::kTN, c->gepi(), c->qkvdim, d, T, c->dqkv, c->qkvdim, c->u, d, g.wqkv, d, nullptr,
+           0, c->gscale()));
   sf::rmsnorm_bwd(Xin, w.g1, c->rstd1, c->du, c->dh, c->dX, c->dXb, c->dg_part, c->dg_parts, T,
                   (int)d, c->sC);
-  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, g.g1, c->sC);
+  grad_parts(c, (int)d, g.g1);
   c->launches += 8;  // swiglu, 2 norm, 2 reduce, 3 attention (GEMMs are counted in gemm())
   return SF_OK;
 }
@@ -1019,8 +1104,11 @@ int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
   sf::sum_f32(c->loss_rows, T, inv_n, c->loss_dev, c->sC);
   sf::rmsnorm_bwd(XL, c->gf, c->rstdf, c->dhf, nullptr, c->dX, c->dXb, c->dg_part, c->dg_parts,
                   T, (int)d, c->sC);
-  sf::reduce_parts_bf16(c->dg_part, c->dg_parts, (int)d, c->dgf, c->sC);
-  sf::cast_f32_bf16(c->dWlm32, c->dWlm16, V * d, c->sC);
+  grad_parts(c, (int)d, c->dgf);
+  if (c->f16g)
+    sf::cast_f32_f16(c->dWlm32, reinterpret_cast<uint16_t*>(c->dWlm16), V * d, c->lscale, c->sC);
+  else
+    sf::cast_f32_bf16(c->dWlm32, c->dWlm16, V * d, c->sC);
   c->launches += 5;
   return SF_OK;
 }
@@ -1053,8 +1141,10 @@ const char* validate(const sf_config* c) {
   if (c->lce_chunk_rows < 0) return "lce_chunk_rows must be >= 0";
   if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.f)) return "rms_eps must be > 0 and rope_base > 1";
   if (c->qkv_bias < 0 || c->qkv_bias > 1 || c->tie_embeddings < 0 || c->tie_embeddings > 1 ||
-      c->deterministic < 0 || c->deterministic > 1 || c->bf16_adam_state < 0 || c->bf16_adam_state > 1)
-    return "qkv_bias, tie_embeddings, deterministic and bf16_adam_state must be 0 or 1";
+      c->deterministic < 0 || c->deterministic > 1 || c->bf16_adam_state < 0 ||
+      c->bf16_adam_state > 1 || c->fp16_grads < 0 || c->fp16_grads > 1)
+    return "qkv_bias, tie_embeddings, deterministic, bf16_adam_state and fp16_grads must be 0 or 1";
+  if (!(c->loss_scale >= 0.f) || c->loss_scale > 16777216.f) return "loss_scale must be in [0, 2^24]";
   return nullptr;
 }
 
@@ -1077,6 +1167,8 @@ int init(sf_ctx* ctx) {
   ctx->bias = cf.qkv_bias != 0;
   ctx->tied = cf.tie_embeddings != 0;
   ctx->cstate = cf.bf16_adam_state != 0;
+  ctx->f16g = cf.fp16_grads != 0;
+  ctx->lscale = cf.loss_scale > 0.f ? cf.loss_scale : 65536.f;
   ctx->off_g1 = 0;
   ctx->off_qkv = round_up(d, A);
   ctx->off_bqkv = round_up(ctx->off_qkv + ctx->qkvdim * d, A);  // only when biased
@@ -1309,6 +1401,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   else RET(wait_tasks(ctx));
   ctx->tok_copy.assign(tokens, tokens + T);
   ctx->phase = phase;
+  ctx->cur_inv = ctx->f16g ? 1.f / ctx->lscale : 0.f;
   const bool updates = phase == kOnly || phase == kLast;  // this micro-batch's tasks update
   ctx->adam_on = adam != nullptr && updates;
   if (ctx->adam_on) {
@@ -1517,6 +1610,8 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   ctx->stats.host_adam_ms = ctx->adam_ms;
   ctx->stats.host_wait_ms = std::chrono::duration<double, std::milli>(Clock::now() - t_gpu_done).count();
   ctx->stats.kernel_launches = ctx->launches;
+  ctx->stats.loss_scale = ctx->f16g ? ctx->lscale : 0.0;
+  ctx->stats.skipped_updates = ctx->skipped.load();
   (void)t_host0;
   trace(ctx, 8, -9);
   return SF_OK;
@@ -1726,6 +1821,17 @@ int train(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int32_t n_m
     fail = fail || need(ctx->lm) || need(ctx->fn);
     if (fail) return SF_ENOMEM;
   }
+  if (ctx->f16g) {  // dynamic loss scale, from the updates skipped so far
+    const int64_t sk = ctx->skipped.load();
+    if (sk != ctx->skipped_seen) {
+      ctx->skipped_seen = sk;
+      ctx->lscale = std::max(1.f, ctx->lscale * 0.5f);
+      ctx->lgood = 0;
+    } else if (ctx->have_loss && ++ctx->lgood >= kScaleWindow) {
+      ctx->lscale = std::min(ctx->lscale * 2.f, 16777216.f);
+      ctx->lgood = 0;
+    }
+  }
   int st = SF_OK;
   double loss = 0.0;
   try {
@@ -1794,11 +1900,13 @@ int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
     return SF_OK;
   }
   const uint16_t* g = hu.retained.data();
+  const float inv = hu.retained_inv;  // fp16 gradients carry the step's loss scale
+  auto cvt = [inv](uint16_t x) { return inv != 0.f ? grd<true>(x, inv) : grd<false>(x, inv); };
   if (unit >= 0) {
     for (const Seg& s : ctx->segs)
-      for (int64_t i = 0; i < s.n; ++i) out[s.src + i] = bf2f(g[s.dst + i]);
+      for (int64_t i = 0; i < s.n; ++i) out[s.src + i] = cvt(g[s.dst + i]);
   } else {
-    for (size_t i = 0; i < numel; ++i) out[i] = bf2f(g[i]);
+    for (size_t i = 0; i < numel; ++i) out[i] = cvt(g[i]);
   }
   return SF_OK;
 }

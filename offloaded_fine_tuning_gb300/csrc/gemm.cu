@@ -15,6 +15,7 @@
 // x [64 MN] boxes placed 8 KB apart.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -115,6 +116,25 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (col + j < p.N) c[j] = __float2bfloat16_rn(__uint_as_float(r[j]) * a + bv[j]);
+    }
+  } else if constexpr (EPI == kEpiF16) {
+    __half* c = reinterpret_cast<__half*>(p.C) + (int64_t)row * p.ldc + col;
+    if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          __half2 h = __floats2half2_rn(__uint_as_float(r[8 * q + 2 * k]) * a,
+                                        __uint_as_float(r[8 * q + 2 * k + 1]) * a);
+          w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        reinterpret_cast<uint4*>(c)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col + j < p.N) c[j] = __float2half_rn(__uint_as_float(r[j]) * a);
     }
   } else {
     float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
@@ -397,6 +417,9 @@ static int launch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, con
     case kEpiBF16Bias:  // forward projections only (Y = X W^T + b)
       if constexpr (!A_MN && !B_MN) return launch_t<A_MN, B_MN, BN, kEpiBF16Bias>(ta, tb, p, st, why);
       break;
+    case kEpiF16:  // weight gradients only (dW = dY^T X)
+      if constexpr (A_MN && B_MN) return launch_t<A_MN, B_MN, BN, kEpiF16>(ta, tb, p, st, why);
+      break;
   }
   snprintf(why, 64, "gemm: bad epilogue %d", epi);
   return -1;
@@ -408,8 +431,8 @@ int gemm_check(const GemmArgs& a, char* why) {
     snprintf(why, 64, "gemm: bad sizes");
     return -1;
   }
-  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiBF16Bias ||
-      (a.epi == kEpiBF16Bias && a.layout != kNT)) {
+  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiF16 ||
+      (a.epi == kEpiBF16Bias && a.layout != kNT) || (a.epi == kEpiF16 && a.layout != kTN)) {
     snprintf(why, 64, "gemm: bad layout %d or epilogue %d", a.layout, a.epi);
     return -1;
   }

@@ -14,7 +14,10 @@ namespace sf {
 enum GemmLayout : int { kNT = 0, kNN = 1, kTN = 2 };
 // Epilogues: C bf16 = alpha*acc | C f32 = alpha*acc | C f32 = R + alpha*acc | C f32 += alpha*acc
 // | C bf16 = alpha*acc + bias[col] (bias bf16 [N], 64-byte aligned; layout kNT only)
-enum GemmEpi : int { kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3, kEpiBF16Bias = 4 };
+// | C fp16 = alpha*acc (layout kTN only: scaled fp16 weight gradients)
+enum GemmEpi : int {
+  kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3, kEpiBF16Bias = 4, kEpiF16 = 5
+};
 
 struct GemmArgs {
   int layout = kNT, epi = kEpiBF16;
@@ -45,10 +48,16 @@ void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, cons
                  int64_t rows, int d, cudaStream_t st);
 int rmsnorm_bwd_parts(int64_t rows);
 void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st);
+// The same sum as fp16 after multiplying by scale (a scaled fp16 gradient).
+void reduce_parts_f16(const float* part, int parts, int d, uint16_t* out, float scale,
+                      cudaStream_t st);
 // out[c] = bf16(sum over rows of x[r, c]) for x bf16 [rows, cols] (cols even, row
 // stride ld, 4-byte aligned rows); part: fp32 scratch [parts, cols]
 void bias_grad(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float* part, int parts,
                __nv_bfloat16* out, cudaStream_t st);
+// the column sums as fp16 times scale
+void bias_grad_f16(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, float* part,
+                   int parts, uint16_t* out, float scale, cudaStream_t st);
 void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
                   int head_dim, const float2* cs, int inverse, cudaStream_t st);
 void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn,
@@ -59,6 +68,8 @@ void ce_rows(__nv_bfloat16* z, const int32_t* labels, int64_t rows, int64_t voca
              float inv_n, float* loss_rows, cudaStream_t st);
 void sum_f32(const float* x, int64_t n, float scale, float* out, cudaStream_t st);
 void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st);
+// y = fp16(scale * x)
+void cast_f32_f16(const float* x, uint16_t* y, int64_t n, float scale, cudaStream_t st);
 void cast_bf16_f32(const __nv_bfloat16* x, float* y, int64_t n, cudaStream_t st);
 
 // ---- attention (attention.cu).  qkv [T, (Hq+2Hkv)*hd] bf16, token t = b*S + s.

@@ -241,6 +241,72 @@ def test_bf16_adam_state_tracks_fp32_state_training():
         assert rel_l2(d1, d0) < 0.05, u
 
 
+# ------------------------------------------------------------------ fp16 gradients
+@pytest.mark.parametrize("name", ["small-gqa", "small-qwen"])
+def test_fp16_gradients_match_oracle(name):
+    """Weight gradients sent as loss-scaled fp16 and unscaled on the host."""
+    cfg = TEST_CONFIGS[name]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
+    with make_model(cfg, mast, fp16_grads=1) as m:
+        assert m.train_step(tok, lab) == sf.SF_OK, m.error()
+        compare(cfg, m, loss_ref, g_ref)
+        assert m.stats()["loss_scale"] == 65536.0 and m.stats()["skipped_updates"] == 0
+
+
+def test_fp16_gradient_overflow_skips_the_unit_and_halves_the_scale():
+    """A scale of 2^24 overflows fp16: every unit whose gradient holds an
+    infinity keeps its weights exactly, the others are updated, and the next
+    step runs at half the scale."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=2)
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    adam = sf.Adam(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    with make_model(cfg, mast, fp16_grads=1, loss_scale=2.0 ** 24) as m:
+        assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+        st = m.stats()
+        assert st["loss_scale"] == 2.0 ** 24 and st["skipped_updates"] > 0
+        skipped = 0
+        for u in (0, 1, UNIT_LM_HEAD, UNIT_FINAL_NORM):
+            if np.isfinite(m.grads(u)).all():
+                assert not np.array_equal(m.weights(u), mast[u]), u
+            else:
+                skipped += 1
+                assert np.array_equal(m.weights(u), mast[u]), u
+        assert skipped == st["skipped_updates"]
+        assert not np.array_equal(m.weights(UNIT_EMBED), mast[UNIT_EMBED])  # bf16 input gradient
+        assert m.train_step(tok, lab, adam) == sf.SF_OK
+        assert m.stats()["loss_scale"] == 2.0 ** 23
+
+
+def test_fp16_gradient_adam_tracks_oracle():
+    cfg = CONFIGS["tiny"]
+    mast = masters(cfg)
+    tok, lab = inputs.tokens_and_labels(cfg)
+    lr = 1e-4
+    adam = sf.Adam(lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    theta = {u: a.astype(np.float32).copy() for u, a in mast.items()}
+    mom = {u: (np.zeros_like(a), np.zeros_like(a)) for u, a in theta.items()}
+    with make_model(cfg, mast, fp16_grads=1, async_update=1) as m:
+        for t in range(1, 4):
+            loss_ref, g = oracle.step(oracle_weights(cfg, theta), tok, lab, cfg)
+            assert m.train_step(tok, lab, adam) == sf.SF_OK, m.error()
+            assert abs(m.loss() - loss_ref) / loss_ref < LOSS_RTOL
+            for u in theta:
+                gu = (np.concatenate([g["layers"][u][n].reshape(-1) for n, _ in layer_tensor_shapes(cfg)])
+                      if u >= 0 else {UNIT_EMBED: g["embed"], UNIT_FINAL_NORM: g["final_norm"],
+                                      UNIT_LM_HEAD: g["lm_head"]}[u].reshape(-1))
+                th, mm, vv = oracle.adam_update(theta[u], gu.astype(np.float32), *mom[u], t, lr)
+                theta[u], mom[u] = th.astype(np.float32), (mm.astype(np.float32), vv.astype(np.float32))
+        m.sync()
+        assert m.stats()["skipped_updates"] == 0
+        for u in ALL_UNITS:
+            w = m.weights(u)
+            assert rel_l2(w - mast[u], theta[u] - mast[u]) < 0.1
+            assert rel_l2(w, theta[u]) < 1e-3
+
+
 def test_ring_size_invariance_is_bitwise():
     cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=4)
     mast = masters(cfg)

@@ -76,10 +76,10 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
   const bool full = (col + 32 <= p.N);
   if constexpr (EPI == kEpiBF16 || EPI == kEpiBF16Bias) {
     __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
-    float bv[32];
+    float y[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) bv[j] = 0.f;
-    if constexpr (EPI == kEpiBF16Bias) {
+    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]) * a;
+    if constexpr (EPI == kEpiBF16Bias) {  // + bias[col], in fp32 before the rounding
       if (full) {
         const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col);  // 64-byte aligned: col % 32 == 0
 #pragma unroll
@@ -88,34 +88,30 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            bv[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
-            bv[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+            y[8 * q + 2 * k] += __uint_as_float(w[k] << 16);
+            y[8 * q + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
           }
         }
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (col + j < p.N) bv[j] = __bfloat162float(p.bias[col + j]);
+          if (col + j < p.N) y[j] += __bfloat162float(p.bias[col + j]);
       }
     }
     if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * a + bv[8 * q + 0],
-                          __uint_as_float(r[8 * q + 1]) * a + bv[8 * q + 1]);
-        v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * a + bv[8 * q + 2],
-                          __uint_as_float(r[8 * q + 3]) * a + bv[8 * q + 3]);
-        v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * a + bv[8 * q + 4],
-                          __uint_as_float(r[8 * q + 5]) * a + bv[8 * q + 5]);
-        v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * a + bv[8 * q + 6],
-                          __uint_as_float(r[8 * q + 7]) * a + bv[8 * q + 7]);
+        v.x = pack_bf16x2(y[8 * q + 0], y[8 * q + 1]);
+        v.y = pack_bf16x2(y[8 * q + 2], y[8 * q + 3]);
+        v.z = pack_bf16x2(y[8 * q + 4], y[8 * q + 5]);
+        v.w = pack_bf16x2(y[8 * q + 6], y[8 * q + 7]);
         reinterpret_cast<uint4*>(c)[q] = v;
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (col + j < p.N) c[j] = __float2bfloat16_rn(__uint_as_float(r[j]) * a + bv[j]);
+        if (col + j < p.N) c[j] = __float2bfloat16_rn(y[j]);
     }
   } else if constexpr (EPI == kEpiF16) {
     __half* c = reinterpret_cast<__half*>(p.C) + (int64_t)row * p.ldc + col;

@@ -41,12 +41,13 @@ constexpr int kAttThreads = 192;
 template <int HD>
 struct AttCfg {
   static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
+  static constexpr int KST = 3;                 // K stages (V has 2, P one buffer)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = TILE;
-  static constexpr int OFF_V = OFF_K + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + KST * TILE;
   static constexpr int OFF_P = OFF_V + 2 * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * 32768;  // P: 2 buffers of 128 rows x 128 keys
-  static constexpr int NBAR = 14;
+  static constexpr int OFF_BAR = OFF_P + 32768;  // P: 128 rows x 128 keys
+  static constexpr int NBAR = 20;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 
@@ -95,14 +96,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sP = s0 + C::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
+  // K and V stages have their own barriers: a K stage is free as soon as its
+  // S = Q K^T has completed, so K loads run ahead of the P V products.
   const uint32_t q_full = b0;
-  auto kv_full = [&](int s) { return b0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return b0 + 8u * (3 + s); };
-  auto s_full = [&](int s) { return b0 + 8u * (5 + s); };
-  auto s_free = [&](int s) { return b0 + 8u * (7 + s); };
-  auto p_full = [&](int s) { return b0 + 8u * (9 + s); };
-  auto o_done = [&](int s) { return b0 + 8u * (11 + s); };
-  const uint32_t drain = b0 + 8u * 13;
+  auto s_full = [&](int s) { return b0 + 8u * (1 + s); };
+  auto s_free = [&](int s) { return b0 + 8u * (3 + s); };
+  auto p_full = [&](int s) { return b0 + 8u * (5 + s); };
+  auto o_done = [&](int s) { return b0 + 8u * (7 + s); };
+  const uint32_t drain = b0 + 8u * 9;
+  auto v_full = [&](int s) { return b0 + 8u * (10 + s); };
+  auto v_empty = [&](int s) { return b0 + 8u * (12 + s); };
+  auto k_full = [&](int s) { return b0 + 8u * (14 + s); };   // C::KST stages
+  auto k_empty = [&](int s) { return b0 + 8u * (17 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -118,9 +123,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
       mbar_init(s_free(s), 128);
     }
@@ -147,36 +156,50 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_arrive_expect_tx(q_full, C::TILE);
 #pragma unroll
     for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, colQ + 64 * c, q0, b);
-    bool ok = true;
-    int issued = 0;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(kv_empty(st), ph ^ 1u, abort_flag)) { ok = false; break; }
-      mbar_arrive_expect_tx(kv_full(st), 2 * C::TILE);
+    // K runs two blocks ahead of V: K(j + 2) needs S(j - 1) done, V(j) needs P V(j - 2) done
+    auto load_k = [&](int kb) -> bool {
+      const int st = kb % C::KST;
+      if (!mbar_wait(k_empty(st), ((kb / C::KST) & 1) ^ 1u, abort_flag)) return false;
+      mbar_arrive_expect_tx(k_full(st), C::TILE);
 #pragma unroll
-      for (int c = 0; c < NB; ++c) {
-        tma_load_3d(sK + st * C::TILE + c * 16384, &tm, kv_full(st), colK + 64 * c, j * 128, b);
-        tma_load_3d(sV + st * C::TILE + c * 16384, &tm, kv_full(st), colV + 64 * c, j * 128, b);
+      for (int c = 0; c < NB; ++c)
+        tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, kb * 128, b);
+      return true;
+    };
+    bool ok = load_k(0) && (nkv < 2 || load_k(1));
+    int k_issued = ok ? (nkv < 2 ? 1 : 2) : 0, v_issued = 0;
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 2 < nkv) {
+        if (!load_k(j + 2)) { ok = false; break; }
+        k_issued = j + 3;
       }
-      issued = j + 1;
+      const int st = j & 1;
+      if (!mbar_wait(v_empty(st), ((j >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(v_full(st), C::TILE);
+#pragma unroll
+      for (int c = 0; c < NB; ++c)
+        tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, b);
+      v_issued = j + 1;
     }
     if (!ok) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       // let the copies already issued land before the CTA's shared memory goes away
       mbar_wait(q_full, 0, nullptr);
-      for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
-        mbar_wait(kv_full(j & 1), (j >> 1) & 1, nullptr);
+      for (int kb = k_issued - 1; kb >= 0 && kb >= k_issued - C::KST; --kb)
+        mbar_wait(k_full(kb % C::KST), (kb / C::KST) & 1, nullptr);
+      for (int kb = v_issued - 1; kb >= 0 && kb >= v_issued - 2; --kb)
+        mbar_wait(v_full(kb & 1), (kb >> 1) & 1, nullptr);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     bool ok = mbar_wait(q_full, 0, abort_flag);
     for (int j = 0; ok && j <= nkv; ++j) {
       if (j < nkv) {  // S_j = Q K_j^T into S buffer j % 2
-        const int st = j & 1;
+        const int st = j & 1, ks = j % C::KST;
         const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(kv_full(st), ph, abort_flag) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag)) {
+        if (!mbar_wait(k_full(ks), (j / C::KST) & 1, abort_flag) ||
+            !mbar_wait(s_free(st), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -185,23 +208,28 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           umma_bf16(tmem_base + st * 128, smem_desc_sw128(sQ + off, 16, 1024),
-                    smem_desc_sw128(sK + st * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+                    smem_desc_sw128(sK + ks * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
         }
         umma_commit(s_full(st));
+        umma_commit(k_empty(ks));  // K stage free once S has been computed
       }
       if (j > 0) {  // O += P_{j-1} V_{j-1}
         const int jp = j - 1, st = jp & 1;
-        if (!mbar_wait(p_full(st), (jp >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(p_full(st), (jp >> 1) & 1, abort_flag) ||
+            !mbar_wait(v_full(st), (jp >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           umma_bf16(tmem_base + O_COL,
-                    smem_desc_sw128(sP + st * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                     smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
                     (jp > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(o_done(st));
-        umma_commit(kv_empty(st));
+        umma_commit(v_empty(st));
       }
     }
     if (!ok) {
@@ -228,28 +256,32 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       if (!ok) break;
       tc_fence_after();
       float s[128];
+      {  // the row's 128 scores: four loads in flight, one wait
+        uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r);
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[c][i]);
       }
       tc_fence_before();
       mbar_arrive(s_free(st));
-      float mx = -INFINITY;
       if (j == qb) {  // diagonal block: keys after the query are masked
         const int lim = q - j * 128;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
-          mx = fmaxf(mx, s[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
       }
+      // row max with eight independent accumulators (short dependency chains)
+      float mx8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx8[a] = s[a];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       mx *= scale_log2;  // the scale is positive: the max commutes with it
       const bool grow = mx > m + 8.f;
       const float m_new = grow ? mx : m;
@@ -270,21 +302,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         tmem_st_wait();
       }
-      float ps = 0.f;
+      float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
         const float p = ex2_approx(fmaf(s[i], scale_log2, -m_new));
         s[i] = p;
-        ps += p;
+        ps8[i & 7] += p;
       }
+      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       l = l * corr + ps;
       m = m_new;
-      if (j >= 2) {  // P buffer st was read by P_{j-2} V_{j-2}
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done(st), ((j - 2) >> 1) & 1, abort_flag));
+      if (j >= 1) {  // the P buffer was read by P_{j-1} V_{j-1}
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
       }
       // row of P, bf16, in the 128-byte swizzled K-major layout
-      const uint32_t prow = sP + st * 32768 + (uint32_t)row * 128u;
+      const uint32_t prow = sP + (uint32_t)row * 128u;
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll

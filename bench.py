@@ -335,6 +335,18 @@ def run_ours(args, c):
     m.sync()
     e2e_s = time.perf_counter() - t0
 
+    # the GPU path alone: two steps without the optimizer (no host Adam), synchronous
+    gpu_path_ms = None
+    if not args.no_gpu_path:
+        m.sync()
+        torch.cuda.synchronize()
+        g0 = time.perf_counter()
+        for i in range(2):
+            tok, lab = batches[args.warmup + i]
+            st = m.train_step(tok, lab) if n_micro == 1 else m.train_step_accum(tok, lab)
+            assert st == sf.SF_OK, m.error()
+        gpu_path_ms = (time.perf_counter() - g0) * 1e3 / 2
+
     dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_s * 1e3], dist, device="cuda")
     ms_step = dev_ms / args.steps
     value = job_throughput(T, args.steps, world, dev_ms)
@@ -399,6 +411,9 @@ def run_ours(args, c):
                           "attn_tflops": attn_fl / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None,
                           "host_adam_ms": statistics.mean(s["host_adam_ms"] for s in stats),
                           "host_tail_ms": statistics.mean(s["host_wait_ms"] for s in stats)},
+        "gpu_path": None if gpu_path_ms is None else {
+            "ms_per_step": gpu_path_ms, "tokens_per_s": T / (gpu_path_ms / 1e3),
+            "what": "same step without the optimizer update (no host Adam), host wall clock"},
         "clocks": clk,
         "loss": losses[-1],
         "cpu_baseline": cpu,
@@ -532,6 +547,8 @@ def main():
     ap.add_argument("--ring", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gpu-path", action="store_true",
+                    help="skip the two extra steps timed without the optimizer")
     ap.add_argument("--offload-activations", action="store_true",
                     help="sliding activations: layer checkpoints go to pinned host memory")
     ap.add_argument("--bf16-adam-state", action="store_true",

@@ -249,6 +249,18 @@ int sf_sync(sf_ctx* ctx);
 /* Loss of the last step.  Errors: SF_ESTATE before the first step. */
 int sf_loss(sf_ctx* ctx, float* out);
 
+/* The fused LM head + cross-entropy as a standalone call on host buffers (for
+ * a head-only workload such as a large-vocabulary stress test): h bf16 [n, d],
+ * w bf16 [v, d], labels int32 [n] where ignore_index marks ignored rows (any
+ * other label must lie in [0, v)).  Writes loss (mean over valid rows), dh
+ * bf16 [n, d] and dw fp32 [v, d], with the same kernels and chunked logits as
+ * the training step.  ctx may be NULL (then the current device is used); the
+ * call stages its inputs in device memory it allocates and frees.  Errors:
+ * SF_EINVAL (sizes, pointers, labels), SF_ENOMEM, SF_ECUDA, SF_EDEVICE. */
+int sf_lce_step(sf_ctx* ctx, const uint16_t* h, const uint16_t* w, const int32_t* labels,
+                int64_t n, int32_t d, int32_t v, int32_t ignore_index, float* loss, uint16_t* dh,
+                float* dw);
+
 /* Per-kernel timing of the steps that follow: 1 records CUDA events around
  * every GEMM and attention launch (small overhead), 0 turns it off. */
 int sf_set_timing(sf_ctx* ctx, int32_t enabled);

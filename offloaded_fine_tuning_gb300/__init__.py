@@ -91,6 +91,7 @@ _SIGS = {
     "sf_get_adam_step": (ctypes.c_int, [_VP, ctypes.POINTER(_I64)]),
     "sf_set_adam_step": (ctypes.c_int, [_VP, _I64]),
     "sf_loss": (ctypes.c_int, [_VP, ctypes.POINTER(_F32)]),
+    "sf_lce_step": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _VP, _VP, _VP]),
     "sf_sync": (ctypes.c_int, [_VP]),
     "sf_set_timing": (ctypes.c_int, [_VP, _I32]),
     "sf_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(Stats)]),
@@ -343,6 +344,25 @@ def op_rope(x, ld, tokens, seq, heads, head_dim, table, inverse=0, stream=0) -> 
 
 def op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, stream=0) -> int:
     return lib().sf_op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, _s(stream))
+
+
+def lce_step(h_bf16: np.ndarray, w_bf16: np.ndarray, labels: np.ndarray,
+             ignore_index: int = IGNORE_INDEX, model=None):
+    """Fused LM head + cross-entropy on host arrays (uint16 bf16 bits):
+    returns (loss, dh as uint16 bf16 bits [n, d], dw fp32 [v, d])."""
+    h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    y = np.ascontiguousarray(labels, dtype=np.int32).reshape(-1)
+    n, d = h.shape
+    v = w.shape[0]
+    loss = _F32()
+    dh = np.empty((n, d), dtype=np.uint16)
+    dw = np.empty((v, d), dtype=np.float32)
+    st = lib().sf_lce_step(model.h if model is not None else None, h.ctypes.data, w.ctypes.data,
+                           y.ctypes.data, n, d, v, ignore_index, ctypes.byref(loss),
+                           dh.ctypes.data, dw.ctypes.data)
+    _check(st, model.h if model is not None else None, "sf_lce_step")
+    return float(loss.value), dh, dw
 
 
 def op_gemm_bias(M, N, K, A, lda, B, ldb, C, ldc, bias, alpha=1.0, stream=0) -> int:

@@ -1930,6 +1930,87 @@ int sf_get_weights(sf_ctx* ctx, int32_t unit, float* out, size_t numel) {
   return SF_OK;
 }
 
+// Host-pointer LM head + cross-entropy for a standalone workload (no model):
+// stages the inputs on the device, runs sf_op_lce, returns loss, dh (bf16)
+// and dw (fp32).
+int sf_lce_step(sf_ctx* ctx, const uint16_t* h, const uint16_t* w, const int32_t* labels,
+                int64_t n, int32_t d, int32_t v, int32_t ignore_index, float* loss, uint16_t* dh,
+                float* dw) {
+  if (!h || !w || !labels || !loss || !dh || !dw || n < 1 || d < 8 || d % 8 || d > 16384 ||
+      v < 8 || v % 8)
+    return SF_EINVAL;
+  std::vector<int32_t> lab((size_t)n);
+  int64_t n_valid = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    const int32_t y = labels[t];
+    if (y == ignore_index) {
+      lab[t] = SF_IGNORE_INDEX;
+    } else if (y < 0 || y >= v) {
+      if (ctx) ctx->set_err("sf_lce_step: label %d at row %lld outside [0, %d)", y, (long long)t, v);
+      return SF_EINVAL;
+    } else {
+      lab[t] = y;
+      ++n_valid;
+    }
+  }
+  if (ctx && cudaSetDevice(ctx->cfg.device) != cudaSuccess) return SF_ECUDA;
+  int64_t chunk = ((int64_t)1 << 30) / (2 * (int64_t)v);
+  chunk = std::min<int64_t>(n, std::max<int64_t>(128, chunk / 128 * 128));
+  const int64_t ws = sf_op_lce_workspace_bytes(n, v, chunk);
+  void *dH = nullptr, *dW = nullptr, *dLab = nullptr, *dLoss = nullptr, *dDh = nullptr,
+       *dDw = nullptr, *dWs = nullptr, *dDh16 = nullptr;
+  cudaStream_t st = nullptr;
+  int rc = SF_OK;
+  auto alloc = [&](void** ptr, size_t bytes) {
+    if (rc == SF_OK && cudaMalloc(ptr, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      rc = SF_ENOMEM;
+    }
+  };
+  alloc(&dH, (size_t)n * d * 2);
+  alloc(&dW, (size_t)v * d * 2);
+  alloc(&dLab, (size_t)n * 4);
+  alloc(&dLoss, 256);
+  alloc(&dDh, (size_t)n * d * 4);
+  alloc(&dDw, (size_t)v * d * 4);
+  alloc(&dWs, (size_t)ws);
+  alloc(&dDh16, (size_t)n * d * 2);
+  if (rc == SF_OK && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) rc = SF_ECUDA;
+  if (rc == SF_OK) {
+    bool ok = cudaMemcpyAsync(dH, h, (size_t)n * d * 2, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(dW, w, (size_t)v * d * 2, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(dLab, lab.data(), (size_t)n * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    if (ok) {
+      rc = sf_op_lce(static_cast<const uint16_t*>(dH), static_cast<const uint16_t*>(dW),
+                     static_cast<const int32_t*>(dLab), n, d, v, n_valid, chunk, dWs,
+                     static_cast<float*>(dLoss), static_cast<float*>(dDh), static_cast<float*>(dDw), st);
+    } else {
+      rc = SF_ECUDA;
+    }
+    if (rc == SF_OK) {
+      sf::cast_f32_bf16(static_cast<const float*>(dDh), static_cast<bf16*>(dDh16), n * d, st);
+      ok = cudaMemcpyAsync(loss, dLoss, 4, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+           cudaMemcpyAsync(dh, dDh16, (size_t)n * d * 2, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+           cudaMemcpyAsync(dw, dDw, (size_t)v * d * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+           cudaStreamSynchronize(st) == cudaSuccess;
+      if (!ok) rc = SF_ECUDA;
+    }
+    if (rc == SF_OK) {
+      int32_t e = 0;
+      if (sf_op_device_error(&e) != SF_OK) rc = SF_ECUDA;
+      else if (e != 0) rc = SF_EDEVICE;
+    }
+  }
+  if (st) {
+    cudaStreamSynchronize(st);
+    cudaStreamDestroy(st);
+  }
+  for (void* q : {dH, dW, dLab, dLoss, dDh, dDw, dWs, dDh16})
+    if (q) cudaFree(q);
+  if (rc != SF_OK && ctx) ctx->set_err("sf_lce_step failed with status %d", rc);
+  return rc;
+}
+
 int sf_sync(sf_ctx* ctx) {
   if (!ctx) return SF_EINVAL;
   return wait_tasks(ctx);

@@ -371,6 +371,27 @@ def lce_run(h, w, lab, chunk):
     return float(host(loss)[0]), host(dh), host(dw)
 
 
+def test_lce_step_on_host_buffers_matches_unfused_cross_entropy():
+    """sf_lce_step (host buffers, its own ignore value) against the oracle."""
+    from inputs.configs import LceConfig
+    c = LceConfig("small", 384, 3000, 2, 250, 0.1)
+    h, w, lab = inputs.lce_inputs(c)
+    h, w = bf16_values(h), bf16_values(w)
+    z = h.astype(np.float64) @ w.astype(np.float64).T
+    loss_ref, dz, _ = oracle.cross_entropy_fwd_bwd(z, lab)
+    mine = np.where(lab == sf.IGNORE_INDEX, -1, lab).astype(np.int32)
+    bits = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    loss, dh, dw = sf.lce_step(bits(h), bits(w), mine, ignore_index=-1)
+    dh32 = torch.from_numpy(dh.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert abs(loss - loss_ref) / loss_ref < 1e-3
+    assert rel_l2(dh32, dz @ w.astype(np.float64)) < 1e-2
+    assert rel_l2(dw, dz.T @ h.astype(np.float64)) < 1e-2
+    bad = mine.copy()
+    bad[3] = c.vocab
+    with pytest.raises(sf.SfError):
+        sf.lce_step(bits(h), bits(w), bad, ignore_index=-1)
+
+
 @pytest.mark.parametrize("chunk", [128, 500, 1000])
 def test_lce_matches_unfused_cross_entropy(chunk):
     from inputs.configs import LceConfig

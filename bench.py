@@ -437,6 +437,8 @@ def run_op(args, c):
     W = (Hq + 2 * Hkv) * hd
     attn_fwd_flops = 2.0 * B * Hq * hd * S * (S + 1)
     bf16_peak, bf16_sust, hbm, src = peaks()
+    if args.op in ("rmsnorm_fwd", "rmsnorm_bwd", "rope", "swiglu_fwd", "swiglu_bwd"):
+        return run_op_hbm(args, c, sf, torch, st, hbm, src)
     if args.op.startswith("attn"):
         qkv = torch.randn(T, W, device="cuda").to(torch.bfloat16)
         o = torch.empty(T, Hq * hd, device="cuda", dtype=torch.bfloat16)
@@ -478,6 +480,72 @@ def run_op(args, c):
     print(json.dumps({"op": args.op, "workload": c.name, "shape": shape, "ms": ms, "tflops": tf,
                       "peak": bf16_peak, "frac": tf / bf16_peak,
                       "peak_source": f"{src} bf16 burst (kernel timed alone)"}), flush=True)
+
+
+def run_op_hbm(args, c, sf, torch, st, hbm, src):
+    """The memory-bound kernels of a decoder layer at the workload's shapes:
+    time per launch and algorithmic bytes (each tensor read or written once)
+    against the measured HBM copy bandwidth."""
+    T, d, F = c.batch * c.seq, c.hidden, c.ffn
+    q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    bf = torch.bfloat16
+    dev = "cuda"
+    if args.op == "rmsnorm_fwd":
+        x = torch.randn(T, d, device=dev)
+        g = torch.ones(d, device=dev, dtype=bf)
+        y = torch.empty(T, d, device=dev, dtype=bf)
+        rstd = torch.empty(T, device=dev)
+        run = lambda: sf.op_rmsnorm_fwd(x.data_ptr(), g.data_ptr(), y.data_ptr(), rstd.data_ptr(), T, d, c.rms_eps, st)
+        nbytes = T * d * (4 + 2) + T * 4 + d * 2
+        shape = {"rows": T, "d": d, "bytes": "x fp32 in, y bf16 + rstd out"}
+    elif args.op == "rmsnorm_bwd":
+        x, dy, dres = (torch.randn(T, d, device=dev) for _ in range(3))
+        g = torch.ones(d, device=dev, dtype=bf)
+        rstd = torch.ones(T, device=dev)
+        dx = torch.empty(T, d, device=dev)
+        dxb = torch.empty(T, d, device=dev, dtype=bf)
+        dg = torch.empty(d, device=dev, dtype=bf)
+        scr = torch.empty(sf.rmsnorm_bwd_scratch(T, d), device=dev)
+        run = lambda: sf.op_rmsnorm_bwd(x.data_ptr(), g.data_ptr(), rstd.data_ptr(), dy.data_ptr(), dres.data_ptr(),
+                                        dx.data_ptr(), dxb.data_ptr(), dg.data_ptr(), scr.data_ptr(), T, d, st)
+        nbytes = T * d * (4 + 4 + 4 + 4 + 2) + T * 4 + d * 2
+        shape = {"rows": T, "d": d, "bytes": "x, dy, residual grad fp32 in; dx fp32 + bf16 out"}
+    elif args.op == "rope":
+        W = q + 2 * kv
+        x = torch.randn(T, W, device=dev).to(bf)
+        tab = torch.from_numpy(sf.rope_table(c.seq, c.head_dim, c.rope_base)).to(dev)
+        run = lambda: sf.op_rope(x.data_ptr(), W, T, c.seq, c.n_heads + c.n_kv_heads, c.head_dim,
+                                 tab.data_ptr(), 0, st)
+        nbytes = T * (q + kv) * 2 * 2
+        shape = {"tokens": T, "heads": c.n_heads + c.n_kv_heads, "hd": c.head_dim, "bytes": "Q, K bf16 read and written in place"}
+    elif args.op == "swiglu_fwd":
+        ab = torch.randn(T, 2 * F, device=dev).to(bf)
+        m = torch.empty(T, F, device=dev, dtype=bf)
+        run = lambda: sf.op_swiglu_fwd(ab.data_ptr(), m.data_ptr(), T, F, st)
+        nbytes = T * F * (4 + 2)
+        shape = {"rows": T, "ffn": F, "bytes": "[a|b] bf16 in, m bf16 out"}
+    else:
+        ab = torch.randn(T, 2 * F, device=dev).to(bf)
+        dm = torch.randn(T, F, device=dev).to(bf)
+        dab = torch.empty(T, 2 * F, device=dev, dtype=bf)
+        run = lambda: sf.op_swiglu_bwd(dm.data_ptr(), ab.data_ptr(), dab.data_ptr(), T, F, st)
+        nbytes = T * F * (2 + 4 + 4)
+        shape = {"rows": T, "ffn": F, "bytes": "dm, [a|b] bf16 in, [da|db] bf16 out"}
+    for _ in range(args.warmup):
+        assert run() == 0
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    assert sf.device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"op": args.op, "workload": c.name, "shape": shape, "ms": ms,
+                      "algorithmic_bytes": nbytes, "gbs": gbs, "peak": hbm, "frac": gbs / hbm,
+                      "peak_source": f"{src} HBM copy bandwidth"}), flush=True)
 
 
 def run_sweep(args, c):
@@ -558,7 +626,8 @@ def main():
     ap.add_argument("--sweep-batch", default="",
                     help="comma-separated batch sizes: measure the backward overlap condition per layer")
     ap.add_argument("--trace", default="", help="write the host timeline of the timed steps (JSON)")
-    ap.add_argument("--op", default="", choices=["", "attn_fwd", "attn_bwd", "gemm"],
+    ap.add_argument("--op", default="", choices=["", "attn_fwd", "attn_bwd", "gemm", "rmsnorm_fwd",
+                                                 "rmsnorm_bwd", "rope", "swiglu_fwd", "swiglu_bwd"],
                     help="time one kernel instead of the training step")
     ap.add_argument("--shape", default="16384,6144,4096", help="M,N,K for --op gemm")
     ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])

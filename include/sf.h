@@ -403,9 +403,10 @@ int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows);
  * (16 MiB) that the library reserves on every GPU that loads it, until the
  * process exits.  The paper has no counterpart to this entry point.
  *   - Size limit: returns SF_EINVAL when the row partition needs more than
- *     SF_STATIC_SCRATCH_FLOATS floats, i.e. when P * d > 4194304 with
- *     P = min(rows, 2 * number of SMs) (on a 152-SM GPU: any rows for
- *     d <= 13792, at most 256 rows for d = 16384).
+ *     SF_STATIC_SCRATCH_FLOATS floats, i.e. when P * d > 4194304, with
+ *     P = min(rows, 4 * number of SMs) where 4 * SMs * d fits the array and
+ *     P = min(rows, 2 * number of SMs) otherwise (on a 152-SM GPU: any rows
+ *     for d <= 13792, at most 256 rows for d = 16384).
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array: calls whose kernels overlap on the GPU

@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <cstdint>
 
+#include "sf.h"
 #include "sf_internal.h"
 
 namespace sf {
@@ -97,7 +98,7 @@ void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float
 constexpr int kNormThreads = 256;
 
 template <int CH>
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(kNormThreads, CH <= 4 ? 4 : (CH <= 8 ? 2 : 1))
     rmsnorm_bwd_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
                        const float* __restrict__ rstd, const float* __restrict__ dy,
                        const float* __restrict__ dres, float* __restrict__ dx,
@@ -171,8 +172,13 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
-int rmsnorm_bwd_parts(int64_t rows) {
-  const int p = 2 * num_sms();
+// Row partition of the RMSNorm backward (and of the bias column sums): four
+// CTAs per SM (up to d = 4096 the kernel is held to 64 registers, so four
+// 256-thread CTAs fit) when the fp32 partials [parts, d] still fit the
+// allocation-free variant's fixed array, else two.
+int rmsnorm_bwd_parts(int64_t rows, int d) {
+  const int sms = num_sms();
+  const int p = ((int64_t)4 * sms * d <= (int64_t)SF_STATIC_SCRATCH_FLOATS) ? 4 * sms : 2 * sms;
   return rows < p ? (int)(rows > 0 ? rows : 1) : p;
 }
 

@@ -1196,7 +1196,7 @@ int init(sf_ctx* ctx) {
     c = std::max<int64_t>(128, c / 128 * 128);
     ctx->chunk_rows = std::min<int64_t>(c, T);
   }
-  ctx->dg_parts = sf::rmsnorm_bwd_parts(T);
+  ctx->dg_parts = sf::rmsnorm_bwd_parts(T, (int)d);
 
   if (cudaSetDevice(cf.device) != cudaSuccess) {
     cudaGetLastError();

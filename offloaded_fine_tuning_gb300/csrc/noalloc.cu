@@ -60,7 +60,7 @@ extern "C" int sf_op_rmsnorm_bwd_noalloc(const float* x, const uint16_t* g, cons
       (dres && !aligned16(dres)) || (reinterpret_cast<uintptr_t>(g) & 7))
     return SF_EINVAL;
   // same partition of rows as the scratch-taking entry point: identical sums
-  const int parts = sf::rmsnorm_bwd_parts(rows);
+  const int parts = sf::rmsnorm_bwd_parts(rows, d);
   if ((int64_t)parts * d > (int64_t)SF_STATIC_SCRATCH_FLOATS) return SF_EINVAL;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SF_ECUDA;

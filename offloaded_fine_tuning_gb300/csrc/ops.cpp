@@ -81,7 +81,7 @@ int sf_op_gemm_bias(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 
 int64_t sf_op_bias_grad_scratch(int64_t rows, int32_t cols) {
   if (rows < 0 || cols < 0) return -1;
-  return (int64_t)sf::rmsnorm_bwd_parts(rows) * cols;
+  return (int64_t)sf::rmsnorm_bwd_parts(rows, cols) * cols;
 }
 
 int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, float* part,
@@ -90,7 +90,7 @@ int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, 
   if (!dy || !part || !db || (reinterpret_cast<uintptr_t>(dy) & 3)) return SF_EINVAL;
   if (rows == 0) return SF_EINVAL;
   sf::bias_grad(reinterpret_cast<const bf16*>(dy), ld, rows, cols, part,
-                sf::rmsnorm_bwd_parts(rows), reinterpret_cast<bf16*>(db), S(stream));
+                sf::rmsnorm_bwd_parts(rows, cols), reinterpret_cast<bf16*>(db), S(stream));
   return cudaGetLastError() == cudaSuccess ? SF_OK : SF_ECUDA;
 }
 
@@ -106,7 +106,7 @@ int sf_op_rmsnorm_fwd(const float* x, const uint16_t* g, uint16_t* y, float* rst
 }
 
 int64_t sf_op_rmsnorm_bwd_scratch(int64_t rows, int32_t d) {
-  return (int64_t)sf::rmsnorm_bwd_parts(rows) * d;
+  return (int64_t)sf::rmsnorm_bwd_parts(rows, d) * d;
 }
 
 int sf_op_rmsnorm_bwd(const float* x, const uint16_t* g, const float* rstd, const float* dy,
@@ -117,7 +117,7 @@ int sf_op_rmsnorm_bwd(const float* x, const uint16_t* g, const float* rstd, cons
   if (!al16(x) || !al16(dy) || !al16(dx) || !al16(dxb) || !al16(scratch) ||
       (dres && !al16(dres)) || (reinterpret_cast<uintptr_t>(g) & 7))
     return SF_EINVAL;
-  const int parts = sf::rmsnorm_bwd_parts(rows);
+  const int parts = sf::rmsnorm_bwd_parts(rows, d);
   sf::rmsnorm_bwd(x, reinterpret_cast<const bf16*>(g), rstd, dy, dres, dx,
                   reinterpret_cast<bf16*>(dxb), scratch, parts, rows, d, S(stream));
   sf::reduce_parts_bf16(scratch, parts, d, reinterpret_cast<bf16*>(dg), S(stream));

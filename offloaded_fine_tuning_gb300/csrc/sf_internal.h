@@ -46,7 +46,7 @@ void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float
 void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, const float* dy,
                  const float* dres, float* dx, __nv_bfloat16* dxb, float* dg_part, int parts,
                  int64_t rows, int d, cudaStream_t st);
-int rmsnorm_bwd_parts(int64_t rows);
+int rmsnorm_bwd_parts(int64_t rows, int d);
 void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st);
 // The same sum as fp16 after multiplying by scale (a scaled fp16 gradient).
 void reduce_parts_f16(const float* part, int parts, int d, uint16_t* out, float scale,

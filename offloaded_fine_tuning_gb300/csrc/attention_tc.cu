@@ -13,7 +13,11 @@
 //              S0 | S1 | O)
 //   warps 2-5  softmax: tcgen05.ld of a row of S, scale, causal mask,
 //              max / exp2 / sum, rescale of the O row in TMEM when the row
-//              max grows, swizzled store of the row of P
+//              max grows, swizzled store of the row of P; at the end the
+//              normalised O row goes into the P buffer, and one thread
+//              stores the O tile with the TMA unit (whole rows per request,
+//              where per-thread row stores would split every warp store
+//              into 32 transactions)
 //
 // Operands: Q, K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
 // columns per box); V is the MN-major operand of P V ([128 keys][64 hd] boxes);
@@ -79,7 +83,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 template <int HD>
 __global__ void __launch_bounds__(kAttThreads, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, __nv_bfloat16* __restrict__ out,
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_o,
                        float* __restrict__ lse, int S, int Hq, int Hkv, float scale_log2,
                        int* err) {
   using C = AttCfg<HD>;
@@ -334,28 +338,32 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       tc_fence_before();
       mbar_arrive(p_full(st));
     }
+    // the last P V has read the P buffer once O is complete
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, abort_flag));
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = out + ((int64_t)b * S + q) * ((int64_t)Hq * HD) + (int64_t)h * HD;
+      // the O row, bf16, into the P buffer in the tensor map's swizzled layout:
+      // box c / 2 holds columns [64 (c / 2), 64 (c / 2) + 64)
+      const uint32_t orow = sP + (uint32_t)row * 128u;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
         tmem_ld_wait();
-        if (q < S) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack2_bf16(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
-            v.y = pack2_bf16(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
-            v.z = pack2_bf16(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
-            v.w = pack2_bf16(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * k) = v;
-          }
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
+          const uint32_t addr = orow + (c >> 1) * 16384 + (uint32_t)((chunk ^ (row & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack2_bf16(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv)),
+                       "r"(pack2_bf16(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv)),
+                       "r"(pack2_bf16(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv)),
+                       "r"(pack2_bf16(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv))
+                       : "memory");
         }
       }
+      fence_proxy_async_smem();
       if (q < S) lse[((int64_t)b * Hq + h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
     } else if (lane == 0) {
       record_error(err, kDevAttnTimeout);
@@ -367,6 +375,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  } else if (threadIdx.x == 64 && !*abort_flag) {
+    // rows past the sequence end are outside the tensor map and not written
+#pragma unroll
+    for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sP + c * 16384, h * HD + 64 * c, q0, b);
+    bulk_commit_group();
+    bulk_wait_group0();
   }
 }
 
@@ -913,7 +927,6 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
     const int key = k0 + r;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const int tid = threadIdx.x - 64;
-    const int64_t ldo = (int64_t)Hq * HD;
     bool ok = true;
     auto fetch = [&](int it_, float& lv, float& dv) {
       lv = 0.f;
@@ -1141,15 +1154,20 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
   using C = AttCfg<HD>;
   auto fn = encode_fn_att();
   if (!fn) return -3;
-  const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD;
-  CUtensorMap tm;
+  const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
+  CUtensorMap tm, tm_o;
   cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)(W * 2), (cuuint64_t)(S * W * 2)};
+  cuuint64_t dims_o[3] = {(cuuint64_t)WO, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides_o[2] = {(cuuint64_t)(WO * 2), (cuuint64_t)(S * WO * 2)};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(qkv), dims, strides,
          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      fn(&tm_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dims_o, strides_o, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
   static bool set = false;
   if (!set) {
@@ -1159,7 +1177,7 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
     set = true;
   }
   dim3 grid((S + 127) / 128, Hq, B);
-  attn_fwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(tm, o, lse, S, Hq, Hkv,
+  attn_fwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(tm, tm_o, lse, S, Hq, Hkv,
                                                              1.4426950408889634f / sqrtf((float)HD), err);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -761,9 +761,9 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
     attn_bwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_kv,
                         const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_do,
-                        const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
-                        const float* __restrict__ delta,
-                        __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ cs, int S,
+                        const __grid_constant__ CUtensorMap tm_dq,
+                        const __grid_constant__ CUtensorMap tm_dkv, const float* __restrict__ lse,
+                        const float* __restrict__ delta, const float2* __restrict__ cs, int S,
                         int Hq, int Hkv, float scale, float scale_log2, int* err) {
   using C = AttBwd2Cfg;
   constexpr int HD = 128;
@@ -1064,7 +1064,17 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (ok) {
       tc_fence_after();
-      const int64_t ld = (int64_t)(Hq + 2 * Hkv) * HD;
+      // dK and dV rows go into the K and V tiles' shared memory (every MMA
+      // that read them has completed), in the tensor map's swizzled layout;
+      // one thread then stores both tiles with the TMA unit.
+      auto put = [&](uint32_t tile, int col, uint32_t a, uint32_t b_, uint32_t c_, uint32_t d_) {
+        const int chunk = (col & 63) >> 3;  // 16-byte chunk of the 128-byte row
+        const uint32_t addr = tile + (uint32_t)(col >> 6) * 16384u + (uint32_t)r * 128u +
+                              (uint32_t)((chunk ^ (r & 7)) * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b_),
+                     "r"(c_), "r"(d_)
+                     : "memory");
+      };
       // dK: pairs (d, d + HD/2) get the inverse rotation of the key's position;
       // this warp takes d in [32 half, 32 half + 32) and its partners
       {
@@ -1073,16 +1083,16 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
         tmem_ld_32x32b_x32(lane_base + COL_DK + 32 * c, x1);
         tmem_ld_32x32b_x32(lane_base + COL_DK + HD / 2 + 32 * c, x2);
         tmem_ld_wait();
-        if (key < S) {
-          __nv_bfloat16* krow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + g) * HD;
+        {
+          const int kp = key < S ? key : S - 1;  // rows past the end are computed, not stored
           uint32_t o1[16], o2[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             float a1 = __uint_as_float(x1[e]) * scale, b1 = __uint_as_float(x1[e + 1]) * scale;
             float a2 = __uint_as_float(x2[e]) * scale, b2 = __uint_as_float(x2[e + 1]) * scale;
             if (cs) {
-              const float2 ca = cs[(int64_t)key * (HD / 2) + 32 * c + e];
-              const float2 cb = cs[(int64_t)key * (HD / 2) + 32 * c + e + 1];
+              const float2 ca = cs[(int64_t)kp * (HD / 2) + 32 * c + e];
+              const float2 cb = cs[(int64_t)kp * (HD / 2) + 32 * c + e + 1];
               const float y1a = a1 * ca.x + a2 * ca.y, y2a = a2 * ca.x - a1 * ca.y;
               const float y1b = b1 * cb.x + b2 * cb.y, y2b = b2 * cb.x - b1 * cb.y;
               a1 = y1a; a2 = y2a; b1 = y1b; b2 = y2b;
@@ -1092,8 +1102,8 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            *reinterpret_cast<uint4*>(krow + 32 * c + 8 * k) = make_uint4(o1[4 * k], o1[4 * k + 1], o1[4 * k + 2], o1[4 * k + 3]);
-            *reinterpret_cast<uint4*>(krow + HD / 2 + 32 * c + 8 * k) = make_uint4(o2[4 * k], o2[4 * k + 1], o2[4 * k + 2], o2[4 * k + 3]);
+            put(sK, 32 * c + 8 * k, o1[4 * k], o1[4 * k + 1], o1[4 * k + 2], o1[4 * k + 3]);
+            put(sK, HD / 2 + 32 * c + 8 * k, o2[4 * k], o2[4 * k + 1], o2[4 * k + 2], o2[4 * k + 3]);
           }
         }
       }
@@ -1104,19 +1114,14 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
         uint32_t v[32];
         tmem_ld_32x32b_x32(lane_base + COL_DV + 32 * c, v);
         tmem_ld_wait();
-        if (key < S) {
-          __nv_bfloat16* vrow = dqkv + ((int64_t)b * S + key) * ld + (int64_t)(Hq + Hkv + g) * HD;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 u;
-            u.x = pack2_bf16(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1]));
-            u.y = pack2_bf16(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3]));
-            u.z = pack2_bf16(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5]));
-            u.w = pack2_bf16(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7]));
-            *reinterpret_cast<uint4*>(vrow + 32 * c + 8 * k) = u;
-          }
-        }
+        for (int k = 0; k < 4; ++k)
+          put(sV, 32 * c + 8 * k, pack2_bf16(__uint_as_float(v[8 * k + 0]), __uint_as_float(v[8 * k + 1])),
+              pack2_bf16(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+              pack2_bf16(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+              pack2_bf16(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
       }
+      fence_proxy_async_smem();
     } else if (lane == 0) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
@@ -1128,6 +1133,15 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  } else if (threadIdx.x == 64 && !*abort_flag) {
+    // dK and dV tiles; key rows past the sequence end are outside the map
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      tma_store_3d(&tm_dkv, sK + c * 16384, (Hq + g) * HD + 64 * c, k0, b);
+      tma_store_3d(&tm_dkv, sV + c * 16384, (Hq + Hkv + g) * HD + 64 * c, k0, b);
+    }
+    bulk_commit_group();
+    bulk_wait_group0();
   }
 }
 
@@ -1232,7 +1246,7 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
   auto fn = encode_fn_att();
   if (!fn) return -3;
   const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
-  CUtensorMap tkv, tq, td, tdq;
+  CUtensorMap tkv, tq, td, tdq, tdkv;
   cuuint32_t box_kv[3] = {64, 128, 1}, box_q[3] = {64, 64, 1}, box_dq[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   cuuint64_t dq[3] = {(cuuint64_t)W, (cuuint64_t)S, (cuuint64_t)B};
@@ -1249,7 +1263,7 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
   const int nkb = (S + 127) / 128;
   cuuint64_t ddq[3] = {(cuuint64_t)WO, (cuuint64_t)S, (cuuint64_t)(DET ? B * nkb : B)};
   if (!enc(&tkv, qkv, dq, sq, box_kv) || !enc(&tq, qkv, dq, sq, box_q) ||
-      !enc(&td, dout, dd, sd, box_q) ||
+      !enc(&td, dout, dd, sd, box_q) || !enc(&tdkv, dqkv, dq, sq, box_kv) ||
       fn(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, ddq, sdq, box_dq, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -1268,7 +1282,7 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
   const float scale = 1.f / sqrtf((float)HD);
   dim3 grid((S + 127) / 128, Hkv, B);
   attn_bwd_tc2_kernel<DET><<<grid, kAttBwd2Threads, C::SMEM, st>>>(
-      tkv, tq, td, tdq, lse, delta, dqkv, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
+      tkv, tq, td, tdq, tdkv, lse, delta, cs, S, Hq, Hkv, scale, scale * 1.4426950408889634f, err);
   attn_dq_finalize(dq_acc, dqkv, B, S, Hq, Hkv, HD, scale, cs, DET ? nkb : 0, st);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -45,13 +45,12 @@ constexpr int kAttThreads = 192;
 template <int HD>
 struct AttCfg {
   static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
-  static constexpr int KST = 3;                 // K stages (V has 2, P one buffer)
+  static constexpr int KST = 4;                 // K stages (V has 2; P lives in TMEM)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = TILE;
   static constexpr int OFF_V = OFF_K + KST * TILE;
-  static constexpr int OFF_P = OFF_V + 2 * TILE;
-  static constexpr int OFF_BAR = OFF_P + 32768;  // P: 128 rows x 128 keys
-  static constexpr int NBAR = 20;
+  static constexpr int OFF_BAR = OFF_V + 2 * TILE;
+  static constexpr int NBAR = 14 + 2 * KST;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 
@@ -92,12 +91,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   constexpr uint32_t ID_O = umma_idesc_bf16(128, HD, false, true);
   constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t O_COL = 256;
+  constexpr uint32_t P_COL = 384;  // P: 128 rows x 128 keys of bf16, two per column
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
-  const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sP = s0 + C::OFF_P;
+  const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
   // K and V stages have their own barriers: a K stage is free as soon as its
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   auto v_full = [&](int s) { return b0 + 8u * (10 + s); };
   auto v_empty = [&](int s) { return b0 + 8u * (12 + s); };
   auto k_full = [&](int s) { return b0 + 8u * (14 + s); };   // C::KST stages
-  auto k_empty = [&](int s) { return b0 + 8u * (17 + s); };
+  auto k_empty = [&](int s) { return b0 + 8u * (14 + C::KST + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_arrive_expect_tx(q_full, C::TILE);
 #pragma unroll
     for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, colQ + 64 * c, q0, b);
-    // K runs two blocks ahead of V: K(j + 2) needs S(j - 1) done, V(j) needs P V(j - 2) done
+    // K runs three blocks ahead of V: K(j + 3) needs S(j - 1) done, V(j) needs P V(j - 2) done
     auto load_k = [&](int kb) -> bool {
       const int st = kb % C::KST;
       if (!mbar_wait(k_empty(st), ((kb / C::KST) & 1) ^ 1u, abort_flag)) return false;
@@ -170,12 +170,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, kb * 128, b);
       return true;
     };
-    bool ok = load_k(0) && (nkv < 2 || load_k(1));
-    int k_issued = ok ? (nkv < 2 ? 1 : 2) : 0, v_issued = 0;
+    constexpr int KA = C::KST - 1;  // K blocks loaded ahead of the V block being loaded
+    bool ok = true;
+    int k_issued = 0, v_issued = 0;
+    for (int kb = 0; ok && kb < KA && kb < nkv; ++kb) {
+      ok = load_k(kb);
+      if (ok) k_issued = kb + 1;
+    }
     for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 2 < nkv) {
-        if (!load_k(j + 2)) { ok = false; break; }
-        k_issued = j + 3;
+      if (j + KA < nkv) {
+        if (!load_k(j + KA)) { ok = false; break; }
+        k_issued = j + KA + 1;
       }
       const int st = j & 1;
       if (!mbar_wait(v_empty(st), ((j >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
@@ -227,10 +232,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16(tmem_base + O_COL,
-                    smem_desc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                    smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
-                    (jp > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + O_COL, tmem_base + P_COL + kk * 8,
+                       smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
+                       (jp > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(o_done(st));
         umma_commit(v_empty(st));
@@ -316,36 +320,31 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       l = l * corr + ps;
       m = m_new;
-      if (j >= 1) {  // the P buffer was read by P_{j-1} V_{j-1}
+      if (j >= 1) {  // P in TMEM was read by P_{j-1} V_{j-1}
         ok = __all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
+        tc_fence_after();
       }
-      // row of P, bf16, in the 128-byte swizzled K-major layout
-      const uint32_t prow = sP + (uint32_t)row * 128u;
+      // the row of P, bf16 pairs, into the TMEM A operand of P V
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const float* p8 = s + kb * 64 + jj * 8;
-          const uint32_t addr = prow + kb * 16384 + (uint32_t)((jj ^ (row & 7)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "r"(pack2_bf16(p8[0], p8[1])), "r"(pack2_bf16(p8[2], p8[3])),
-                       "r"(pack2_bf16(p8[4], p8[5])), "r"(pack2_bf16(p8[6], p8[7]))
-                       : "memory");
-        }
+        for (int i = 0; i < 32; ++i) pk[i] = pack2_bf16(s[64 * hh + 2 * i], s[64 * hh + 2 * i + 1]);
+        tmem_st_32x32b_x32(lane_base + P_COL + 32 * hh, pk);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full(st));
     }
-    // the last P V has read the P buffer once O is complete
+    // every MMA has completed once O is: K stage 0 is free for the O tile
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, abort_flag));
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-      // the O row, bf16, into the P buffer in the tensor map's swizzled layout:
+      // the O row, bf16, into K stage 0 in the tensor map's swizzled layout:
       // box c / 2 holds columns [64 (c / 2), 64 (c / 2) + 64)
-      const uint32_t orow = sP + (uint32_t)row * 128u;
+      const uint32_t orow = sK + (uint32_t)row * 128u;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t r[32];
@@ -378,7 +377,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   } else if (threadIdx.x == 64 && !*abort_flag) {
     // rows past the sequence end are outside the tensor map and not written
 #pragma unroll
-    for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sP + c * 16384, h * HD + 64 * c, q0, b);
+    for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sK + c * 16384, h * HD + 64 * c, q0, b);
     bulk_commit_group();
     bulk_wait_group0();
   }

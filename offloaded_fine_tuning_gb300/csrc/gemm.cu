@@ -10,7 +10,14 @@
 //   warps 2-5   epilogue: tcgen05.ld rows out of TMEM, convert, store
 // Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Tiles are visited in groups of 8 M-tiles so that the B panel of
-// a group stays in L2.  All operands use the 128-byte swizzle: a K-major tile
+// a group stays in L2.
+//
+// With BN = 256 the CTAs run in clusters of two that take M-tiles 2u and
+// 2u + 1 of the same N-tile: each loads its own A and half of the shared B
+// tile, which the TMA unit writes into both CTAs' shared memory (multicast),
+// and each MMA warp releases a stage in both CTAs.  The tensor cores waited
+// on operand loads for about a third of the main loop; this cuts the bytes
+// each SM requests per k-block from 48 KB to 32 KB.  All operands use the 128-byte swizzle: a K-major tile
 // is [rows][64] with 128-byte rows; an MN-major tile is a set of [64 K rows]
 // x [64 MN] boxes placed 8 KB apart.
 #include <cuda.h>
@@ -162,10 +169,11 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
   }
 }
 
-template <bool A_MN, bool B_MN, int BN, int EPI>
+template <bool A_MN, bool B_MN, int BN, int EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   using Cfg = GemmCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
@@ -190,10 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // CTA rank in the cluster: which M-tile of the pair, and which half of B it loads
+  const int crank = CL == 2 ? (int)cluster_ctarank() : 0;
+  constexpr uint16_t kPair = 0x3;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // released by the MMA warp of every CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -210,13 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL == 2) cluster_sync_all();  // the peer's barriers exist before its first multicast
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // work units: CL M-tiles of one N-tile, one per CTA of the cluster
   const int num_m = (p.M + kBM - 1) / kBM;
+  const int num_mu = (num_m + CL - 1) / CL;
   const int num_n = (p.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
+  const int num_units = num_mu * num_n;
+  const int unit0 = (int)blockIdx.x / CL, unit_step = (int)gridDim.x / CL;
   const int nk = (p.K + kBK - 1) / kBK;
 
   if (warp == 0 && lane == 0) {
@@ -225,11 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     long issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      int tm, tn;
-      tile_coords(tile, num_m, num_n, tm, tn);
-      const int m0 = tm * kBM, n0 = tn * BN;
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
+      int tmu, tn;
+      tile_coords(unit, num_mu, num_n, tmu, tn);
+      const int m0 = (tmu * CL + crank) * kBM, n0 = tn * BN;
       for (int kb = 0; kb < nk; ++kb) {
+        // free in every CTA of the cluster: this CTA's half of B lands in all of them
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
         const int k0 = kb * kBK;
@@ -240,15 +256,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tma_load_2d(a_dst, &tmA, full_bar(stage), k0, m0);
         }
-        if constexpr (B_MN) {
+        if constexpr (CL == 1) {
+          if constexpr (B_MN) {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(b_dst, &tmB, full_bar(stage), k0, n0);
+          }
         } else {
-          tma_load_2d(b_dst, &tmB, full_bar(stage), k0, n0);
+          constexpr int HB = BN / 2;  // B rows (K-major) or columns (MN-major) per CTA
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = crank * (HB / 64); j < (crank + 1) * (HB / 64); ++j)
+              tma_load_2d_mc(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0, kPair);
+          } else {
+            tma_load_2d_mc(b_dst + crank * HB * 128, &tmB, full_bar(stage), k0, n0 + crank * HB, kPair);
+          }
         }
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
+    }
+    if (ok) {
+      // every stage this CTA loaded has been released by both MMA warps, so no
+      // arrival from the peer is still on its way to this CTA's barriers
+      const long n = issued < STAGES ? issued : STAGES;
+      int st = stage;
+      uint32_t ph = phase;
+      for (long i = 0; i < n && ok; ++i) {
+        if (st == 0) { st = STAGES - 1; ph ^= 1u; } else { --st; }
+        ok = mbar_wait(empty_bar(st), ph, abort_flag);
+      }
+      if (!ok) { record_error(p.err, kDevGemmTimeout); *abort_flag = 1; }
     }
     if (!ok) {
       record_error(p.err, kDevGemmTimeout);
@@ -266,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int iter = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++iter) {
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -285,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           else bd = smem_desc_sw128(b_base + k * 32, 16, 1024);
           umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        umma_commit(empty_bar(stage));
+        if constexpr (CL == 2) umma_commit_mc(empty_bar(stage), kPair);
+        else umma_commit(empty_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -301,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     int iter = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
-      int tm, tn;
-      tile_coords(tile, num_m, num_n, tm, tn);
+    for (int unit = unit0; unit < num_units; unit += unit_step, ++iter) {
+      int tmu, tn;
+      tile_coords(unit, num_mu, num_n, tmu, tn);
+      const int tm = tmu * CL + crank;
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
       bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag);
@@ -366,6 +407,9 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t row
   return r == CUDA_SUCCESS;
 }
 
+// CTAs per cluster: pairs that share the B tile for the wide tiles.
+constexpr int gemm_cluster(int BN) { return BN == 256 ? 2 : 1; }
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -381,19 +425,38 @@ template <bool A_MN, bool B_MN, int BN, int EPI>
 static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                     cudaStream_t st, char* why) {
   using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
+  constexpr int CL = gemm_cluster(BN);
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, CL>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_ctas = 0;  // per instantiation: CTAs that can be resident at once
+  if (max_ctas == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
         cudaSuccess) {
       snprintf(why, 64, "gemm: cannot reserve %d B shared memory", Cfg::SMEM);
       return -3;
     }
-    attr_set = true;
+    int clusters = 0;
+    cfg.gridDim = dim3(CL * num_sms());
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+      cudaGetLastError();
+      snprintf(why, 64, "gemm: no resident cluster of %d CTAs", CL);
+      return -3;
+    }
+    max_ctas = clusters * CL < num_sms() ? clusters * CL : num_sms() / CL * CL;
   }
-  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kThreads, Cfg::SMEM, st>>>(ta, tb, p);
+  const int units = ((p.M + kBM * CL - 1) / (kBM * CL)) * ((p.N + BN - 1) / BN);
+  cfg.gridDim = dim3(units * CL < max_ctas ? units * CL : max_ctas);
+  cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(why, 64, "gemm launch: %s", cudaGetErrorString(e));
@@ -466,8 +529,9 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   CUtensorMap ta, tb;
   bool ok = a_mn ? make_map(&ta, a.A, a.M, a.K, a.lda, 64, 64)
                  : make_map(&ta, a.A, a.K, a.M, a.lda, 64, kBM);
+  // with clusters each CTA loads half of a K-major B tile
   ok = ok && (b_mn ? make_map(&tb, a.B, a.N, a.K, a.ldb, 64, 64)
-                   : make_map(&tb, a.B, a.K, a.N, a.ldb, 64, BN));
+                   : make_map(&tb, a.B, a.K, a.N, a.ldb, 64, BN / gemm_cluster(BN)));
   if (!ok) {
     snprintf(why, 64, "gemm: tensor map encode failed");
     return -3;

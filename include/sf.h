@@ -332,7 +332,8 @@ int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, 
 int64_t sf_op_bias_grad_scratch(int64_t rows, int32_t cols);
 
 /* y[r] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)), rstd[r] = 1/sqrt(...);
- * x fp32 [rows, d], g bf16 [d], y bf16 [rows, d], rstd fp32 [rows]. */
+ * x fp32 [rows, d], g bf16 [d], y bf16 [rows, d], rstd fp32 [rows];
+ * d a multiple of 8 in [8, 16384] (SF_EINVAL otherwise). */
 int sf_op_rmsnorm_fwd(const float* x, const uint16_t* g, uint16_t* y, float* rstd, int64_t rows,
                       int32_t d, float eps, void* stream);
 

@@ -5,25 +5,26 @@
 // query rows of one head; per 128-key block the tensor core computes
 // S = Q K^T into one of two TMEM buffers, four softmax warps (one thread per
 // query row, so row max and row sum need no shuffles) turn S into bf16 P in
-// shared memory, and the tensor core accumulates O += P V in TMEM.  S of the
-// next block is computed while the softmax warps work on the current one.
+// TMEM, and the tensor core accumulates O += P V in TMEM with P as its
+// tensor-memory A operand.  S of the next block is computed while the
+// softmax warps work on the current one.
 //
-//   warp 0     TMA: Q once, then K and V blocks into a 2-stage ring
+//   warp 0     TMA: Q once, then K blocks into a 4-stage ring (three blocks
+//              ahead) and V blocks into a 2-stage ring
 //   warp 1     MMA issuer (tcgen05.mma, one thread); TMEM owner (512 columns:
-//              S0 | S1 | O)
+//              S0 | S1 | O | P)
 //   warps 2-5  softmax: tcgen05.ld of a row of S, scale, causal mask,
 //              max / exp2 / sum, rescale of the O row in TMEM when the row
-//              max grows, swizzled store of the row of P; at the end the
-//              normalised O row goes into the P buffer, and one thread
-//              stores the O tile with the TMA unit (whole rows per request,
-//              where per-thread row stores would split every warp store
-//              into 32 transactions)
+//              max grows, tcgen05.st of the row of P as bf16 pairs; at the
+//              end the normalised O row goes into K stage 0 (free once O is
+//              complete), and one thread stores the O tile with the TMA unit
+//              (whole rows per request, where per-thread row stores would
+//              split every warp store into 32 transactions)
 //
 // Operands: Q, K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
-// columns per box); V is the MN-major operand of P V ([128 keys][64 hd] boxes);
-// P is written by the softmax threads in the same swizzled K-major layout the
-// TMA would produce.  The qkv rows are read through a 3-D tensor map
-// (column, position, batch), so rows past the sequence end arrive as zeros.
+// columns per box); V is the MN-major operand of P V ([128 keys][64 hd]
+// boxes).  The qkv rows are read through a 3-D tensor map (column, position,
+// batch), so rows past the sequence end arrive as zeros.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

@@ -52,50 +52,73 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return u;
 }
 
+constexpr int kNormThreads = 256;
+
 // ------------------------------------------------------------------ RMSNorm forward
 // One CTA per row: y = bf16(g * x * rstd), rstd = 1/sqrt(mean(x^2) + eps).
-__global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
-                                   __nv_bfloat16* __restrict__ y, float* __restrict__ rstd_out,
-                                   int d, float eps) {
+// Thread t holds the float4 columns t, t+256, ... (CH of them) in registers
+// between the sum of squares and the scaling, so x is read once.
+template <int CH>
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_fwd_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
+                       __nv_bfloat16* __restrict__ y, float* __restrict__ rstd_out, int d,
+                       float eps) {
   __shared__ float sh[32];
   const int64_t row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + row * d);
   const int n4 = d >> 2;
+  float4 v[CH];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    float4 v = xr[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int i = threadIdx.x + c * kNormThreads;
+    v[c] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[c].x * v[c].x + v[c].y * v[c].y + v[c].z * v[c].z + v[c].w * v[c].w;
   }
   ss = block_sum(ss, sh);
   const float rstd = rsqrtf(ss / d + eps);
   if (threadIdx.x == 0) rstd_out[row] = rstd;
   const uint2* gr = reinterpret_cast<const uint2*>(g);
   uint2* yr = reinterpret_cast<uint2*>(y + row * d);
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    float4 v = xr[i];
-    uint2 gu = gr[i];
-    float2 g01 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.x));
-    float2 g23 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.y));
-    __nv_bfloat162 o01 = __floats2bfloat162_rn(v.x * rstd * g01.x, v.y * rstd * g01.y);
-    __nv_bfloat162 o23 = __floats2bfloat162_rn(v.z * rstd * g23.x, v.w * rstd * g23.y);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t*>(&o01);
-    o.y = *reinterpret_cast<uint32_t*>(&o23);
-    yr[i] = o;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int i = threadIdx.x + c * kNormThreads;
+    if (i < n4) {
+      uint2 gu = gr[i];
+      float2 g01 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.x));
+      float2 g23 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.y));
+      __nv_bfloat162 o01 = __floats2bfloat162_rn(v[c].x * rstd * g01.x, v[c].y * rstd * g01.y);
+      __nv_bfloat162 o23 = __floats2bfloat162_rn(v[c].z * rstd * g23.x, v[c].w * rstd * g23.y);
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&o01);
+      o.y = *reinterpret_cast<uint32_t*>(&o23);
+      yr[i] = o;
+    }
   }
+}
+
+template <int CH>
+static void rmsnorm_fwd_ch(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float* rstd,
+                           int64_t rows, int d, float eps, cudaStream_t st) {
+  rmsnorm_fwd_kernel<CH><<<(unsigned)rows, kNormThreads, 0, st>>>(x, g, y, rstd, d, eps);
 }
 
 void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float* rstd,
                  int64_t rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return;
-  rmsnorm_fwd_kernel<<<(unsigned)rows, 256, 0, st>>>(x, g, y, rstd, d, eps);
+  const int ch = (d / 4 + kNormThreads - 1) / kNormThreads;  // d <= 16384: at most 16
+  if (ch <= 1) rmsnorm_fwd_ch<1>(x, g, y, rstd, rows, d, eps, st);
+  else if (ch <= 2) rmsnorm_fwd_ch<2>(x, g, y, rstd, rows, d, eps, st);
+  else if (ch <= 4) rmsnorm_fwd_ch<4>(x, g, y, rstd, rows, d, eps, st);
+  else if (ch <= 8) rmsnorm_fwd_ch<8>(x, g, y, rstd, rows, d, eps, st);
+  else if (ch <= 12) rmsnorm_fwd_ch<12>(x, g, y, rstd, rows, d, eps, st);
+  else rmsnorm_fwd_ch<16>(x, g, y, rstd, rows, d, eps, st);
 }
 
 // ------------------------------------------------------------------ RMSNorm backward
 // CTAs stride over rows; thread t owns the float4 columns t, t+256, ... (CH of
 // them) so the gain gradient sum over the CTA's rows stays in registers.  The
 // second pass over a row re-reads x and dy, which are still in L1/L2.
-constexpr int kNormThreads = 256;
 
 template <int CH>
 __global__ void __launch_bounds__(kNormThreads, CH <= 4 ? 4 : (CH <= 8 ? 2 : 1))

@@ -96,7 +96,7 @@ int sf_op_bias_grad(const uint16_t* dy, int64_t ld, int64_t rows, int32_t cols, 
 
 int sf_op_rmsnorm_fwd(const float* x, const uint16_t* g, uint16_t* y, float* rstd, int64_t rows,
                       int32_t d, float eps, void* stream) {
-  if (rows < 0 || d < 8 || d % 8 || !(eps > 0.f)) return SF_EINVAL;
+  if (rows < 0 || d < 8 || d % 8 || d > 16384 || !(eps > 0.f)) return SF_EINVAL;
   if (rows == 0) return SF_OK;
   if (!x || !g || !y || !rstd || !al16(x) || !al16(y) || (reinterpret_cast<uintptr_t>(g) & 7))
     return SF_EINVAL;

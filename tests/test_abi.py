@@ -71,6 +71,7 @@ def test_kernel_api_rejects_bad_arguments_without_launching(sf):
     assert sfp.op_gemm(sfp.NT, sfp.EPI_BF16, 10, 10, 10, 8, 10, 0, 10, 0, 10) == sfp.SF_EINVAL
     assert sfp.op_gemm(7, 0, 1, 1, 1, 0, 1, 0, 1, 0, 1) == sfp.SF_EINVAL
     assert sfp.op_attn_fwd(0, 0, 0, 1, 16, 4, 3, 64) == sfp.SF_EINVAL
+    assert sfp.op_rmsnorm_fwd(16, 16, 16, 16, 1, 16392, 1e-5) == sfp.SF_EINVAL  # d above 16384
     assert sfp.op_attn_fwd(0, 0, 0, 1, 16, 4, 2, 96) == sfp.SF_EINVAL
     assert sfp.op_swiglu_fwd(0, 0, 4, 12) == sfp.SF_EINVAL
     assert sfp.lce_workspace_bytes(100, 1000, 64) >= 64 * 1000 * 2 + 400

@@ -135,7 +135,8 @@ def test_gemm_full_size_sampled_rows():
 
 
 # ------------------------------------------------------------------ RMSNorm
-@pytest.mark.parametrize("rows,d", [(37, 256), (300, 4096), (5, 12288), (1, 8)])
+@pytest.mark.parametrize("rows,d", [(37, 256), (300, 4096), (5, 12288), (1, 8), (3, 16384),
+                                    (7, 3584), (2, 6152)])
 def test_rmsnorm_fwd_bwd(rows, d):
     x = rnd(1, (rows, d), 2.0)
     g = bf16_values(1.0 + 0.1 * rnd(2, (d,)))

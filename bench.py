@@ -607,7 +607,7 @@ def run_sweep(args, c):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="8b", choices=sorted(ALL_CONFIGS))
     ap.add_argument("--micro", type=int, default=1,

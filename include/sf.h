@@ -20,8 +20,9 @@
  * The model is a pre-norm Llama-style decoder (section 4 names Llama, Qwen
  * and Mistral): RMSNorm, QKV projection with rotary embedding (rotate-half
  * pairs), causal grouped-query attention, output projection, RMSNorm, SwiGLU
- * FFN; untied embedding and LM head; loss = mean token cross-entropy over
- * labels != SF_IGNORE_INDEX.
+ * FFN; embedding and LM head untied (options: Q/K/V biases and a tied LM
+ * head, the Qwen layer); loss = mean token cross-entropy over labels !=
+ * SF_IGNORE_INDEX.
  *
  * Conventions for every entry point:
  *   - Return value: SF_OK (0) or a negative status below.  No exception and
@@ -170,7 +171,9 @@ typedef struct {
 
 /* Number of fp32 values of `unit` (see SF_UNIT_*): for a decoder layer the
  * concatenation g1[d], Wq[Hq*hd, d], Wk[Hkv*hd, d], Wv[Hkv*hd, d],
- * Wo[d, Hq*hd], g2[d], Wg[F, d], Wu[F, d], Wd[d, F].  0 for a bad unit. */
+ * (with qkv_bias: bq[Hq*hd], bk[Hkv*hd], bv[Hkv*hd],) Wo[d, Hq*hd], g2[d],
+ * Wg[F, d], Wu[F, d], Wd[d, F].  0 for a bad unit, and for SF_UNIT_LM_HEAD
+ * when tie_embeddings is set. */
 size_t sf_unit_numel(const sf_config* cfg, int32_t unit);
 
 /* Validate cfg, allocate the ring slots, checkpoint and workspace buffers on

@@ -53,6 +53,8 @@ GEMM_CASES = [
     (sf.TN, sf.EPI_F32_ACC, 384, 512, 256),
     (sf.NT, sf.EPI_BF16, 1024, 2304, 1536),
     (sf.TN, sf.EPI_F32, 1152, 1024, 2048),
+    # more 2-CTA work units than clusters fit at once, an odd number of M-tiles
+    (sf.NN, sf.EPI_BF16, 4224, 2560, 256),
 ]
 
 

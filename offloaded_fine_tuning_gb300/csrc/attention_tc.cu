@@ -1,25 +1,28 @@
 // Causal grouped-query attention forward on the tcgen05 tensor cores.
 //
 // Online softmax over key blocks (Milakov & Gimelshein 2018; the blocking of
-// Dao et al., FlashAttention 2022), laid out for sm_103a: one CTA owns 128
-// query rows of one head; per 128-key block the tensor core computes
-// S = Q K^T into one of two TMEM buffers, four softmax warps (one thread per
-// query row, so row max and row sum need no shuffles) turn S into bf16 P in
-// TMEM, and the tensor core accumulates O += P V in TMEM with P as its
-// tensor-memory A operand.  S of the next block is computed while the
-// softmax warps work on the current one.
+// Dao et al., FlashAttention 2022), laid out for sm_103a.  The kernel is
+// persistent: one CTA per SM walks (128-query block, head, batch) tiles in
+// longest-first order, so the barrier and TMEM setup happen once per SM and
+// the next tile's Q and K loads overlap the current tile's last blocks and
+// epilogue.  Per 128-key block the tensor core computes S = Q K^T into one of
+// two TMEM buffers, four softmax warps (one thread per query row, so row max
+// and row sum need no shuffles) turn S into bf16 P in TMEM, and the tensor
+// core accumulates O += P V in TMEM with P as its tensor-memory A operand.
+// S of the next block is computed while the softmax warps work on the
+// current one.
 //
-//   warp 0     TMA: Q once, then K blocks into a 4-stage ring (three blocks
-//              ahead) and V blocks into a 2-stage ring
+//   warp 0     TMA: Q of each tile once the previous tile's last S has read
+//              the Q buffer, K blocks into a 3-stage ring, V into a 2-stage ring
 //   warp 1     MMA issuer (tcgen05.mma, one thread); TMEM owner (512 columns:
 //              S0 | S1 | O | P)
 //   warps 2-5  softmax: tcgen05.ld of a row of S, scale, causal mask,
 //              max / exp2 / sum, rescale of the O row in TMEM when the row
-//              max grows, tcgen05.st of the row of P as bf16 pairs; at the
-//              end the normalised O row goes into K stage 0 (free once O is
-//              complete), and one thread stores the O tile with the TMA unit
-//              (whole rows per request, where per-thread row stores would
-//              split every warp store into 32 transactions)
+//              max grows, tcgen05.st of the row of P as bf16 pairs; at a
+//              tile's end the normalised O row goes into a staging buffer
+//   warp 6     stores each staged O tile with the TMA unit (whole rows per
+//              request, where per-thread row stores would split every warp
+//              store into 32 transactions)
 //
 // Operands: Q, K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
 // columns per box); V is the MN-major operand of P V ([128 keys][64 hd]
@@ -42,16 +45,18 @@ namespace sf {
 namespace {
 
 constexpr int kAttThreads = 192;
+constexpr int kAttFwdThreads = 224;  // + a warp that stores O tiles
 
 template <int HD>
 struct AttCfg {
   static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
-  static constexpr int KST = 4;                 // K stages (V has 2; P lives in TMEM)
+  static constexpr int KST = 3;                 // K stages (V has 2; P lives in TMEM)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = TILE;
   static constexpr int OFF_V = OFF_K + KST * TILE;
-  static constexpr int OFF_BAR = OFF_V + 2 * TILE;
-  static constexpr int NBAR = 14 + 2 * KST;
+  static constexpr int OFF_O = OFF_V + 2 * TILE;  // staging of the O tile for its TMA store
+  static constexpr int OFF_BAR = OFF_O + TILE;
+  static constexpr int NBAR = 18 + 2 * KST;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 
@@ -82,9 +87,9 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 }  // namespace
 
 template <int HD>
-__global__ void __launch_bounds__(kAttThreads, 1)
+__global__ void __launch_bounds__(kAttFwdThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_o,
-                       float* __restrict__ lse, int S, int Hq, int Hkv, float scale_log2,
+                       float* __restrict__ lse, int S, int Hq, int Hkv, int B, float scale_log2,
                        int* err) {
   using C = AttCfg<HD>;
   constexpr int NB = HD / 64;  // 64-column boxes per tile
@@ -98,36 +103,49 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
-  const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V;
+  const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sO = s0 + C::OFF_O;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
   // K and V stages have their own barriers: a K stage is free as soon as its
-  // S = Q K^T has completed, so K loads run ahead of the P V products.
-  const uint32_t q_full = b0;
-  auto s_full = [&](int s) { return b0 + 8u * (1 + s); };
-  auto s_free = [&](int s) { return b0 + 8u * (3 + s); };
-  auto p_full = [&](int s) { return b0 + 8u * (5 + s); };
-  auto o_done = [&](int s) { return b0 + 8u * (7 + s); };
-  const uint32_t drain = b0 + 8u * 9;
-  auto v_full = [&](int s) { return b0 + 8u * (10 + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (12 + s); };
-  auto k_full = [&](int s) { return b0 + 8u * (14 + s); };   // C::KST stages
-  auto k_empty = [&](int s) { return b0 + 8u * (14 + C::KST + s); };
+  // S = Q K^T has completed, so K loads run ahead of the P V products.  Every
+  // ring and buffer index below counts over all tiles of the CTA.
+  const uint32_t q_full = b0, q_empty = b0 + 8u;
+  auto s_full = [&](int s) { return b0 + 8u * (2 + s); };
+  auto s_free = [&](int s) { return b0 + 8u * (4 + s); };
+  auto p_full = [&](int s) { return b0 + 8u * (6 + s); };
+  auto o_done = [&](int s) { return b0 + 8u * (8 + s); };
+  const uint32_t drain = b0 + 8u * 10;
+  const uint32_t o_free = b0 + 8u * 11;    // a tile's O has left TMEM: the next may overwrite it
+  const uint32_t st_ready = b0 + 8u * 12;  // a tile's O rows are in the staging buffer
+  const uint32_t st_free = b0 + 8u * 13;   // the staging buffer has been read by the TMA store
+  auto v_full = [&](int s) { return b0 + 8u * (14 + s); };
+  auto v_empty = [&](int s) { return b0 + 8u * (16 + s); };
+  auto k_full = [&](int s) { return b0 + 8u * (18 + s); };   // C::KST stages
+  auto k_empty = [&](int s) { return b0 + 8u * (18 + C::KST + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (S + 127) / 128;
-  int rank, h, b;
-  grid_rank_first(rank, h, b);
-  const int qb = nqb - 1 - rank;  // longest rows first
-  const int g = h / (Hq / Hkv);
-  const int q0 = qb * 128;
-  const int nkv = qb + 1;
-  const int colQ = h * HD, colK = (Hq + g) * HD, colV = (Hq + Hkv + g) * HD;
+  const int per_rank = Hq * B;
+  const int num_tiles = nqb * per_rank;
+  // Tile t in longest-first order: every tile of query block nqb - 1 (the most
+  // keys) comes before any of block nqb - 2, and so on; CTA c takes tiles c,
+  // c + gridDim.x, ...
+  struct Tile { int h, b, qb, nkv; };
+  auto tile_of = [&](int t) -> Tile {
+    const int rank = t / per_rank, rem = t - rank * per_rank;
+    Tile x;
+    x.h = rem % Hq;
+    x.b = rem / Hq;
+    x.qb = nqb - 1 - rank;
+    x.nkv = x.qb + 1;
+    return x;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -137,15 +155,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
       mbar_init(s_free(s), 128);
-    }
-    for (int s = 0; s < 2; ++s) {
       mbar_init(p_full(s), 128);
       mbar_init(o_done(s), 1);
     }
     mbar_init(drain, 1);
+    mbar_init(o_free, 128);
+    mbar_init(st_ready, 128);
+    mbar_init(st_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -158,88 +178,110 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    mbar_arrive_expect_tx(q_full, C::TILE);
-#pragma unroll
-    for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, colQ + 64 * c, q0, b);
-    // K runs three blocks ahead of V: K(j + 3) needs S(j - 1) done, V(j) needs P V(j - 2) done
-    auto load_k = [&](int kb) -> bool {
-      const int st = kb % C::KST;
-      if (!mbar_wait(k_empty(st), ((kb / C::KST) & 1) ^ 1u, abort_flag)) return false;
-      mbar_arrive_expect_tx(k_full(st), C::TILE);
-#pragma unroll
-      for (int c = 0; c < NB; ++c)
-        tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, kb * 128, b);
-      return true;
-    };
-    constexpr int KA = C::KST - 1;  // K blocks loaded ahead of the V block being loaded
+    // Per tile: Q once the previous tile's last S has read the Q buffer, then
+    // K blocks (K(j) needs S(j - KST) done) two ahead of V blocks (V(j) needs
+    // P V(j - 2) done).
     bool ok = true;
-    int k_issued = 0, v_issued = 0;
-    for (int kb = 0; ok && kb < KA && kb < nkv; ++kb) {
-      ok = load_k(kb);
-      if (ok) k_issued = kb + 1;
-    }
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + KA < nkv) {
-        if (!load_k(j + KA)) { ok = false; break; }
-        k_issued = j + KA + 1;
-      }
-      const int st = j & 1;
-      if (!mbar_wait(v_empty(st), ((j >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
-      mbar_arrive_expect_tx(v_full(st), C::TILE);
+    long gk = 0, gv = 0;  // K and V loads issued so far
+    int it = 0;
+    int inflight_q = 0;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
+      const Tile x = tile_of(t);
+      const int g = x.h / (Hq / Hkv);
+      const int colK = (Hq + g) * HD, colV = (Hq + Hkv + g) * HD;
+      inflight_q = 0;  // a Q load of this tile not issued yet
+      if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(q_full, C::TILE);
 #pragma unroll
-      for (int c = 0; c < NB; ++c)
-        tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, b);
-      v_issued = j + 1;
+      for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, x.h * HD + 64 * c, x.qb * 128, x.b);
+      inflight_q = 1;
+      auto load_k = [&](int kb) -> bool {
+        const int st = (int)(gk % C::KST);
+        if (!mbar_wait(k_empty(st), (uint32_t)((gk / C::KST) & 1) ^ 1u, abort_flag)) return false;
+        mbar_arrive_expect_tx(k_full(st), C::TILE);
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, kb * 128, x.b);
+        ++gk;
+        return true;
+      };
+      constexpr int KA = C::KST - 1;
+      int kn = 0;
+      for (; ok && kn < KA && kn < x.nkv; ++kn) ok = load_k(kn);
+      for (int j = 0; ok && j < x.nkv; ++j) {
+        if (kn < x.nkv) {
+          if (!load_k(kn)) { ok = false; break; }
+          ++kn;
+        }
+        const int st = (int)(gv & 1);
+        if (!mbar_wait(v_empty(st), (uint32_t)((gv >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(v_full(st), C::TILE);
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, x.b);
+        ++gv;
+      }
     }
     if (!ok) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       // let the copies already issued land before the CTA's shared memory goes away
-      mbar_wait(q_full, 0, nullptr);
-      for (int kb = k_issued - 1; kb >= 0 && kb >= k_issued - C::KST; --kb)
-        mbar_wait(k_full(kb % C::KST), (kb / C::KST) & 1, nullptr);
-      for (int kb = v_issued - 1; kb >= 0 && kb >= v_issued - 2; --kb)
-        mbar_wait(v_full(kb & 1), (kb >> 1) & 1, nullptr);
+      if (inflight_q) mbar_wait(q_full, (it & 1), nullptr);
+      for (long k = gk - 1; k >= 0 && k >= gk - C::KST; --k)
+        mbar_wait(k_full((int)(k % C::KST)), (uint32_t)((k / C::KST) & 1), nullptr);
+      for (long k = gv - 1; k >= 0 && k >= gv - 2; --k)
+        mbar_wait(v_full((int)(k & 1)), (uint32_t)((k >> 1) & 1), nullptr);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    bool ok = mbar_wait(q_full, 0, abort_flag);
-    for (int j = 0; ok && j <= nkv; ++j) {
-      if (j < nkv) {  // S_j = Q K_j^T into S buffer j % 2
-        const int st = j & 1, ks = j % C::KST;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(k_full(ks), (j / C::KST) & 1, abort_flag) ||
-            !mbar_wait(s_free(st), ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    bool ok = true;
+    long gb = 0;  // global index of the tile's first key block
+    int it = 0;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
+      const Tile x = tile_of(t);
+      if (!mbar_wait(q_full, it & 1, abort_flag)) { ok = false; break; }
+      for (int j = 0; ok && j <= x.nkv; ++j) {
+        if (j < x.nkv) {  // S_j = Q K_j^T into S buffer G % 2
+          const long G = gb + j;
+          const int st = (int)(G & 1), ks = (int)(G % C::KST);
+          if (!mbar_wait(k_full(ks), (uint32_t)((G / C::KST) & 1), abort_flag) ||
+              !mbar_wait(s_free(st), (uint32_t)((G >> 1) & 1) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem_base + st * 128, smem_desc_sw128(sQ + off, 16, 1024),
-                    smem_desc_sw128(sK + ks * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tmem_base + st * 128, smem_desc_sw128(sQ + off, 16, 1024),
+                      smem_desc_sw128(sK + ks * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(st));
+          umma_commit(k_empty(ks));  // K stage free once S has been computed
+          if (j == x.nkv - 1) umma_commit(q_empty);  // and Q once the tile's last S has
         }
-        umma_commit(s_full(st));
-        umma_commit(k_empty(ks));  // K stage free once S has been computed
-      }
-      if (j > 0) {  // O += P_{j-1} V_{j-1}
-        const int jp = j - 1, st = jp & 1;
-        if (!mbar_wait(p_full(st), (jp >> 1) & 1, abort_flag) ||
-            !mbar_wait(v_full(st), (jp >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        if (j > 0) {  // O += P_{j-1} V_{j-1}
+          const long G = gb + j - 1;
+          const int st = (int)(G & 1);
+          // the first P V of a tile overwrites O: the previous tile's O must have left TMEM
+          if (j == 1 && it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(p_full(st), (uint32_t)((G >> 1) & 1), abort_flag) ||
+              !mbar_wait(v_full(st), (uint32_t)((G >> 1) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16_ts(tmem_base + O_COL, tmem_base + P_COL + kk * 8,
-                       smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
-                       (jp > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            umma_bf16_ts(tmem_base + O_COL, tmem_base + P_COL + kk * 8,
+                         smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
+                         (j > 1 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(o_done(st));
+          umma_commit(v_empty(st));
         }
-        umma_commit(o_done(st));
-        umma_commit(v_empty(st));
       }
+      gb += x.nkv;
     }
     if (!ok) {
       record_error(err, kDevAttnTimeout);
@@ -247,105 +289,134 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       umma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp >= 2) {
+  } else if (warp == 6 && lane == 0) {
+    // ---------------------------------------------------------------- O store
+    bool ok = true;
+    int it = 0;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
+      const Tile x = tile_of(t);
+      if (!mbar_wait(st_ready, it & 1, abort_flag)) { ok = false; break; }
+      // rows past the sequence end are outside the tensor map and not written
+#pragma unroll
+      for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sO + c * 16384, x.h * HD + 64 * c, x.qb * 128, x.b);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+      mbar_arrive(st_free);
+    }
+    bulk_wait_group0();
+    if (!ok) {
+      record_error(err, kDevAttnTimeout);
+      *abort_flag = 1;
+    }
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------------------- softmax
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int q = q0 + row;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    // m: the row max in log2 units that the exponentials are taken against.
-    // It only moves when a block's max exceeds it by more than 8 (a factor of
-    // 256), so O in TMEM is rarely rescaled; the result O / l does not depend
-    // on the choice of m.
-    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full(st), (j >> 1) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      float s[128];
-      {  // the row's 128 scores: four loads in flight, one wait
-        uint32_t r[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[c][i]);
-      }
-      tc_fence_before();
-      mbar_arrive(s_free(st));
-      if (j == qb) {  // diagonal block: keys after the query are masked
-        const int lim = q - j * 128;
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > lim) s[i] = -INFINITY;
-      }
-      // row max with eight independent accumulators (short dependency chains)
-      float mx8[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mx8[a] = s[a];
-#pragma unroll
-      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      mx *= scale_log2;  // the scale is positive: the max commutes with it
-      const bool grow = mx > m + 8.f;
-      const float m_new = grow ? mx : m;
-      const float corr = ex2_approx(m - m_new);  // 1 without growth, 0 on the first block
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // P_{j-1} V_{j-1} must have landed before the O row is rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag));
+    long gb = 0;
+    int it = 0;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
+      const Tile x = tile_of(t);
+      const int q = x.qb * 128 + row;
+      // m: the row max in log2 units that the exponentials are taken against.
+      // It only moves when a block's max exceeds it by more than 8 (a factor
+      // of 256), so O in TMEM is rarely rescaled; the result O / l does not
+      // depend on the choice of m.
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < x.nkv; ++j) {
+        const long G = gb + j;
+        const int st = (int)(G & 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(st), (uint32_t)((G >> 1) & 1), abort_flag));
         if (!ok) break;
         tc_fence_after();
+        float s[128];
+        {  // the row's 128 scores: four loads in flight, one wait
+          uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-          tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[c][i]);
+        }
+        tc_fence_before();
+        mbar_arrive(s_free(st));
+        if (j == x.qb) {  // diagonal block: keys after the query are masked
+          const int lim = q - j * 128;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i > lim) s[i] = -INFINITY;
+        }
+        // row max with eight independent accumulators (short dependency chains)
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = s[a];
+#pragma unroll
+        for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        mx *= scale_log2;  // the scale is positive: the max commutes with it
+        const bool grow = mx > m + 8.f;
+        const float m_new = grow ? mx : m;
+        const float corr = ex2_approx(m - m_new);  // 1 without growth, 0 on the first block
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // P_{j-1} V_{j-1} must have landed before the O row is rescaled
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(o_done((int)((G - 1) & 1)), (uint32_t)(((G - 1) >> 1) & 1), abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+            tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
+          }
+          tmem_st_wait();
+        }
+        float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const float p = ex2_approx(fmaf(s[i], scale_log2, -m_new));
+          s[i] = p;
+          ps8[i & 7] += p;
+        }
+        const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+        l = l * corr + ps;
+        m = m_new;
+        if (G >= 1) {  // P in TMEM was read by the previous P V (of this tile or the last)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(o_done((int)((G - 1) & 1)), (uint32_t)(((G - 1) >> 1) & 1), abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // the row of P, bf16 pairs, into the TMEM A operand of P V
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack2_bf16(s[64 * hh + 2 * i], s[64 * hh + 2 * i + 1]);
+          tmem_st_32x32b_x32(lane_base + P_COL + 32 * hh, pk);
         }
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(st));
       }
-      float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float p = ex2_approx(fmaf(s[i], scale_log2, -m_new));
-        s[i] = p;
-        ps8[i & 7] += p;
-      }
-      const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      l = l * corr + ps;
-      m = m_new;
-      if (j >= 1) {  // P in TMEM was read by P_{j-1} V_{j-1}
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // the row of P, bf16 pairs, into the TMEM A operand of P V
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack2_bf16(s[64 * hh + 2 * i], s[64 * hh + 2 * i + 1]);
-        tmem_st_32x32b_x32(lane_base + P_COL + 32 * hh, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full(st));
-    }
-    // every MMA has completed once O is: K stage 0 is free for the O tile
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, abort_flag));
-    if (ok) {
+      if (!ok) break;
+      const long GL = gb + x.nkv - 1;  // the tile's last block
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done((int)(GL & 1)), (uint32_t)((GL >> 1) & 1), abort_flag));
+      // the staging buffer is free once the previous tile's store has read it
+      if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait(st_free, (it - 1) & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / l;
-      // the O row, bf16, into K stage 0 in the tensor map's swizzled layout:
-      // box c / 2 holds columns [64 (c / 2), 64 (c / 2) + 64)
-      const uint32_t orow = sK + (uint32_t)row * 128u;
+      // the O row, bf16, into the staging buffer in the tensor map's swizzled
+      // layout: box c / 2 holds columns [64 (c / 2), 64 (c / 2) + 64)
+      const uint32_t orow = sO + (uint32_t)row * 128u;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t r[32];
@@ -363,9 +434,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                        : "memory");
         }
       }
+      tc_fence_before();
+      mbar_arrive(o_free);  // O has left TMEM
       fence_proxy_async_smem();
-      if (q < S) lse[((int64_t)b * Hq + h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
-    } else if (lane == 0) {
+      mbar_arrive(st_ready);
+      if (q < S) lse[((int64_t)x.b * Hq + x.h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
+      gb += x.nkv;
+    }
+    if (!ok && lane == 0) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
     }
@@ -375,12 +451,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
-  } else if (threadIdx.x == 64 && !*abort_flag) {
-    // rows past the sequence end are outside the tensor map and not written
-#pragma unroll
-    for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sK + c * 16384, h * HD + 64 * c, q0, b);
-    bulk_commit_group();
-    bulk_wait_group0();
   }
 }
 
@@ -1190,9 +1260,11 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
       return -3;
     set = true;
   }
-  dim3 grid((S + 127) / 128, Hq, B);
-  attn_fwd_tc_kernel<HD><<<grid, kAttThreads, C::SMEM, st>>>(tm, tm_o, lse, S, Hq, Hkv,
-                                                             1.4426950408889634f / sqrtf((float)HD), err);
+  // persistent: one CTA per SM walks the tiles in longest-first order
+  const int tiles = ((S + 127) / 128) * Hq * B;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  attn_fwd_tc_kernel<HD><<<grid, kAttFwdThreads, C::SMEM, st>>>(tm, tm_o, lse, S, Hq, Hkv, B,
+                                                                1.4426950408889634f / sqrtf((float)HD), err);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

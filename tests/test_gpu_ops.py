@@ -246,7 +246,9 @@ def test_bias_grad_is_the_column_sum(rows, cols, ld):
 # ------------------------------------------------------------------ attention
 ATTN_CASES = [(2, 200, 6, 2, 64), (1, 130, 4, 1, 128), (1, 64, 2, 2, 64), (2, 1, 4, 2, 128),
               (1, 300, 12, 1, 128), (1, 64, 2, 2, 128), (3, 257, 8, 2, 128), (1, 40, 4, 4, 128),
-              (2, 150, 8, 2, 64)]
+              (2, 150, 8, 2, 64),
+              # more (query block, head) tiles than SMs: some persistent CTAs take two
+              (1, 1100, 20, 4, 128)]
 
 
 def attn_inputs(B, S, Hq, Hkv, hd, seed=1):

@@ -5,8 +5,9 @@ batch 8 x seq 2048, bf16 weights streamed from pinned host memory through a
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b] [--impl ours|reference]
 
-Prints one JSON line.  value = tokens/s over K synchronous steps timed with
-CUDA events (device clock, Adam included); e2e = the same through the public
+Prints one JSON line.  value = tokens/s over K steps timed with CUDA events
+(device clock; every step's host Adam update, the last one's included, lies
+inside the timed region); e2e = the same through the public
 call with host wall clock, including the per-step staging of the token batch
 and the read of the loss.  --impl reference times the CPU oracle on a bounded
 sample of the same workload.  N > 1 (torchrun) runs independent replicas, one

@@ -184,17 +184,16 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
     bool ok = true;
     long gk = 0, gv = 0;  // K and V loads issued so far
     int it = 0;
-    int inflight_q = 0;
+    int q_issued = -1;  // tile index of the last Q load issued
     for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
       const Tile x = tile_of(t);
       const int g = x.h / (Hq / Hkv);
       const int colK = (Hq + g) * HD, colV = (Hq + Hkv + g) * HD;
-      inflight_q = 0;  // a Q load of this tile not issued yet
       if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(q_full, C::TILE);
 #pragma unroll
       for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, x.h * HD + 64 * c, x.qb * 128, x.b);
-      inflight_q = 1;
+      q_issued = it;
       auto load_k = [&](int kb) -> bool {
         const int st = (int)(gk % C::KST);
         if (!mbar_wait(k_empty(st), (uint32_t)((gk / C::KST) & 1) ^ 1u, abort_flag)) return false;
@@ -226,7 +225,7 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       // let the copies already issued land before the CTA's shared memory goes away
-      if (inflight_q) mbar_wait(q_full, (it & 1), nullptr);
+      if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, nullptr);
       for (long k = gk - 1; k >= 0 && k >= gk - C::KST; --k)
         mbar_wait(k_full((int)(k % C::KST)), (uint32_t)((k / C::KST) & 1), nullptr);
       for (long k = gv - 1; k >= 0 && k >= gv - 2; --k)

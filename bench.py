@@ -10,8 +10,13 @@ Prints one JSON line.  value = tokens/s over K steps timed with CUDA events
 inside the timed region); e2e = the same through the public
 call with host wall clock, including the per-step staging of the token batch
 and the read of the loss.  --impl reference times the CPU oracle on a bounded
-sample of the same workload.  N > 1 (torchrun) runs independent replicas, one
-per GPU (the step has no cross-GPU exchange on one node's replicas).
+sample of the same workload.
+
+The library drives one GPU: its GEMM clusters share weight tiles by TMA
+multicast within that GPU's own memory, and the step has no cross-GPU
+exchange.  A launch on more than one GPU (--gpus N > 1, or WORLD_SIZE > 1
+under torchrun) is refused: rank 0 prints one JSON line with an
+"unavailable" reason and every rank exits 0 without touching a GPU.
 """
 from __future__ import annotations
 
@@ -107,20 +112,28 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def max_over_ranks(values, dist=None, device="cpu"):
-    """Element-wise maximum of per-rank timings over all ranks (the slowest
-    replica sets the whole job's time); identity without a process group."""
-    if dist is None:
-        return [float(v) for v in values]
-    import torch
-    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(x) for x in t.tolist()]
+def job_throughput(tokens_per_step, steps, elapsed_ms):
+    """Tokens/s of the whole job: every step's tokens over the timed region."""
+    return tokens_per_step * steps / (elapsed_ms / 1e3)
 
 
-def job_throughput(tokens_per_rank_step, steps, world, slowest_ms):
-    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
-    return world * tokens_per_rank_step * steps / (slowest_ms / 1e3)
+def world_size(args) -> int:
+    return max(int(os.environ.get("WORLD_SIZE", "1")), args.gpus)
+
+
+def refuse_multi_gpu(args) -> bool:
+    """True (after rank 0 printed why) when the launch asks for more than one
+    GPU: the library is single-GPU by design (its GEMMs multicast weight
+    tiles between the two CTAs of a cluster, inside one GPU's memory)."""
+    n = world_size(args)
+    if n <= 1:
+        return False
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps({"metric": METRIC, "unit": UNIT, "n_gpus": n, "impl": args.impl,
+                          "unavailable": "single-GPU library: the layer-sliding step runs on one "
+                                         "GPU (GEMM clusters multicast tiles within that GPU's "
+                                         "memory; no cross-GPU path is built)"}), flush=True)
+    return True
 
 
 def link_probe(torch, nbytes=1 << 30):
@@ -257,14 +270,8 @@ def host_adam_bytes(c, micro=1, bf16_state=False):
 def run_ours(args, c):
     import torch
     import offloaded_fine_tuning_gb300 as sf
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
     sf.lib(build_if_needed=True)
     bf16_peak, bf16_sust, hbm, peak_src = peaks()
     link = link_probe(torch)
@@ -273,13 +280,13 @@ def run_ours(args, c):
     m = load_model(sf, c, args.ring or c.ring_slots, 0 if args.sync_updates else 1,
                    1 if args.offload_activations else 0, 1 if args.bf16_adam_state else 0)
     adam = sf.Adam(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
-    # a fresh batch each step (rank-specific seeds for replicas); with --micro N
+    # a fresh batch each step; with --micro N
     # a step is N micro-batches of the workload's batch, summed before the update
     n_micro = max(1, args.micro)
     n_batches = args.warmup + 2 * args.steps
 
     def make_batch(i):
-        parts = [inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + 1000 * rank + n_micro * i + j)
+        parts = [inputs.tokens_and_labels(c, seed=inputs.SEED_TOKENS + n_micro * i + j)
                  for j in range(n_micro)]
         if n_micro == 1:
             return parts[0]
@@ -300,8 +307,6 @@ def run_ours(args, c):
     m.set_timing(True)
     clocks = ClockSampler(local)
     clocks.start()
-    if dist:
-        dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -314,8 +319,6 @@ def run_ours(args, c):
     e1.record()
     timeline = m.trace()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     dev_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     m.set_timing(False)
@@ -348,10 +351,10 @@ def run_ours(args, c):
             assert st == sf.SF_OK, m.error()
         gpu_path_ms = (time.perf_counter() - g0) * 1e3 / 2
 
-    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_s * 1e3], dist, device="cuda")
+    e2e_ms = e2e_s * 1e3
     ms_step = dev_ms / args.steps
-    value = job_throughput(T, args.steps, world, dev_ms)
-    e2e = job_throughput(T, args.steps, world, e2e_ms)
+    value = job_throughput(T, args.steps, dev_ms)
+    e2e = job_throughput(T, args.steps, e2e_ms)
 
     gemm_ms = sum(s["gemm_ms"] for s in stats)
     gemm_fl = sum(s["gemm_flops"] for s in stats)
@@ -376,20 +379,18 @@ def run_ours(args, c):
     if args.trace:
         with open(args.trace, "w") as f:
             json.dump(timeline, f)
-    if rank != 0:
-        return
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         v, secs, desc = oracle_sample(c)
         cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": c.name, "global_batch": n_micro * c.batch * world, "seq_len": c.seq,
+        "config": {"workload": c.name, "global_batch": n_micro * c.batch, "seq_len": c.seq,
                    "micro_batches": n_micro,
                    "layers": c.n_layers, "ring_slots": args.ring or c.ring_slots,
-                   "parallelism": "replicas" if world > 1 else "single-gpu layer sliding",
+                   "parallelism": "single-gpu layer sliding",
                    "host_updates": "synchronous" if args.sync_updates else "overlap next step",
                    "activations": "sliding (host)" if args.offload_activations else "resident",
                    "adam_state": "bf16, stochastic rounding" if args.bf16_adam_state else "fp32",
@@ -421,8 +422,6 @@ def run_ours(args, c):
     }
     print(json.dumps(line), flush=True)
     m.close()
-    if dist:
-        dist.destroy_process_group()
 
 
 def run_op(args, c):
@@ -634,12 +633,16 @@ def main():
     ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])
     args = ap.parse_args()
     c = ALL_CONFIGS[args.config]
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it, on the host cores
+        run_reference(args, c)
+        return
+    if refuse_multi_gpu(args):
+        return
     if args.sweep_batch:
         run_sweep(args, c)
     elif args.op:
         run_op(args, c)
-    elif args.impl == "reference":
-        run_reference(args, c)
     else:
         run_ours(args, c)
 

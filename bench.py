@@ -52,23 +52,94 @@ def peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def layer_matmul_params(c):
+    """P_m: the matmul parameters of one decoder layer."""
+    q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    return c.hidden * q + 2 * c.hidden * kv + q * c.hidden + 3 * c.hidden * c.ffn
+
+
+def attn_fwd_flops(c, batch=None):
+    """Exact causal attention forward count (QK^T and PV over the causal
+    half, diagonal included): 2 B Hq hd S (S + 1)."""
+    B = c.batch if batch is None else batch
+    return 2.0 * B * c.n_heads * c.head_dim * c.seq * (c.seq + 1)
+
+
+def algorithmic_step_flops(c, n_micro=1):
+    """F_step, the algorithmic work of one step: every decoder layer four
+    times its forward (forward, recompute, backward = 2x forward) with the
+    exact causal attention count, plus the fused head's three products
+    (logits, dH, dW) over the valid rows: L 4 (2 P_m T + A) + 3 2 d V n_valid."""
+    T = c.batch * c.seq
+    n_valid = c.batch * (c.seq - 1)
+    fwd = 2.0 * layer_matmul_params(c) * T + attn_fwd_flops(c)
+    return n_micro * (c.n_layers * 4 * fwd + 3 * 2.0 * c.hidden * c.vocab * n_valid)
+
+
 def step_flops(c, executed=True):
-    """Algorithmic FLOPs of one step.  Decoder layers: forward + recompute +
-    backward (2x forward) of the four projections and causal attention; the
-    recompute skips the down projection, whose output the backward does not
-    need (executed=True counts what runs; False counts the full 4x)."""
+    """FLOPs the engine runs in one step: the recompute skips the down
+    projection (its output is not needed) and the last layer is not
+    recomputed; the head runs over all T rows (ignored rows included).
+    executed=False gives algorithmic_step_flops."""
+    if not executed:
+        return algorithmic_step_flops(c)
     d, F, T = c.hidden, c.ffn, c.batch * c.seq
     q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
     proj = {"qkv": 2 * T * d * (q + 2 * kv), "o": 2 * T * q * d, "gu": 2 * T * d * 2 * F, "down": 2 * T * F * d}
-    attn = 2.0 * c.batch * c.n_heads * c.head_dim * c.seq * (c.seq + 1)  # QK^T + PV, causal
+    attn = attn_fwd_flops(c)
     fwd = sum(proj.values()) + attn
-    rec = fwd - (proj["down"] if executed else 0)
+    rec = fwd - proj["down"]
     bwd = 2 * sum(proj.values()) + 2.5 * attn
-    layers = c.n_layers * fwd + (c.n_layers - 1) * rec + c.n_layers * bwd if executed else \
-        c.n_layers * (fwd + fwd + 2 * fwd)
-    n_valid = c.batch * (c.seq - 1)
-    head = 3 * 2.0 * d * c.vocab * (T if executed else n_valid)
+    layers = c.n_layers * fwd + (c.n_layers - 1) * rec + c.n_layers * bwd
+    head = 3 * 2.0 * d * c.vocab * T
     return layers + head
+
+
+def phase_bound_ms(c, peak_tflops, link, ring):
+    """The phase-aware bound of a step: the sum over its phases of the slower
+    of tensor work at peak and that phase's host-link copies, instead of the
+    global max(F / peak, bytes / link).  Phases: each layer's forward (its
+    weights' H2D of 2 P_l bytes hides under the previous layer's forward), the
+    head (the LM head's H2D and its gradient's D2H), and each layer's
+    recompute + backward (3x the forward; its gradients' D2H, plus the H2D of
+    the layer R places earlier when that one is not resident, both ways at
+    once)."""
+    P = peak_tflops * 1e12
+    P_l = layer_matmul_params(c) + 2 * c.hidden + (c.n_heads + 2 * c.n_kv_heads) * c.head_dim * bool(c.qkv_bias)
+    lay = 2.0 * P_l
+    T = c.batch * c.seq
+    fwd = (2.0 * layer_matmul_params(c) * T + attn_fwd_flops(c)) / P
+    head_fl = 3 * 2.0 * c.hidden * c.vocab * c.batch * (c.seq - 1) / P
+    wlm = 2.0 * c.vocab * c.hidden
+    bw = {k: v * 1e9 for k, v in link.items()}
+    t = c.n_layers * max(fwd, lay / bw["h2d"])
+    t += max(head_fl, wlm / bw["h2d"] + wlm / bw["d2h"])
+    R = min(ring, c.n_layers)
+    for l in range(c.n_layers - 1, -1, -1):
+        link_t = (2 * lay / bw["bidir"]) if l - R >= 0 else lay / bw["d2h"]
+        t += max(3 * fwd, link_t)
+    return t * 1e3
+
+
+def gemm_traffic_summary(path=None):
+    """Per-launch DRAM traffic of the step's GEMMs from the committed ncu
+    summary, if it was taken of the GEMM source as it stands (its SHA-256
+    prefix is recorded beside the number); else None."""
+    import hashlib
+    import re
+    path = path or os.path.join(ROOT, "profiles", "gemm_8b_step_traffic.md")
+    src = os.path.join(ROOT, "offloaded_fine_tuning_gb300", "csrc", "gemm.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    m = re.search(r"gemm_cu_sha256_16:\s*([0-9a-f]{16})", text)
+    b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    a = re.search(r"algorithmic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m and b) or m.group(1) != sha:
+        return None
+    return {"bytes": float(b.group(1)), "algorithmic": float(a.group(1)) if a else None,
+            "source": os.path.relpath(path, ROOT)}
 
 
 class ClockSampler:
@@ -208,6 +279,57 @@ def oracle_sample(c, reps=1):
     return c.batch * S / t_step, t_layer + t_head, desc
 
 
+def oracle_full_step(c):
+    """Time one whole CPU oracle step (float32) of a small workload as it is:
+    returns (tokens/s, seconds, description)."""
+    import oracle
+    d, V = c.hidden, c.vocab
+    layers = [{k: oracle.bf16_round(v) for k, v in inputs.split_layer(c, inputs.layer_master(c, l)).items()}
+              for l in range(c.n_layers)]
+    r = lambda u: oracle.bf16_round(inputs.unit_master(c, u))
+    w = oracle.ModelWeights(layers=layers, embed=r(UNIT_EMBED).reshape(V, d), final_norm=r(UNIT_FINAL_NORM),
+                            lm_head=r(UNIT_LM_HEAD).reshape(V, d))
+    tok, lab = inputs.tokens_and_labels(c)
+    t0 = time.perf_counter()
+    oracle.step(w, tok, lab, c, dtype=np.float32)
+    secs = time.perf_counter() - t0
+    return c.batch * c.seq / secs, secs, f"the whole {c.name} step ({c.batch} x {c.seq} tokens), float32 numpy"
+
+
+def oracle_lce_sample(c, rows=1024):
+    """Time the CPU oracle's unfused LM head + cross-entropy forward and
+    backward on a block of rows of the large-vocabulary workload, float32:
+    returns (rows/s of the whole workload, seconds, description)."""
+    import oracle
+    h, w, lab = inputs.lce_inputs(c)
+    W = oracle.bf16_round(w)
+    hb = oracle.bf16_round(h[:rows])
+    t0 = time.perf_counter()
+    _, dz, _ = oracle.cross_entropy_fwd_bwd(hb @ W.T, lab[:rows])
+    _ = dz @ W
+    _ = dz.T @ hb
+    secs = time.perf_counter() - t0
+    n = c.batch * c.seq
+    return rows / secs, secs, (f"{rows} of {n} rows of {c.name}: logits, loss, dH and dW "
+                               f"(float32 numpy), rows/s")
+
+
+def oracle_timings():
+    """The CPU oracle, as it stands, on a bounded sample of every other
+    workload (the tiny one whole; one sequence through one layer plus the
+    head, extrapolated, for the decoder stacks; a block of rows for the
+    large-vocabulary head)."""
+    from inputs import LCE_STRESS
+    out = {}
+    for name in ("tiny", "1.3b", "123b-slice"):
+        c = CONFIGS[name]
+        v, secs, desc = oracle_full_step(c) if name == "tiny" else oracle_sample(c)
+        out[c.name] = {"value": v, "unit": UNIT, "seconds": secs, "sample": desc}
+    v, secs, desc = oracle_lce_sample(LCE_STRESS)
+    out[LCE_STRESS.name] = {"value": v, "unit": UNIT, "seconds": secs, "sample": desc}
+    return out
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -340,7 +462,7 @@ def run_ours(args, c):
     e2e_s = time.perf_counter() - t0
 
     # the GPU path alone: two steps without the optimizer (no host Adam), synchronous
-    gpu_path_ms = None
+    gpu_path_ms, gp_stats = None, []
     if not args.no_gpu_path:
         m.sync()
         torch.cuda.synchronize()
@@ -350,6 +472,15 @@ def run_ours(args, c):
             st = m.train_step(tok, lab) if n_micro == 1 else m.train_step_accum(tok, lab)
             assert st == sf.SF_OK, m.error()
         gpu_path_ms = (time.perf_counter() - g0) * 1e3 / 2
+        # the same steps with the engine's event timeline: the compute stream's
+        # waits are then waits for copies alone (no host update to wait for)
+        m.set_timing(True)
+        for i in range(2):
+            tok, lab = batches[args.warmup + i]
+            st = m.train_step(tok, lab) if n_micro == 1 else m.train_step_accum(tok, lab)
+            assert st == sf.SF_OK, m.error()
+            gp_stats.append(m.stats())
+        m.set_timing(False)
 
     e2e_ms = e2e_s * 1e3
     ms_step = dev_ms / args.steps
@@ -367,9 +498,14 @@ def run_ours(args, c):
     gpu_step = n_micro * statistics.mean(s["step_ms"] for s in stats)
     achieved = gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
     F_exec = n_micro * step_flops(c, executed=True)
-    t_tensor = F_exec / (bf16_sust * 1e12)
+    F_step = algorithmic_step_flops(c, n_micro)
+    t_tensor = F_step / (bf16_sust * 1e12)
     t_link = (h2d + d2h) / (link["bidir"] * 1e9)
     t_roof = max(t_tensor, t_link)
+    t_phase = n_micro * phase_bound_ms(c, bf16_sust, link, args.ring or c.ring_slots)
+    exposed = n_micro * statistics.mean(s["exposed_ms"] for s in stats)
+    traffic = gemm_traffic_summary()
+    n_launch = n_micro * gemm_n / args.steps
     # host memory: the Adam update of every unit (28 B per layer / LM-head
     # parameter: bf16 grad in, fp32 master, m, v read and written, bf16 out;
     # 24 B per embedding parameter, whose gradient is fp32) plus the DMA copies
@@ -382,7 +518,8 @@ def run_ours(args, c):
     cpu = None
     if not args.no_cpu_baseline:
         v, secs, desc = oracle_sample(c)
-        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc,
+               "other_workloads": oracle_timings()}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -400,12 +537,30 @@ def run_ours(args, c):
         "gpu_launches": int(n_micro * sum(s["kernel_launches"] for s in stats)),
         "roofline": {"kernel": "gemm_tcgen05", "bound": "tensor", "achieved": achieved,
                      "peak": bf16_sust, "unit": "TFLOP/s",
-                     "frac": achieved / bf16_sust if achieved else None, "traffic": None,
+                     "frac": achieved / bf16_sust if achieved else None,
+                     "traffic": traffic["bytes"] if traffic else None,
+                     "traffic_algorithmic": traffic["algorithmic"] if traffic else None,
+                     "traffic_source": traffic["source"] if traffic else
+                     "no ncu capture of the current GEMM source",
+                     "flops_per_launch": gemm_fl / max(1, gemm_n),
                      "peak_source": f"{peak_src} bf16 sustained (cuBLAS, long loop)",
-                     "launches": n_micro * gemm_n, "gemm_ms_per_step": n_micro * gemm_ms / args.steps},
-        "step_roofline": {"flops": F_exec, "t_tensor_ms": t_tensor * 1e3, "h2d_bytes": h2d,
+                     "launches_per_step": n_launch,
+                     "gemm_ms_per_step": n_micro * gemm_ms / args.steps},
+        "step_roofline": {"flops": F_step, "flops_executed": F_exec,
+                          "t_tensor_ms": t_tensor * 1e3, "h2d_bytes": h2d,
                           "d2h_bytes": d2h, "link_gbs": link, "t_link_ms": t_link * 1e3,
                           "t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                          "phase_bound_ms": t_phase, "phase_frac": t_phase / ms_step,
+                          "exposed_copy_ms": n_micro * statistics.mean(x["exposed_ms"] for x in gp_stats)
+                          if gp_stats else None,
+                          "exposed_copy_what": "compute-stream time not covered by layer and head "
+                                               "compute in the steps without the optimizer (waits for "
+                                               "weight, checkpoint and batch copies)",
+                          "compute_stream_wait_ms": exposed,
+                          "compute_stream_wait_what": "the same in the timed steps, where a layer's "
+                                                      "weight copy also waits for its host update",
+                          "compute_stream_ms": n_micro * statistics.mean(s["compute_ms"] for s in stats),
+                          "head_ms": n_micro * statistics.mean(s["head_ms"] for s in stats),
                           "host_memory": {"bytes": host_bytes, "adam_bytes": adam_bytes,
                                           "probe_gbs": host_gbs, "t_ms": t_host * 1e3,
                                           "frac": t_host * 1e3 / ms_step},
@@ -422,6 +577,109 @@ def run_ours(args, c):
     }
     print(json.dumps(line), flush=True)
     m.close()
+
+
+def run_lce(args):
+    """The large-vocabulary LM head + cross-entropy workload (4 x 4096 rows of
+    hidden 3584, vocabulary 152064, 10% of labels ignored): value = rows/s of
+    the fused chunked forward + backward on device-resident inputs (CUDA
+    events; W alone is 1.09 GB, larger than L2); e2e = the same through
+    sf_lce_step on host buffers (its H2D of h, W, labels and D2H of loss, dH,
+    dW inside the timed region)."""
+    import torch
+    import offloaded_fine_tuning_gb300 as sf
+    from inputs import LCE_STRESS as c
+    sf.lib(build_if_needed=True)
+    bf16_peak, bf16_sust, hbm, peak_src = peaks()
+    h, w, lab = inputs.lce_inputs(c)
+    n, d, V = h.shape[0], c.hidden, c.vocab
+    bits = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+    hb, wb = bits(h), bits(w)
+    H, W, Y = hb.cuda(), wb.cuda(), torch.from_numpy(lab.astype(np.int32)).cuda()
+    n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
+    cap = max(128, ((2 << 30) // (6 * V)) // 128 * 128)  # as the library's automatic chunk
+    chunks = -(-n // cap)
+    chunk = min(n, (-(-n // chunks) + 127) // 128 * 128)
+    ws = torch.empty(sf.lce_workspace_bytes(n, V, chunk), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    dh = torch.empty((n, d), device="cuda")
+    dw = torch.empty((V, d), device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    run = lambda: sf.op_lce(H.data_ptr(), W.data_ptr(), Y.data_ptr(), n, d, V, n_valid, chunk,
+                            ws.data_ptr(), loss.data_ptr(), dh.data_ptr(), dw.data_ptr(), st)
+    for _ in range(args.warmup):
+        assert run() == 0
+    torch.cuda.synchronize()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert sf.device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    # end to end through the public call on host buffers (bf16 bits)
+    hbits = hb.view(torch.int16).numpy().view(np.uint16)
+    wbits = wb.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        l_host, _, _ = sf.lce_step(hbits, wbits, lab)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    flops = 3 * 2.0 * n * V * d
+    tf = flops / (ms / 1e3) / 1e12
+    n_chunks = (n + chunk - 1) // chunk
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, secs, desc = oracle_lce_sample(c)
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": n / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": c.name, "global_batch": c.batch, "seq_len": c.seq, "hidden": d,
+                   "vocab": V, "ignored": c.ignore_frac, "chunk_rows": chunk,
+                   "parallelism": "single-gpu", "l2": "inputs larger than L2 (W_lm 1.09 GB)",
+                   "what": "fused chunked LM head + cross-entropy forward and backward (tokens = rows)"},
+        "e2e": {"value": n / e2e_s, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
+                "h2d_bytes_per_step": n * d * 2 + V * d * 2 + n * 4,
+                "d2h_bytes_per_step": 4 + n * d * 2 + V * d * 4},
+        "gpu_launches": args.steps * (4 * n_chunks + 1),
+        "roofline": {"kernel": "fused LM head (3 GEMMs per chunk + row softmax)", "bound": "tensor",
+                     "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
+                     "traffic": None, "flops_per_step": flops,
+                     "peak_source": f"{peak_src} bf16 burst (one op timed alone)"},
+        "clocks": clk, "loss": float(loss.item()), "loss_e2e": l_host, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_lce(args):
+    """--impl reference on the large-vocabulary workload: the CPU oracle on a
+    block of rows per step, as it stands."""
+    from inputs import LCE_STRESS as c
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_lce_sample(c)
+    vals = []
+    for _ in range(args.steps):
+        v, secs, desc = oracle_lce_sample(c)
+        vals.append(v)
+    value = statistics.median(vals)
+    n = c.batch * c.seq
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": n / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": c.name, "global_batch": c.batch, "seq_len": c.seq,
+                                        "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
 
 
 def run_op(args, c):
@@ -609,7 +867,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="8b", choices=sorted(ALL_CONFIGS))
+    ap.add_argument("--config", default="8b", choices=sorted(ALL_CONFIGS) + ["lce-stress"])
     ap.add_argument("--micro", type=int, default=1,
                     help="gradient accumulation: micro-batches (of the workload's batch) per step")
     ap.add_argument("--ring", type=int, default=0)
@@ -632,6 +890,12 @@ def main():
     ap.add_argument("--shape", default="16384,6144,4096", help="M,N,K for --op gemm")
     ap.add_argument("--layout", default="nt", choices=["nt", "nn", "tn"])
     args = ap.parse_args()
+    if args.config == "lce-stress":
+        if args.impl == "reference":
+            run_reference_lce(args)
+        elif not refuse_multi_gpu(args):
+            run_lce(args)
+        return
     c = ALL_CONFIGS[args.config]
     if args.impl == "reference":
         # the CPU oracle: rank 0 alone runs it, on the host cores

@@ -165,6 +165,11 @@ typedef struct {
   double update_layer_ms;  /* host Adam of one layer (wall time, update thread) */
   double loss_scale;       /* fp16_grads: the scale of this step's gradients; else 0 */
   int64_t skipped_updates; /* fp16_grads: unit updates skipped for overflow, in total */
+  /* the compute stream's timeline (timing enabled): */
+  double head_ms;          /* final norm + fused LM head / cross-entropy, forward and backward */
+  double compute_ms;       /* all layer forwards, recompute-and-backwards and the head */
+  double exposed_ms;       /* step_ms - compute_ms: time the compute stream waited, mostly
+                              for weight / checkpoint copies that compute did not hide */
 } sf_stats;
 
 /* ---------------------------------------------------------------- model API */
@@ -180,6 +185,13 @@ size_t sf_unit_numel(const sf_config* cfg, int32_t unit);
  * the device, pinned host buffers for every unit, fp32 master / Adam state in
  * host memory, streams, events and the host worker threads.  Every buffer the
  * step needs is allocated here (the step itself allocates nothing).
+ * Source: gist.science summary, technical summary 2.B "Efficiënt Heterogeen
+ * Geheugenbeheer", item "Pre-allocated GPU Cache Queue" (the
+ * GPU holds a small window of layer units, reused without new allocation;
+ * here ring_slots identical buffers of one layer's weights and gradients)
+ * and "Layer-Adam Optimizer" (optimizer state in host memory); the
+ * sciencestack abstract page, Abstract (state in CPU memory, GPU as a
+ * compute engine over a window of layers).
  * Errors: SF_EINVAL (bad cfg), SF_ENOMEM, SF_ECUDA. */
 int sf_init_model(const sf_config* cfg, sf_ctx** out);
 
@@ -192,14 +204,28 @@ const char* sf_last_error(const sf_ctx* ctx);
 
 /* Set the fp32 master weights of `unit` (numel == sf_unit_numel) and reset
  * its Adam moments; the bf16 copy that streams to the GPU is rounded from it
- * (round-to-nearest-even).  Errors: SF_EINVAL, SF_ESTATE. */
+ * (round-to-nearest-even).
+ * Source: gist.science summary, technical summary 2.B "Gedeelde
+ * CPU-buffers" (the fp32 -> bf16/fp16 conversion lives in fixed host
+ * buffers that the layer's weights stream from) and 2.A (parameters of layer
+ * L_i are fetched host-to-device ahead of their use).
+ * Errors: SF_EINVAL, SF_ESTATE. */
 int sf_load_layer_weights(sf_ctx* ctx, int32_t unit, const float* fp32_master, size_t numel);
 
 /* One training step on tokens/labels [batch, seq] (int32, host memory):
  * forward over all layers through the GPU ring, fused LM-head cross-entropy,
  * recompute-and-backward over the layers in reverse order, gradient
  * streaming to the host and, if adam != NULL, the Adam update of every unit
- * (adam == NULL: gradients only, weights unchanged).  On return the loss is
+ * (adam == NULL: gradients only, weights unchanged).
+ * Source: gist.science summary, technical summary 2.A "Light-Weight
+ * Asynchronous Engine" (after layer L_i's backward its gradients go to host
+ * memory asynchronously while the GPU runs L_{i-1}'s backward and fetches
+ * L_{i-2}; separate CUDA streams for copies and compute; the condition
+ * T_compute >= T_transfer + T_update), 2.C "Fused LinearCrossEntropy" (the
+ * projection and the loss fused so the full logits never exist, with no
+ * loss of accuracy) and 2.B "Layer-Adam Optimizer"; the sciencestack
+ * abstract page, figure 3 and 5 captions (the backward overlaps the
+ * parameter updates and the GPU-CPU transfers).  On return the loss is
  * ready and, unless async_update is set, every update is done.  tokens in
  * [0, vocab); labels in [0, vocab) or SF_IGNORE_INDEX; batch*seq <=
  * max_batch*max_seq and seq <= max_seq.  With no valid label the loss and all
@@ -223,7 +249,10 @@ int sf_train_step_accum(sf_ctx* ctx, const int32_t* tokens, const int32_t* label
 
 /* Gradient of the last step for `unit`, in sf_unit_numel order, upcast from
  * the bf16 values that were streamed to the host (the embedding gradient is
- * accumulated in fp32).  Needs retain_grads = 1, else SF_ESTATE. */
+ * accumulated in fp32).  Needs retain_grads = 1, else SF_ESTATE.
+ * Source: gist.science summary, technical summary 2.B "Gedeelde CPU-buffers"
+ * (gradients cast to bf16/fp16 and kept in shared fixed host buffers) and
+ * 2.A (the d2h transfer of a finished layer's gradients). */
 int sf_get_grads(sf_ctx* ctx, int32_t unit, float* out, size_t numel);
 
 /* Current fp32 master weights of `unit`.  Errors: SF_EINVAL. */
@@ -249,7 +278,11 @@ int sf_set_adam_step(sf_ctx* ctx, int64_t t);
  * A no-op when async_update is 0.  Errors: SF_ETIMEOUT, SF_ESTATE. */
 int sf_sync(sf_ctx* ctx);
 
-/* Loss of the last step.  Errors: SF_ESTATE before the first step. */
+/* Loss of the last step: the mean token cross-entropy over the valid labels.
+ * Source: gist.science summary, technical summary 2.C "Fused
+ * LinearCrossEntropy" (the loss computed inside the fused output layer) and
+ * section 4 "Betekenis en Impact" (standard training objectives).
+ * Errors: SF_ESTATE before the first step. */
 int sf_loss(sf_ctx* ctx, float* out);
 
 /* The fused LM head + cross-entropy as a standalone call on host buffers (for
@@ -384,14 +417,45 @@ int sf_op_swiglu_fwd(const uint16_t* ab, uint16_t* m, int64_t rows, int32_t ffn,
 int sf_op_swiglu_bwd(const uint16_t* dm, const uint16_t* ab, uint16_t* dab, int64_t rows,
                      int32_t ffn, void* stream);
 
+/* The Q/K/V projection with its rotary embedding, in one GEMM: the fp32
+ * accumulator of A[M,K] * B[N,K]^T (plus bias[N] when bias != NULL, added
+ * first, 64-byte aligned) is rotated on the columns [0, rope_cols) (heads of
+ * head_dim columns, pair (j, j + head_dim/2) rotated by the table angle of
+ * position row % seq, as sf_op_rope) and rounded to bf16 once into C[M,N].
+ * head_dim in {64, 128}; N and rope_cols multiples of head_dim; table: device
+ * copy of sf_rope_table (16-byte aligned).  Other arguments as sf_op_gemm. */
+int sf_op_gemm_qkv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                   int64_t ldb, uint16_t* C, int64_t ldc, const uint16_t* bias, const float* table,
+                   int32_t seq, int32_t rope_cols, int32_t head_dim, void* stream);
+
+/* The gate/up projection with SwiGLU, in one GEMM: B = [Wg; Wu] bf16 [2F, K]
+ * (Wu starts F rows after Wg, same row stride ldb); a = A Wg^T and b = A Wu^T
+ * (fp32 accumulators of the same tile), m[M,F] bf16 = silu(a) * b.  When
+ * ab != NULL the fp32 a and b are also written: ab[r, j] = a, ab[r, F + j] = b
+ * (row stride ldab >= 2F, 16-byte aligned), for the backward.  F multiple of
+ * 8.  Other arguments as sf_op_gemm with layout 0. */
+int sf_op_gemm_swiglu(int64_t M, int64_t F, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, uint16_t* m, int64_t ldm, float* ab,
+                      int64_t ldab, void* stream);
+
+/* The down projection's input gradient taken through SwiGLU, in one GEMM:
+ * dm = dy[M,K] * wd[K,F] (layout 1, fp32 accumulator, never stored), then with
+ * a = ab[r, j], b = ab[r, F + j] (fp32, from sf_op_gemm_swiglu) and
+ * s = sigmoid(a): dab[r, j] = bf16(dm b s (1 + a (1 - s))),
+ * dab[r, F + j] = bf16(dm a s).  ldab, lddab >= 2F; F multiple of 8. */
+int sf_op_gemm_swiglu_bwd(int64_t M, int64_t F, int64_t K, const void* dy, int64_t lddy,
+                          const void* wd, int64_t ldw, const float* ab, int64_t ldab,
+                          uint16_t* dab, int64_t lddab, void* stream);
+
 /* Fused chunked LM-head + cross-entropy forward and backward on device data:
- * z = h W^T (never stored beyond one chunk of `chunk_rows` rows),
+ * z = h W^T in fp32 (never stored beyond one chunk of `chunk_rows` rows),
  * loss = (1/n_valid) sum_valid (logsumexp(z_t) - z_t[label_t]),
  * dh = dZ W (fp32 [n, d]), dw = dZ^T h (fp32 [v, d]) with
  * dZ = (softmax(z) - onehot)/n_valid on valid rows, 0 on ignored rows.
  * h bf16 [n, d], w bf16 [v, d], labels int32 [n] (device), loss fp32 [1].
  * n_valid is the number of labels != SF_IGNORE_INDEX (the caller counts it).
- * workspace: sf_op_lce_workspace_bytes(n, v, chunk_rows) bytes, 256-aligned. */
+ * workspace: sf_op_lce_workspace_bytes(n, v, chunk_rows) bytes, 256-aligned:
+ * a chunk's fp32 logits and bf16 dZ (6 bytes per logit) and n fp32 row losses. */
 int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64_t n, int32_t d,
               int32_t v, int64_t n_valid, int64_t chunk_rows, void* workspace, float* loss,
               float* dh, float* dw, void* stream);
@@ -408,9 +472,8 @@ int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows);
  * process exits.  The paper has no counterpart to this entry point.
  *   - Size limit: returns SF_EINVAL when the row partition needs more than
  *     SF_STATIC_SCRATCH_FLOATS floats, i.e. when P * d > 4194304, with
- *     P = min(rows, 4 * number of SMs) where 4 * SMs * d fits the array and
- *     P = min(rows, 2 * number of SMs) otherwise (on a 152-SM GPU: any rows
- *     for d <= 13792, at most 256 rows for d = 16384).
+ *     P = min(rows, 2 * number of SMs of the current device) (on a 152-SM
+ *     GPU: any rows for d <= 13792, at most 256 rows for d = 16384).
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array: calls whose kernels overlap on the GPU

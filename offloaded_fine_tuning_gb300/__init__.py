@@ -60,7 +60,8 @@ class Stats(ctypes.Structure):
                 ("timing_enabled", ctypes.c_int32)] + \
                [(n, ctypes.c_double) for n in
                 ("fwd_layer_ms", "bwd_layer_ms", "d2h_layer_ms", "update_layer_ms", "loss_scale")] + \
-               [("skipped_updates", ctypes.c_int64)]
+               [("skipped_updates", ctypes.c_int64)] + \
+               [(n, ctypes.c_double) for n in ("head_ms", "compute_ms", "exposed_ms")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -106,6 +107,12 @@ _SIGS = {
     "sf_op_rmsnorm_bwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_rope_table": (ctypes.c_int, [_I32, _I32, _F32, _VP]),
     "sf_op_rope": (ctypes.c_int, [_VP, _I64, _I64, _I32, _I32, _I32, _VP, _I32, _VP]),
+    "sf_op_gemm_qkv": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _VP, _VP,
+                                      _I32, _I32, _I32, _VP]),
+    "sf_op_gemm_swiglu": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _VP,
+                                         _I64, _VP]),
+    "sf_op_gemm_swiglu_bwd": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64,
+                                             _VP, _I64, _VP]),
     "sf_op_gemm_bias": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _VP,
                                        ctypes.c_float, _VP]),
     "sf_op_bias_grad": (ctypes.c_int, [_VP, _I64, _I64, _I32, _VP, _VP, _VP]),
@@ -367,6 +374,23 @@ def lce_step(h_bf16: np.ndarray, w_bf16: np.ndarray, labels: np.ndarray,
 
 def op_gemm_bias(M, N, K, A, lda, B, ldb, C, ldc, bias, alpha=1.0, stream=0) -> int:
     return lib().sf_op_gemm_bias(M, N, K, A, lda, B, ldb, C, ldc, bias, alpha, _s(stream))
+
+
+def op_gemm_qkv(M, N, K, A, lda, B, ldb, C, ldc, bias, table, seq, rope_cols, head_dim,
+                stream=0) -> int:
+    """Q/K/V projection + optional bias + rotary embedding, one bf16 rounding."""
+    return lib().sf_op_gemm_qkv(M, N, K, A, lda, B, ldb, C, ldc, bias or None, table, seq,
+                                rope_cols, head_dim, _s(stream))
+
+
+def op_gemm_swiglu(M, F, K, A, lda, B, ldb, m, ldm, ab=0, ldab=0, stream=0) -> int:
+    """Gate/up projection with SwiGLU: m = silu(A Wg^T) * (A Wu^T), B = [Wg; Wu]."""
+    return lib().sf_op_gemm_swiglu(M, F, K, A, lda, B, ldb, m, ldm, ab or None, ldab, _s(stream))
+
+
+def op_gemm_swiglu_bwd(M, F, K, dy, lddy, wd, ldw, ab, ldab, dab, lddab, stream=0) -> int:
+    """dm = dy wd through the SwiGLU backward into [da | db] (bf16)."""
+    return lib().sf_op_gemm_swiglu_bwd(M, F, K, dy, lddy, wd, ldw, ab, ldab, dab, lddab, _s(stream))
 
 
 def op_bias_grad(dy, ld, rows, cols, part, db, stream=0) -> int:

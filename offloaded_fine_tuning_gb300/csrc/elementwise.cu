@@ -8,6 +8,7 @@
 
 #include <cfloat>
 #include <cstdint>
+#include <type_traits>
 
 #include "sf.h"
 #include "sf_internal.h"
@@ -117,8 +118,9 @@ void rmsnorm_fwd(const float* x, const __nv_bfloat16* g, __nv_bfloat16* y, float
 
 // ------------------------------------------------------------------ RMSNorm backward
 // CTAs stride over rows; thread t owns the float4 columns t, t+256, ... (CH of
-// them) so the gain gradient sum over the CTA's rows stays in registers.  The
-// second pass over a row re-reads x and dy, which are still in L1/L2.
+// them) so the gain gradient sum over the CTA's rows stays in registers.  For
+// d above 4096 the second pass over a row re-reads x and dy, which are still
+// in L1/L2.
 
 template <int CH>
 __global__ void __launch_bounds__(kNormThreads, CH <= 4 ? 4 : (CH <= 8 ? 2 : 1))
@@ -195,58 +197,157 @@ __global__ void __launch_bounds__(kNormThreads, CH <= 4 ? 4 : (CH <= 8 ? 2 : 1))
   }
 }
 
-// Row partition of the RMSNorm backward (and of the bias column sums): four
-// CTAs per SM (up to d = 4096 the kernel is held to 64 registers, so four
-// 256-thread CTAs fit) when the fp32 partials [parts, d] still fit the
-// allocation-free variant's fixed array, else two.
+// Up to d = 4096: 512-thread CTAs, two per SM, that load a row's x, dy and
+// residual gradient into registers before the row's reduction (every load of
+// the row in flight at once, and no second pass over x and dy).
+constexpr int kNormBwdThreads = 512;
+
+template <int CH>
+__global__ void __launch_bounds__(kNormBwdThreads, 2)
+    rmsnorm_bwd_hold_kernel(const float* __restrict__ x, const __nv_bfloat16* __restrict__ g,
+                            const float* __restrict__ rstd, const float* __restrict__ dy,
+                            const float* __restrict__ dres, float* __restrict__ dx,
+                            __nv_bfloat16* __restrict__ dxb, float* __restrict__ dg_part,
+                            int64_t rows, int d) {
+  __shared__ float sh[32];
+  const int n4 = d >> 2;
+  float4 gacc[CH], gg[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    gacc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    gg[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int i = threadIdx.x + c * kNormBwdThreads;
+    if (i < n4) {
+      uint2 gu = reinterpret_cast<const uint2*>(g)[i];
+      float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.x));
+      float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gu.y));
+      gg[c] = make_float4(a.x, a.y, b.x, b.y);
+    }
+  }
+  const float inv_d = 1.f / d;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float r = rstd[row];
+    const float4* xr = reinterpret_cast<const float4*>(x + row * d);
+    const float4* dyr = reinterpret_cast<const float4*>(dy + row * d);
+    const float4* drr = dres ? reinterpret_cast<const float4*>(dres + row * d) : nullptr;
+    float4 xv[CH], dv[CH], qv[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int i = threadIdx.x + c * kNormBwdThreads;
+      const bool in = i < n4;
+      xv[c] = in ? xr[i] : zero;
+      dv[c] = in ? dyr[i] : zero;
+      qv[c] = (in && drr) ? drr[i] : zero;
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const float4 xh = make_float4(xv[c].x * r, xv[c].y * r, xv[c].z * r, xv[c].w * r);
+      dot += gg[c].x * dv[c].x * xh.x + gg[c].y * dv[c].y * xh.y + gg[c].z * dv[c].z * xh.z +
+             gg[c].w * dv[c].w * xh.w;
+      gacc[c].x += dv[c].x * xh.x; gacc[c].y += dv[c].y * xh.y;
+      gacc[c].z += dv[c].z * xh.z; gacc[c].w += dv[c].w * xh.w;
+    }
+    dot = block_sum(dot, sh) * inv_d;
+    float4* dxr = reinterpret_cast<float4*>(dx + row * d);
+    uint2* dbr = reinterpret_cast<uint2*>(dxb + row * d);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int i = threadIdx.x + c * kNormBwdThreads;
+      if (i < n4) {
+        float4 o;
+        o.x = r * (gg[c].x * dv[c].x - xv[c].x * r * dot) + qv[c].x;
+        o.y = r * (gg[c].y * dv[c].y - xv[c].y * r * dot) + qv[c].y;
+        o.z = r * (gg[c].z * dv[c].z - xv[c].z * r * dot) + qv[c].z;
+        o.w = r * (gg[c].w * dv[c].w - xv[c].w * r * dot) + qv[c].w;
+        dxr[i] = o;
+        __nv_bfloat162 a = __floats2bfloat162_rn(o.x, o.y), b = __floats2bfloat162_rn(o.z, o.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&a);
+        u.y = *reinterpret_cast<uint32_t*>(&b);
+        dbr[i] = u;
+      }
+    }
+  }
+  float4* part = reinterpret_cast<float4*>(dg_part + (int64_t)blockIdx.x * d);
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int i = threadIdx.x + c * kNormBwdThreads;
+    if (i < n4) part[i] = gacc[c];
+  }
+}
+
+// Row partition of the RMSNorm backward (and of the bias column sums): two
+// CTAs per SM (two 512-thread CTAs up to d = 4096, two 256-thread CTAs up to
+// d = 8192, one beyond), each summing the gain gradient of its rows.
 int rmsnorm_bwd_parts(int64_t rows, int d) {
-  const int sms = num_sms();
-  const int p = ((int64_t)4 * sms * d <= (int64_t)SF_STATIC_SCRATCH_FLOATS) ? 4 * sms : 2 * sms;
+  (void)d;
+  const int p = 2 * num_sms();
   return rows < p ? (int)(rows > 0 ? rows : 1) : p;
 }
 
 void rmsnorm_bwd(const float* x, const __nv_bfloat16* g, const float* rstd, const float* dy,
                  const float* dres, float* dx, __nv_bfloat16* dxb, float* dg_part, int parts,
                  int64_t rows, int d, cudaStream_t st) {
+  if (d <= 2 * 4 * kNormBwdThreads) {
+    if (d <= 4 * kNormBwdThreads)
+      rmsnorm_bwd_hold_kernel<1><<<parts, kNormBwdThreads, 0, st>>>(x, g, rstd, dy, dres, dx, dxb,
+                                                                     dg_part, rows, d);
+    else
+      rmsnorm_bwd_hold_kernel<2><<<parts, kNormBwdThreads, 0, st>>>(x, g, rstd, dy, dres, dx, dxb,
+                                                                     dg_part, rows, d);
+    return;
+  }
   const int need = (d / 4 + kNormThreads - 1) / kNormThreads;  // float4 chunks per thread
 #define SF_NORM_BWD(CH) \
   rmsnorm_bwd_kernel<CH><<<parts, kNormThreads, 0, st>>>(x, g, rstd, dy, dres, dx, dxb, dg_part, rows, d)
-  if (need <= 1) SF_NORM_BWD(1);
-  else if (need <= 2) SF_NORM_BWD(2);
-  else if (need <= 4) SF_NORM_BWD(4);
-  else if (need <= 8) SF_NORM_BWD(8);
+  if (need <= 8) SF_NORM_BWD(8);
   else if (need <= 12) SF_NORM_BWD(12);
   else SF_NORM_BWD(16);
 #undef SF_NORM_BWD
 }
 
-// out[j] = bf16(sum_p part[p, j])   (fixed order: deterministic)
-__global__ void reduce_parts_kernel(const float* __restrict__ part, int parts, int d,
-                                    __nv_bfloat16* __restrict__ out) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
+// out[j] = sum_p part[p, j] over the partials [parts, d], in a fixed order
+// (deterministic).  A CTA takes 32 columns with 8 warps: warp w sums the
+// partials w, w + 8, w + 16, ... of its lane's column (each warp reads 128
+// contiguous bytes per partial), then the eight sums are added in warp order.
+constexpr int kRedWarps = 8;
+
+template <typename OUT>
+__global__ void __launch_bounds__(32 * kRedWarps)
+    reduce_parts_kernel(const float* __restrict__ part, int parts, int d, OUT* __restrict__ out,
+                        float scale) {
+  __shared__ float sh[kRedWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int p = 0; p < parts; ++p) s += part[(int64_t)p * d + j];
-  out[j] = __float2bfloat16_rn(s);
+  if (j < d) {
+    int p = w;
+#pragma unroll 4
+    for (; p < parts; p += kRedWarps) s += part[(int64_t)p * d + j];
+  }
+  sh[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && j < d) {
+    float t = sh[0][lane];
+#pragma unroll
+    for (int k = 1; k < kRedWarps; ++k) t += sh[k][lane];
+    if constexpr (sizeof(OUT) == 2 && std::is_same<OUT, __half>::value)
+      out[j] = __float2half_rn(t * scale);
+    else
+      out[j] = __float2bfloat16_rn(t);
+  }
 }
 
 void reduce_parts_bf16(const float* part, int parts, int d, __nv_bfloat16* out, cudaStream_t st) {
-  reduce_parts_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d, out);
-}
-
-__global__ void reduce_parts_f16_kernel(const float* __restrict__ part, int parts, int d,
-                                        __half* __restrict__ out, float scale) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
-  float s = 0.f;
-  for (int p = 0; p < parts; ++p) s += part[(int64_t)p * d + j];
-  out[j] = __float2half_rn(s * scale);
+  reduce_parts_kernel<__nv_bfloat16><<<(d + 31) / 32, 32 * kRedWarps, 0, st>>>(part, parts, d, out, 1.f);
 }
 
 void reduce_parts_f16(const float* part, int parts, int d, uint16_t* out, float scale,
                       cudaStream_t st) {
-  reduce_parts_f16_kernel<<<(d + 255) / 256, 256, 0, st>>>(part, parts, d,
-                                                            reinterpret_cast<__half*>(out), scale);
+  reduce_parts_kernel<__half><<<(d + 31) / 32, 32 * kRedWarps, 0, st>>>(
+      part, parts, d, reinterpret_cast<__half*>(out), scale);
 }
 
 // Column sums of x [rows, cols] bf16 (row stride ld) as fp32 partials:
@@ -377,44 +478,42 @@ void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16*
 }
 
 // ------------------------------------------------------------------ cross-entropy rows
-// One CTA per logits row (bf16, in place):  lse by an online max / sum-exp
-// pass, then dz = (exp(z - lse) - [v == label]) * inv_n written over z; rows
-// whose label is ignore (-100) get dz = 0 and loss 0.
+// One CTA per row of fp32 logits: lse by an online max / sum-exp pass, then
+// dz = (exp(z - lse) - [v == label]) * inv_n as bf16 into its own buffer (the
+// operand of the dH and dW products); rows whose label is ignore (-100) get
+// dz = 0 and loss 0.  The second pass re-reads the row, mostly from L2.
 constexpr int kCeThreads = 512;
 
 __global__ void __launch_bounds__(kCeThreads)
-    ce_rows_kernel(__nv_bfloat16* __restrict__ z, const int32_t* __restrict__ labels, int64_t vocab,
-                   float inv_n, float* __restrict__ loss_rows) {
+    ce_rows_f32_kernel(const float* __restrict__ z, __nv_bfloat16* __restrict__ dz,
+                       const int32_t* __restrict__ labels, int64_t vocab, float inv_n,
+                       float* __restrict__ loss_rows) {
   __shared__ float shm[32], shs[32];
   const int64_t row = blockIdx.x;
-  __nv_bfloat16* zr = z + row * vocab;
+  const float4* zr = reinterpret_cast<const float4*>(z + row * vocab);
+  uint2* dr = reinterpret_cast<uint2*>(dz + row * vocab);
   const int label = labels[row];
-  const int64_t n8 = vocab >> 3;  // vocab % 8 == 0 (checked by the caller)
-  const uint4* zv = reinterpret_cast<const uint4*>(zr);
+  const int64_t n4 = vocab >> 2;  // vocab % 8 == 0 (checked by the caller)
   if (label < 0) {
-    uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) reinterpret_cast<uint4*>(zr)[i] = zero;
+    const uint2 zero = make_uint2(0, 0);
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) dr[i] = zero;
     if (threadIdx.x == 0) loss_rows[row] = 0.f;
     return;
   }
   float m = -FLT_MAX, s = 0.f;
-  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
-    float f[8];
-    unpack8(zv[i], f);
-    float lm = f[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) lm = fmaxf(lm, f[k]);
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 f = zr[i];
+    const float lm = fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w));
     if (lm > m) {
       s *= __expf(m - lm);
       m = lm;
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s += __expf(f[k] - m);
+    s += __expf(f.x - m) + __expf(f.y - m) + __expf(f.z - m) + __expf(f.w - m);
   }
   // combine (m, s) across the block
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  float wm = warp_max(m);
-  s *= __expf(m - wm);
+  const float wm = warp_max(m);
+  s = (m == -FLT_MAX) ? 0.f : s * __expf(m - wm);
   s = warp_sum(s);
   if (lane == 0) { shm[w] = wm; shs[w] = s; }
   __syncthreads();
@@ -423,26 +522,23 @@ __global__ void __launch_bounds__(kCeThreads)
   float bs = 0.f;
   for (int i = 0; i < nw; ++i) bs += shs[i] * __expf(shm[i] - bm);
   const float lse = bm + __logf(bs);
-  const float z_label = __bfloat162float(zr[label]);
-  __syncthreads();  // everyone has read zr[label] before it is overwritten
-  if (threadIdx.x == 0) loss_rows[row] = lse - z_label;
-  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
-    float f[8];
-    unpack8(zv[i], f);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float p = __expf(f[k] - lse);
-      if (i * 8 + k == label) p -= 1.f;
-      f[k] = p * inv_n;
-    }
-    reinterpret_cast<uint4*>(zr)[i] = pack8(f);
+  if (threadIdx.x == 0) loss_rows[row] = lse - z[row * vocab + label];
+  for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 f = zr[i];
+    float p[4] = {__expf(f.x - lse), __expf(f.y - lse), __expf(f.z - lse), __expf(f.w - lse)};
+    const int64_t k = label - i * 4;
+    if (k >= 0 && k < 4) p[k] -= 1.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(p[0] * inv_n, p[1] * inv_n);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(p[2] * inv_n, p[3] * inv_n);
+    dr[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
 }
 
-void ce_rows(__nv_bfloat16* z, const int32_t* labels, int64_t rows, int64_t vocab, float inv_n,
-             float* loss_rows, cudaStream_t st) {
+void ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
+                 int64_t vocab, float inv_n, float* loss_rows, cudaStream_t st) {
   if (rows <= 0) return;
-  ce_rows_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, labels, vocab, inv_n, loss_rows);
+  ce_rows_f32_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, dz, labels, vocab, inv_n,
+                                                            loss_rows);
 }
 
 // ------------------------------------------------------------------ reductions / casts

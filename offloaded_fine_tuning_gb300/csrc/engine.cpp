@@ -203,15 +203,16 @@ struct sf_ctx {
   bool xoff = false;        // sliding activations: checkpoints live in pinned host memory
   float* x_pin = nullptr;   // [L][Tmax * d] host copies of the checkpoints
   cudaEvent_t ev_xused[4] = {}, ev_xfree[4] = {}, ev_xready[4] = {};
-  bf16 *u = nullptr, *qkv = nullptr, *o = nullptr, *w2 = nullptr, *ab = nullptr, *mb = nullptr;
+  bf16 *u = nullptr, *qkv = nullptr, *o = nullptr, *w2 = nullptr, *mb = nullptr;
+  float* ab32 = nullptr;  // gate and up outputs [T, 2F] fp32, kept for the SwiGLU backward
   float *rstd1 = nullptr, *rstd2 = nullptr, *rstdf = nullptr, *lse = nullptr, *h = nullptr;
   float *dX = nullptr, *dw2 = nullptr, *dh = nullptr, *du = nullptr, *dq_acc = nullptr,
         *delta = nullptr, *dg_part = nullptr;
-  bf16 *dXb = nullptr, *dm = nullptr, *dab = nullptr, *dhb = nullptr, *dob = nullptr,
-       *dqkv = nullptr;
+  bf16 *dXb = nullptr, *dab = nullptr, *dhb = nullptr, *dob = nullptr, *dqkv = nullptr;
   bf16 *hf = nullptr, *Wlm = nullptr, *gf = nullptr, *dWlm16 = nullptr, *dgf = nullptr,
-       *logits = nullptr, *x0b = nullptr;
-  float *dhf = nullptr, *dWlm32 = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
+       *dz = nullptr, *x0b = nullptr;
+  // one chunk of fp32 logits, and its bf16 dZ
+  float *zf = nullptr, *dhf = nullptr, *dWlm32 = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
   float2* rope_cs = nullptr;
   int32_t* labels_dev = nullptr;
   int* dev_err = nullptr;
@@ -913,7 +914,7 @@ struct Timed {
   double flops;
   cudaEvent_t b = nullptr, e = nullptr;
   cudaStream_t st;
-  // kind: 0 GEMM, 1 attention, 2 layer forward, 3 layer backward, 4 gradient D2H
+  // kind: 0 GEMM, 1 attention, 2 layer forward, 3 layer backward, 4 gradient D2H, 5 head
   Timed(sf_ctx* c, int k, double f, cudaStream_t s = nullptr)
       : ctx(c), kind(k), flops(f), st(s ? s : c->sC) {
     if (!ctx->timing) return;
@@ -934,18 +935,13 @@ struct Timed {
   }
 };
 
-int gemm(sf_ctx* ctx, int layout, int epi, int64_t M, int64_t N, int64_t K, const void* A,
-         int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R = nullptr,
-         int64_t ldr = 0, float alpha = 1.f, const void* bias = nullptr) {
-  sf::GemmArgs g;
-  g.layout = layout; g.epi = epi; g.M = M; g.N = N; g.K = K;
-  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.R = R; g.ldr = ldr;
-  g.alpha = alpha;
-  g.bias = bias;
+// A GEMM with the fused epilogues' extra arguments (flops: the algorithmic
+// count when it is not 2*M*N*K, e.g. the gated tile's two products).
+int gemm_args(sf_ctx* ctx, const sf::GemmArgs& g, double flops = 0.0) {
   int st;
   char why[128] = {0};
   {
-    Timed t(ctx, 0, 2.0 * M * N * K);
+    Timed t(ctx, 0, flops > 0.0 ? flops : 2.0 * g.M * g.N * g.K);
     st = sf::gemm(g, ctx->dev_err, ctx->sC, why);
   }
   ctx->launches += 1;
@@ -956,6 +952,17 @@ int gemm(sf_ctx* ctx, int layout, int epi, int64_t M, int64_t N, int64_t K, cons
     return st == -3 ? SF_ECUDA : SF_EINVAL;
   }
   return SF_OK;
+}
+
+int gemm(sf_ctx* ctx, int layout, int epi, int64_t M, int64_t N, int64_t K, const void* A,
+         int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, const float* R = nullptr,
+         int64_t ldr = 0, float alpha = 1.f, const void* bias = nullptr) {
+  sf::GemmArgs g;
+  g.layout = layout; g.epi = epi; g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.R = R; g.ldr = ldr;
+  g.alpha = alpha;
+  g.bias = bias;
+  return gemm_args(ctx, g);
 }
 
 double attn_fwd_flops(int64_t B, int64_t S, int64_t Hq, int64_t hd) {
@@ -1005,19 +1012,24 @@ void grad_parts(sf_ctx* c, int d, bf16* out) {
 
 // Forward of one layer from X_l (fp32) to X_{l+1}; with `full == false` the
 // final down projection is skipped (recompute for the backward needs only the
-// intermediates).
+// intermediates).  keep_ab stores the gate and up outputs in fp32 for the
+// SwiGLU backward (the recompute, and the last layer, whose backward follows
+// the head without a recompute).
 int layer_forward(sf_ctx* c, const LayerW& w, const float* Xin, float* Xout, int B, int S,
-                  bool full) {
+                  bool full, bool keep_ab) {
   sf_ctx* ctx = c;
   const int64_t T = (int64_t)B * S, d = c->d, F = c->F;
   const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
   sf::rmsnorm_fwd(Xin, w.g1, c->u, c->rstd1, T, (int)d, c->cfg.rms_eps, c->sC);
-  if (w.bqkv)  // projection biases, added to the fp32 accumulator before RoPE
-    RET(gemm(c, sf::kNT, sf::kEpiBF16Bias, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim,
-             nullptr, 0, 1.f, w.bqkv));
-  else
-    RET(gemm(c, sf::kNT, sf::kEpiBF16, T, c->qkvdim, d, c->u, d, w.wqkv, d, c->qkv, c->qkvdim));
-  sf::rope_inplace(c->qkv, c->qkvdim, T, S, Hq + Hkv, hd, c->rope_cs, 0, c->sC);
+  {
+    // Q/K/V projection; its epilogue adds the biases (if any) to the fp32
+    // accumulator, rotates the Q and K heads and rounds to bf16 once
+    sf::GemmArgs g;
+    g.layout = sf::kNT; g.epi = sf::kEpiQKV; g.M = T; g.N = c->qkvdim; g.K = d;
+    g.A = c->u; g.lda = d; g.B = w.wqkv; g.ldb = d; g.C = c->qkv; g.ldc = c->qkvdim;
+    g.bias = w.bqkv; g.cs = c->rope_cs; g.seq = S; g.rope_cols = (int)((Hq + Hkv) * hd); g.hd = hd;
+    RET(gemm_args(c, g));
+  }
   {
     Timed t(c, 1, attn_fwd_flops(B, S, Hq, hd));
     if (sf::attn_fwd(c->qkv, c->o, c->lse, B, S, Hq, Hkv, hd, c->dev_err, c->sC) != 0) {
@@ -1028,9 +1040,16 @@ int layer_forward(sf_ctx* c, const LayerW& w, const float* Xin, float* Xout, int
   RET(gemm(c, sf::kNT, sf::kEpiF32Add, T, d, c->qdim, c->o, c->qdim, w.wo, c->qdim, c->h, d,
            Xin, d));
   sf::rmsnorm_fwd(c->h, w.g2, c->w2, c->rstd2, T, (int)d, c->cfg.rms_eps, c->sC);
-  RET(gemm(c, sf::kNT, sf::kEpiBF16, T, 2 * F, d, c->w2, d, w.wgu, d, c->ab, 2 * F));
-  sf::swiglu_fwd(c->ab, c->mb, T, (int)F, c->sC);
-  c->launches += 5;
+  {
+    // gate/up projection; its epilogue forms m = silu(a) * b from the fp32
+    // accumulator (and keeps a, b in fp32 when the backward needs them)
+    sf::GemmArgs g;
+    g.layout = sf::kNT; g.epi = sf::kEpiGLU; g.M = T; g.N = F; g.K = d;
+    g.A = c->w2; g.lda = d; g.B = w.wgu; g.ldb = d; g.C = c->mb; g.ldc = F;
+    if (keep_ab) { g.aux = c->ab32; g.ldaux = 2 * F; }
+    RET(gemm_args(c, g, 2.0 * T * 2 * F * d));
+  }
+  c->launches += 3;
   if (full)
     RET(gemm(c, sf::kNT, sf::kEpiF32Add, T, d, F, c->mb, F, w.wd, F, Xout, d, c->h, d));
   return SF_OK;
@@ -1042,10 +1061,10 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   sf_ctx* ctx = c;
   const int64_t T = (int64_t)B * S, d = c->d, F = c->F;
   const int Hq = c->cfg.n_heads, Hkv = c->cfg.n_kv_heads, hd = c->cfg.head_dim;
-  // down projection: X_{l+1} = h + m Wd^T
-  RET(gemm(c, sf::kNN, sf::kEpiBF16, T, F, d, c->dXb, d, w.wd, F, c->dm, F));
+  // down projection: X_{l+1} = h + m Wd^T.  dm = dX Wd stays in the fp32
+  // accumulator: the epilogue takes it through SwiGLU into [da | db]
+  RET(gemm(c, sf::kNN, sf::kEpiGLUBwd, T, F, d, c->dXb, d, w.wd, F, c->dab, 2 * F, c->ab32, 2 * F));
   RET(gemm(c, sf::kTN, c->gepi(), d, F, T, c->dXb, d, c->mb, F, g.wd, F, nullptr, 0, c->gscale()));
-  sf::swiglu_bwd(c->dm, c->ab, c->dab, T, (int)F, c->sC);
   // gate/up projection from w2 = RMSNorm(h; g2)
   RET(gemm(c, sf::kNN, sf::kEpiF32, T, d, 2 * F, c->dab, 2 * F, w.wgu, d, c->dw2, d));
   RET(gemm(c, sf::kTN, c->gepi(), 2 * F, d, T, c->dab, 2 * F, c->w2, d, g.wgu, d, nullptr, 0,
@@ -1081,7 +1100,7 @@ int layer_backward(sf_ctx* c, const LayerW& w, const LayerG& g, const float* Xin
   sf::rmsnorm_bwd(Xin, w.g1, c->rstd1, c->du, c->dh, c->dX, c->dXb, c->dg_part, c->dg_parts, T,
                   (int)d, c->sC);
   grad_parts(c, (int)d, g.g1);
-  c->launches += 8;  // swiglu, 2 norm, 2 reduce, 3 attention (GEMMs are counted in gemm())
+  c->launches += 7;  // 2 norm, 2 reduce, 3 attention (GEMMs are counted in gemm())
   return SF_OK;
 }
 
@@ -1094,23 +1113,41 @@ int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
   const float inv_n = n_valid > 0 ? 1.f / (float)n_valid : 0.f;
   for (int64_t r0 = 0; r0 < T; r0 += c->chunk_rows) {
     const int64_t n = std::min(c->chunk_rows, T - r0);
-    RET(gemm(c, sf::kNT, sf::kEpiBF16, n, V, d, c->hf + r0 * d, d, c->Wlm, d, c->logits, V));
-    sf::ce_rows(c->logits, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0, c->sC);
-    RET(gemm(c, sf::kNN, sf::kEpiF32, n, d, V, c->logits, V, c->Wlm, d, c->dhf + r0 * d, d));
-    RET(gemm(c, sf::kTN, r0 == 0 ? sf::kEpiF32 : sf::kEpiF32Acc, V, d, n, c->logits, V,
-             c->hf + r0 * d, d, c->dWlm32, d));
+    const bool first = r0 == 0, last = r0 + n >= T;
+    // fp32 logits of the chunk; the row softmax writes dZ (bf16) beside them
+    RET(gemm(c, sf::kNT, sf::kEpiF32, n, V, d, c->hf + r0 * d, d, c->Wlm, d, c->zf, V));
+    sf::ce_rows_f32(c->zf, c->dz, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0, c->sC);
+    RET(gemm(c, sf::kNN, sf::kEpiF32, n, d, V, c->dz, V, c->Wlm, d, c->dhf + r0 * d, d));
+    // dW_lm: fp32 sums over the chunks; the last chunk's product adds the sum
+    // and rounds the bf16 gradient in its epilogue
+    if (last && !c->f16g)
+      RET(gemm(c, sf::kTN, sf::kEpiBF16Acc, V, d, n, c->dz, V, c->hf + r0 * d, d, c->dWlm16, d,
+               first ? nullptr : c->dWlm32, d));
+    else
+      RET(gemm(c, sf::kTN, first ? sf::kEpiF32 : sf::kEpiF32Acc, V, d, n, c->dz, V,
+               c->hf + r0 * d, d, c->dWlm32, d));
     c->launches += 1;
   }
   sf::sum_f32(c->loss_rows, T, inv_n, c->loss_dev, c->sC);
   sf::rmsnorm_bwd(XL, c->gf, c->rstdf, c->dhf, nullptr, c->dX, c->dXb, c->dg_part, c->dg_parts,
                   T, (int)d, c->sC);
   grad_parts(c, (int)d, c->dgf);
-  if (c->f16g)
+  c->launches += 4;
+  if (c->f16g) {
     sf::cast_f32_f16(c->dWlm32, reinterpret_cast<uint16_t*>(c->dWlm16), V * d, c->lscale, c->sC);
-  else
-    sf::cast_f32_bf16(c->dWlm32, c->dWlm16, V * d, c->sC);
-  c->launches += 5;
+    c->launches += 1;
+  }
   return SF_OK;
+}
+
+// Rows of one chunk of the fused LM head: a chunk holds fp32 logits and their
+// bf16 dZ (6 bytes per logit) within 2 GiB, in equal chunks of a multiple of
+// 128 rows (at the 8B shape: 6 chunks of 2816 rows, 2.2 GB).
+int64_t lce_chunk_rows(int64_t T, int64_t V) {
+  const int64_t cap = std::max<int64_t>(128, (((int64_t)2 << 30) / (6 * V)) / 128 * 128);
+  const int64_t chunks = (T + cap - 1) / cap;
+  const int64_t rows = ((T + chunks - 1) / chunks + 127) / 128 * 128;
+  return std::min<int64_t>(rows, T);
 }
 
 size_t unit_numel_cfg(const sf_config* c, int32_t unit) {
@@ -1192,9 +1229,7 @@ int init(sf_ctx* ctx) {
   if (cf.lce_chunk_rows > 0) {
     ctx->chunk_rows = std::min<int64_t>(cf.lce_chunk_rows, T);
   } else {
-    int64_t c = ((int64_t)1 << 30) / (2 * V);
-    c = std::max<int64_t>(128, c / 128 * 128);
-    ctx->chunk_rows = std::min<int64_t>(c, T);
+    ctx->chunk_rows = lce_chunk_rows(T, V);
   }
   ctx->dg_parts = sf::rmsnorm_bwd_parts(T, (int)d);
 
@@ -1214,7 +1249,7 @@ int init(sf_ctx* ctx) {
   ok = ok && dalloc(ctx, &ctx->X, (ctx->xoff ? 4 : L + 1) * T * d);
   ok = ok && dalloc(ctx, &ctx->u, T * d) && dalloc(ctx, &ctx->qkv, T * ctx->qkvdim) &&
        dalloc(ctx, &ctx->o, T * ctx->qdim) && dalloc(ctx, &ctx->w2, T * d) &&
-       dalloc(ctx, &ctx->ab, T * 2 * F) && dalloc(ctx, &ctx->mb, T * F) &&
+       dalloc(ctx, &ctx->ab32, T * 2 * F) && dalloc(ctx, &ctx->mb, T * F) &&
        dalloc(ctx, &ctx->rstd1, T) && dalloc(ctx, &ctx->rstd2, T) && dalloc(ctx, &ctx->rstdf, T) &&
        dalloc(ctx, &ctx->lse, T * cf.n_heads) && dalloc(ctx, &ctx->h, T * d);
   ok = ok && dalloc(ctx, &ctx->dX, T * d) && dalloc(ctx, &ctx->dw2, T * d) &&
@@ -1223,12 +1258,13 @@ int init(sf_ctx* ctx) {
        dalloc(ctx, &ctx->delta, T * cf.n_heads) &&
        dalloc(ctx, &ctx->dg_part, (int64_t)ctx->dg_parts * std::max(d, ctx->qkvdim)) &&
        dalloc(ctx, &ctx->dXb, T * d) &&
-       dalloc(ctx, &ctx->dm, T * F) && dalloc(ctx, &ctx->dab, T * 2 * F) &&
+       dalloc(ctx, &ctx->dab, T * 2 * F) &&
        dalloc(ctx, &ctx->dhb, T * d) && dalloc(ctx, &ctx->dob, T * ctx->qdim) &&
        dalloc(ctx, &ctx->dqkv, T * ctx->qkvdim);
   ok = ok && dalloc(ctx, &ctx->hf, T * d) && dalloc(ctx, &ctx->Wlm, V * d) &&
        dalloc(ctx, &ctx->gf, round_up(d, A)) && dalloc(ctx, &ctx->dWlm16, V * d) &&
-       dalloc(ctx, &ctx->dgf, round_up(d, A)) && dalloc(ctx, &ctx->logits, ctx->chunk_rows * V) &&
+       dalloc(ctx, &ctx->dgf, round_up(d, A)) && dalloc(ctx, &ctx->zf, ctx->chunk_rows * V) &&
+       dalloc(ctx, &ctx->dz, ctx->chunk_rows * V) &&
        dalloc(ctx, &ctx->x0b, T * d) && dalloc(ctx, &ctx->dhf, T * d) &&
        dalloc(ctx, &ctx->dWlm32, V * d) && dalloc(ctx, &ctx->loss_rows, T) &&
        dalloc(ctx, &ctx->loss_dev, 1) && dalloc(ctx, &ctx->labels_dev, T) &&
@@ -1476,7 +1512,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     if (ctx->xoff && l + 1 >= 4) CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_xfree[(l + 1) % 4], 0));
     {
       Timed tl(ctx, 2, 0.0);
-      RET(layer_forward(ctx, slot_w(ctx, s), Xin, Xout, B, S, true));
+      RET(layer_forward(ctx, slot_w(ctx, s), Xin, Xout, B, S, true, l == L - 1));
     }
     CK(cudaEventRecord(ctx->ev_free[s], ctx->sC));
     if (ctx->xoff) {  // the checkpoint slides to the host while the next layers compute
@@ -1491,7 +1527,10 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
 
   // ---- A10: fused LM head + cross-entropy, forward and backward
   CK(cudaStreamWaitEvent(ctx->sC, ctx->ev_lm, 0));
-  RET(head_fwd_bwd(ctx, T, n_valid_total));
+  {
+    Timed th(ctx, 5, 0.0);
+    RET(head_fwd_bwd(ctx, T, n_valid_total));
+  }
   CK(cudaEventRecord(ctx->ev_head, ctx->sC));
   // sliding: bring checkpoint l back into slot l % 4 once that slot's last user
   // is done (the head for the slot of X_L, else the backward of layer l + 4)
@@ -1523,7 +1562,7 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
     // the last layer's intermediates are still in the workspace from the forward
     {
       Timed tl(ctx, 3, 0.0);
-      if (l != L - 1) RET(layer_forward(ctx, w, Xin, nullptr, B, S, false));
+      if (l != L - 1) RET(layer_forward(ctx, w, Xin, nullptr, B, S, false, true));
       RET(layer_backward(ctx, w, slot_g(ctx, s), Xin, B, S));
     }
     CK(cudaEventRecord(ctx->ev_grads[s], ctx->sC));
@@ -1594,9 +1633,15 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
       ctx->stats.fwd_layer_ms += x / L;
     } else if (ctx->t_kind[i] == 3) {
       ctx->stats.bwd_layer_ms += x / L;
+    } else if (ctx->t_kind[i] == 5) {
+      ctx->stats.head_ms += x;
     } else {
       ctx->stats.d2h_layer_ms += x / L;
     }
+  }
+  if (ctx->timing) {
+    ctx->stats.compute_ms = L * (ctx->stats.fwd_layer_ms + ctx->stats.bwd_layer_ms) + ctx->stats.head_ms;
+    ctx->stats.exposed_ms = std::max(0.0, ctx->stats.step_ms - ctx->stats.compute_ms);
   }
   {
     std::lock_guard<std::mutex> l(ctx->aq_m);
@@ -1954,8 +1999,7 @@ int sf_lce_step(sf_ctx* ctx, const uint16_t* h, const uint16_t* w, const int32_t
     }
   }
   if (ctx && cudaSetDevice(ctx->cfg.device) != cudaSuccess) return SF_ECUDA;
-  int64_t chunk = ((int64_t)1 << 30) / (2 * (int64_t)v);
-  chunk = std::min<int64_t>(n, std::max<int64_t>(128, chunk / 128 * 128));
+  const int64_t chunk = lce_chunk_rows(n, v);
   const int64_t ws = sf_op_lce_workspace_bytes(n, v, chunk);
   void *dH = nullptr, *dW = nullptr, *dLab = nullptr, *dLoss = nullptr, *dDh = nullptr,
        *dDw = nullptr, *dWs = nullptr, *dDh16 = nullptr;

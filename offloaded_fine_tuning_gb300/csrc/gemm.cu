@@ -42,8 +42,17 @@ struct GemmParams {
   int64_t ldr;
   float alpha;
   int* err;
-  const __nv_bfloat16* bias;  // kEpiBF16Bias: one value per output column
+  const __nv_bfloat16* bias;  // kEpiBF16Bias, kEpiQKV: one value per output column (or null)
+  const float2* cs;           // kEpiQKV: (cos, sin) [seq, hd/2]
+  int seq, rope_cols, hd;
+  float* aux;                 // kEpiGLU: fp32 a | b (or null)
+  int64_t ldaux;
 };
+
+// Output columns of one work unit: the gated tile computes a and b for 128
+// output columns in its 256 accumulator columns.
+template <int BN, int EPI>
+__host__ __device__ constexpr int unit_cols() { return EPI == kEpiGLU ? BN / 2 : BN; }
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -75,11 +84,133 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 32 bf16 values to c[0..32): four 16-byte stores when the row has all of
+// them and c is aligned, else one per column below n.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* c, const float (&y)[32], int n) {
+  if (n >= 32 && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 v;
+      v.x = pack_bf16x2(y[8 * q + 0], y[8 * q + 1]);
+      v.y = pack_bf16x2(y[8 * q + 2], y[8 * q + 3]);
+      v.z = pack_bf16x2(y[8 * q + 4], y[8 * q + 5]);
+      v.w = pack_bf16x2(y[8 * q + 6], y[8 * q + 7]);
+      reinterpret_cast<uint4*>(c)[q] = v;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) c[j] = __float2bfloat16_rn(y[j]);
+  }
+}
+
+__device__ __forceinline__ void store_f32x32(float* c, const float (&y)[32], int n) {
+  if (n >= 32 && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      reinterpret_cast<float4*>(c)[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) c[j] = y[j];
+  }
+}
+
+__device__ __forceinline__ void load_f32x32(const float* c, float (&y)[32], int n) {
+  if (n >= 32 && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = reinterpret_cast<const float4*>(c)[q];
+      y[4 * q] = v.x; y[4 * q + 1] = v.y; y[4 * q + 2] = v.z; y[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] = j < n ? c[j] : 0.f;
+  }
+}
+
+// y[j] += bias[col + j] for the columns below n (bias 64-byte aligned, col % 32 == 0)
+__device__ __forceinline__ void add_bias32(float (&y)[32], const __nv_bfloat16* bias, int n) {
+  if (n >= 32) {
+    const uint4* b4 = reinterpret_cast<const uint4*>(bias);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = b4[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        y[8 * q + 2 * k] += __uint_as_float(w[k] << 16);
+        y[8 * q + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) y[j] += __bfloat162float(bias[j]);
+  }
+}
+
+// The Q/K/V projection's epilogue for 32 rotation pairs of one head: x1 holds
+// the accumulator columns [col1, col1 + 32), x2 the columns 
+// [col1 + hd/2, ...) of the same head; pair index jp = first pair's index j.
+__device__ __forceinline__ void epi_qkv_pairs(const GemmParams& p, int row, int col1, int jp,
+                                              const uint32_t (&r1)[32], const uint32_t (&r2)[32]) {
+  const int half = p.hd >> 1;
+  const int col2 = col1 + half;
+  float x1[32], x2[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    x1[j] = __uint_as_float(r1[j]) * p.alpha;
+    x2[j] = __uint_as_float(r2[j]) * p.alpha;
+  }
+  if (p.bias) {  // added before the rotation, in fp32
+    add_bias32(x1, p.bias + col1, 32);
+    add_bias32(x2, p.bias + col2, 32);
+  }
+  if (col1 < p.rope_cols) {
+    const int s = row % p.seq;
+    const float4* t = reinterpret_cast<const float4*>(p.cs + (int64_t)s * half + jp);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 c = t[q];  // (cos, sin) of pairs jp + 2q and jp + 2q + 1
+      const float a0 = x1[2 * q], b0 = x2[2 * q], a1 = x1[2 * q + 1], b1 = x2[2 * q + 1];
+      x1[2 * q] = a0 * c.x - b0 * c.y;
+      x2[2 * q] = b0 * c.x + a0 * c.y;
+      x1[2 * q + 1] = a1 * c.z - b1 * c.w;
+      x2[2 * q + 1] = b1 * c.z + a1 * c.w;
+    }
+  }
+  __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc;
+  store_bf16x32(c + col1, x1, 32);
+  store_bf16x32(c + col2, x2, 32);
+}
+
+// The gate/up projection's SwiGLU epilogue for output columns [j, j + 32):
+// ra holds a (gate), rb holds b (up).
+__device__ __forceinline__ void epi_glu(const GemmParams& p, int row, int j,
+                                        const uint32_t (&ra)[32], const uint32_t (&rb)[32]) {
+  const int n = min(32, p.N - j);
+  float a[32], b[32], m[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    a[k] = __uint_as_float(ra[k]) * p.alpha;
+    b[k] = __uint_as_float(rb[k]) * p.alpha;
+    m[k] = a[k] / (1.f + __expf(-a[k])) * b[k];
+  }
+  store_bf16x32(reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + j, m, n);
+  if (p.aux) {
+    float* x = p.aux + (int64_t)row * p.ldaux + j;
+    store_f32x32(x, a, n);
+    store_f32x32(x + p.N, b, n);
+  }
+}
+
 // Store 32 accumulator columns [col, col+32) of one output row.
 template <int EPI>
 __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
                                           const uint32_t (&r)[32]) {
   const float a = p.alpha;
+  const float a_ = a;
   const bool full = (col + 32 <= p.N);
   if constexpr (EPI == kEpiBF16 || EPI == kEpiBF16Bias) {
     __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
@@ -120,6 +251,30 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
       for (int j = 0; j < 32; ++j)
         if (col + j < p.N) c[j] = __float2bfloat16_rn(y[j]);
     }
+  } else if constexpr (EPI == kEpiGLUBwd) {
+    // dm = alpha*acc; a, b from the forward (fp32); da | db as bf16
+    const int n = min(32, p.N - col);
+    const float* ar = p.R + (int64_t)row * p.ldr + col;
+    float a[32], b[32], da[32], db[32];
+    load_f32x32(ar, a, n);
+    load_f32x32(ar + p.N, b, n);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float g = __uint_as_float(r[j]) * a_;
+      const float sg = 1.f / (1.f + __expf(-a[j]));
+      da[j] = g * b[j] * sg * (1.f + a[j] * (1.f - sg));
+      db[j] = g * a[j] * sg;
+    }
+    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
+    store_bf16x32(c, da, n);
+    store_bf16x32(c + p.N, db, n);
+  } else if constexpr (EPI == kEpiBF16Acc) {
+    const int n = min(32, p.N - col);
+    float y[32];
+    if (p.R) load_f32x32(p.R + (int64_t)row * p.ldr + col, y, n);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]) * a_ + (p.R ? y[j] : 0.f);
+    store_bf16x32(reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col, y, n);
   } else if constexpr (EPI == kEpiF16) {
     __half* c = reinterpret_cast<__half*>(p.C) + (int64_t)row * p.ldc + col;
     if (full && ((reinterpret_cast<uintptr_t>(c) & 15) == 0)) {
@@ -172,8 +327,14 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
 template <bool A_MN, bool B_MN, int BN, int EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
+  // the gated tile: the cluster's two CTAs load the gate rows (tmB) and the
+  // up rows (tmB2) of the same 128 output columns
+  constexpr bool GATED = (EPI == kEpiGLU);
+  static_assert(!GATED || (CL == 2 && BN == 256 && !B_MN), "gated tiles: 2-CTA clusters, K-major B");
+  constexpr int UC = unit_cols<BN, EPI>();
   using Cfg = GemmCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
@@ -215,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (GATED) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -229,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // work units: CL M-tiles of one N-tile, one per CTA of the cluster
   const int num_m = (p.M + kBM - 1) / kBM;
   const int num_mu = (num_m + CL - 1) / CL;
-  const int num_n = (p.N + BN - 1) / BN;
+  const int num_n = (p.N + UC - 1) / UC;
   const int num_units = num_mu * num_n;
   const int unit0 = (int)blockIdx.x / CL, unit_step = (int)gridDim.x / CL;
   const int nk = (p.K + kBK - 1) / kBK;
@@ -269,6 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = crank * (HB / 64); j < (crank + 1) * (HB / 64); ++j)
               tma_load_2d_mc(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0, kPair);
+          } else if constexpr (GATED) {
+            tma_load_2d_mc(b_dst + crank * HB * 128, crank ? &tmB2 : &tmB, full_bar(stage), k0,
+                           tn * UC, kPair);
           } else {
             tma_load_2d_mc(b_dst + crank * HB * 128, &tmB, full_bar(stage), k0, n0 + crank * HB, kPair);
           }
@@ -356,13 +521,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row = tm * kBM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      for (int c = 0; c < BN; c += 32) {
-        const int col = tn * BN + c;
-        if (col >= p.N) break;  // uniform across the warp
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c, r);
-        tmem_ld_wait();
-        if (row < p.M) epi_store<EPI>(p, row, col, r);
+      if constexpr (EPI == kEpiQKV) {
+        // head by head: the pair (j, j + hd/2) meets in one thread
+        const int half = p.hd >> 1;
+        for (int h0 = 0; h0 < BN; h0 += p.hd) {
+          const int col0 = tn * BN + h0;
+          if (col0 >= p.N) break;  // uniform across the warp
+          for (int j = 0; j < half; j += 32) {
+            uint32_t r1[32], r2[32];
+            tmem_ld_32x32b_x32(taddr + h0 + j, r1);
+            tmem_ld_32x32b_x32(taddr + h0 + half + j, r2);
+            tmem_ld_wait();
+            if (row < p.M) epi_qkv_pairs(p, row, col0 + j, j, r1, r2);
+          }
+        }
+      } else if constexpr (GATED) {
+        // accumulator columns [0, 128): a; [128, 256): b, for the same outputs
+        for (int c = 0; c < UC; c += 32) {
+          const int col = tn * UC + c;
+          if (col >= p.N) break;
+          uint32_t ra[32], rb[32];
+          tmem_ld_32x32b_x32(taddr + c, ra);
+          tmem_ld_32x32b_x32(taddr + UC + c, rb);
+          tmem_ld_wait();
+          if (row < p.M) epi_glu(p, row, col, ra, rb);
+        }
+      } else {
+        for (int c = 0; c < BN; c += 32) {
+          const int col = tn * BN + c;
+          if (col >= p.N) break;  // uniform across the warp
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_wait();
+          if (row < p.M) epi_store<EPI>(p, row, col, r);
+        }
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
@@ -410,22 +602,39 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t row
 // CTAs per cluster: pairs that share the B tile for the wide tiles.
 constexpr int gemm_cluster(int BN) { return BN == 256 ? 2 : 1; }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+constexpr int kMaxDevices = 64;
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return -1;
   }
-  return n;
+  return dev;
+}
+
+// SM count of the current device, looked up once per device.
+int num_sms() {
+  static int n[kMaxDevices] = {0};
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  if (n[dev] == 0) {  // idempotent: racing threads store the same value
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      v = 1;
+    }
+    n[dev] = v;
+  }
+  return n[dev];
 }
 
 template <bool A_MN, bool B_MN, int BN, int EPI>
-static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                    cudaStream_t st, char* why) {
+static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                    const GemmParams& p, cudaStream_t st, char* why) {
   using Cfg = GemmCfg<BN>;
   constexpr int CL = gemm_cluster(BN);
+  constexpr int UC = unit_cols<BN, EPI>();
   auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, CL>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -438,25 +647,39 @@ static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPara
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_ctas = 0;  // per instantiation: CTAs that can be resident at once
-  if (max_ctas == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess) {
-      snprintf(why, 64, "gemm: cannot reserve %d B shared memory", Cfg::SMEM);
-      return -3;
-    }
-    int clusters = 0;
-    cfg.gridDim = dim3(CL * num_sms());
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
-      cudaGetLastError();
-      snprintf(why, 64, "gemm: no resident cluster of %d CTAs", CL);
-      return -3;
-    }
-    max_ctas = clusters * CL < num_sms() ? clusters * CL : num_sms() / CL * CL;
+  // per instantiation and device: the shared-memory attribute is set and the
+  // number of CTAs that can be resident at once is found on first use there
+  static int max_ctas[kMaxDevices] = {0};
+  static std::mutex mu;
+  const int dev = current_device();
+  if (dev < 0) {
+    snprintf(why, 64, "gemm: no current device");
+    return -3;
   }
-  const int units = ((p.M + kBM * CL - 1) / (kBM * CL)) * ((p.N + BN - 1) / BN);
-  cfg.gridDim = dim3(units * CL < max_ctas ? units * CL : max_ctas);
-  cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  int ctas;
+  {
+    std::lock_guard<std::mutex> l(mu);
+    if (max_ctas[dev] == 0) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        snprintf(why, 64, "gemm: cannot reserve %d B shared memory", Cfg::SMEM);
+        return -3;
+      }
+      int clusters = 0;
+      cfg.gridDim = dim3(CL * num_sms());
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        snprintf(why, 64, "gemm: no resident cluster of %d CTAs", CL);
+        return -3;
+      }
+      max_ctas[dev] = clusters * CL < num_sms() ? clusters * CL : num_sms() / CL * CL;
+    }
+    ctas = max_ctas[dev];
+  }
+  const int units = ((p.M + kBM * CL - 1) / (kBM * CL)) * ((p.N + UC - 1) / UC);
+  cfg.gridDim = dim3(units * CL < ctas ? units * CL : ctas);
+  cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(why, 64, "gemm launch: %s", cudaGetErrorString(e));
@@ -466,23 +689,37 @@ static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPara
 }
 
 template <bool A_MN, bool B_MN, int BN>
-static int launch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                      cudaStream_t st, char* why) {
+static int launch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb,
+                      const CUtensorMap& tb2, const GemmParams& p, cudaStream_t st, char* why) {
   switch (epi) {
-    case kEpiBF16: return launch_t<A_MN, B_MN, BN, kEpiBF16>(ta, tb, p, st, why);
-    case kEpiF32: return launch_t<A_MN, B_MN, BN, kEpiF32>(ta, tb, p, st, why);
-    case kEpiF32Add: return launch_t<A_MN, B_MN, BN, kEpiF32Add>(ta, tb, p, st, why);
-    case kEpiF32Acc: return launch_t<A_MN, B_MN, BN, kEpiF32Acc>(ta, tb, p, st, why);
+    case kEpiBF16: return launch_t<A_MN, B_MN, BN, kEpiBF16>(ta, tb, tb2, p, st, why);
+    case kEpiF32: return launch_t<A_MN, B_MN, BN, kEpiF32>(ta, tb, tb2, p, st, why);
+    case kEpiF32Add: return launch_t<A_MN, B_MN, BN, kEpiF32Add>(ta, tb, tb2, p, st, why);
+    case kEpiF32Acc: return launch_t<A_MN, B_MN, BN, kEpiF32Acc>(ta, tb, tb2, p, st, why);
     case kEpiBF16Bias:  // forward projections only (Y = X W^T + b)
-      if constexpr (!A_MN && !B_MN) return launch_t<A_MN, B_MN, BN, kEpiBF16Bias>(ta, tb, p, st, why);
+      if constexpr (!A_MN && !B_MN) return launch_t<A_MN, B_MN, BN, kEpiBF16Bias>(ta, tb, tb2, p, st, why);
+      break;
+    case kEpiQKV:  // the Q/K/V projection with its rotation
+      if constexpr (!A_MN && !B_MN) return launch_t<A_MN, B_MN, BN, kEpiQKV>(ta, tb, tb2, p, st, why);
+      break;
+    case kEpiGLU:  // the gate/up projection with SwiGLU: 256-column gated tiles only
+      if constexpr (!A_MN && !B_MN && BN == 256) return launch_t<A_MN, B_MN, BN, kEpiGLU>(ta, tb, tb2, p, st, why);
+      break;
+    case kEpiGLUBwd:  // the down projection's input gradient through SwiGLU
+      if constexpr (!A_MN && B_MN) return launch_t<A_MN, B_MN, BN, kEpiGLUBwd>(ta, tb, tb2, p, st, why);
       break;
     case kEpiF16:  // weight gradients only (dW = dY^T X)
-      if constexpr (A_MN && B_MN) return launch_t<A_MN, B_MN, BN, kEpiF16>(ta, tb, p, st, why);
+      if constexpr (A_MN && B_MN) return launch_t<A_MN, B_MN, BN, kEpiF16>(ta, tb, tb2, p, st, why);
+      break;
+    case kEpiBF16Acc:  // the last chunk of a summed weight gradient
+      if constexpr (A_MN && B_MN) return launch_t<A_MN, B_MN, BN, kEpiBF16Acc>(ta, tb, tb2, p, st, why);
       break;
   }
   snprintf(why, 64, "gemm: bad epilogue %d", epi);
   return -1;
 }
+
+static bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int gemm_check(const GemmArgs& a, char* why) {
   if (a.M == 0 || a.N == 0) return 0;
@@ -490,22 +727,23 @@ int gemm_check(const GemmArgs& a, char* why) {
     snprintf(why, 64, "gemm: bad sizes");
     return -1;
   }
-  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiF16 ||
-      (a.epi == kEpiBF16Bias && a.layout != kNT) || (a.epi == kEpiF16 && a.layout != kTN)) {
+  const int need_layout[] = {-1, -1, -1, -1, kNT, kTN, kNT, kNT, kNN, kTN};
+  if (a.layout < kNT || a.layout > kTN || a.epi < kEpiBF16 || a.epi > kEpiBF16Acc ||
+      (need_layout[a.epi] >= 0 && a.layout != need_layout[a.epi])) {
     snprintf(why, 64, "gemm: bad layout %d or epilogue %d", a.layout, a.epi);
     return -1;
   }
-  if (!a.A || !a.B || !a.C || (a.epi == kEpiF32Add && !a.R) || (a.epi == kEpiBF16Bias && !a.bias)) {
+  if (!a.A || !a.B || !a.C || (a.epi == kEpiF32Add && !a.R) || (a.epi == kEpiBF16Bias && !a.bias) ||
+      (a.epi == kEpiGLUBwd && !a.R) || (a.epi == kEpiQKV && !a.cs)) {
     snprintf(why, 64, "gemm: null operand");
     return -1;
   }
-  if (a.epi == kEpiBF16Bias && (reinterpret_cast<uintptr_t>(a.bias) & 63)) {
+  if ((a.epi == kEpiBF16Bias || a.epi == kEpiQKV) && a.bias && !al(a.bias, 64)) {
     snprintf(why, 64, "gemm: bias must be 64-byte aligned");
     return -1;
   }
   // TMA: 16-byte aligned bases and row strides.
-  if ((reinterpret_cast<uintptr_t>(a.A) & 15) || (reinterpret_cast<uintptr_t>(a.B) & 15) ||
-      (a.lda % 8) || (a.ldb % 8)) {
+  if (!al(a.A, 16) || !al(a.B, 16) || (a.lda % 8) || (a.ldb % 8)) {
     snprintf(why, 64, "gemm: operands must be 16-byte aligned");
     return -1;
   }
@@ -513,9 +751,27 @@ int gemm_check(const GemmArgs& a, char* why) {
   const bool b_mn = (a.layout == kNN || a.layout == kTN);
   // row extents of the stored matrices must fit their leading dimensions
   const int64_t a_cols = a_mn ? a.M : a.K, b_cols = b_mn ? a.N : a.K;
-  if (a.lda < a_cols || a.ldb < b_cols || a.ldc < a.N || (a.epi == kEpiF32Add && a.ldr < a.N)) {
+  const bool reads_r = a.epi == kEpiF32Add || a.epi == kEpiGLUBwd || (a.epi == kEpiBF16Acc && a.R);
+  const int64_t r_cols = a.epi == kEpiGLUBwd ? 2 * a.N : a.N;
+  const int64_t c_cols = a.epi == kEpiGLUBwd ? 2 * a.N : a.N;
+  if (a.lda < a_cols || a.ldb < b_cols || a.ldc < c_cols || (reads_r && a.ldr < r_cols)) {
     snprintf(why, 64, "gemm: leading dimension too small");
     return -1;
+  }
+  if (a.epi == kEpiQKV) {
+    if ((a.hd != 64 && a.hd != 128) || a.seq < 1 || a.N % a.hd || a.rope_cols < 0 ||
+        a.rope_cols % a.hd || a.rope_cols > a.N || a.ldc % 8 || !al(a.C, 16) || !al(a.cs, 16)) {
+      snprintf(why, 64, "gemm: bad rotation arguments");
+      return -1;
+    }
+  }
+  if (a.epi == kEpiGLU || a.epi == kEpiGLUBwd) {
+    // the gated tile holds 2 x 128 columns; SwiGLU halves sit N apart
+    if (a.N % 8 || (a.epi == kEpiGLU && a.aux && (a.ldaux < 2 * a.N || a.ldaux % 4 || !al(a.aux, 16))) ||
+        (a.epi == kEpiGLUBwd && (a.ldr % 4 || !al(a.R, 16)))) {
+      snprintf(why, 64, "gemm: bad SwiGLU arguments");
+      return -1;
+    }
   }
   return 0;
 }
@@ -525,27 +781,35 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   if (int c = gemm_check(a, why)) return c;
   const bool a_mn = (a.layout == kTN);
   const bool b_mn = (a.layout == kNN || a.layout == kTN);
-  const int BN = (a.N > 128) ? 256 : 128;
-  CUtensorMap ta, tb;
+  const bool gated = (a.epi == kEpiGLU);
+  const int BN = (gated || a.N > 128) ? 256 : 128;
+  CUtensorMap ta, tb, tb2;
   bool ok = a_mn ? make_map(&ta, a.A, a.M, a.K, a.lda, 64, 64)
                  : make_map(&ta, a.A, a.K, a.M, a.lda, 64, kBM);
-  // with clusters each CTA loads half of a K-major B tile
+  // with clusters each CTA loads half of a K-major B tile; the gated tile's
+  // halves are the gate rows [0, N) and the up rows [N, 2N) of B
   ok = ok && (b_mn ? make_map(&tb, a.B, a.N, a.K, a.ldb, 64, 64)
                    : make_map(&tb, a.B, a.K, a.N, a.ldb, 64, BN / gemm_cluster(BN)));
+  if (gated)
+    ok = ok && make_map(&tb2, static_cast<const __nv_bfloat16*>(a.B) + a.N * a.ldb, a.K, a.N,
+                        a.ldb, 64, BN / gemm_cluster(BN));
+  else
+    tb2 = tb;
   if (!ok) {
     snprintf(why, 64, "gemm: tensor map encode failed");
     return -3;
   }
   GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err,
-               reinterpret_cast<const __nv_bfloat16*>(a.bias)};
+               reinterpret_cast<const __nv_bfloat16*>(a.bias), a.cs, a.seq, a.rope_cols, a.hd,
+               a.aux, a.ldaux};
   if (BN == 256) {
-    if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, p, st, why);
-    if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, p, st, why);
-    return launch_epi<true, true, 256>(a.epi, ta, tb, p, st, why);
+    if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, tb2, p, st, why);
+    if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, tb2, p, st, why);
+    return launch_epi<true, true, 256>(a.epi, ta, tb, tb2, p, st, why);
   }
-  if (a.layout == kNT) return launch_epi<false, false, 128>(a.epi, ta, tb, p, st, why);
-  if (a.layout == kNN) return launch_epi<false, true, 128>(a.epi, ta, tb, p, st, why);
-  return launch_epi<true, true, 128>(a.epi, ta, tb, p, st, why);
+  if (a.layout == kNT) return launch_epi<false, false, 128>(a.epi, ta, tb, tb2, p, st, why);
+  if (a.layout == kNN) return launch_epi<false, true, 128>(a.epi, ta, tb, tb2, p, st, why);
+  return launch_epi<true, true, 128>(a.epi, ta, tb, tb2, p, st, why);
 }
 
 }  // namespace sf

@@ -202,9 +202,10 @@ int sf_op_swiglu_bwd(const uint16_t* dm, const uint16_t* ab, uint16_t* dab, int6
 int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows) {
   if (n < 1 || v < 8 || chunk_rows < 1) return -1;
   const int64_t c = chunk_rows < n ? chunk_rows : n;
-  const int64_t logits = (c * v * 2 + 255) / 256 * 256;
+  const int64_t logits = (c * v * 4 + 255) / 256 * 256;  // fp32 logits of a chunk
+  const int64_t dz = (c * v * 2 + 255) / 256 * 256;      // their bf16 dZ
   const int64_t rows = (n * 4 + 255) / 256 * 256;
-  return logits + rows;
+  return logits + dz + rows;
 }
 
 int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64_t n, int32_t d,
@@ -218,9 +219,12 @@ int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64
   int* err = dev_err_word();
   if (!err) return SF_ECUDA;
   const int64_t c = chunk_rows < n ? chunk_rows : n;
-  bf16* logits = reinterpret_cast<bf16*>(workspace);
-  float* loss_rows = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) +
-                                              (c * v * 2 + 255) / 256 * 256);
+  char* ws = reinterpret_cast<char*>(workspace);
+  float* zf = reinterpret_cast<float*>(ws);
+  ws += (c * v * 4 + 255) / 256 * 256;
+  bf16* dz = reinterpret_cast<bf16*>(ws);
+  ws += (c * v * 2 + 255) / 256 * 256;
+  float* loss_rows = reinterpret_cast<float*>(ws);
   const bf16* H = reinterpret_cast<const bf16*>(h);
   const bf16* W = reinterpret_cast<const bf16*>(w);
   const float inv_n = n_valid > 0 ? 1.f / (float)n_valid : 0.f;
@@ -229,21 +233,61 @@ int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64
   for (int64_t r0 = 0; r0 < n; r0 += c) {
     const int64_t rows = (c < n - r0) ? c : n - r0;
     sf::GemmArgs z;
-    z.layout = sf::kNT; z.epi = sf::kEpiBF16; z.M = rows; z.N = v; z.K = d;
-    z.A = H + r0 * d; z.lda = d; z.B = W; z.ldb = d; z.C = logits; z.ldc = v;
+    z.layout = sf::kNT; z.epi = sf::kEpiF32; z.M = rows; z.N = v; z.K = d;
+    z.A = H + r0 * d; z.lda = d; z.B = W; z.ldb = d; z.C = zf; z.ldc = v;
     if (sf::gemm(z, err, st, why) != 0) return SF_ECUDA;
-    sf::ce_rows(logits, labels + r0, rows, v, inv_n, loss_rows + r0, st);
+    sf::ce_rows_f32(zf, dz, labels + r0, rows, v, inv_n, loss_rows + r0, st);
     sf::GemmArgs gx;
     gx.layout = sf::kNN; gx.epi = sf::kEpiF32; gx.M = rows; gx.N = d; gx.K = v;
-    gx.A = logits; gx.lda = v; gx.B = W; gx.ldb = d; gx.C = dh + r0 * d; gx.ldc = d;
+    gx.A = dz; gx.lda = v; gx.B = W; gx.ldb = d; gx.C = dh + r0 * d; gx.ldc = d;
     if (sf::gemm(gx, err, st, why) != 0) return SF_ECUDA;
     sf::GemmArgs gw;
     gw.layout = sf::kTN; gw.epi = r0 == 0 ? sf::kEpiF32 : sf::kEpiF32Acc; gw.M = v; gw.N = d;
-    gw.K = rows; gw.A = logits; gw.lda = v; gw.B = H + r0 * d; gw.ldb = d; gw.C = dw; gw.ldc = d;
+    gw.K = rows; gw.A = dz; gw.lda = v; gw.B = H + r0 * d; gw.ldb = d; gw.C = dw; gw.ldc = d;
     if (sf::gemm(gw, err, st, why) != 0) return SF_ECUDA;
   }
   sf::sum_f32(loss_rows, n, inv_n, loss, st);
   return launched();
+}
+
+// The fused-epilogue projections: argument checks in sf::gemm_check.
+static int run_gemm(const sf::GemmArgs& g, cudaStream_t st) {
+  char why[128];
+  if (sf::gemm_check(g, why) != 0) return SF_EINVAL;
+  if (g.M == 0 || g.N == 0) return SF_OK;
+  int* err = dev_err_word();
+  if (!err) return SF_ECUDA;
+  const int rc = sf::gemm(g, err, st, why);
+  if (rc == -1) return SF_EINVAL;
+  return rc == 0 ? SF_OK : SF_ECUDA;
+}
+
+int sf_op_gemm_qkv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                   int64_t ldb, uint16_t* C, int64_t ldc, const uint16_t* bias, const float* table,
+                   int32_t seq, int32_t rope_cols, int32_t head_dim, void* stream) {
+  sf::GemmArgs g;
+  g.layout = sf::kNT; g.epi = sf::kEpiQKV; g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc; g.bias = bias;
+  g.cs = reinterpret_cast<const float2*>(table); g.seq = seq; g.rope_cols = rope_cols; g.hd = head_dim;
+  return run_gemm(g, S(stream));
+}
+
+int sf_op_gemm_swiglu(int64_t M, int64_t F, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, uint16_t* m, int64_t ldm, float* ab,
+                      int64_t ldab, void* stream) {
+  sf::GemmArgs g;
+  g.layout = sf::kNT; g.epi = sf::kEpiGLU; g.M = M; g.N = F; g.K = K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = m; g.ldc = ldm; g.aux = ab; g.ldaux = ldab;
+  return run_gemm(g, S(stream));
+}
+
+int sf_op_gemm_swiglu_bwd(int64_t M, int64_t F, int64_t K, const void* dy, int64_t lddy,
+                          const void* wd, int64_t ldw, const float* ab, int64_t ldab,
+                          uint16_t* dab, int64_t lddab, void* stream) {
+  sf::GemmArgs g;
+  g.layout = sf::kNN; g.epi = sf::kEpiGLUBwd; g.M = M; g.N = F; g.K = K;
+  g.A = dy; g.lda = lddy; g.B = wd; g.ldb = ldw; g.C = dab; g.ldc = lddab; g.R = ab; g.ldr = ldab;
+  return run_gemm(g, S(stream));
 }
 
 int sf_op_device_error(int32_t* out) {

@@ -15,8 +15,22 @@ enum GemmLayout : int { kNT = 0, kNN = 1, kTN = 2 };
 // Epilogues: C bf16 = alpha*acc | C f32 = alpha*acc | C f32 = R + alpha*acc | C f32 += alpha*acc
 // | C bf16 = alpha*acc + bias[col] (bias bf16 [N], 64-byte aligned; layout kNT only)
 // | C fp16 = alpha*acc (layout kTN only: scaled fp16 weight gradients)
+// | kEpiQKV (layout kNT): y = alpha*acc (+ bias[col] when bias != null), then the
+//   rotary embedding on the columns below rope_cols (heads of hd columns, pair
+//   (j, j + hd/2), position row % seq, (cos, sin) from cs[pos * hd/2 + j]) and
+//   one bf16 rounding: the Q/K/V projection with its rotation
+// | kEpiGLU (layout kNT): B holds 2N rows, [Bg; Bu]; a = alpha*A Bg^T and
+//   b = alpha*A Bu^T share one accumulator tile, C bf16 [M, N] = silu(a) * b;
+//   when aux != null, a and b are also stored as fp32: aux[r, j] = a,
+//   aux[r, N + j] = b (the SwiGLU forward of the gate/up projection)
+// | kEpiGLUBwd (layout kNN): dm = alpha*acc, with a = R[r, j], b = R[r, N + j]
+//   (fp32) C[r, j] = bf16(dm b s (1 + a (1 - s))), C[r, N + j] = bf16(dm a s),
+//   s = sigmoid(a) (the down projection's input gradient through SwiGLU)
+// | kEpiBF16Acc (layout kTN): C bf16 = alpha*acc + R (R fp32, may be null):
+//   the last of a chunked sum of weight gradients, rounded once
 enum GemmEpi : int {
-  kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3, kEpiBF16Bias = 4, kEpiF16 = 5
+  kEpiBF16 = 0, kEpiF32 = 1, kEpiF32Add = 2, kEpiF32Acc = 3, kEpiBF16Bias = 4, kEpiF16 = 5,
+  kEpiQKV = 6, kEpiGLU = 7, kEpiGLUBwd = 8, kEpiBF16Acc = 9
 };
 
 struct GemmArgs {
@@ -31,7 +45,13 @@ struct GemmArgs {
   const float* R = nullptr;
   int64_t ldr = 0;
   float alpha = 1.f;
-  const void* bias = nullptr;  // kEpiBF16Bias
+  const void* bias = nullptr;  // kEpiBF16Bias; kEpiQKV (optional)
+  // kEpiQKV: rotation table (cos, sin) [seq, hd/2], columns [0, rope_cols) rotated
+  const float2* cs = nullptr;
+  int seq = 0, rope_cols = 0, hd = 0;
+  // kEpiGLU: optional fp32 copy of the gate and up outputs, row stride ldaux
+  float* aux = nullptr;
+  int64_t ldaux = 0;
 };
 
 // Returns 0, or a negative status with a message in `why` (64 chars at least).
@@ -60,12 +80,15 @@ void bias_grad_f16(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, f
                    int parts, uint16_t* out, float scale, cudaStream_t st);
 void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
                   int head_dim, const float2* cs, int inverse, cudaStream_t st);
+// The fused cross-entropy rows on fp32 logits z [rows, vocab]: lse by an
+// online max / sum-exp, loss_rows[r] = lse - z[r, label] (0 when ignored) and
+// dz [rows, vocab] bf16 = (softmax(z) - onehot) * inv_n (0 on ignored rows).
+void ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
+                 int64_t vocab, float inv_n, float* loss_rows, cudaStream_t st);
 void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn,
                 cudaStream_t st);
 void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16* dab,
                 int64_t rows, int ffn, cudaStream_t st);
-void ce_rows(__nv_bfloat16* z, const int32_t* labels, int64_t rows, int64_t vocab,
-             float inv_n, float* loss_rows, cudaStream_t st);
 void sum_f32(const float* x, int64_t n, float scale, float* out, cudaStream_t st);
 void cast_f32_bf16(const float* x, __nv_bfloat16* y, int64_t n, cudaStream_t st);
 // y = fp16(scale * x)

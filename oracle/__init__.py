@@ -23,6 +23,9 @@ Parity status per function (all pinned; see tests/test_oracle_pins.py):
                    gradient rows sum to zero, ignored rows zero
   step             pinned: torch autograd of an independently assembled model,
                    central finite differences in float64
+  step_streamed    the same step with layer weights fetched one at a time
+                   (step is built on it; pinned through step, and equal to
+                   step bit for bit)
   adam_update      pinned: torch.optim.AdamW step, first-step closed form
   adam_update_bf16_states
                    pinned: unbiased stochastic rounding (mean over many
@@ -33,5 +36,5 @@ Parity status per function (all pinned; see tests/test_oracle_pins.py):
 from .llama_step import (  # noqa: F401
     IGNORE_INDEX, bf16_round, rmsnorm_fwd, rmsnorm_bwd, rope_tables, rope_fwd, rope_bwd,
     attention_fwd, attention_bwd, swiglu_fwd, swiglu_bwd, cross_entropy_fwd_bwd,
-    layer_fwd, layer_bwd, step, adam_update, ModelWeights,
+    layer_fwd, layer_bwd, step, step_streamed, adam_update, ModelWeights,
     lowbias32, sr_key, sr_bits, bf16_round_stochastic, adam_update_bf16_states)

@@ -256,31 +256,55 @@ def step(w: ModelWeights, tokens, labels, cfg, dtype=np.float64, return_hidden=F
     (w.lm_head None) grads["lm_head"] is None and grads["embed"] holds both
     uses of the embedding.  With return_hidden the per-layer inputs X_l, the
     final hidden states and the logits are returned too."""
+    cast = lambda a: np.asarray(a, dtype=dtype)
+    layers = [{k: cast(v) for k, v in lp.items()} for lp in w.layers]
+    return step_streamed(lambda i: layers[i], len(layers), w.embed, w.final_norm, w.lm_head,
+                         tokens, labels, cfg, dtype=dtype, return_hidden=return_hidden)
+
+
+def step_streamed(get_layer, n_layers, embed, final_norm, lm_head, tokens, labels, cfg,
+                  dtype=np.float64, on_layer_grads=None, return_hidden=False):
+    """step() with the decoder layers' weights fetched one layer at a time:
+    get_layer(i) returns layer i's weight dict (called once in the forward and
+    once in the backward), so only the activations of the stack are held, not
+    all of its weights.  When on_layer_grads is given, layer i's gradients go
+    to on_layer_grads(i, grads) as the backward produces them (and
+    grads["layers"] is None); otherwise they are collected as in step()."""
     tokens = np.asarray(tokens)
     B, S = tokens.shape
     T, d = B * S, cfg.hidden
     cast = lambda a: np.asarray(a, dtype=dtype)
-    layers = [{k: cast(v) for k, v in lp.items()} for lp in w.layers]
-    E, gf = cast(w.embed), cast(w.final_norm)
-    tied = w.lm_head is None
-    Wlm = E if tied else cast(w.lm_head)
+    E, gf = cast(embed), cast(final_norm)
+    tied = lm_head is None
+    Wlm = E if tied else cast(lm_head)
     cos, sin = rope_tables(S, cfg.head_dim, cfg.rope_base, dtype)
 
     x = E[tokens]                                  # [B, S, d]
     xs, caches = [], []
-    for p in layers:
+    for i in range(n_layers):
+        p = {k: cast(v) for k, v in get_layer(i).items()}
         xs.append(x)
         x, c = layer_fwd(x, p, cfg, cos, sin)
         caches.append(c)
+        del p
     hf, cf = rmsnorm_fwd(x.reshape(T, d), gf, cfg.rms_eps)
     z = hf @ Wlm.T
     loss, dz, _ = cross_entropy_fwd_bwd(z, labels)
 
     g_lm = dz.T @ hf
     dx, g_gf = rmsnorm_bwd(dz @ Wlm, gf, cf)
-    g_layers = [None] * len(layers)
-    for i in range(len(layers) - 1, -1, -1):
-        dx, g_layers[i] = layer_bwd(dx, layers[i], caches[i], cfg, cos, sin)
+    if not return_hidden:
+        del z, dz
+    g_layers = None if on_layer_grads else [None] * n_layers
+    for i in range(n_layers - 1, -1, -1):
+        p = {k: cast(v) for k, v in get_layer(i).items()}
+        dx, g = layer_bwd(dx, p, caches[i], cfg, cos, sin)
+        caches[i] = None
+        del p
+        if on_layer_grads:
+            on_layer_grads(i, g)
+        else:
+            g_layers[i] = g
     g_E = np.zeros_like(E)
     np.add.at(g_E, tokens.reshape(T), dx)
     if tied:  # one tensor used twice: its gradient is the sum of both uses

@@ -27,25 +27,35 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ backward
-// delta[b, h, s] = sum_j dO[t, h*hd + j] * O[t, h*hd + j]   (one warp per row)
+// delta[b, h, s] = sum_j dO[t, h*hd + j] * O[t, h*hd + j]: TPR = hd / 8
+// threads per (token, head) row, each reading 16 bytes of O and of dO, summed
+// across the row's threads with shuffles.  Consecutive rows are consecutive
+// heads of a token, so a warp reads contiguous memory.
+template <int TPR>
 __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
-                                  float* __restrict__ delta, int64_t rows, int S, int Hq, int hd) {
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= rows) return;
-  const int64_t t = w / Hq;
-  const int h = (int)(w % Hq);
-  const bf16* orow = o + t * (int64_t)Hq * hd + (int64_t)h * hd;
-  const bf16* drow = dout + t * (int64_t)Hq * hd + (int64_t)h * hd;
+                                  float* __restrict__ delta, int64_t rows, int S, int Hq) {
+  constexpr int HD = TPR * 8;
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t w = g / TPR;
+  const int sub = (int)(g % TPR);
   float acc = 0.f;
-  for (int j = lane * 2; j < hd; j += 64) {
-    float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(orow + j));
-    float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(drow + j));
-    acc += a.x * c.x + a.y * c.y;
+  if (w < rows) {  // no early return: every lane takes part in the shuffles
+    const int64_t off = w * HD + sub * 8;  // row w = t * Hq + h starts at t*Hq*hd + h*hd
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 c = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(c2[i]);
+      acc += x.x * y.x + x.y * y.y;
+    }
   }
 #pragma unroll
-  for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
-  if (lane == 0) {
+  for (int k = TPR / 2; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+  if (sub == 0 && w < rows) {
+    const int64_t t = w / Hq;
+    const int h = (int)(w % Hq);
     const int64_t b = t / S, s = t % S;
     delta[(b * Hq + h) * S + s] = acc;
   }
@@ -108,7 +118,12 @@ __global__ void attn_dq_kernel(const float* __restrict__ dq_acc, bf16* __restric
 void attn_delta(const bf16* o, const bf16* dout, float* delta, int B, int S, int Hq, int hd,
                 cudaStream_t st) {
   const int64_t rows = (int64_t)B * S * Hq;
-  attn_delta_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, rows, S, Hq, hd);
+  const int64_t threads = rows * (hd / 8);
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (hd == 128)
+    attn_delta_kernel<16><<<grid, 256, 0, st>>>(o, dout, delta, rows, S, Hq);
+  else
+    attn_delta_kernel<8><<<grid, 256, 0, st>>>(o, dout, delta, rows, S, Hq);
 }
 
 void attn_dq_finalize(const float* dq_acc, bf16* dqkv, int B, int S, int Hq, int Hkv, int hd,

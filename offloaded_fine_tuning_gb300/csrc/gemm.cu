@@ -5,26 +5,32 @@
 //
 // Design (one persistent CTA per SM, 192 threads):
 //   warp 0      TMA producer: A and B tiles of BK = 64 into a STAGES-deep ring
-//   warp 1      MMA issuer: tcgen05.mma 128 x BN x 16 into a TMEM accumulator;
-//               also allocates / frees TMEM (512 columns = 2 accumulators)
+//   warp 1      MMA issuer: tcgen05.mma into a TMEM accumulator; also
+//               allocates / frees TMEM (512 columns = 2 accumulators)
 //   warps 2-5   epilogue: tcgen05.ld rows out of TMEM, convert, store
 // Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
-// tile i+1.  Tiles are visited in groups of 8 M-tiles so that the B panel of
-// a group stays in L2.
+// tile i+1.
 //
-// With BN = 256 the CTAs run in clusters of two that take M-tiles 2u and
-// 2u + 1 of the same N-tile: each loads its own A and half of the shared B
-// tile, which the TMA unit writes into both CTAs' shared memory (multicast),
-// and each MMA warp releases a stage in both CTAs.  The tensor cores waited
-// on operand loads for about a third of the main loop; this cuts the bytes
-// each SM requests per k-block from 48 KB to 32 KB.  All operands use the 128-byte swizzle: a K-major tile
-// is [rows][64] with 128-byte rows; an MN-major tile is a set of [64 K rows]
-// x [64 MN] boxes placed 8 KB apart.
+// Work units are visited in groups along M or N (tile_coords, unit_order), so
+// that the operand panels a group shares stay in L2.
+//
+// With BN = 256 the CTAs run in clusters of two that compute one 256 x 256
+// tile with cta_group::2 MMAs (M = 256 across the pair): each CTA loads its
+// own 128 rows of A and its half of B into its own shared memory (32 KB per
+// k-block instead of the 48 KB a 128 x 256 tile needs), the leader's MMA
+// warp issues for both SMs, whose tensor cores read A from their own shared
+// memory and B from both, and each CTA's TMEM holds its 128 rows of D.  With
+// half the operand bytes per SM in shared memory the ring has six stages, and
+// the GEMMs went from 0.87-0.91 to 0.94-0.99 of the measured cuBLAS burst
+// rate.  All operands use the 128-byte swizzle: a K-major tile is [rows][64]
+// with 128-byte rows; an MN-major tile is a set of [64 K rows] x [64 MN]
+// boxes placed 8 KB apart.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -47,6 +53,7 @@ struct GemmParams {
   int seq, rope_cols, hd;
   float* aux;                 // kEpiGLU: fp32 a | b (or null)
   int64_t ldaux;
+  int group;                  // work-unit order (tile_coords)
 };
 
 // Output columns of one work unit: the gated tile computes a and b for 128
@@ -58,25 +65,42 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
 
-template <int BN>
+// Shared memory of one CTA: STAGES x (A tile + B tile).  A pair of CTAs
+// under one cta_group::2 MMA holds half of the B tile in each CTA.
+template <int BN, bool PAIR = false>
 struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
+  static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : 6);
   static constexpr int BAR_OFF = STAGES * (A_BYTES + B_BYTES);
   // full[S], empty[S], tfull[2], tempty[2], drain; then tmem slot and abort flag
   static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn) {
-  constexpr int G = 8;
-  const int per_group = G * num_n;
-  const int group = tile / per_group;
-  const int first_m = group * G;
-  const int gsize = min(num_m - first_m, G);
-  const int r = tile % per_group;
-  tm = first_m + r % gsize;
-  tn = r / gsize;
+// Work-unit order.  Units are visited in groups: with group > 0, groups of
+// `group` M-units crossed with every N-tile (the group's A panels stay in L2
+// while the B panel streams through once per group); with group < 0, groups
+// of -group N-tiles crossed with every M-unit (the group's B panels stay in
+// L2 while A streams through once per group).  The host picks the side whose
+// re-reads cost fewer bytes, with the resident panels within a share of L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int& tm,
+                                            int& tn) {
+  if (group > 0) {
+    const int per_group = group * num_n;
+    const int first_m = (tile / per_group) * group;
+    const int gsize = min(num_m - first_m, group);
+    const int r = tile % per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+  } else {
+    const int g = -group;
+    const int per_group = g * num_m;
+    const int first_n = (tile / per_group) * g;
+    const int gsize = min(num_n - first_n, g);
+    const int r = tile % per_group;
+    tn = first_n + r % gsize;
+    tm = r / gsize;
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -324,22 +348,31 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, int row, int col,
   }
 }
 
+// CL == 2 (the 256-wide tiles): the two CTAs of a cluster run one
+// cta_group::2 MMA of 256 x BN: each loads its own 128 rows of A and half of
+// B into its own shared memory, both counted on the leader's (rank 0) full
+// barrier; the leader's MMA warp issues for the pair and its commits reach
+// both CTAs; each CTA's epilogue reads its own 128 rows from its own TMEM and
+// reports to the leader that the buffer is free.  CL == 1 (narrow tiles):
+// one CTA, one 128 x BN MMA.
 template <bool A_MN, bool B_MN, int BN, int EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
+  constexpr bool PAIR = (CL == 2);
+  static_assert(!PAIR || BN == 256, "pair MMAs: 256-wide tiles");
   // the gated tile: the cluster's two CTAs load the gate rows (tmB) and the
   // up rows (tmB2) of the same 128 output columns
   constexpr bool GATED = (EPI == kEpiGLU);
   static_assert(!GATED || (CL == 2 && BN == 256 && !B_MN), "gated tiles: 2-CTA clusters, K-major B");
   constexpr int UC = unit_cols<BN, EPI>();
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, PAIR>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
   constexpr uint32_t TMEM_COLS = 512;
-  constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = umma_idesc_bf16(PAIR ? 2 * kBM : kBM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -365,11 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // released by the MMA warp of every CTA of the cluster
+      mbar_init(empty_bar(s), 1);  // by the commit of the (pair's) MMA warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 128);
+      // pair: one arrival per epilogue warp of both CTAs, on the leader's barrier
+      mbar_init(tempty_bar(b), PAIR ? 8 : 128);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -379,11 +413,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (GATED) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  if constexpr (CL == 2) cluster_sync_all();  // the peer's barriers exist before its first multicast
+  if constexpr (CL == 2) cluster_sync_all();  // the peer's barriers exist before its first remote arrival
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -404,47 +443,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
       int tmu, tn;
-      tile_coords(unit, num_mu, num_n, tmu, tn);
+      tile_coords(unit, num_mu, num_n, p.group, tmu, tn);
       const int m0 = (tmu * CL + crank) * kBM, n0 = tn * BN;
       for (int kb = 0; kb < nk; ++kb) {
-        // free in every CTA of the cluster: this CTA's half of B lands in all of them
+        // the stage is free once the MMAs that read it (the pair's, for a pair) completed
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
         const int k0 = kb * kBK;
         const uint32_t a_dst = sA + stage * A_BYTES, b_dst = sB + stage * B_BYTES;
+        if constexpr (PAIR) {
+          // both CTAs' tiles count on the leader's full barrier
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (crank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_BYTES + B_BYTES));
+          if constexpr (A_MN) {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(a_dst + j * 8192, &tmA, fb, m0 + 64 * j, k0);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+          }
+          constexpr int HB = BN / 2;  // this CTA's half of B
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = 0; j < HB / 64; ++j)
+              tma_load_2d_pair(b_dst + j * 8192, &tmB, fb, n0 + crank * HB + 64 * j, k0);
+          } else if constexpr (GATED) {
+            tma_load_2d_pair(b_dst, crank ? &tmB2 : &tmB, fb, k0, tn * UC);
+          } else {
+            tma_load_2d_pair(b_dst, &tmB, fb, k0, n0 + crank * HB);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          continue;
+        }
+        mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
         if constexpr (A_MN) {
 #pragma unroll
           for (int j = 0; j < kBM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, full_bar(stage), m0 + 64 * j, k0);
         } else {
           tma_load_2d(a_dst, &tmA, full_bar(stage), k0, m0);
         }
-        if constexpr (CL == 1) {
-          if constexpr (B_MN) {
+        if constexpr (B_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0);
-          } else {
-            tma_load_2d(b_dst, &tmB, full_bar(stage), k0, n0);
-          }
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0);
         } else {
-          constexpr int HB = BN / 2;  // B rows (K-major) or columns (MN-major) per CTA
-          if constexpr (B_MN) {
-#pragma unroll
-            for (int j = crank * (HB / 64); j < (crank + 1) * (HB / 64); ++j)
-              tma_load_2d_mc(b_dst + j * 8192, &tmB, full_bar(stage), n0 + 64 * j, k0, kPair);
-          } else if constexpr (GATED) {
-            tma_load_2d_mc(b_dst + crank * HB * 128, crank ? &tmB2 : &tmB, full_bar(stage), k0,
-                           tn * UC, kPair);
-          } else {
-            tma_load_2d_mc(b_dst + crank * HB * 128, &tmB, full_bar(stage), k0, n0 + crank * HB, kPair);
-          }
+          tma_load_2d(b_dst, &tmB, full_bar(stage), k0, n0);
         }
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (ok) {
-      // every stage this CTA loaded has been released by both MMA warps, so no
-      // arrival from the peer is still on its way to this CTA's barriers
+      // every stage this CTA loaded has been released by the MMAs, so no
+      // arrival is still on its way to the barriers and no MMA reads the tiles
       const long n = issued < STAGES ? issued : STAGES;
       int st = stage;
       uint32_t ph = phase;
@@ -457,14 +506,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       record_error(p.err, kDevGemmTimeout);
       *abort_flag = 1;
-      // let the copies already issued land before the CTA's shared memory goes away
+      // let the copies already issued land before the CTA's shared memory goes
+      // away (a pair's loads count on the leader's barriers: the leader waits)
       const long n = issued < STAGES ? issued : STAGES;
-      for (long i = 0; i < n; ++i) {
-        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        mbar_wait(full_bar(stage), phase, nullptr);
+      if (!PAIR || crank == 0) {
+        for (long i = 0; i < n; ++i) {
+          if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+          mbar_wait(full_bar(stage), phase, nullptr);
+        }
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && (!PAIR || crank == 0)) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0;
     uint32_t phase = 0;
@@ -487,19 +539,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           else ad = smem_desc_sw128(a_base + k * 32, 16, 1024);
           if constexpr (B_MN) bd = smem_desc_sw128(b_base + k * 2048, 8192, 1024);
           else bd = smem_desc_sw128(b_base + k * 32, 16, 1024);
-          umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          else umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        if constexpr (CL == 2) umma_commit_mc(empty_bar(stage), kPair);
+        if constexpr (PAIR) umma_commit_pair(empty_bar(stage), kPair);
         else umma_commit(empty_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      umma_commit(tfull_bar(acc));
+      if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), kPair);
+      else umma_commit(tfull_bar(acc));
     }
     if (!ok) {
       record_error(p.err, kDevGemmTimeout);
       *abort_flag = 1;
-      umma_commit(drain_bar);
+      if constexpr (PAIR) umma_commit_pair(drain_bar, 0x1);
+      else umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, nullptr);
     }
   } else if (warp >= 2) {
@@ -508,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int iter = 0;
     for (int unit = unit0; unit < num_units; unit += unit_step, ++iter) {
       int tmu, tn;
-      tile_coords(unit, num_mu, num_n, tmu, tn);
+      tile_coords(unit, num_mu, num_n, p.group, tmu, tn);
       const int tm = tmu * CL + crank;
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
@@ -557,14 +612,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if constexpr (PAIR) {
+        // the leader's MMA warp reuses the buffer once both CTAs' warps are done
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+      } else {
+        mbar_arrive(tempty_bar(acc));
+      }
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    // the pair's MMAs read both CTAs' shared memory and write both TMEMs:
+    // neither CTA frees them before the other is done
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -599,7 +667,7 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t row
   return r == CUDA_SUCCESS;
 }
 
-// CTAs per cluster: pairs that share the B tile for the wide tiles.
+// CTAs per cluster: the wide tiles run as cta_group::2 pair MMAs.
 constexpr int gemm_cluster(int BN) { return BN == 256 ? 2 : 1; }
 
 constexpr int kMaxDevices = 64;
@@ -632,8 +700,8 @@ int num_sms() {
 template <bool A_MN, bool B_MN, int BN, int EPI>
 static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
                     const GemmParams& p, cudaStream_t st, char* why) {
-  using Cfg = GemmCfg<BN>;
   constexpr int CL = gemm_cluster(BN);
+  using Cfg = GemmCfg<BN, CL == 2>;
   constexpr int UC = unit_cols<BN, EPI>();
   auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, CL>;
   cudaLaunchConfig_t cfg = {};
@@ -776,6 +844,27 @@ int gemm_check(const GemmArgs& a, char* why) {
   return 0;
 }
 
+// The unit order of tile_coords.  By default groups of 8 M-units: the ~76
+// clusters that run at once then cover about 8 M-units x 9 N-tiles, a near
+// square window whose panels the L2 serves without hot spots.  Two cases do
+// better with a whole side resident in L2 (each of its panels then leaves
+// DRAM once), as measured at the step's shapes: all M-units in one group when
+// their A panels fit in 40 MB (the LM head's logits: -2%), and all N-tiles in
+// one group when there are at most 16 and their B panels fit (the output
+// projection and its dX product: -4 to -5%; the LM head's dW: -2%).  The Q/K/V
+// projection's 24 N-tiles make an all-N window of 3 x 24 that ran 3% slower
+// than groups of 8, and 16 panels of 50 MB in all (the Q/K/V dX product) 2%.
+static int unit_order(int64_t M, int64_t N, int64_t K, int BN, bool gated) {
+  const int64_t CL = gemm_cluster(BN);
+  const int64_t uc = gated ? BN / 2 : BN;
+  const int64_t num_mu = (M + kBM * CL - 1) / (kBM * CL), num_n = (N + uc - 1) / uc;
+  const int64_t a_unit = kBM * CL * K * 2, b_unit = (int64_t)BN * K * 2;  // bytes per unit panel
+  const int64_t budget = (int64_t)40 << 20;
+  if (num_mu > 8 && num_mu * a_unit <= budget) return (int)num_mu;
+  if (num_n <= 16 && num_n * b_unit <= budget && num_mu > 8) return -(int)num_n;
+  return 8;
+}
+
 int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   if (a.M == 0 || a.N == 0) return 0;
   if (int c = gemm_check(a, why)) return c;
@@ -801,7 +890,7 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   }
   GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err,
                reinterpret_cast<const __nv_bfloat16*>(a.bias), a.cs, a.seq, a.rope_cols, a.hd,
-               a.aux, a.ldaux};
+               a.aux, a.ldaux, unit_order(a.M, a.N, a.K, BN, gated)};
   if (BN == 256) {
     if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, tb2, p, st, why);
     if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, tb2, p, st, why);

@@ -55,6 +55,8 @@ GEMM_CASES = [
     (sf.TN, sf.EPI_F32, 1152, 1024, 2048),
     # more 2-CTA work units than clusters fit at once, an odd number of M-tiles
     (sf.NN, sf.EPI_BF16, 4224, 2560, 256),
+    # long M: units grouped along N (every N-tile's weight panel held in L2), ragged M
+    (sf.NT, sf.EPI_F32, 13000, 896, 4096),
 ]
 
 

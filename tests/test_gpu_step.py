@@ -488,27 +488,127 @@ def test_full_1p3b_step_properties():
         assert np.isfinite(a).all() and np.array_equal(a, b)
 
 
+def depth_tolerance(name):
+    """Per-tensor bounds of a whole-stack comparison at the workload's depth:
+    the stated bar (2e-2), or, where the bf16-operand rounding model (written
+    by tests/golden/make_bf16_depth_error.py from the oracle alone) already
+    moves the gradients by more, 1.25x that model's error.  The model rounds
+    only where any bf16 tensor-core path must (projection and attention
+    operands, P and dS, the gradient cast), so no storage choice of this path
+    sets the bound.  1.25 covers the scatter between two independent
+    realisations of the same rounding noise (this path's and the model's)."""
+    import json
+    import os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                       f"bf16_depth_error_{name}.json")))
+    assert gold["workload"] == CONFIGS[name].name
+    k = 1.25
+    return gold, {"layers": max(GRAD_RL2, k * gold["layer_max"]),
+                  "median": max(GRAD_RL2, k * gold["layer_median"]),
+                  "lm_head": max(GRAD_RL2, k * gold["lm_head"]),
+                  "final_norm": max(GRAD_RL2, k * gold["final_norm"]),
+                  "embed": max(GRAD_RL2, k * gold["embed"])}
+
+
+def load_streamed(cfg, m):
+    """Load every unit's fp32 masters, generating one layer at a time."""
+    for l in range(cfg.n_layers):
+        m.load(l, inputs.layer_master(cfg, l))
+    for u in (UNIT_EMBED, UNIT_FINAL_NORM, UNIT_LM_HEAD):
+        m.load(u, inputs.unit_master(cfg, u))
+
+
+def compare_streamed(cfg, m, tol):
+    """The float32 oracle's step, layer by layer (each layer's bf16 weights
+    regenerated from the seeded generator), against the engine's retained
+    gradients, tensor by tensor as the oracle's backward produces them."""
+    shapes = layer_tensor_shapes(cfg)
+    errs = {}
+
+    def layer(i):  # rounded tensor by tensor: smaller temporaries than the whole layer
+        return {k: oracle.bf16_round(v) for k, v in inputs.split_layer(cfg, inputs.layer_master(cfg, i)).items()}
+
+    def check(i, g):
+        flat = m.grads(i)
+        off = 0
+        for name, shape in shapes:
+            n = int(np.prod(shape))
+            errs[f"{i}.{name}"] = rel_l2(flat[off:off + n].reshape(shape), g[name])
+            off += n
+
+    d, V = cfg.hidden, cfg.vocab
+    r = lambda u: oracle.bf16_round(inputs.unit_master(cfg, u))
+    tok, lab = inputs.tokens_and_labels(cfg)
+    loss_ref, g = oracle.step_streamed(layer, cfg.n_layers, r(UNIT_EMBED).reshape(V, d),
+                                       r(UNIT_FINAL_NORM), r(UNIT_LM_HEAD).reshape(V, d), tok, lab,
+                                       cfg, dtype=np.float32, on_layer_grads=check)
+    layer_errs = np.array(list(errs.values()))
+    errs["loss"] = abs(m.loss() - loss_ref) / abs(loss_ref)
+    errs["embed"] = rel_l2(m.grads(UNIT_EMBED).reshape(V, d), g["embed"])
+    errs["final_norm"] = rel_l2(m.grads(UNIT_FINAL_NORM), g["final_norm"])
+    errs["lm_head"] = rel_l2(m.grads(UNIT_LM_HEAD).reshape(V, d), g["lm_head"])
+    errs["layer_median"] = float(np.median(layer_errs))
+    bad = {k: v for k, v in errs.items() if k[0].isdigit() and v > tol["layers"]}
+    assert not bad, f"outside tolerance {tol['layers']:.4f}: {bad}"
+    assert errs["loss"] <= LOSS_RTOL, errs["loss"]
+    for k in ("embed", "final_norm", "lm_head"):
+        assert errs[k] <= tol[k], (k, errs[k], tol[k])
+    assert errs["layer_median"] <= tol["median"], (errs["layer_median"], tol["median"])
+    return errs
+
+
 def test_full_1p3b_step_matches_oracle():
     """The whole 1.3B-shape step (24 layers, hidden 2048, 16 x 64 heads, FFN
     5504, vocab 32000, 8 x 1024 tokens) against the float32 oracle, tensor by
-    tensor (the oracle needs a couple of minutes of the host's cores).
-
-    Tolerance: at this depth bf16 storage of activations by itself moves the
-    gradients by more than 2e-2.  tests/golden/bf16_depth_error.json (written
-    by tests/golden/make_bf16_depth_error.py from the oracle with bf16
-    rounding at the points where this path stores bf16) gives that error; the
-    path must stay within 1.5x of it (the loss keeps the 1e-3 bar)."""
-    import json
-    import os
-    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "bf16_depth_error.json")))
+    tensor (the oracle needs a couple of minutes of the host's cores).  Loss
+    within 1e-3; gradients within depth_tolerance("1.3b")."""
     cfg = CONFIGS["1.3b"]
-    assert gold["workload"] == cfg.name
+    gold, tol = depth_tolerance("1.3b")
+    with make_model(cfg, {}) as m:
+        load_streamed(cfg, m)
+        assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()
+        errs = compare_streamed(cfg, m, tol)
+    print({k: v for k, v in errs.items() if not k[0].isdigit()}, "model:", gold["layer_max"])
+
+
+def test_full_8b_stack_matches_oracle():
+    """The whole 32-layer 8B-shape GQA stack (hidden 4096, 32/8 heads x 128,
+    FFN 14336, vocab 128256, RoPE base 500000) streamed through the 3-slot
+    ring, one sequence of 2048 tokens, against the float32 oracle tensor by
+    tensor.  The optimizer state is kept as bf16 (no update runs here) so the
+    engine's host memory and the oracle's activations fit the host together."""
+    cfg = CONFIGS["8b"].with_(batch=1)
+    gold, tol = depth_tolerance("8b")
+    with make_model(cfg, {}, ring_slots=3, bf16_adam_state=1) as m:
+        load_streamed(cfg, m)
+        assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()
+        errs = compare_streamed(cfg, m, tol)
+    print({k: v for k, v in errs.items() if not k[0].isdigit()}, "model:", gold["layer_max"])
+
+
+def test_full_123b_slice_matches_oracle():
+    """The 123B-shape slice as configured (4 layers of hidden 12288, 96/8
+    heads x 128, FFN 28672, vocab 32768, 2-slot ring), one sequence of 1024
+    tokens, against the float32 oracle tensor by tensor."""
+    cfg = CONFIGS["123b-slice"].with_(batch=1)
+    gold, tol = depth_tolerance("123b-slice")
+    with make_model(cfg, {}, ring_slots=2, bf16_adam_state=1) as m:
+        load_streamed(cfg, m)
+        assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()
+        errs = compare_streamed(cfg, m, tol)
+    print({k: v for k, v in errs.items() if not k[0].isdigit()}, "model:", gold["layer_max"])
+
+
+@pytest.mark.parametrize("asyn", [0, 1])
+def test_sliding_activations_match_oracle(asyn):
+    """Sliding activations (checkpoints to pinned host memory after the
+    forward, back before the backward) against the oracle, tensor by tensor,
+    with more layers than the 4-slot device window."""
+    cfg = TEST_CONFIGS["small-gqa"].with_(n_layers=6)
     mast = masters(cfg)
     tok, lab = inputs.tokens_and_labels(cfg)
-    with make_model(cfg, mast) as m:
+    loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg)
+    with make_model(cfg, mast, offload_activations=1, ring_slots=2, async_update=asyn) as m:
         assert m.train_step(tok, lab) == sf.SF_OK, m.error()
-        loss_ref, g_ref = oracle.step(oracle_weights(cfg, mast), tok, lab, cfg, dtype=np.float32)
-        tol_layers = max(GRAD_RL2, 1.5 * gold["layer_max"])
-        errs = compare(cfg, m, loss_ref, g_ref, tol=tol_layers)
-    assert errs["lm_head"] <= max(GRAD_RL2, 1.5 * gold["lm_head"])
-    assert errs["final_norm"] <= max(GRAD_RL2, 1.5 * gold["final_norm"])
+        compare(cfg, m, loss_ref, g_ref)
+        assert m.stats()["d2h_bytes"] > cfg.n_layers * cfg.batch * cfg.seq * cfg.hidden * 4

@@ -36,6 +36,8 @@
 #include <cstdint>
 #include <mutex>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "ptx.cuh"
 #include "sf_internal.h"
@@ -1217,6 +1219,28 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
 // ------------------------------------------------------------------ host side
 namespace {
 
+// Reserve `bytes` of dynamic shared memory for `kern` on the current device,
+// once per kernel and device (the attribute is per device).
+bool smem_attr_set(const void* kern, int bytes) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> l(mu);
+  for (const auto& e : done)
+    if (e.first == kern && e.second == dev) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  done.emplace_back(kern, dev);
+  return true;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_att() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1252,13 +1276,7 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
-  static bool set = false;
-  if (!set) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return -3;
-    set = true;
-  }
+  if (!smem_attr_set(reinterpret_cast<const void*>(attn_fwd_tc_kernel<HD>), C::SMEM)) return -3;
   // persistent: one CTA per SM walks the tiles in longest-first order
   const int tiles = ((S + 127) / 128) * Hq * B;
   const int grid = tiles < num_sms() ? tiles : num_sms();
@@ -1289,13 +1307,7 @@ int bwd_tc(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
-  static bool set = false;
-  if (!set) {
-    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<HD, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return -3;
-    set = true;
-  }
+  if (!smem_attr_set(reinterpret_cast<const void*>(attn_bwd_tc_kernel<HD, DET>), C::SMEM)) return -3;
   const int64_t T = (int64_t)B * S;
   if (!DET && cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess)
     return -3;
@@ -1339,13 +1351,7 @@ int bwd_tc2(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat1
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
-  static bool set = false;
-  if (!set) {
-    if (cudaFuncSetAttribute(attn_bwd_tc2_kernel<DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return -3;
-    set = true;
-  }
+  if (!smem_attr_set(reinterpret_cast<const void*>(attn_bwd_tc2_kernel<DET>), C::SMEM)) return -3;
   const int64_t T = (int64_t)B * S;
   if (!DET && cudaMemsetAsync(dq_acc, 0, (size_t)T * WO * sizeof(float), st) != cudaSuccess)
     return -3;

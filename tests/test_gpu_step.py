@@ -548,6 +548,7 @@ def compare_streamed(cfg, m, tol):
     errs["final_norm"] = rel_l2(m.grads(UNIT_FINAL_NORM), g["final_norm"])
     errs["lm_head"] = rel_l2(m.grads(UNIT_LM_HEAD).reshape(V, d), g["lm_head"])
     errs["layer_median"] = float(np.median(layer_errs))
+    errs["layer_max"] = float(layer_errs.max())
     bad = {k: v for k, v in errs.items() if k[0].isdigit() and v > tol["layers"]}
     assert not bad, f"outside tolerance {tol['layers']:.4f}: {bad}"
     assert errs["loss"] <= LOSS_RTOL, errs["loss"]

@@ -488,7 +488,7 @@ def test_full_1p3b_step_properties():
         assert np.isfinite(a).all() and np.array_equal(a, b)
 
 
-def depth_tolerance(name):
+def depth_tolerance(name, batch):
     """Per-tensor bounds of a whole-stack comparison at the workload's depth:
     the stated bar (2e-2), or, where the bf16-operand rounding model (written
     by tests/golden/make_bf16_depth_error.py from the oracle alone) already
@@ -496,7 +496,10 @@ def depth_tolerance(name):
     only where any bf16 tensor-core path must (projection and attention
     operands, P and dS, the gradient cast), so no storage choice of this path
     sets the bound.  1.25 covers the scatter between two independent
-    realisations of the same rounding noise (this path's and the model's)."""
+    realisations of the same rounding noise (this path's and the model's).
+    Where the test runs the golden's own tokens (batch and sequence length
+    equal), each tensor is also held to 1.15x the model's error for that
+    very tensor."""
     import json
     import os
     gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
@@ -507,7 +510,17 @@ def depth_tolerance(name):
                   "median": max(GRAD_RL2, k * gold["layer_median"]),
                   "lm_head": max(GRAD_RL2, k * gold["lm_head"]),
                   "final_norm": max(GRAD_RL2, k * gold["final_norm"]),
-                  "embed": max(GRAD_RL2, k * gold["embed"])}
+                  "embed": max(GRAD_RL2, k * gold["embed"]),
+                  # where the test runs the golden's own tokens (one sequence),
+                  # each tensor against the model's error for that tensor
+                  "per_tensor": ({t: max(GRAD_RL2, PER_TENSOR_K * e) for t, e in gold["per_tensor"].items()}
+                                 if gold["batch"] == batch and gold["seq"] == CONFIGS[name].seq else None)}
+
+
+# Per-tensor bound on the golden's own tokens: this path's error and the
+# model's are two draws of the same rounding noise on the same inputs; they
+# agree to a few percent of each other (medians to 0.2%), so 1.15x.
+PER_TENSOR_K = 1.15
 
 
 def load_streamed(cfg, m):
@@ -551,6 +564,13 @@ def compare_streamed(cfg, m, tol):
     errs["layer_max"] = float(layer_errs.max())
     bad = {k: v for k, v in errs.items() if k[0].isdigit() and v > tol["layers"]}
     assert not bad, f"outside tolerance {tol['layers']:.4f}: {bad}"
+    if tol.get("per_tensor") is not None:
+        over = {t: (v, tol["per_tensor"][t]) for t, v in errs.items()
+                if t in tol["per_tensor"] and v > tol["per_tensor"][t]}
+        assert not over, f"above {PER_TENSOR_K}x the model's own error for the tensor: {over}"
+        ratio = [v / e for t, v in errs.items() if t in tol["per_tensor"]
+                 for e in [tol["per_tensor"][t] / PER_TENSOR_K] if e > 0]
+        errs["ratio_to_model_max"] = float(max(ratio))
     assert errs["loss"] <= LOSS_RTOL, errs["loss"]
     for k in ("embed", "final_norm", "lm_head"):
         assert errs[k] <= tol[k], (k, errs[k], tol[k])
@@ -564,7 +584,7 @@ def test_full_1p3b_step_matches_oracle():
     tensor (the oracle needs a couple of minutes of the host's cores).  Loss
     within 1e-3; gradients within depth_tolerance("1.3b")."""
     cfg = CONFIGS["1.3b"]
-    gold, tol = depth_tolerance("1.3b")
+    gold, tol = depth_tolerance("1.3b", cfg.batch)
     with make_model(cfg, {}) as m:
         load_streamed(cfg, m)
         assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()
@@ -579,7 +599,7 @@ def test_full_8b_stack_matches_oracle():
     tensor.  The optimizer state is kept as bf16 (no update runs here) so the
     engine's host memory and the oracle's activations fit the host together."""
     cfg = CONFIGS["8b"].with_(batch=1)
-    gold, tol = depth_tolerance("8b")
+    gold, tol = depth_tolerance("8b", cfg.batch)
     with make_model(cfg, {}, ring_slots=3, bf16_adam_state=1) as m:
         load_streamed(cfg, m)
         assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()
@@ -592,7 +612,7 @@ def test_full_123b_slice_matches_oracle():
     heads x 128, FFN 28672, vocab 32768, 2-slot ring), one sequence of 1024
     tokens, against the float32 oracle tensor by tensor."""
     cfg = CONFIGS["123b-slice"].with_(batch=1)
-    gold, tol = depth_tolerance("123b-slice")
+    gold, tol = depth_tolerance("123b-slice", cfg.batch)
     with make_model(cfg, {}, ring_slots=2, bf16_adam_state=1) as m:
         load_streamed(cfg, m)
         assert m.train_step(*inputs.tokens_and_labels(cfg)) == sf.SF_OK, m.error()

@@ -1,30 +1,26 @@
-// Causal grouped-query attention forward on the tcgen05 tensor cores.
+// Causal grouped-query attention, forward and backward, on the tcgen05
+// tensor cores.
 //
-// Online softmax over key blocks (Milakov & Gimelshein 2018; the blocking of
-// Dao et al., FlashAttention 2022), laid out for sm_103a.  The kernel is
-// persistent: one CTA per SM walks (128-query block, head, batch) tiles in
-// longest-first order, so the barrier and TMEM setup happen once per SM and
-// the next tile's Q and K loads overlap the current tile's last blocks and
-// epilogue.  Per 128-key block the tensor core computes S = Q K^T into one of
-// two TMEM buffers, four softmax warps (one thread per query row, so row max
-// and row sum need no shuffles) turn S into bf16 P in TMEM, and the tensor
-// core accumulates O += P V in TMEM with P as its tensor-memory A operand.
-// S of the next block is computed while the softmax warps work on the
-// current one.
+// Forward: online softmax over key blocks (Milakov & Gimelshein 2018; the
+// blocking of Dao et al., FlashAttention 2022), laid out for sm_103a.  The
+// kernel is persistent: one CTA per SM walks items of two 128-query tiles in
+// longest-first order.  Both tiles of an item read the same K and V blocks,
+// and they take turns on the tensor core: while one tile's softmax warps turn
+// S into P, the tensor core runs the other tile's O += P V and next S = Q K^T.
+// Four softmax warps per tile give one thread per query row, so the row max
+// and row sum need no shuffles.  P goes back into TMEM over its S columns, as
+// the tensor-memory A operand of P V.
 //
-//   warp 0     TMA: Q of each tile once the previous tile's last S has read
-//              the Q buffer, K blocks into a 3-stage ring, V into a 2-stage ring
-//   warp 1     MMA issuer (tcgen05.mma, one thread); TMEM owner (512 columns:
-//              S0 | S1 | O | P)
-//   warps 2-5  softmax: tcgen05.ld of a row of S, scale, causal mask,
-//              max / exp2 / sum, rescale of the O row in TMEM when the row
-//              max grows, tcgen05.st of the row of P as bf16 pairs; at a
-//              tile's end the normalised O row goes into a staging buffer
-//   warp 6     stores each staged O tile with the TMA unit (whole rows per
-//              request, where per-thread row stores would split every warp
-//              store into 32 transactions)
+// Two measurements on GB300 set the shape of the softmax code.
+//   - One thread issues every MMA, and each 128 x 128 x 16 MMA runs only
+//     about 64 cycles.
+//   - Scalar fp32 max instructions in the softmax warps slow that issuing
+//     warp more than twice over.
+// So the row max uses three-input maxima, the exponent arguments and row
+// sums use paired fp32 instructions, and the causal mask is compiled only
+// into the diagonal block's code.
 //
-// Operands: Q, K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
+// Operands: Q and K tiles are K-major [128 rows][hd] (128-byte swizzle, 64
 // columns per box); V is the MN-major operand of P V ([128 keys][64 hd]
 // boxes).  The qkv rows are read through a 3-D tensor map (column, position,
 // batch), so rows past the sequence end arrive as zeros.
@@ -47,21 +43,6 @@ namespace sf {
 namespace {
 
 constexpr int kAttThreads = 192;
-constexpr int kAttFwdThreads = 224;  // + a warp that stores O tiles
-
-template <int HD>
-struct AttCfg {
-  static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
-  static constexpr int KST = 3;                 // K stages (V has 2; P lives in TMEM)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = TILE;
-  static constexpr int OFF_V = OFF_K + KST * TILE;
-  static constexpr int OFF_O = OFF_V + 2 * TILE;  // staging of the O tile for its TMA store
-  static constexpr int OFF_BAR = OFF_O + TILE;
-  static constexpr int NBAR = 18 + 2 * KST;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-};
-
 // Grid position in longest-first order: the CTAs are dispatched roughly in
 // linear block order, so every CTA of rank 0 (the most work) is placed before
 // any CTA of rank 1, and so on, whatever the other two coordinates.
@@ -81,6 +62,36 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// (x, y) * c + (d, d) as one paired fp32 FMA (round to nearest)
+__device__ __forceinline__ void fma2_scalar(float& x, float& y, float c, float d) {
+  asm("{\n\t.reg .b64 t, u, w;\n\t"
+      "mov.b64 t, {%0, %1};\n\t"
+      "mov.b64 u, {%2, %2};\n\t"
+      "mov.b64 w, {%3, %3};\n\t"
+      "fma.rn.f32x2 t, t, u, w;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "+f"(x), "+f"(y)
+      : "f"(c), "f"(d));
+}
+
+// (x, y) += (a, b) as one paired fp32 add
+__device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
+  asm("{\n\t.reg .b64 t, u;\n\t"
+      "mov.b64 t, {%0, %1};\n\t"
+      "mov.b64 u, {%2, %3};\n\t"
+      "add.rn.f32x2 t, t, u;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "+f"(x), "+f"(y)
+      : "f"(a), "f"(b));
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -88,18 +99,59 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 }  // namespace
 
+// ------------------------------------------------------------------ forward, two query tiles per CTA
+// The same online softmax with two 128-query tiles per CTA that share every
+// K and V tile: two query heads of one kv group at the same query block when
+// the group size is even, else query blocks 2p and 2p + 1 of one head (block
+// 2p + 1 is then fully masked for the first tile).  Sharing halves the K/V
+// bytes each tensor-core FLOP pulls from L2, and the two tiles ping-pong: the
+// tensor core runs one tile's P V and next Q K^T while the other tile's
+// softmax warps work, so each tile's TMEM holds one S (P written over it as
+// bf16) and one O.
+//
+//   warp 0      TMA: K and V blocks (2- and 2-stage rings at head dim 128),
+//               both Q tiles at an item's first block
+//   warp 1      MMA issuer; TMEM owner (S0 | S1 | O0 | O1)
+//   warp 2      TMA store of each staged O tile
+//   warps 3-6   softmax of tile 0, one thread per query row
+//   warps 7-10  softmax of tile 1
+//
+// Per block G the MMA thread issues O0 += P0 V, S0' = Q0 K'^T, O1 += P1 V,
+// S1' = Q1 K'^T.  S' overwrites the columns that held P: the tensor core
+// executes one thread's MMAs in issue order, so P is read before it is
+// overwritten.  A commit after S' also covers every earlier P V of the CTA,
+// so once a softmax thread sees S' it may rescale its O row: no P V of its
+// tile is in flight until it publishes the next P.
+namespace {
+constexpr int kAttFwd2Threads = 352;
+
 template <int HD>
-__global__ void __launch_bounds__(kAttFwdThreads, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_o,
+struct AttFwd2Cfg {
+  static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
+  static constexpr int KST = HD == 128 ? 2 : 4;
+  static constexpr int VST = 2;
+  static constexpr int OFF_Q = 0;  // Q of tile 0, then of tile 1
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + KST * TILE;
+  static constexpr int OFF_O = OFF_V + VST * TILE;  // staging of an O tile for its TMA store
+  static constexpr int OFF_BAR = OFF_O + TILE;
+  static constexpr int NBAR = 13 + 2 * KST + 2 * VST;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+};
+static_assert(AttFwd2Cfg<128>::SMEM <= 232448, "forward shared memory");
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(kAttFwd2Threads, 1)
+    attn_fwd_pp_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_o,
                        float* __restrict__ lse, int S, int Hq, int Hkv, int B, float scale_log2,
-                       int* err) {
-  using C = AttCfg<HD>;
+                       int pair_heads, int* err) {
+  using C = AttFwd2Cfg<HD>;
   constexpr int NB = HD / 64;  // 64-column boxes per tile
   constexpr uint32_t ID_S = umma_idesc_bf16(128, 128, false, false);
   constexpr uint32_t ID_O = umma_idesc_bf16(128, HD, false, true);
   constexpr uint32_t TMEM_COLS = 512;
-  constexpr uint32_t O_COL = 256;
-  constexpr uint32_t P_COL = 384;  // P: 128 rows x 128 keys of bf16, two per column
+  constexpr uint32_t O_COL = 256;  // O of tile t at O_COL + t * HD; S (and P) of tile t at t * 128
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -108,62 +160,69 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
   const uint32_t sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sO = s0 + C::OFF_O;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
-  // K and V stages have their own barriers: a K stage is free as soon as its
-  // S = Q K^T has completed, so K loads run ahead of the P V products.  Every
-  // ring and buffer index below counts over all tiles of the CTA.
-  const uint32_t q_full = b0, q_empty = b0 + 8u;
-  auto s_full = [&](int s) { return b0 + 8u * (2 + s); };
-  auto s_free = [&](int s) { return b0 + 8u * (4 + s); };
-  auto p_full = [&](int s) { return b0 + 8u * (6 + s); };
-  auto o_done = [&](int s) { return b0 + 8u * (8 + s); };
-  const uint32_t drain = b0 + 8u * 10;
-  const uint32_t o_free = b0 + 8u * 11;    // a tile's O has left TMEM: the next may overwrite it
-  const uint32_t st_ready = b0 + 8u * 12;  // a tile's O rows are in the staging buffer
-  const uint32_t st_free = b0 + 8u * 13;   // the staging buffer has been read by the TMA store
-  auto v_full = [&](int s) { return b0 + 8u * (14 + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (16 + s); };
-  auto k_full = [&](int s) { return b0 + 8u * (18 + s); };   // C::KST stages
-  auto k_empty = [&](int s) { return b0 + 8u * (18 + C::KST + s); };
+  auto q_full = [&](int t) { return b0 + 8u * t; };
+  auto q_empty = [&](int t) { return b0 + 8u * (2 + t); };
+  auto s_full = [&](int t) { return b0 + 8u * (4 + t); };
+  auto p_full = [&](int t) { return b0 + 8u * (6 + t); };
+  auto o_done = [&](int t) { return b0 + 8u * (8 + t); };
+  const uint32_t st_ready = b0 + 8u * 10;  // an O tile's rows are in the staging buffer
+  const uint32_t st_free = b0 + 8u * 11;   // the staging buffer has been read by the TMA store
+  const uint32_t drain = b0 + 8u * 12;
+  auto k_full = [&](int s) { return b0 + 8u * (13 + s); };
+  auto k_empty = [&](int s) { return b0 + 8u * (13 + C::KST + s); };
+  auto v_full = [&](int s) { return b0 + 8u * (13 + 2 * C::KST + s); };
+  auto v_empty = [&](int s) { return b0 + 8u * (13 + 2 * C::KST + C::VST + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (S + 127) / 128;
-  const int per_rank = Hq * B;
-  const int num_tiles = nqb * per_rank;
-  // Tile t in longest-first order: every tile of query block nqb - 1 (the most
-  // keys) comes before any of block nqb - 2, and so on; CTA c takes tiles c,
-  // c + gridDim.x, ...
-  struct Tile { int h, b, qb, nkv; };
-  auto tile_of = [&](int t) -> Tile {
+  const int grp = Hq / Hkv;
+  // Items in longest-first order (every item of the most keys comes first);
+  // CTA c takes items c, c + gridDim.x, ...
+  const int npb = pair_heads ? nqb : (nqb + 1) / 2;  // query positions of an item
+  const int per_rank = pair_heads ? (Hq / 2) * B : Hq * B;
+  const int num_items = npb * per_rank;
+  struct Item { int h0, h1, qb0, qb1, b, g, nkv; };
+  auto item_of = [&](int t) -> Item {
     const int rank = t / per_rank, rem = t - rank * per_rank;
-    Tile x;
-    x.h = rem % Hq;
-    x.b = rem / Hq;
-    x.qb = nqb - 1 - rank;
-    x.nkv = x.qb + 1;
+    Item x;
+    if (pair_heads) {
+      const int hp = rem % (Hq / 2);
+      x.b = rem / (Hq / 2);
+      x.h0 = 2 * hp;
+      x.h1 = 2 * hp + 1;
+      x.qb0 = x.qb1 = nqb - 1 - rank;
+    } else {
+      x.h0 = x.h1 = rem % Hq;
+      x.b = rem / Hq;
+      x.qb0 = 2 * (npb - 1 - rank);
+      x.qb1 = x.qb0 + 1;
+    }
+    x.g = x.h0 / grp;
+    x.nkv = x.qb1 + 1 < nqb ? x.qb1 + 1 : nqb;
     return x;
   };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(q_full(t), 1);
+      mbar_init(q_empty(t), 1);
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), 128);
+      mbar_init(o_done(t), 1);
+    }
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::VST; ++s) {
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
-      mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 128);
-      mbar_init(p_full(s), 128);
-      mbar_init(o_done(s), 1);
     }
-    mbar_init(drain, 1);
-    mbar_init(o_free, 128);
     mbar_init(st_ready, 128);
     mbar_init(st_free, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm);
@@ -180,109 +239,131 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    // Per tile: Q once the previous tile's last S has read the Q buffer, then
-    // K blocks (K(j) needs S(j - KST) done) two ahead of V blocks (V(j) needs
-    // P V(j - 2) done).
+    // Per item: K(0), both Q tiles (each once the previous item's last S of
+    // that tile has read the buffer), V(0), K(1), V(1), ...
     bool ok = true;
-    long gk = 0, gv = 0;  // K and V loads issued so far
-    int it = 0;
-    int q_issued = -1;  // tile index of the last Q load issued
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
-      const Tile x = tile_of(t);
-      const int g = x.h / (Hq / Hkv);
-      const int colK = (Hq + g) * HD, colV = (Hq + Hkv + g) * HD;
-      if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
-      mbar_arrive_expect_tx(q_full, C::TILE);
+    long gk = 0, gv = 0;
+    int it = 0, q_issued[2] = {-1, -1};
+    for (int t = blockIdx.x; ok && t < num_items; t += gridDim.x, ++it) {
+      const Item x = item_of(t);
+      const int colK = (Hq + x.g) * HD, colV = (Hq + Hkv + x.g) * HD;
+      for (int j = 0; j < x.nkv; ++j) {
+        {
+          const int st = (int)(gk % C::KST);
+          if (!mbar_wait(k_empty(st), (uint32_t)((gk / C::KST) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(k_full(st), C::TILE);
 #pragma unroll
-      for (int c = 0; c < NB; ++c) tma_load_3d(sQ + c * 16384, &tm, q_full, x.h * HD + 64 * c, x.qb * 128, x.b);
-      q_issued = it;
-      auto load_k = [&](int kb) -> bool {
-        const int st = (int)(gk % C::KST);
-        if (!mbar_wait(k_empty(st), (uint32_t)((gk / C::KST) & 1) ^ 1u, abort_flag)) return false;
-        mbar_arrive_expect_tx(k_full(st), C::TILE);
-#pragma unroll
-        for (int c = 0; c < NB; ++c)
-          tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, kb * 128, x.b);
-        ++gk;
-        return true;
-      };
-      constexpr int KA = C::KST - 1;
-      int kn = 0;
-      for (; ok && kn < KA && kn < x.nkv; ++kn) ok = load_k(kn);
-      for (int j = 0; ok && j < x.nkv; ++j) {
-        if (kn < x.nkv) {
-          if (!load_k(kn)) { ok = false; break; }
-          ++kn;
+          for (int c = 0; c < NB; ++c)
+            tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, j * 128, x.b);
+          ++gk;
         }
-        const int st = (int)(gv & 1);
-        if (!mbar_wait(v_empty(st), (uint32_t)((gv >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(v_full(st), C::TILE);
+        if (j == 0) {
+          for (int tt = 0; tt < 2; ++tt) {
+            if (it > 0 && !mbar_wait(q_empty(tt), (uint32_t)((it - 1) & 1), abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(q_full(tt), C::TILE);
+            const int h = tt ? x.h1 : x.h0, qb = tt ? x.qb1 : x.qb0;
 #pragma unroll
-        for (int c = 0; c < NB; ++c)
-          tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, x.b);
-        ++gv;
+            for (int c = 0; c < NB; ++c)
+              tma_load_3d(sQ + tt * C::TILE + c * 16384, &tm, q_full(tt), h * HD + 64 * c, qb * 128, x.b);
+            q_issued[tt] = it;
+          }
+          if (!ok) break;
+        }
+        {
+          const int st = (int)(gv % C::VST);
+          if (!mbar_wait(v_empty(st), (uint32_t)((gv / C::VST) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(v_full(st), C::TILE);
+#pragma unroll
+          for (int c = 0; c < NB; ++c)
+            tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, x.b);
+          ++gv;
+        }
       }
     }
     if (!ok) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       // let the copies already issued land before the CTA's shared memory goes away
-      if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, nullptr);
+      for (int tt = 0; tt < 2; ++tt)
+        if (q_issued[tt] >= 0) mbar_wait(q_full(tt), (uint32_t)(q_issued[tt] & 1), nullptr);
       for (long k = gk - 1; k >= 0 && k >= gk - C::KST; --k)
         mbar_wait(k_full((int)(k % C::KST)), (uint32_t)((k / C::KST) & 1), nullptr);
-      for (long k = gv - 1; k >= 0 && k >= gv - 2; --k)
-        mbar_wait(v_full((int)(k & 1)), (uint32_t)((k >> 1) & 1), nullptr);
+      for (long k = gv - 1; k >= 0 && k >= gv - C::VST; --k)
+        mbar_wait(v_full((int)(k % C::VST)), (uint32_t)((k / C::VST) & 1), nullptr);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     bool ok = true;
-    long gb = 0;  // global index of the tile's first key block
+    // Descriptors of the buffers' first rows; an operand at byte offset o
+    // within a buffer is the base descriptor plus o / 16 (the address field
+    // cannot carry: shared addresses stay below 2^18).
+    const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024), dK = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t dV = smem_desc_sw128(sV, 16384, 1024);
+    // S_t = Q_t K(G)^T into the S columns of tile t
+    auto issue_s = [&](int tt, long G) {
+      const uint32_t ks = (uint32_t)(G % C::KST);
+      const uint64_t a0 = dQ + (uint32_t)(tt * C::TILE / 16), b0 = dK + ks * (uint32_t)(C::TILE / 16);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) / 16;
+        umma_bf16(tmem_base + tt * 128, a0 + off, b0 + off, ID_S, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(s_full(tt));
+    };
+    long G = 0;  // global index of the current key block over the CTA's items
     int it = 0;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
-      const Tile x = tile_of(t);
-      if (!mbar_wait(q_full, it & 1, abort_flag)) { ok = false; break; }
-      for (int j = 0; ok && j <= x.nkv; ++j) {
-        if (j < x.nkv) {  // S_j = Q K_j^T into S buffer G % 2
-          const long G = gb + j;
-          const int st = (int)(G & 1), ks = (int)(G % C::KST);
-          if (!mbar_wait(k_full(ks), (uint32_t)((G / C::KST) & 1), abort_flag) ||
-              !mbar_wait(s_free(st), (uint32_t)((G >> 1) & 1) ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(tmem_base + st * 128, smem_desc_sw128(sQ + off, 16, 1024),
-                      smem_desc_sw128(sK + ks * C::TILE + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full(st));
-          umma_commit(k_empty(ks));  // K stage free once S has been computed
-          if (j == x.nkv - 1) umma_commit(q_empty);  // and Q once the tile's last S has
+    int t = blockIdx.x;
+    if (t < num_items) {  // the first item's S of both tiles
+      const Item x = item_of(t);
+      for (int tt = 0; ok && tt < 2; ++tt) {
+        if ((tt == 0 && !mbar_wait(k_full(0), 0, abort_flag)) || !mbar_wait(q_full(tt), 0, abort_flag)) {
+          ok = false;
+          break;
         }
-        if (j > 0) {  // O += P_{j-1} V_{j-1}
-          const long G = gb + j - 1;
-          const int st = (int)(G & 1);
-          // the first P V of a tile overwrites O: the previous tile's O must have left TMEM
-          if (j == 1 && it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(p_full(st), (uint32_t)((G >> 1) & 1), abort_flag) ||
-              !mbar_wait(v_full(st), (uint32_t)((G >> 1) & 1), abort_flag)) {
+        tc_fence_after();
+        issue_s(tt, 0);
+        if (x.nkv == 1) umma_commit(q_empty(tt));
+      }
+      if (ok) umma_commit(k_empty(0));
+    }
+    for (; ok && t < num_items; t += gridDim.x, ++it) {
+      const Item x = item_of(t);
+      const bool has_next_item = t + (int)gridDim.x < num_items;
+      const int nkv_next = has_next_item ? item_of(t + gridDim.x).nkv : 0;
+      for (int j = 0; ok && j < x.nkv; ++j, ++G) {
+        const bool last = j + 1 == x.nkv;
+        const bool has_next = !last || has_next_item;
+        const long Gn = G + 1;
+        // the next block's S: the last of its item releases that item's Q tile
+        const bool next_is_last = last ? nkv_next == 1 : j + 2 == x.nkv;
+        const int vs = (int)(G % C::VST);
+        for (int tt = 0; tt < 2; ++tt) {
+          if (!mbar_wait(p_full(tt), (uint32_t)(G & 1), abort_flag) ||
+              (tt == 0 && !mbar_wait(v_full(vs), (uint32_t)((G / C::VST) & 1), abort_flag))) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint64_t bv = dV + (uint32_t)vs * (uint32_t)(C::TILE / 16);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            umma_bf16_ts(tmem_base + O_COL, tmem_base + P_COL + kk * 8,
-                         smem_desc_sw128(sV + st * C::TILE + kk * 2048, 16384, 1024), ID_O,
-                         (j > 1 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)  // O_t += P_t V: P as the tensor-memory A operand
+            umma_bf16_ts(tmem_base + O_COL + tt * HD, tmem_base + tt * 128 + kk * 8, bv + kk * (2048 / 16),
+                         ID_O, (j > 0 || kk > 0) ? 1u : 0u);
+          if (tt == 1) umma_commit(v_empty(vs));
+          if (last) umma_commit(o_done(tt));
+          if (has_next) {
+            if ((tt == 0 && !mbar_wait(k_full((int)(Gn % C::KST)), (uint32_t)((Gn / C::KST) & 1), abort_flag)) ||
+                (last && !mbar_wait(q_full(tt), (uint32_t)((it + 1) & 1), abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(tt, Gn);
+            if (tt == 1) umma_commit(k_empty((int)(Gn % C::KST)));
+            if (next_is_last) umma_commit(q_empty(tt));
           }
-          umma_commit(o_done(st));
-          umma_commit(v_empty(st));
         }
       }
-      gb += x.nkv;
     }
     if (!ok) {
       record_error(err, kDevAttnTimeout);
@@ -290,128 +371,131 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
       umma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp == 6 && lane == 0) {
+  } else if (warp == 2 && lane == 0) {
     // ---------------------------------------------------------------- O store
     bool ok = true;
-    int it = 0;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
-      const Tile x = tile_of(t);
-      if (!mbar_wait(st_ready, it & 1, abort_flag)) { ok = false; break; }
-      // rows past the sequence end are outside the tensor map and not written
+    int c = 0;  // O tiles stored so far: tile 0 then tile 1 of each item
+    for (int t = blockIdx.x; ok && t < num_items; t += gridDim.x) {
+      const Item x = item_of(t);
+      for (int tt = 0; tt < 2; ++tt, ++c) {
+        if (!mbar_wait(st_ready, (uint32_t)(c & 1), abort_flag)) { ok = false; break; }
+        const int h = tt ? x.h1 : x.h0, qb = tt ? x.qb1 : x.qb0;
+        if (qb * 128 < S) {  // rows past the sequence end are outside the tensor map and not written
 #pragma unroll
-      for (int c = 0; c < NB; ++c) tma_store_3d(&tm_o, sO + c * 16384, x.h * HD + 64 * c, x.qb * 128, x.b);
-      bulk_commit_group();
-      bulk_wait_group_read0();
-      mbar_arrive(st_free);
+          for (int cc = 0; cc < NB; ++cc) tma_store_3d(&tm_o, sO + cc * 16384, h * HD + 64 * cc, qb * 128, x.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(st_free);
+      }
     }
     bulk_wait_group0();
     if (!ok) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 3) {
     // ---------------------------------------------------------------- softmax
-    const int quarter = warp & 3;
+    const int tt = (warp - 3) >> 2;
+    const int quarter = warp & 3;  // TMEM lanes a warp may access: 32 x (warp % 4)
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_col = (uint32_t)tt * 128u, o_col = O_COL + (uint32_t)tt * HD;
     bool ok = true;
-    long gb = 0;
+    long G = 0;
     int it = 0;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
-      const Tile x = tile_of(t);
-      const int q = x.qb * 128 + row;
-      // m: the row max in log2 units that the exponentials are taken against.
-      // It only moves when a block's max exceeds it by more than 8 (a factor
-      // of 256), so O in TMEM is rarely rescaled; the result O / l does not
-      // depend on the choice of m.
+    for (int t = blockIdx.x; ok && t < num_items; t += gridDim.x, ++it) {
+      const Item x = item_of(t);
+      const int qb = tt ? x.qb1 : x.qb0, h = tt ? x.h1 : x.h0;
+      const int q = qb * 128 + row;
+      // m: the row max in log2 units that the exponentials are taken against;
+      // it only moves when a block's max exceeds it by more than 8, so O in
+      // TMEM is rarely rescaled (O / l does not depend on the choice of m).
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < x.nkv; ++j) {
-        const long G = gb + j;
-        const int st = (int)(G & 1);
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full(st), (uint32_t)((G >> 1) & 1), abort_flag));
-        if (!ok) break;
+      // One key block: S from TMEM, P back over it.  Compiled twice, with the
+      // causal mask (the diagonal block and any block past it) and without.
+      auto block = [&](int j, long G, auto diag) -> bool {
+        constexpr bool DIAG = decltype(diag)::value;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(tt), (uint32_t)(G & 1), abort_flag))) return false;
         tc_fence_after();
         float s[128];
-        {  // the row's 128 scores: four loads in flight, one wait
+        {
           uint32_t r[4][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + st * 128 + 32 * c, r[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + s_col + 32 * c, r[c]);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[c][i]);
         }
-        tc_fence_before();
-        mbar_arrive(s_free(st));
-        if (j == x.qb) {  // diagonal block: keys after the query are masked
+        if (DIAG) {  // keys after the query are masked (every key of a block past the diagonal)
           const int lim = q - j * 128;
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i > lim) s[i] = -INFINITY;
         }
-        // row max with eight independent accumulators (short dependency chains)
+        // row max: eight chains of three-input maxima over columns 16..127
         float mx8[8];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = s[a];
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(s[a], s[a + 8]);
 #pragma unroll
-        for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int i = 16; i < 128; i += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx8[a] = max3f(mx8[a], s[i + a], s[i + 8 + a]);
+        float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         mx *= scale_log2;  // the scale is positive: the max commutes with it
         const bool grow = mx > m + 8.f;
         const float m_new = grow ? mx : m;
         const float corr = ex2_approx(m - m_new);  // 1 without growth, 0 on the first block
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // P_{j-1} V_{j-1} must have landed before the O row is rescaled
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(o_done((int)((G - 1) & 1)), (uint32_t)(((G - 1) >> 1) & 1), abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-            tmem_st_32x32b_x32(lane_base + O_COL + 32 * c, r);
-          }
-          tmem_st_wait();
-        }
+        // p = 2^(s * scale - m): the arguments and the partial row sums as
+        // paired fp32 operations, the exponentials on the special-function unit
         float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const float p = ex2_approx(fmaf(s[i], scale_log2, -m_new));
-          s[i] = p;
-          ps8[i & 7] += p;
+        for (int i = 0; i < 128; i += 2) {
+          fma2_scalar(s[i], s[i + 1], scale_log2, -m_new);
+          s[i] = ex2_approx(s[i]);
+          s[i + 1] = ex2_approx(s[i + 1]);
+          add2(ps8[i & 7], ps8[(i & 7) + 1], s[i], s[i + 1]);
         }
         const float ps = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
         l = l * corr + ps;
         m = m_new;
-        if (G >= 1) {  // P in TMEM was read by the previous P V (of this tile or the last)
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(o_done((int)((G - 1) & 1)), (uint32_t)(((G - 1) >> 1) & 1), abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // the row of P, bf16 pairs, into the TMEM A operand of P V
+        // the row of P, bf16 pairs, over the first 64 columns of S
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = pack2_bf16(s[64 * hh + 2 * i], s[64 * hh + 2 * i + 1]);
-          tmem_st_32x32b_x32(lane_base + P_COL + 32 * hh, pk);
+          tmem_st_32x32b_x32(lane_base + s_col + 32 * hh, pk);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // every P V of this tile so far has completed (the S commit covers
+          // them), and the next waits for this thread's P arrival below
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(lane_base + o_col + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+            tmem_st_32x32b_x32(lane_base + o_col + 32 * c, r);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(st));
+        mbar_arrive(p_full(tt));
+        return true;
+      };
+      for (int j = 0; j < x.nkv; ++j, ++G) {
+        ok = j >= qb ? block(j, G, std::true_type{}) : block(j, G, std::false_type{});
+        if (!ok) break;
       }
       if (!ok) break;
-      const long GL = gb + x.nkv - 1;  // the tile's last block
-      ok = __all_sync(0xffffffffu, mbar_wait(o_done((int)(GL & 1)), (uint32_t)((GL >> 1) & 1), abort_flag));
-      // the staging buffer is free once the previous tile's store has read it
-      if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait(st_free, (it - 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done(tt), (uint32_t)(it & 1), abort_flag));
+      // the staging buffer is free once the previous O tile's store has read it
+      const int c = 2 * it + tt;
+      if (ok && c > 0) ok = __all_sync(0xffffffffu, mbar_wait(st_free, (uint32_t)((c - 1) & 1), abort_flag));
       if (!ok) break;
       tc_fence_after();
       const float inv = 1.f / l;
@@ -419,14 +503,14 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
       // layout: box c / 2 holds columns [64 (c / 2), 64 (c / 2) + 64)
       const uint32_t orow = sO + (uint32_t)row * 128u;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int cc = 0; cc < HD / 32; ++cc) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_base + O_COL + 32 * c, r);
+        tmem_ld_32x32b_x32(lane_base + o_col + 32 * cc, r);
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int chunk = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
-          const uint32_t addr = orow + (c >> 1) * 16384 + (uint32_t)((chunk ^ (row & 7)) * 16);
+          const int chunk = (cc & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
+          const uint32_t addr = orow + (cc >> 1) * 16384 + (uint32_t)((chunk ^ (row & 7)) * 16);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                        "r"(pack2_bf16(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv)),
                        "r"(pack2_bf16(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv)),
@@ -435,12 +519,12 @@ __global__ void __launch_bounds__(kAttFwdThreads, 1)
                        : "memory");
         }
       }
+      // O has left TMEM: the next item's first P V of this tile (issued after
+      // this thread's next P arrival) may overwrite it
       tc_fence_before();
-      mbar_arrive(o_free);  // O has left TMEM
       fence_proxy_async_smem();
       mbar_arrive(st_ready);
-      if (q < S) lse[((int64_t)x.b * Hq + x.h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
-      gb += x.nkv;
+      if (q < S) lse[((int64_t)x.b * Hq + h) * S + q] = (m + log2f(l)) * 0.69314718055994531f;
     }
     if (!ok && lane == 0) {
       record_error(err, kDevAttnTimeout);
@@ -1256,9 +1340,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_att() {
 }
 
 template <int HD>
-int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq, int Hkv,
+int fwd_pp(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S, int Hq, int Hkv,
            int* err, cudaStream_t st) {
-  using C = AttCfg<HD>;
+  using C = AttFwd2Cfg<HD>;
   auto fn = encode_fn_att();
   if (!fn) return -3;
   const int64_t W = (int64_t)(Hq + 2 * Hkv) * HD, WO = (int64_t)Hq * HD;
@@ -1276,12 +1360,15 @@ int fwd_tc(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int S,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -3;
-  if (!smem_attr_set(reinterpret_cast<const void*>(attn_fwd_tc_kernel<HD>), C::SMEM)) return -3;
-  // persistent: one CTA per SM walks the tiles in longest-first order
-  const int tiles = ((S + 127) / 128) * Hq * B;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  attn_fwd_tc_kernel<HD><<<grid, kAttFwdThreads, C::SMEM, st>>>(tm, tm_o, lse, S, Hq, Hkv, B,
-                                                                1.4426950408889634f / sqrtf((float)HD), err);
+  if (!smem_attr_set(reinterpret_cast<const void*>(attn_fwd_pp_kernel<HD>), C::SMEM)) return -3;
+  // two query heads of a group per item when the group size is even, else
+  // two consecutive query blocks of one head
+  const int pair_heads = (Hq / Hkv) % 2 == 0 ? 1 : 0;
+  const int nqb = (S + 127) / 128;
+  const int items = pair_heads ? nqb * (Hq / 2) * B : ((nqb + 1) / 2) * Hq * B;
+  const int grid = items < num_sms() ? items : num_sms();
+  attn_fwd_pp_kernel<HD><<<grid, kAttFwd2Threads, C::SMEM, st>>>(
+      tm, tm_o, lse, S, Hq, Hkv, B, 1.4426950408889634f / sqrtf((float)HD), pair_heads, err);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1388,8 +1475,8 @@ int attn_fwd(const __nv_bfloat16* qkv, __nv_bfloat16* o, float* lse, int B, int 
   if (B <= 0 || S <= 0) return 0;
   if (Hkv <= 0 || Hq % Hkv) return -1;
   if ((reinterpret_cast<uintptr_t>(qkv) & 15) != 0) return -1;
-  if (hd == 64) return fwd_tc<64>(qkv, o, lse, B, S, Hq, Hkv, err, st);
-  if (hd == 128) return fwd_tc<128>(qkv, o, lse, B, S, Hq, Hkv, err, st);
+  if (hd == 64) return fwd_pp<64>(qkv, o, lse, B, S, Hq, Hkv, err, st);
+  if (hd == 128) return fwd_pp<128>(qkv, o, lse, B, S, Hq, Hkv, err, st);
   return -1;
 }
 

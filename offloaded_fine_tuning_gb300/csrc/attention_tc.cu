@@ -81,6 +81,29 @@ __device__ __forceinline__ void fma2_scalar(float& x, float& y, float c, float d
       : "f"(c), "f"(d));
 }
 
+// (x, y) * c + (d0, d1) as one paired fp32 FMA (round to nearest)
+__device__ __forceinline__ void fma2(float& x, float& y, float c, float d0, float d1) {
+  asm("{\n\t.reg .b64 t, u, w;\n\t"
+      "mov.b64 t, {%0, %1};\n\t"
+      "mov.b64 u, {%2, %2};\n\t"
+      "mov.b64 w, {%3, %4};\n\t"
+      "fma.rn.f32x2 t, t, u, w;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "+f"(x), "+f"(y)
+      : "f"(c), "f"(d0), "f"(d1));
+}
+
+// (x, y) *= (a, b) as one paired fp32 multiply
+__device__ __forceinline__ void mul2(float& x, float& y, float a, float b) {
+  asm("{\n\t.reg .b64 t, u;\n\t"
+      "mov.b64 t, {%0, %1};\n\t"
+      "mov.b64 u, {%2, %3};\n\t"
+      "mul.rn.f32x2 t, t, u;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t}"
+      : "+f"(x), "+f"(y)
+      : "f"(a), "f"(b));
+}
+
 // (x, y) += (a, b) as one paired fp32 add
 __device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
   asm("{\n\t.reg .b64 t, u;\n\t"
@@ -1024,20 +1047,28 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     bool ok = mbar_wait(kv_full, 0, abort_flag);
+    // Descriptors of each operand's first row (K-major views, then the
+    // MN-major views of the P V-style products); an operand at byte offset o
+    // is the base plus o / 16 (shared addresses stay below 2^18, so the
+    // 14-bit address field cannot carry).
+    const uint64_t dK = smem_desc_sw128(sK, 16, 1024), dV = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t dQk = smem_desc_sw128(sQ, 16, 1024), dDOk = smem_desc_sw128(sDO, 16, 1024);
+    const uint64_t dPt = smem_desc_sw128(sPt, 16, 1024), dDSt = smem_desc_sw128(sDSt, 16, 1024);
+    const uint64_t dQm = smem_desc_sw128(sQ, 8192, 1024), dDOm = smem_desc_sw128(sDO, 8192, 1024);
+    const uint64_t dKm = smem_desc_sw128(sK, 16384, 1024), dDStm = smem_desc_sw128(sDSt, 16384, 1024);
     for (int it = 0; ok && it <= n_it; ++it) {
       if (it < n_it) {  // S^T and dP^T of block it, once the threads hold block it - 1's
         const int bq = it % C::NQ;
         if (!mbar_wait(qdo_full(bq), (it / C::NQ) & 1, abort_flag)) { ok = false; break; }
         if (it >= 1 && !mbar_wait(s_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t qo = (uint32_t)bq * (uint32_t)(C::QT / 16);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;   // K / V: 128-row boxes
-          const uint32_t qa = (kk >> 2) * 8192 + (kk & 3) * 32;    // Q / dO: 64-row boxes
-          umma_bf16(tmem_base, smem_desc_sw128(sK + ka, 16, 1024),
-                    smem_desc_sw128(sQ + bq * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
-          umma_bf16(tmem_base + COL_DP, smem_desc_sw128(sV + ka, 16, 1024),
-                    smem_desc_sw128(sDO + bq * C::QT + qa, 16, 1024), ID_SP, kk > 0 ? 1u : 0u);
+          const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) / 16;  // K / V: 128-row boxes
+          const uint32_t qa = ((kk >> 2) * 8192 + (kk & 3) * 32) / 16;    // Q / dO: 64-row boxes
+          umma_bf16(tmem_base, dK + ka, dQk + qo + qa, ID_SP, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem_base + COL_DP, dV + ka, dDOk + qo + qa, ID_SP, kk > 0 ? 1u : 0u);
         }
         umma_commit(sp_full);
       }
@@ -1046,18 +1077,16 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
         if (!mbar_wait(ps_full, ip & 1, abort_flag)) { ok = false; break; }
         if (ip >= 2 && !mbar_wait(dq_free(bd), ((ip >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t qo = (uint32_t)bq * (uint32_t)(C::QT / 16);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // over the 64 queries
           const uint32_t acc = (ip > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16(tmem_base + COL_DV, smem_desc_sw128(sPt + kk * 32, 16, 1024),
-                    smem_desc_sw128(sDO + bq * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
-          umma_bf16(tmem_base + COL_DK, smem_desc_sw128(sDSt + kk * 32, 16, 1024),
-                    smem_desc_sw128(sQ + bq * C::QT + kk * 2048, 8192, 1024), ID_KV, acc);
+          umma_bf16(tmem_base + COL_DV, dPt + kk * 2, dDOm + qo + kk * 128, ID_KV, acc);
+          umma_bf16(tmem_base + COL_DK, dDSt + kk * 2, dQm + qo + kk * 128, ID_KV, acc);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // over the 128 keys
-          umma_bf16(tmem_base + COL_DQ + 64 * bd, smem_desc_sw128(sK + kk * 2048, 16384, 1024),
-                    smem_desc_sw128(sDSt + kk * 2048, 16384, 1024), ID_Q, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem_base + COL_DQ + 64 * bd, dKm + kk * 128, dDStm + kk * 128, ID_Q, kk > 0 ? 1u : 0u);
         umma_commit(dq_full(bd));
         umma_commit(qdo_empty(bq));
         umma_commit(pds_free);
@@ -1177,12 +1206,23 @@ __global__ void __launch_bounds__(kAttBwd2Threads, 1)
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], sv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 4; i += 2) {
             const int e = 4 * k + i;
-            float x = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -lv[i]));
-            if (kMask && !(qb + e < S && key <= qb + e)) x = 0.f;
-            pv[i] = x;
-            sv[i] = x * (__uint_as_float(dr[e]) - dv[i]);
+            // (x0, x1) = s * scale_log2 - lse * log2(e), one paired FMA
+            float x0 = __uint_as_float(sr[e]), x1 = __uint_as_float(sr[e + 1]);
+            fma2(x0, x1, scale_log2, -lv[i], -lv[i + 1]);
+            x0 = ex2_approx(x0);
+            x1 = ex2_approx(x1);
+            if (kMask && !(qb + e < S && key <= qb + e)) x0 = 0.f;
+            if (kMask && !(qb + e + 1 < S && key <= qb + e + 1)) x1 = 0.f;
+            pv[i] = x0;
+            pv[i + 1] = x1;
+            // dS = P (dP - D): a paired subtract and a paired multiply
+            float d0 = __uint_as_float(dr[e]), d1 = __uint_as_float(dr[e + 1]);
+            add2(d0, d1, -dv[i], -dv[i + 1]);
+            mul2(d0, d1, x0, x1);
+            sv[i] = d0;
+            sv[i + 1] = d1;
           }
           pp[2 * k] = pack2_bf16(pv[0], pv[1]);
           pp[2 * k + 1] = pack2_bf16(pv[2], pv[3]);

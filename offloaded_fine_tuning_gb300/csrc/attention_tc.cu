@@ -151,14 +151,13 @@ constexpr int kAttFwd2Threads = 352;
 template <int HD>
 struct AttFwd2Cfg {
   static constexpr int TILE = HD / 64 * 16384;  // 128 rows x HD bf16
-  static constexpr int KST = HD == 128 ? 2 : 4;
-  static constexpr int VST = 2;
+  static constexpr int NE = HD == 128 ? 2 : 4;  // stages of the K/V ring (K and V tiles each)
   static constexpr int OFF_Q = 0;  // Q of tile 0, then of tile 1
   static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + KST * TILE;
-  static constexpr int OFF_O = OFF_V + VST * TILE;  // staging of an O tile for its TMA store
+  static constexpr int OFF_V = OFF_K + NE * TILE;
+  static constexpr int OFF_O = OFF_V + NE * TILE;  // staging of an O tile for its TMA store
   static constexpr int OFF_BAR = OFF_O + TILE;
-  static constexpr int NBAR = 13 + 2 * KST + 2 * VST;
+  static constexpr int NBAR = 13 + 2 * NE;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 static_assert(AttFwd2Cfg<128>::SMEM <= 232448, "forward shared memory");
@@ -191,10 +190,12 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
   const uint32_t st_ready = b0 + 8u * 10;  // an O tile's rows are in the staging buffer
   const uint32_t st_free = b0 + 8u * 11;   // the staging buffer has been read by the TMA store
   const uint32_t drain = b0 + 8u * 12;
-  auto k_full = [&](int s) { return b0 + 8u * (13 + s); };
-  auto k_empty = [&](int s) { return b0 + 8u * (13 + C::KST + s); };
-  auto v_full = [&](int s) { return b0 + 8u * (13 + 2 * C::KST + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (13 + 2 * C::KST + C::VST + s); };
+  // Entry e of the K/V ring holds K(e) in K stage e % NE and V(e - 1) in V
+  // stage (e - 1) % NE, G counting key blocks over all items of the CTA: the
+  // MMA step of block G reads V(G) and K(G + 1), i.e. entry G + 1, and frees
+  // it at the step's end.
+  auto kv_full = [&](int s) { return b0 + 8u * (13 + s); };
+  auto kv_empty = [&](int s) { return b0 + 8u * (13 + C::NE + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -235,13 +236,9 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
       mbar_init(p_full(t), 128);
       mbar_init(o_done(t), 1);
     }
-    for (int s = 0; s < C::KST; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
-    }
-    for (int s = 0; s < C::VST; ++s) {
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+    for (int s = 0; s < C::NE; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
     }
     mbar_init(st_ready, 128);
     mbar_init(st_free, 1);
@@ -262,24 +259,40 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    // Per item: K(0), both Q tiles (each once the previous item's last S of
-    // that tile has read the buffer), V(0), K(1), V(1), ...
+    // Entries in order: entry e carries K(e) and V(e - 1); both Q tiles of an
+    // item follow the entry with the item's first K (each once the previous
+    // item's last S of that tile has read the buffer); a last entry carries
+    // the last V alone.
     bool ok = true;
-    long gk = 0, gv = 0;
+    long e = 0;  // entries issued
     int it = 0, q_issued[2] = {-1, -1};
+    int pv_col = 0, pv_row = 0, pv_b = 0;  // where the previous block's V comes from
+    auto entry = [&](bool with_k, int colK, int krow, int kb) -> bool {
+      const int st = (int)(e % C::NE);
+      if (!mbar_wait(kv_empty(st), (uint32_t)((e / C::NE) & 1) ^ 1u, abort_flag)) return false;
+      mbar_arrive_expect_tx(kv_full(st), (uint32_t)((with_k ? C::TILE : 0) + (e > 0 ? C::TILE : 0)));
+      if (with_k) {
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          tma_load_3d(sK + st * C::TILE + c * 16384, &tm, kv_full(st), colK + 64 * c, krow, kb);
+      }
+      if (e > 0) {
+        const int vs = (int)((e - 1) % C::NE);
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          tma_load_3d(sV + vs * C::TILE + c * 16384, &tm, kv_full(st), pv_col + 64 * c, pv_row, pv_b);
+      }
+      ++e;
+      return true;
+    };
     for (int t = blockIdx.x; ok && t < num_items; t += gridDim.x, ++it) {
       const Item x = item_of(t);
       const int colK = (Hq + x.g) * HD, colV = (Hq + Hkv + x.g) * HD;
       for (int j = 0; j < x.nkv; ++j) {
-        {
-          const int st = (int)(gk % C::KST);
-          if (!mbar_wait(k_empty(st), (uint32_t)((gk / C::KST) & 1) ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(k_full(st), C::TILE);
-#pragma unroll
-          for (int c = 0; c < NB; ++c)
-            tma_load_3d(sK + st * C::TILE + c * 16384, &tm, k_full(st), colK + 64 * c, j * 128, x.b);
-          ++gk;
-        }
+        if (!entry(true, colK, j * 128, x.b)) { ok = false; break; }
+        pv_col = colV;
+        pv_row = j * 128;
+        pv_b = x.b;
         if (j == 0) {
           for (int tt = 0; tt < 2; ++tt) {
             if (it > 0 && !mbar_wait(q_empty(tt), (uint32_t)((it - 1) & 1), abort_flag)) { ok = false; break; }
@@ -292,27 +305,17 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
           }
           if (!ok) break;
         }
-        {
-          const int st = (int)(gv % C::VST);
-          if (!mbar_wait(v_empty(st), (uint32_t)((gv / C::VST) & 1) ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(v_full(st), C::TILE);
-#pragma unroll
-          for (int c = 0; c < NB; ++c)
-            tma_load_3d(sV + st * C::TILE + c * 16384, &tm, v_full(st), colV + 64 * c, j * 128, x.b);
-          ++gv;
-        }
       }
     }
+    if (ok && e > 0 && !entry(false, 0, 0, 0)) ok = false;  // the last V
     if (!ok) {
       record_error(err, kDevAttnTimeout);
       *abort_flag = 1;
       // let the copies already issued land before the CTA's shared memory goes away
       for (int tt = 0; tt < 2; ++tt)
         if (q_issued[tt] >= 0) mbar_wait(q_full(tt), (uint32_t)(q_issued[tt] & 1), nullptr);
-      for (long k = gk - 1; k >= 0 && k >= gk - C::KST; --k)
-        mbar_wait(k_full((int)(k % C::KST)), (uint32_t)((k / C::KST) & 1), nullptr);
-      for (long k = gv - 1; k >= 0 && k >= gv - C::VST; --k)
-        mbar_wait(v_full((int)(k % C::VST)), (uint32_t)((k / C::VST) & 1), nullptr);
+      for (long k = e - 1; k >= 0 && k >= e - C::NE; --k)
+        mbar_wait(kv_full((int)(k % C::NE)), (uint32_t)((k / C::NE) & 1), nullptr);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
     const uint64_t dV = smem_desc_sw128(sV, 16384, 1024);
     // S_t = Q_t K(G)^T into the S columns of tile t
     auto issue_s = [&](int tt, long G) {
-      const uint32_t ks = (uint32_t)(G % C::KST);
+      const uint32_t ks = (uint32_t)(G % C::NE);
       const uint64_t a0 = dQ + (uint32_t)(tt * C::TILE / 16), b0 = dK + ks * (uint32_t)(C::TILE / 16);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
     if (t < num_items) {  // the first item's S of both tiles
       const Item x = item_of(t);
       for (int tt = 0; ok && tt < 2; ++tt) {
-        if ((tt == 0 && !mbar_wait(k_full(0), 0, abort_flag)) || !mbar_wait(q_full(tt), 0, abort_flag)) {
+        if ((tt == 0 && !mbar_wait(kv_full(0), 0, abort_flag)) || !mbar_wait(q_full(tt), 0, abort_flag)) {
           ok = false;
           break;
         }
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
         issue_s(tt, 0);
         if (x.nkv == 1) umma_commit(q_empty(tt));
       }
-      if (ok) umma_commit(k_empty(0));
+      if (ok) umma_commit(kv_empty(0));  // entry 0: K(0) alone
     }
     for (; ok && t < num_items; t += gridDim.x, ++it) {
       const Item x = item_of(t);
@@ -359,10 +362,14 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
         const long Gn = G + 1;
         // the next block's S: the last of its item releases that item's Q tile
         const bool next_is_last = last ? nkv_next == 1 : j + 2 == x.nkv;
-        const int vs = (int)(G % C::VST);
+        const int vs = (int)(G % C::NE);
+        const int es = (int)(Gn % C::NE);  // entry G + 1: V(G) and K(G + 1)
+        if (!mbar_wait(kv_full(es), (uint32_t)((Gn / C::NE) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
         for (int tt = 0; tt < 2; ++tt) {
-          if (!mbar_wait(p_full(tt), (uint32_t)(G & 1), abort_flag) ||
-              (tt == 0 && !mbar_wait(v_full(vs), (uint32_t)((G / C::VST) & 1), abort_flag))) {
+          if (!mbar_wait(p_full(tt), (uint32_t)(G & 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -372,20 +379,19 @@ __global__ void __launch_bounds__(kAttFwd2Threads, 1)
           for (int kk = 0; kk < 8; ++kk)  // O_t += P_t V: P as the tensor-memory A operand
             umma_bf16_ts(tmem_base + O_COL + tt * HD, tmem_base + tt * 128 + kk * 8, bv + kk * (2048 / 16),
                          ID_O, (j > 0 || kk > 0) ? 1u : 0u);
-          if (tt == 1) umma_commit(v_empty(vs));
           if (last) umma_commit(o_done(tt));
           if (has_next) {
-            if ((tt == 0 && !mbar_wait(k_full((int)(Gn % C::KST)), (uint32_t)((Gn / C::KST) & 1), abort_flag)) ||
-                (last && !mbar_wait(q_full(tt), (uint32_t)((it + 1) & 1), abort_flag))) {
+            if (last && !mbar_wait(q_full(tt), (uint32_t)((it + 1) & 1), abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_s(tt, Gn);
-            if (tt == 1) umma_commit(k_empty((int)(Gn % C::KST)));
             if (next_is_last) umma_commit(q_empty(tt));
           }
         }
+        if (!ok) break;
+        umma_commit(kv_empty(es));  // V(G) and K(G + 1) have been read
       }
     }
     if (!ok) {

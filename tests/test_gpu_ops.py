@@ -368,7 +368,10 @@ ATTN_CASES = [(2, 200, 6, 2, 64), (1, 130, 4, 1, 128), (1, 64, 2, 2, 64), (2, 1,
               (1, 300, 12, 1, 128), (1, 64, 2, 2, 128), (3, 257, 8, 2, 128), (1, 40, 4, 4, 128),
               (2, 150, 8, 2, 64),
               # more (query block, head) tiles than SMs: some persistent CTAs take two
-              (1, 1100, 20, 4, 128)]
+              (1, 1100, 20, 4, 128),
+              # odd group size (query blocks paired per head), an odd number of
+              # query blocks, and more items than SMs (CTAs walk two or more)
+              (3, 1100, 20, 4, 128)]
 
 
 def attn_inputs(B, S, Hq, Hkv, hd, seed=1):

@@ -621,12 +621,16 @@ def run_lce(args):
     clk = clocks.stop()
     assert sf.device_error() == 0
     ms = e0.elapsed_time(e1) / args.steps
-    # end to end through the public call on host buffers (bf16 bits)
-    hbits = hb.view(torch.int16).numpy().view(np.uint16)
-    wbits = wb.view(torch.int16).numpy().view(np.uint16)
+    # end to end through the public call on host buffers (bf16 bits), in
+    # page-locked memory as a training loop would keep them
+    hbits = hb.view(torch.int16).pin_memory().numpy().view(np.uint16)
+    wbits = wb.view(torch.int16).pin_memory().numpy().view(np.uint16)
+    labp = torch.from_numpy(lab.astype(np.int32)).pin_memory().numpy()
+    dh_host = torch.empty((n, d), dtype=torch.int16).pin_memory().numpy().view(np.uint16)
+    dw_host = torch.empty((V, d), dtype=torch.float32).pin_memory().numpy()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        l_host, _, _ = sf.lce_step(hbits, wbits, lab)
+        l_host, _, _ = sf.lce_step(hbits, wbits, labp, dh_out=dh_host, dw_out=dw_host)
     e2e_s = (time.perf_counter() - t0) / args.steps
     flops = 3 * 2.0 * n * V * d
     tf = flops / (ms / 1e3) / 1e12

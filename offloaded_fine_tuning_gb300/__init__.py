@@ -354,17 +354,24 @@ def op_attn_fwd(qkv, o, lse, B, S, Hq, Hkv, hd, stream=0) -> int:
 
 
 def lce_step(h_bf16: np.ndarray, w_bf16: np.ndarray, labels: np.ndarray,
-             ignore_index: int = IGNORE_INDEX, model=None):
+             ignore_index: int = IGNORE_INDEX, model=None, dh_out=None, dw_out=None):
     """Fused LM head + cross-entropy on host arrays (uint16 bf16 bits):
-    returns (loss, dh as uint16 bf16 bits [n, d], dw fp32 [v, d])."""
+    returns (loss, dh as uint16 bf16 bits [n, d], dw fp32 [v, d]).  dh_out
+    and dw_out, if given, are contiguous arrays of those shapes and types
+    that receive the gradients (page-locked ones let the copies run at the
+    link's rate)."""
     h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
     w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
     y = np.ascontiguousarray(labels, dtype=np.int32).reshape(-1)
     n, d = h.shape
     v = w.shape[0]
     loss = _F32()
-    dh = np.empty((n, d), dtype=np.uint16)
-    dw = np.empty((v, d), dtype=np.float32)
+    dh = np.empty((n, d), dtype=np.uint16) if dh_out is None else dh_out
+    dw = np.empty((v, d), dtype=np.float32) if dw_out is None else dw_out
+    if dh.shape != (n, d) or dh.dtype != np.uint16 or not dh.flags.c_contiguous:
+        raise ValueError("lce_step: dh_out must be a contiguous uint16 array of shape (n, d)")
+    if dw.shape != (v, d) or dw.dtype != np.float32 or not dw.flags.c_contiguous:
+        raise ValueError("lce_step: dw_out must be a contiguous float32 array of shape (v, d)")
     st = lib().sf_lce_step(model.h if model is not None else None, h.ctypes.data, w.ctypes.data,
                            y.ctypes.data, n, d, v, ignore_index, ctypes.byref(loss),
                            dh.ctypes.data, dw.ctypes.data)

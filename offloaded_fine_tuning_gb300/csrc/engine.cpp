@@ -937,6 +937,9 @@ struct Timed {
 
 // A GEMM with the fused epilogues' extra arguments (flops: the algorithmic
 // count when it is not 2*M*N*K, e.g. the gated tile's two products).
+// Vocabulary ranges of the LM head's dH product (split-K, fixed-order sum).
+constexpr int kHeadSplitK = 4;
+
 int gemm_args(sf_ctx* ctx, const sf::GemmArgs& g, double flops = 0.0) {
   int st;
   char why[128] = {0};
@@ -1117,7 +1120,16 @@ int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
     // fp32 logits of the chunk; the row softmax writes dZ (bf16) beside them
     RET(gemm(c, sf::kNT, sf::kEpiF32, n, V, d, c->hf + r0 * d, d, c->Wlm, d, c->zf, V));
     sf::ce_rows_f32(c->zf, c->dz, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0, c->sC);
-    RET(gemm(c, sf::kNN, sf::kEpiF32, n, d, V, c->dz, V, c->Wlm, d, c->dhf + r0 * d, d));
+    {  // dH = dZ W_lm, over up to kHeadSplitK vocabulary ranges when that fills
+       // the SMs better; the partial sums go to the chunk's fp32 logits, which
+       // the cross-entropy kernel has already read
+      sf::GemmArgs g;
+      g.layout = sf::kNN; g.epi = sf::kEpiF32; g.M = n; g.N = d; g.K = V;
+      g.A = c->dz; g.lda = V; g.B = c->Wlm; g.ldb = d; g.C = c->dhf + r0 * d; g.ldc = d;
+      g.splitk_max = (int)std::min<int64_t>(kHeadSplitK, 1 + (c->chunk_rows * V) / (n * d));
+      g.ws = c->zf;
+      RET(gemm_args(c, g));
+    }
     // dW_lm: fp32 sums over the chunks; the last chunk's product adds the sum
     // and rounds the bf16 gradient in its epilogue
     if (last && !c->f16g)

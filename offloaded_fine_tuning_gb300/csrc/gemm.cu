@@ -54,6 +54,9 @@ struct GemmParams {
   float* aux;                 // kEpiGLU: fp32 a | b (or null)
   int64_t ldaux;
   int group;                  // work-unit order (tile_coords)
+  int splitk;                 // K ranges (kEpiF32): split s > 0 writes ws + (s - 1) * ws_stride
+  float* ws;
+  int64_t ws_stride;
 };
 
 // Output columns of one work unit: the gated tile computes a and b for 128
@@ -427,13 +430,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // work units: CL M-tiles of one N-tile, one per CTA of the cluster
+  // work units: CL M-tiles of one N-tile, one per CTA of the cluster, times
+  // the K ranges (all tiles of range 0 first)
   const int num_m = (p.M + kBM - 1) / kBM;
   const int num_mu = (num_m + CL - 1) / CL;
   const int num_n = (p.N + UC - 1) / UC;
-  const int num_units = num_mu * num_n;
+  const int num_mn = num_mu * num_n;
+  const int splitk = p.splitk > 1 ? p.splitk : 1;
+  const int num_units = num_mn * splitk;
   const int unit0 = (int)blockIdx.x / CL, unit_step = (int)gridDim.x / CL;
   const int nk = (p.K + kBK - 1) / kBK;
+  const int kps = (nk + splitk - 1) / splitk;  // k-blocks per range (the host keeps every range non-empty)
+  auto krange = [&](int unit, int& umn, int& kb0, int& kb1) {
+    const int ks = unit / num_mn;
+    umn = unit - ks * num_mn;
+    kb0 = ks * kps;
+    kb1 = kb0 + kps < nk ? kb0 + kps : nk;
+  };
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
@@ -442,10 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     long issued = 0;
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
-      int tmu, tn;
-      tile_coords(unit, num_mu, num_n, p.group, tmu, tn);
+      int tmu, tn, umn, kb0, kb1;
+      krange(unit, umn, kb0, kb1);
+      tile_coords(umn, num_mu, num_n, p.group, tmu, tn);
       const int m0 = (tmu * CL + crank) * kBM, n0 = tn * BN;
-      for (int kb = 0; kb < nk; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         // the stage is free once the MMAs that read it (the pair's, for a pair) completed
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const int k0 = kb * kBK;
@@ -528,7 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < nk; ++kb) {
+      int umn, kb0, kb1;
+      krange(unit, umn, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a_base = sA + stage * A_BYTES, b_base = sB + stage * B_BYTES;
@@ -539,8 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           else ad = smem_desc_sw128(a_base + k * 32, 16, 1024);
           if constexpr (B_MN) bd = smem_desc_sw128(b_base + k * 2048, 8192, 1024);
           else bd = smem_desc_sw128(b_base + k * 32, 16, 1024);
-          if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-          else umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+          if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, accum);
+          else umma_bf16(d_tmem, ad, bd, IDESC, accum);
         }
         if constexpr (PAIR) umma_commit_pair(empty_bar(stage), kPair);
         else umma_commit(empty_bar(stage));
@@ -562,8 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     int iter = 0;
     for (int unit = unit0; unit < num_units; unit += unit_step, ++iter) {
-      int tmu, tn;
-      tile_coords(unit, num_mu, num_n, p.group, tmu, tn);
+      int tmu, tn, umn, kb0, kb1;
+      krange(unit, umn, kb0, kb1);
+      tile_coords(umn, num_mu, num_n, p.group, tmu, tn);
       const int tm = tmu * CL + crank;
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
@@ -602,13 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row < p.M) epi_glu(p, row, col, ra, rb);
         }
       } else {
+        // a K range after the first (kEpiF32) writes into its workspace slice
+        GemmParams q = p;
+        if constexpr (EPI == kEpiF32) {
+          if (unit >= num_mn) q.C = p.ws + (int64_t)(unit / num_mn - 1) * p.ws_stride;
+        }
         for (int c = 0; c < BN; c += 32) {
           const int col = tn * BN + c;
           if (col >= p.N) break;  // uniform across the warp
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c, r);
           tmem_ld_wait();
-          if (row < p.M) epi_store<EPI>(p, row, col, r);
+          if (row < p.M) epi_store<EPI>(q, row, col, r);
         }
       }
       tc_fence_before();
@@ -745,7 +768,7 @@ static int launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
     }
     ctas = max_ctas[dev];
   }
-  const int units = ((p.M + kBM * CL - 1) / (kBM * CL)) * ((p.N + UC - 1) / UC);
+  const int units = ((p.M + kBM * CL - 1) / (kBM * CL)) * ((p.N + UC - 1) / UC) * (p.splitk > 1 ? p.splitk : 1);
   cfg.gridDim = dim3(units * CL < ctas ? units * CL : ctas);
   cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
   cudaError_t e = cudaGetLastError();
@@ -865,6 +888,46 @@ static int unit_order(int64_t M, int64_t N, int64_t K, int BN, bool gated) {
   return 8;
 }
 
+// C[r, c] += sum over s of ws[s][r, c], s in order: the partial sums of the
+// K ranges after the first, so the result does not depend on timing.
+__global__ void splitk_sum_kernel(float* __restrict__ C, int64_t ldc, const float* __restrict__ ws,
+                                  int64_t stride, int64_t M, int64_t N, int parts) {
+  const int64_t n4 = N / 4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < M * n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / n4, c = (i - r * n4) * 4;
+    float4 v = *reinterpret_cast<const float4*>(C + r * ldc + c);
+    for (int s = 0; s < parts; ++s) {
+      const float4 w = *reinterpret_cast<const float4*>(ws + s * stride + r * ldc + c);
+      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+    }
+    *reinterpret_cast<float4*>(C + r * ldc + c) = v;
+  }
+}
+
+// Number of K ranges for a plain fp32 GEMM: the one of 1..max whose work
+// units fill the waves of pairs (or CTAs) best, each range keeping at least
+// 16 k-blocks; ties go to fewer ranges.
+static int choose_splitk(int64_t M, int64_t N, int64_t K, int BN, int max_split) {
+  const int64_t CL = gemm_cluster(BN);
+  const int64_t mn = ((M + kBM * CL - 1) / (kBM * CL)) * ((N + BN - 1) / BN);
+  const int64_t slots = std::max<int64_t>(1, num_sms() / CL);
+  const int64_t nk = (K + kBK - 1) / kBK;
+  int best = 1;
+  double best_eff = 0;
+  for (int s = 1; s <= max_split; ++s) {
+    const int64_t kps = (nk + s - 1) / s;
+    if (s > 1 && (kps < 16 || (s - 1) * kps >= nk)) break;
+    const int64_t units = mn * s;
+    const double eff = (double)units / (double)(((units + slots - 1) / slots) * slots);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
 int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   if (a.M == 0 || a.N == 0) return 0;
   if (int c = gemm_check(a, why)) return c;
@@ -888,17 +951,36 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
     snprintf(why, 64, "gemm: tensor map encode failed");
     return -3;
   }
+  const bool can_split = a.epi == kEpiF32 && a.ws != nullptr && a.splitk_max > 1 && a.N % 4 == 0 &&
+                         a.ldc % 4 == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(a.ws) & 15) == 0;
+  const int splitk = can_split ? choose_splitk(a.M, a.N, a.K, BN, a.splitk_max) : 1;
   GemmParams p{(int)a.M, (int)a.N, (int)a.K, a.C, a.ldc, a.R, a.ldr, a.alpha, dev_err,
                reinterpret_cast<const __nv_bfloat16*>(a.bias), a.cs, a.seq, a.rope_cols, a.hd,
-               a.aux, a.ldaux, unit_order(a.M, a.N, a.K, BN, gated)};
+               a.aux, a.ldaux, unit_order(a.M, a.N, a.K, BN, gated), splitk, a.ws, a.M * a.ldc};
+  int rc;
   if (BN == 256) {
-    if (a.layout == kNT) return launch_epi<false, false, 256>(a.epi, ta, tb, tb2, p, st, why);
-    if (a.layout == kNN) return launch_epi<false, true, 256>(a.epi, ta, tb, tb2, p, st, why);
-    return launch_epi<true, true, 256>(a.epi, ta, tb, tb2, p, st, why);
+    if (a.layout == kNT) rc = launch_epi<false, false, 256>(a.epi, ta, tb, tb2, p, st, why);
+    else if (a.layout == kNN) rc = launch_epi<false, true, 256>(a.epi, ta, tb, tb2, p, st, why);
+    else rc = launch_epi<true, true, 256>(a.epi, ta, tb, tb2, p, st, why);
+  } else if (a.layout == kNT) {
+    rc = launch_epi<false, false, 128>(a.epi, ta, tb, tb2, p, st, why);
+  } else if (a.layout == kNN) {
+    rc = launch_epi<false, true, 128>(a.epi, ta, tb, tb2, p, st, why);
+  } else {
+    rc = launch_epi<true, true, 128>(a.epi, ta, tb, tb2, p, st, why);
   }
-  if (a.layout == kNT) return launch_epi<false, false, 128>(a.epi, ta, tb, tb2, p, st, why);
-  if (a.layout == kNN) return launch_epi<false, true, 128>(a.epi, ta, tb, tb2, p, st, why);
-  return launch_epi<true, true, 128>(a.epi, ta, tb, tb2, p, st, why);
+  if (rc == 0 && splitk > 1) {
+    const int64_t n = a.M * (a.N / 4);
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
+    splitk_sum_kernel<<<blocks, 256, 0, st>>>(static_cast<float*>(a.C), a.ldc, a.ws, a.M * a.ldc, a.M,
+                                              a.N, splitk - 1);
+    if (cudaGetLastError() != cudaSuccess) {
+      snprintf(why, 64, "gemm: split-K sum launch failed");
+      return -3;
+    }
+  }
+  return rc;
 }
 
 }  // namespace sf

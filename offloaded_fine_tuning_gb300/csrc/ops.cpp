@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -237,9 +238,13 @@ int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64
     z.A = H + r0 * d; z.lda = d; z.B = W; z.ldb = d; z.C = zf; z.ldc = v;
     if (sf::gemm(z, err, st, why) != 0) return SF_ECUDA;
     sf::ce_rows_f32(zf, dz, labels + r0, rows, v, inv_n, loss_rows + r0, st);
+    // dH over up to four vocabulary ranges when that fills the SMs better; the
+    // partial sums go to the chunk's fp32 logits, which the row kernel has read
     sf::GemmArgs gx;
     gx.layout = sf::kNN; gx.epi = sf::kEpiF32; gx.M = rows; gx.N = d; gx.K = v;
     gx.A = dz; gx.lda = v; gx.B = W; gx.ldb = d; gx.C = dh + r0 * d; gx.ldc = d;
+    gx.splitk_max = (int)std::min<int64_t>(4, 1 + (c * (int64_t)v) / (rows * (int64_t)d));
+    gx.ws = zf;
     if (sf::gemm(gx, err, st, why) != 0) return SF_ECUDA;
     sf::GemmArgs gw;
     gw.layout = sf::kTN; gw.epi = r0 == 0 ? sf::kEpiF32 : sf::kEpiF32Acc; gw.M = v; gw.N = d;

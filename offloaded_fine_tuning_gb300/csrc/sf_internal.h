@@ -52,6 +52,12 @@ struct GemmArgs {
   // kEpiGLU: optional fp32 copy of the gate and up outputs, row stride ldaux
   float* aux = nullptr;
   int64_t ldaux = 0;
+  // kEpiF32 only: up to splitk_max ranges of K run as separate work units
+  // when that fills the SMs better; split 0 writes C, split s > 0 the fp32
+  // slice ws + (s - 1) * M * ldc, and a fixed-order sum adds the slices into
+  // C (ws: (splitk_max - 1) * M * ldc floats, or null for no split)
+  int splitk_max = 1;
+  float* ws = nullptr;
 };
 
 // Returns 0, or a negative status with a message in `why` (64 chars at least).

@@ -132,15 +132,17 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // softmax warps work, so each tile's TMEM holds one S (P written over it as
 // bf16) and one O.
 //
-//   warp 0      TMA: K and V blocks (2- and 2-stage rings at head dim 128),
-//               both Q tiles at an item's first block
+//   warp 0      TMA: one ring of K/V entries (2 at head dim 128, 4 at 64;
+//               entry G + 1 carries V(G) and K(G + 1), what the MMA step of
+//               block G reads), both Q tiles at an item's first block
 //   warp 1      MMA issuer; TMEM owner (S0 | S1 | O0 | O1)
 //   warp 2      TMA store of each staged O tile
 //   warps 3-6   softmax of tile 0, one thread per query row
 //   warps 7-10  softmax of tile 1
 //
-// Per block G the MMA thread issues O0 += P0 V, S0' = Q0 K'^T, O1 += P1 V,
-// S1' = Q1 K'^T.  S' overwrites the columns that held P: the tensor core
+// Per block G the MMA thread waits once for its K/V entry, issues O0 += P0
+// V, S0' = Q0 K'^T, O1 += P1 V, S1' = Q1 K'^T, and releases the entry once.
+// S' overwrites the columns that held P: the tensor core
 // executes one thread's MMAs in issue order, so P is read before it is
 // overwritten.  A commit after S' also covers every earlier P V of the CTA,
 // so once a softmax thread sees S' it may rescale its O row: no P V of its

@@ -621,6 +621,7 @@ def run_lce(args):
     clk = clocks.stop()
     assert sf.device_error() == 0
     ms = e0.elapsed_time(e1) / args.steps
+    launches_per_step = sf.lce_launches()
     # end to end through the public call on host buffers (bf16 bits), in
     # page-locked memory as a training loop would keep them
     hbits = hb.view(torch.int16).pin_memory().numpy().view(np.uint16)
@@ -634,7 +635,6 @@ def run_lce(args):
     e2e_s = (time.perf_counter() - t0) / args.steps
     flops = 3 * 2.0 * n * V * d
     tf = flops / (ms / 1e3) / 1e12
-    n_chunks = (n + chunk - 1) // chunk
     cpu = None
     if not args.no_cpu_baseline:
         v, secs, desc = oracle_lce_sample(c)
@@ -650,7 +650,7 @@ def run_lce(args):
         "e2e": {"value": n / e2e_s, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
                 "h2d_bytes_per_step": n * d * 2 + V * d * 2 + n * 4,
                 "d2h_bytes_per_step": 4 + n * d * 2 + V * d * 4},
-        "gpu_launches": args.steps * (4 * n_chunks + 1),
+        "gpu_launches": args.steps * launches_per_step,
         "roofline": {"kernel": "fused LM head (3 GEMMs per chunk + row softmax)", "bound": "tensor",
                      "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
                      "traffic": None, "flops_per_step": flops,

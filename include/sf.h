@@ -455,11 +455,20 @@ int sf_op_gemm_swiglu_bwd(int64_t M, int64_t F, int64_t K, const void* dy, int64
  * h bf16 [n, d], w bf16 [v, d], labels int32 [n] (device), loss fp32 [1].
  * n_valid is the number of labels != SF_IGNORE_INDEX (the caller counts it).
  * workspace: sf_op_lce_workspace_bytes(n, v, chunk_rows) bytes, 256-aligned:
- * a chunk's fp32 logits and bf16 dZ (6 bytes per logit) and n fp32 row losses. */
+ * a chunk's fp32 logits and bf16 dZ (6 bytes per logit) and n fp32 row losses.
+ * With c = min(chunk_rows, n) and r(x) = x rounded up to 256: fp32 logits
+ * [c, v] at byte 0, bf16 dZ [c, v] at r(4cv), row losses [n] (lse - z[label],
+ * 0 on ignored rows) at r(4cv) + r(2cv).  On return dZ holds the last chunk's
+ * rows and the row losses all n rows; the logits area is overwritten. */
 int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64_t n, int32_t d,
               int32_t v, int64_t n_valid, int64_t chunk_rows, void* workspace, float* loss,
               float* dh, float* dw, void* stream);
 int64_t sf_op_lce_workspace_bytes(int64_t n, int32_t v, int64_t chunk_rows);
+/* The number of kernels the calling thread's last successful sf_op_lce call
+ * launched (per chunk: the logits GEMM, the cross-entropy rows, the dH GEMM
+ * and, when it ran as vocabulary ranges, their sum, the dW GEMM; then the loss
+ * sum); 0 before any call.  No device work. */
+int64_t sf_op_lce_launches(void);
 
 /* sf_op_rmsnorm_bwd_noalloc: the same operation and results as
  * sf_op_rmsnorm_bwd, for callers that cannot allocate device memory (for

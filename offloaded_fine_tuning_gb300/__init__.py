@@ -124,6 +124,7 @@ _SIGS = {
     "sf_op_swiglu_bwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, _VP]),
     "sf_op_lce": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, _I32, _I64, _I64, _VP, _VP, _VP, _VP, _VP]),
     "sf_op_lce_workspace_bytes": (_I64, [_I64, _I32, _I64]),
+    "sf_op_lce_launches": (_I64, []),
     "sf_op_device_error": (ctypes.c_int, [ctypes.POINTER(_I32)]),
 }
 
@@ -429,6 +430,11 @@ def op_swiglu_bwd(dm, ab, dab, rows, ffn, stream=0) -> int:
 
 def lce_workspace_bytes(n, v, chunk_rows) -> int:
     return int(lib().sf_op_lce_workspace_bytes(n, v, chunk_rows))
+
+
+def lce_launches() -> int:
+    """Kernels launched by this thread's last successful op_lce call."""
+    return int(lib().sf_op_lce_launches())
 
 
 def op_lce(h, w, labels, n, d, v, n_valid, chunk_rows, workspace, loss, dh, dw, stream=0) -> int:

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "ptx.cuh"
 #include "sf.h"
 #include "sf_internal.h"
 
@@ -478,12 +479,162 @@ void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16*
 }
 
 // ------------------------------------------------------------------ cross-entropy rows
-// One CTA per row of fp32 logits: lse by an online max / sum-exp pass, then
+// Per row of fp32 logits z: lse = log sum_v exp(z_v), loss = lse - z_label and
 // dz = (exp(z - lse) - [v == label]) * inv_n as bf16 into its own buffer (the
 // operand of the dH and dW products); rows whose label is ignore (-100) get
-// dz = 0 and loss 0.  The second pass re-reads the row, mostly from L2.
-constexpr int kCeThreads = 512;
+// dz = 0 and loss 0.
+//
+// Cluster form (rows of up to kCeMaxCluster slices of kCeSliceMax bytes):
+// the CTAs of one cluster share a row, each holding a contiguous slice of it
+// in shared memory, copied in by the bulk-copy unit in kCePieces pieces so
+// that the max pass starts on the first piece while the rest lands.  Each
+// CTA takes its slice's max m_r, overwrites its slice with exp(z - m_r)
+// while summing it (s_r), and publishes (m_r, s_r); every CTA combines the
+// cluster's pairs into lse through distributed shared memory and writes dz
+// from its slice as exp(z - m_r) * exp(m_r - lse).  The row is read from HBM
+// once (fp32) and dz written once (bf16): 6 bytes per logit.  (One online
+// max / sum-exp pass with dz = exp(z - lse) recomputed measured 7% slower:
+// two exponentials per logit instead of one.)
+//
+// One cluster per row, several CTAs per SM (slices up to kCeSliceShare bytes
+// let three share an SM), so that one CTA's reductions, cluster barrier and
+// stores overlap the others' copies.  Measured on 2,048 rows of 152,064
+// logits: 256 threads a CTA beat 512 by 7% and 128 by 10%; clusters of 16
+// (38 KB slices, five CTAs per SM) were 15% slower; a persistent form, one
+// CTA per SM with two slice buffers and the next row's copy in flight, was
+// 1.6x slower (each row's reductions and barriers then sit on the SM's
+// critical path).  The published pair is ordered by its one writer's fence;
+// every thread's cluster arrival is relaxed.
 
+// (m, s) <- the pair of the union of two sets given as (max, sum of exp(x - max)).
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  s = s * __expf(m - M) + s2 * __expf(m2 - M);
+  m = M;
+}
+// The pair of the whole warp, in every lane (lane 0's order of combination).
+__device__ __forceinline__ void warp_lse_merge(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+  m = __shfl_sync(0xffffffffu, m, 0);
+  s = __shfl_sync(0xffffffffu, s, 0);
+}
+
+constexpr int kCeThreads = 256;
+constexpr int kCePieces = 4;
+constexpr int kCeSliceMax = 200 * 1024;    // largest slice a CTA holds
+constexpr int kCeSliceShare = 76 * 1024;   // three CTAs per SM up to this slice
+constexpr int kCeMaxCluster = 8;
+
+__global__ void __launch_bounds__(kCeThreads)
+    ce_rows_cluster_kernel(const float* __restrict__ z, __nv_bfloat16* __restrict__ dz,
+                           const int32_t* __restrict__ labels, int64_t vocab, float inv_n,
+                           float* __restrict__ loss_rows, int* err) {
+  extern __shared__ __align__(128) float4 slice[];
+  __shared__ __align__(8) uint64_t bars[kCePieces];
+  __shared__ __align__(8) float2 pub;  // (m_r, s_r), read by the cluster
+  __shared__ float2 red[32];
+  uint32_t ncl;
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncl));
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = blockIdx.x / ncl;
+  const int64_t n4 = vocab >> 2;  // vocab % 8 == 0 (checked by the caller)
+  const int64_t q = (n4 + ncl - 1) / ncl;
+  const int64_t lo = rank * q < n4 ? rank * q : n4;
+  const int len = (int)((lo + q < n4 ? lo + q : n4) - lo);  // float4 of this slice
+  const int pq = (len + kCePieces - 1) / kCePieces;         // float4 per piece
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint2* dr = reinterpret_cast<uint2*>(dz + row * vocab) + lo;
+  const int label = labels[row];
+  if (label < 0) {  // uniform over the cluster: no cluster barrier is reached
+    const uint2 zero = make_uint2(0, 0);
+    for (int i = threadIdx.x; i < len; i += blockDim.x) dr[i] = zero;
+    if (rank == 0 && threadIdx.x == 0) loss_rows[row] = 0.f;
+    return;
+  }
+  if (threadIdx.x == 0) {
+    const float4* src = reinterpret_cast<const float4*>(z + row * vocab) + lo;
+    for (int k = 0; k < kCePieces; ++k) mbar_init(smem_u32(&bars[k]), 1);
+    fence_mbar_init();
+    for (int k = 0; k < kCePieces; ++k) {
+      const int a = k * pq < len ? k * pq : len, b = a + pq < len ? a + pq : len;
+      const uint32_t bytes = (uint32_t)(b - a) * 16u;
+      mbar_arrive_expect_tx(smem_u32(&bars[k]), bytes);
+      if (bytes > 0) bulk_load(smem_u32(slice + a), src + a, bytes, smem_u32(&bars[k]));
+    }
+  }
+  __syncthreads();
+  // the slice's max, piece by piece as the copies land
+  bool ok = true;
+  float m = -FLT_MAX;
+  for (int k = 0; k < kCePieces; ++k) {
+    if (ok && !mbar_wait(smem_u32(&bars[k]), 0, nullptr)) {
+      record_error(err, kDevCeTimeout);
+      ok = false;
+    }
+    const int a = k * pq < len ? k * pq : len, b = a + pq < len ? a + pq : len;
+    if (ok)
+      for (int i = a + threadIdx.x; i < b; i += blockDim.x) {
+        const float4 f = slice[i];
+        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+      }
+  }
+  m = warp_max(m);
+  if (lane == 0) red[w].x = m;
+  __syncthreads();
+  float mr = -FLT_MAX;
+  for (int i = 0; i < nw; ++i) mr = fmaxf(mr, red[i].x);
+  // exp(z - m_r) over the slice, in place, and its sum
+  float s = 0.f;
+  if (ok)
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+      float4 f = slice[i];
+      f.x = __expf(f.x - mr); f.y = __expf(f.y - mr);
+      f.z = __expf(f.z - mr); f.w = __expf(f.w - mr);
+      slice[i] = f;
+      s += (f.x + f.y) + (f.z + f.w);
+    }
+  s = warp_sum(s);
+  if (lane == 0) red[w].y = s;
+  __syncthreads();
+  if (w == 0) {  // the CTA's pair, published for the cluster
+    const float t = warp_sum(lane < nw ? red[lane].y : 0.f);
+    if (lane == 0) {
+      pub = make_float2(mr, t);
+      fence_acq_rel_cluster();  // the pair before this thread's arrival
+    }
+  }
+  cluster_arrive_relaxed();
+  cluster_wait();  // every CTA's pair is published
+  // lane r reads CTA r's pair (one remote round trip), the warp combines
+  // them in lane 0's order: every thread of the cluster has the same lse
+  float2 v = make_float2(-FLT_MAX, 0.f);
+  if (lane < (int)ncl) v = ld_shared_cluster_f32x2(mapa_shared(smem_u32(&pub), lane));
+  warp_lse_merge(v.x, v.y);
+  cluster_arrive_relaxed();  // this CTA no longer reads its peers' shared memory
+  const float lse = v.x + __logf(v.y);
+  if (rank == 0 && threadIdx.x == 0) loss_rows[row] = lse - z[row * vocab + label];
+  const float scale = __expf(mr - lse) * inv_n;
+  const int64_t lab4 = (int64_t)label - lo * 4;  // label offset within the slice
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    const float4 f = slice[i];
+    const int64_t k = lab4 - (int64_t)i * 4;
+    __nv_bfloat162 lo2 = __floats2bfloat162_rn(f.x * scale - (k == 0 ? inv_n : 0.f),
+                                               f.y * scale - (k == 1 ? inv_n : 0.f));
+    __nv_bfloat162 hi2 = __floats2bfloat162_rn(f.z * scale - (k == 2 ? inv_n : 0.f),
+                                               f.w * scale - (k == 3 ? inv_n : 0.f));
+    dr[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+  }
+  if (!ok && threadIdx.x == 0)  // let copies still in flight land before exit
+    for (int k = 0; k < kCePieces; ++k) mbar_wait(smem_u32(&bars[k]), 0, nullptr);
+  __syncwarp();
+  cluster_wait();  // peers have read this CTA's pair
+}
+
+// Two-pass form, for rows longer than the clusters' shared memory holds: one
+// CTA per row takes lse by an online max / sum-exp pass over the row in HBM,
+// then reads the row again for dz (10 bytes per logit).
 __global__ void __launch_bounds__(kCeThreads)
     ce_rows_f32_kernel(const float* __restrict__ z, __nv_bfloat16* __restrict__ dz,
                        const int32_t* __restrict__ labels, int64_t vocab, float inv_n,
@@ -534,11 +685,51 @@ __global__ void __launch_bounds__(kCeThreads)
   }
 }
 
-void ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
-                 int64_t vocab, float inv_n, float* loss_rows, cudaStream_t st) {
-  if (rows <= 0) return;
-  ce_rows_f32_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, dz, labels, vocab, inv_n,
-                                                            loss_rows);
+// CTAs per row of the cluster kernel for `vocab` logits: the smallest power
+// of two up to kCeMaxCluster whose slices let three CTAs share an SM, else
+// kCeMaxCluster while a slice fits kCeSliceMax; 0 (the two-pass kernel) for
+// longer rows.
+int ce_cluster_size(int64_t vocab) {
+  const int64_t n4 = vocab / 4;
+  for (int c = 1; c <= kCeMaxCluster; c *= 2)
+    if ((n4 + c - 1) / c * 16 <= kCeSliceShare) return c;
+  return (n4 + kCeMaxCluster - 1) / kCeMaxCluster * 16 <= kCeSliceMax ? kCeMaxCluster : 0;
+}
+
+int ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
+                int64_t vocab, float inv_n, float* loss_rows, int* err, cudaStream_t st) {
+  if (rows <= 0) return 0;
+  const int ncl = ce_cluster_size(vocab);
+  if (ncl == 0) {
+    ce_rows_f32_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, dz, labels, vocab, inv_n,
+                                                              loss_rows);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (!attr_set[dev]) {  // idempotent: racing threads set the same value
+    if (cudaFuncSetAttribute(ce_rows_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCeSliceMax) != cudaSuccess)
+      return -1;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(rows * ncl));
+  cfg.blockDim = dim3(kCeThreads);
+  cfg.dynamicSmemBytes = (size_t)((vocab / 4 + ncl - 1) / ncl * 16);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, ce_rows_cluster_kernel, z, dz, labels, vocab, inv_n, loss_rows,
+                         err) != cudaSuccess)
+    return -1;
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 // ------------------------------------------------------------------ reductions / casts

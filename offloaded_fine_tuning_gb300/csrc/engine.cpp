@@ -943,11 +943,14 @@ constexpr int kHeadSplitK = 4;
 int gemm_args(sf_ctx* ctx, const sf::GemmArgs& g, double flops = 0.0) {
   int st;
   char why[128] = {0};
+  int launched = 0;
+  sf::GemmArgs a = g;
+  a.launched = &launched;
   {
     Timed t(ctx, 0, flops > 0.0 ? flops : 2.0 * g.M * g.N * g.K);
-    st = sf::gemm(g, ctx->dev_err, ctx->sC, why);
+    st = sf::gemm(a, ctx->dev_err, ctx->sC, why);
   }
-  ctx->launches += 1;
+  ctx->launches += launched;  // the GEMM and, for a split K, its fixed-order sum
   ctx->stats.gemm_launches += 1;
   if (st != 0) {
     ctx->set_err("%s", why);
@@ -1119,7 +1122,11 @@ int head_fwd_bwd(sf_ctx* c, int64_t T, int64_t n_valid) {
     const bool first = r0 == 0, last = r0 + n >= T;
     // fp32 logits of the chunk; the row softmax writes dZ (bf16) beside them
     RET(gemm(c, sf::kNT, sf::kEpiF32, n, V, d, c->hf + r0 * d, d, c->Wlm, d, c->zf, V));
-    sf::ce_rows_f32(c->zf, c->dz, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0, c->sC);
+    if (sf::ce_rows_f32(c->zf, c->dz, c->labels_dev + r0, n, V, inv_n, c->loss_rows + r0,
+                        c->dev_err, c->sC) != 0) {
+      ctx->set_err("cross-entropy launch failed");
+      return SF_ECUDA;
+    }
     {  // dH = dZ W_lm, over up to kHeadSplitK vocabulary ranges when that fills
        // the SMs better; the partial sums go to the chunk's fp32 logits, which
        // the cross-entropy kernel has already read

@@ -970,6 +970,7 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
   } else {
     rc = launch_epi<true, true, 128>(a.epi, ta, tb, tb2, p, st, why);
   }
+  if (rc == 0 && a.launched) *a.launched += 1;
   if (rc == 0 && splitk > 1) {
     const int64_t n = a.M * (a.N / 4);
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
@@ -979,6 +980,7 @@ int gemm(const GemmArgs& a, int* dev_err, cudaStream_t st, char* why) {
       snprintf(why, 64, "gemm: split-K sum launch failed");
       return -3;
     }
+    if (a.launched) *a.launched += 1;
   }
   return rc;
 }

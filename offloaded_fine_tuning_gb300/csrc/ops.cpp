@@ -39,6 +39,9 @@ int* dev_err_word() {
 cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 int launched() { return cudaGetLastError() == cudaSuccess ? SF_OK : SF_ECUDA; }
 
+// Kernels launched by the calling thread's last sf_op_lce call.
+thread_local int64_t lce_launches = 0;
+
 }  // namespace
 
 extern "C" {
@@ -231,29 +234,37 @@ int sf_op_lce(const uint16_t* h, const uint16_t* w, const int32_t* labels, int64
   const float inv_n = n_valid > 0 ? 1.f / (float)n_valid : 0.f;
   char why[128];
   cudaStream_t st = S(stream);
+  int count = 0;  // kernels launched, for sf_op_lce_launches
+  lce_launches = 0;
   for (int64_t r0 = 0; r0 < n; r0 += c) {
     const int64_t rows = (c < n - r0) ? c : n - r0;
     sf::GemmArgs z;
     z.layout = sf::kNT; z.epi = sf::kEpiF32; z.M = rows; z.N = v; z.K = d;
-    z.A = H + r0 * d; z.lda = d; z.B = W; z.ldb = d; z.C = zf; z.ldc = v;
+    z.A = H + r0 * d; z.lda = d; z.B = W; z.ldb = d; z.C = zf; z.ldc = v; z.launched = &count;
     if (sf::gemm(z, err, st, why) != 0) return SF_ECUDA;
-    sf::ce_rows_f32(zf, dz, labels + r0, rows, v, inv_n, loss_rows + r0, st);
+    if (sf::ce_rows_f32(zf, dz, labels + r0, rows, v, inv_n, loss_rows + r0, err, st) != 0)
+      return SF_ECUDA;
+    ++count;
     // dH over up to four vocabulary ranges when that fills the SMs better; the
     // partial sums go to the chunk's fp32 logits, which the row kernel has read
     sf::GemmArgs gx;
     gx.layout = sf::kNN; gx.epi = sf::kEpiF32; gx.M = rows; gx.N = d; gx.K = v;
     gx.A = dz; gx.lda = v; gx.B = W; gx.ldb = d; gx.C = dh + r0 * d; gx.ldc = d;
     gx.splitk_max = (int)std::min<int64_t>(4, 1 + (c * (int64_t)v) / (rows * (int64_t)d));
-    gx.ws = zf;
+    gx.ws = zf; gx.launched = &count;
     if (sf::gemm(gx, err, st, why) != 0) return SF_ECUDA;
     sf::GemmArgs gw;
     gw.layout = sf::kTN; gw.epi = r0 == 0 ? sf::kEpiF32 : sf::kEpiF32Acc; gw.M = v; gw.N = d;
     gw.K = rows; gw.A = dz; gw.lda = v; gw.B = H + r0 * d; gw.ldb = d; gw.C = dw; gw.ldc = d;
+    gw.launched = &count;
     if (sf::gemm(gw, err, st, why) != 0) return SF_ECUDA;
   }
   sf::sum_f32(loss_rows, n, inv_n, loss, st);
+  lce_launches = count + 1;
   return launched();
 }
+
+int64_t sf_op_lce_launches(void) { return lce_launches; }
 
 // The fused-epilogue projections: argument checks in sf::gemm_check.
 static int run_gemm(const sf::GemmArgs& g, cudaStream_t st) {

@@ -58,6 +58,8 @@ struct GemmArgs {
   // C (ws: (splitk_max - 1) * M * ldc floats, or null for no split)
   int splitk_max = 1;
   float* ws = nullptr;
+  // when set, the number of kernels the call launched is added to it
+  int* launched = nullptr;
 };
 
 // Returns 0, or a negative status with a message in `why` (64 chars at least).
@@ -86,11 +88,17 @@ void bias_grad_f16(const __nv_bfloat16* x, int64_t ld, int64_t rows, int cols, f
                    int parts, uint16_t* out, float scale, cudaStream_t st);
 void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int heads,
                   int head_dim, const float2* cs, int inverse, cudaStream_t st);
-// The fused cross-entropy rows on fp32 logits z [rows, vocab]: lse by an
-// online max / sum-exp, loss_rows[r] = lse - z[r, label] (0 when ignored) and
+// The fused cross-entropy rows on fp32 logits z [rows, vocab] (vocab % 8 == 0,
+// z 16-byte aligned): loss_rows[r] = lse - z[r, label] (0 when ignored) and
 // dz [rows, vocab] bf16 = (softmax(z) - onehot) * inv_n (0 on ignored rows).
-void ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
-                 int64_t vocab, float inv_n, float* loss_rows, cudaStream_t st);
+// A cluster of CTAs shares a row held in shared memory, so z is read once;
+// a wait that runs out writes kDevCeTimeout to *err.  Returns 0, or -1 when
+// the launch fails.
+int ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
+                int64_t vocab, float inv_n, float* loss_rows, int* err, cudaStream_t st);
+// CTAs per row of the cross-entropy kernel for this vocabulary (0: one CTA
+// reading the row twice, for rows beyond the clusters' shared memory).
+int ce_cluster_size(int64_t vocab);
 void swiglu_fwd(const __nv_bfloat16* ab, __nv_bfloat16* m, int64_t rows, int ffn,
                 cudaStream_t st);
 void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16* dab,

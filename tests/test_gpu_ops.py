@@ -548,11 +548,68 @@ def test_lce_split_vocabulary_ranges_match_oracle_and_repeat():
     z = h.astype(np.float64) @ w.astype(np.float64).T
     loss_ref, dz, _ = oracle.cross_entropy_fwd_bwd(z, lab)
     runs = [lce_run(h, w, lab, 512) for _ in range(2)]
+    # two chunks of (logits GEMM, rows, dH GEMM, the ranges' sum, dW GEMM) and the loss sum
+    assert sf.lce_launches() == 2 * 5 + 1
     loss, dh, dw = runs[0]
     assert abs(loss - loss_ref) / loss_ref < 1e-3
     assert rel_l2(dh, dz @ w.astype(np.float64)) < 1e-2
     assert rel_l2(dw, dz.T @ h.astype(np.float64)) < 1e-2
     assert np.array_equal(runs[0][1], runs[1][1]) and np.array_equal(runs[0][2], runs[1][2])
+
+
+@pytest.mark.parametrize("vocab,n", [(1000, 160), (32768, 160), (65536, 160), (152064, 160),
+                                     (409600, 48), (409608, 48)])
+def test_lce_dz_and_row_losses_match_oracle(vocab, n):
+    """The cross-entropy rows element by element, read from the workspace of
+    one single-chunk call: every dZ entry against the oracle's
+    (softmax(z) - onehot) / n_valid, and every row loss lse - z[label].  The
+    vocabularies take the row kernel through one, two, four and eight CTAs
+    per row (409600: the longest row a cluster holds) and through the
+    single-CTA kernel that reads a row twice (409608).  Runs of ignored rows
+    sit between valid ones; labels sit on the first and last logit and on both
+    sides of every eighth of the row, where the CTAs of a cluster split it.
+
+    h holds quarter-integers in [-1, 1] and W eighth-integers in [-2, 2]: each
+    product is a multiple of 1/32 below 2 in size, so every partial sum of the
+    64-term logits is exact in fp32 and z reaches the row kernel without
+    error (std ~6, so p spans ~20 orders of magnitude).  What remains is
+    the kernel's own arithmetic: bf16 rounding of dz (2^-9 relative) and the
+    fp32 exponentials and lse (at most ~1e-5 relative in p: the argument of
+    an exponential, up to 60 in size, rounds to 2^-24 of itself, and the sum
+    under the lse runs over thousands of fp32 terms).  The p term of the
+    bound also covers the label column, where p - 1 cancels."""
+    d = 64
+    rng = np.random.default_rng(13)
+    h = rng.integers(-4, 5, (n, d)).astype(np.float32) / 4
+    w = rng.integers(-16, 17, (vocab, d)).astype(np.float32) / 8
+    lab = rng.integers(0, vocab, n).astype(np.int32)
+    edges = [0, vocab - 1] + [k * vocab // 8 + o for k in range(1, 8) for o in (-1, 0)]
+    lab[:len(edges)] = edges
+    lab[[17, 21, 30, 31, 32, 33, n - 1]] = sf.IGNORE_INDEX
+    n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
+    H, W, Y = cuda(h, torch.bfloat16), cuda(w, torch.bfloat16), cuda(lab, torch.int32)
+    ws = torch.zeros(sf.lce_workspace_bytes(n, vocab, n), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    dh = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    dw = torch.empty((vocab, d), dtype=torch.float32, device="cuda")
+    assert sf.op_lce(H.data_ptr(), W.data_ptr(), Y.data_ptr(), n, d, vocab, n_valid, n,
+                     ws.data_ptr(), loss.data_ptr(), dh.data_ptr(), dw.data_ptr(), stream()) == 0
+    sync()
+    assert sf.device_error() == 0
+    r256 = lambda x: (x + 255) // 256 * 256
+    o_dz, o_rows = r256(4 * n * vocab), r256(4 * n * vocab) + r256(2 * n * vocab)
+    dz = ws[o_dz:o_dz + 2 * n * vocab].view(torch.bfloat16).float().cpu().numpy().reshape(n, vocab)
+    rows = ws[o_rows:o_rows + 4 * n].view(torch.float32).cpu().numpy()
+    z = h.astype(np.float64) @ w.astype(np.float64).T
+    loss_ref, dz_ref, lse = oracle.cross_entropy_fwd_bwd(z, lab)
+    valid = lab != sf.IGNORE_INDEX
+    rows_ref = np.where(valid, lse - z[np.arange(n), np.where(valid, lab, 0)], 0.0)
+    assert np.max(np.abs(rows - rows_ref) / (1.0 + np.abs(rows_ref))) < 1e-5
+    assert not np.any(dz[~valid])
+    p_term = np.exp(z - lse[:, None]) * valid[:, None] / n_valid
+    err = np.abs(dz - dz_ref) - (2.0 ** -8 * np.abs(dz_ref) + 3e-5 * p_term)
+    assert np.max(err) <= 0.0, np.unravel_index(np.argmax(err), err.shape)
+    assert abs(float(host(loss)[0]) - loss_ref) < 1e-5 * loss_ref
 
 
 def test_lce_all_ignored_gives_zero():

@@ -548,8 +548,9 @@ def test_lce_split_vocabulary_ranges_match_oracle_and_repeat():
     z = h.astype(np.float64) @ w.astype(np.float64).T
     loss_ref, dz, _ = oracle.cross_entropy_fwd_bwd(z, lab)
     runs = [lce_run(h, w, lab, 512) for _ in range(2)]
-    # two chunks of (logits GEMM, rows, dH GEMM, the ranges' sum, dW GEMM) and the loss sum
-    assert sf.lce_launches() == 2 * 5 + 1
+    # one chunk of 512 rows: logits GEMM, rows, dH GEMM, the ranges' sum, dW
+    # GEMM, then the loss sum
+    assert sf.lce_launches() == 5 + 1
     loss, dh, dw = runs[0]
     assert abs(loss - loss_ref) / loss_ref < 1e-3
     assert rel_l2(dh, dz @ w.astype(np.float64)) < 1e-2

@@ -453,7 +453,10 @@ int sf_op_gemm_swiglu_bwd(int64_t M, int64_t F, int64_t K, const void* dy, int64
  * dh = dZ W (fp32 [n, d]), dw = dZ^T h (fp32 [v, d]) with
  * dZ = (softmax(z) - onehot)/n_valid on valid rows, 0 on ignored rows.
  * h bf16 [n, d], w bf16 [v, d], labels int32 [n] (device), loss fp32 [1].
- * n_valid is the number of labels != SF_IGNORE_INDEX (the caller counts it).
+ * A negative label (SF_IGNORE_INDEX among them) ignores its row; n_valid is
+ * the number of labels in [0, v) (the caller counts it).  The labels live on
+ * the device, so this call cannot check them: a label >= v sets the device
+ * error word to 4 (sf_op_device_error) and its row is ignored.
  * workspace: sf_op_lce_workspace_bytes(n, v, chunk_rows) bytes, 256-aligned:
  * a chunk's fp32 logits and bf16 dZ (6 bytes per logit) and n fp32 row losses.
  * With c = min(chunk_rows, n) and r(x) = x rounded up to 256: fp32 logits
@@ -495,7 +498,10 @@ int sf_op_rmsnorm_bwd_noalloc(const float* x, const uint16_t* g, const float* rs
                               uint16_t* dg, int64_t rows, int32_t d, void* stream);
 
 /* Read and clear the device error word of the kernel API on the current
- * device (nonzero: a bounded device wait ran out).  Synchronises the device. */
+ * device.  0: no error; 1, 2, 3: a bounded wait ran out in a GEMM, an
+ * attention or a cross-entropy kernel; 4: sf_op_lce met a label at or beyond
+ * the vocabulary.  The first code a launch writes stays.  Synchronises the
+ * device. */
 int sf_op_device_error(int32_t* out);
 
 #ifdef __cplusplus

@@ -546,7 +546,11 @@ __global__ void __launch_bounds__(kCeThreads)
   const int pq = (len + kCePieces - 1) / kCePieces;         // float4 per piece
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   uint2* dr = reinterpret_cast<uint2*>(dz + row * vocab) + lo;
-  const int label = labels[row];
+  int label = labels[row];
+  if (label >= vocab) {  // outside the vocabulary: reported, and the row ignored
+    if (rank == 0 && threadIdx.x == 0) record_error(err, kDevCeBadLabel);
+    label = -1;
+  }
   if (label < 0) {  // uniform over the cluster: no cluster barrier is reached
     const uint2 zero = make_uint2(0, 0);
     for (int i = threadIdx.x; i < len; i += blockDim.x) dr[i] = zero;
@@ -638,12 +642,16 @@ __global__ void __launch_bounds__(kCeThreads)
 __global__ void __launch_bounds__(kCeThreads)
     ce_rows_f32_kernel(const float* __restrict__ z, __nv_bfloat16* __restrict__ dz,
                        const int32_t* __restrict__ labels, int64_t vocab, float inv_n,
-                       float* __restrict__ loss_rows) {
+                       float* __restrict__ loss_rows, int* err) {
   __shared__ float shm[32], shs[32];
   const int64_t row = blockIdx.x;
   const float4* zr = reinterpret_cast<const float4*>(z + row * vocab);
   uint2* dr = reinterpret_cast<uint2*>(dz + row * vocab);
-  const int label = labels[row];
+  int label = labels[row];
+  if (label >= vocab) {  // outside the vocabulary: reported, and the row ignored
+    if (threadIdx.x == 0) record_error(err, kDevCeBadLabel);
+    label = -1;
+  }
   const int64_t n4 = vocab >> 2;  // vocab % 8 == 0 (checked by the caller)
   if (label < 0) {
     const uint2 zero = make_uint2(0, 0);
@@ -702,7 +710,7 @@ int ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_
   const int ncl = ce_cluster_size(vocab);
   if (ncl == 0) {
     ce_rows_f32_kernel<<<(unsigned)rows, kCeThreads, 0, st>>>(z, dz, labels, vocab, inv_n,
-                                                              loss_rows);
+                                                              loss_rows, err);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
   }
   static bool attr_set[64] = {false};

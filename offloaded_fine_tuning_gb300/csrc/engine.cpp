@@ -1622,7 +1622,10 @@ int step(sf_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S
   const auto t_gpu_done = Clock::now();
   trace(ctx, 7, -9);
   if (*ctx->err_pin != 0) {
-    ctx->set_err("device wait limit reached in a kernel (code %d)", *ctx->err_pin);
+    ctx->set_err(*ctx->err_pin == sf::kDevCeBadLabel
+                     ? "a label outside the vocabulary reached the cross-entropy kernel (code %d)"
+                     : "device wait limit reached in a kernel (code %d)",
+                 *ctx->err_pin);
     ctx->poisoned = true;
     wait_tasks(ctx);
     return SF_EDEVICE;

@@ -11,15 +11,9 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
-namespace sf {
+#include "sf_internal.h"  // DevErr
 
-// Error codes written to the device error word.
-enum DevErr : int {
-  kDevOk = 0,
-  kDevGemmTimeout = 1,
-  kDevAttnTimeout = 2,
-  kDevCeTimeout = 3,
-};
+namespace sf {
 
 // Two seconds: far longer than any pipeline wait of a healthy launch.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -7,6 +7,15 @@
 
 namespace sf {
 
+// Codes written to the device error word (the first one a launch meets).
+enum DevErr : int {
+  kDevOk = 0,
+  kDevGemmTimeout = 1,
+  kDevAttnTimeout = 2,
+  kDevCeTimeout = 3,
+  kDevCeBadLabel = 4,  // a label at or beyond the vocabulary (the row is ignored)
+};
+
 // Operand layouts of C[M,N] = A * B (all matrices row-major in memory):
 //   kNT: A [M,K] (K contiguous), B [N,K] (K contiguous)   -> Y = X W^T
 //   kNN: A [M,K] (K contiguous), B [K,N] (N contiguous)   -> dX = dY W

@@ -485,10 +485,11 @@ def test_attention_full_size_sampled_heads(det):
 
 
 # ------------------------------------------------------------------ fused LM head + CE
-def lce_run(h, w, lab, chunk):
+def lce_run(h, w, lab, chunk, n_valid=None):
     n, d = h.shape
     V = w.shape[0]
-    n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
+    if n_valid is None:
+        n_valid = int(np.sum(lab != sf.IGNORE_INDEX))
     H, W, Y = cuda(h, torch.bfloat16), cuda(w, torch.bfloat16), cuda(lab, torch.int32)
     ws = torch.empty(sf.lce_workspace_bytes(n, V, chunk), dtype=torch.uint8, device="cuda")
     loss = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -611,6 +612,28 @@ def test_lce_dz_and_row_losses_match_oracle(vocab, n):
     err = np.abs(dz - dz_ref) - (2.0 ** -8 * np.abs(dz_ref) + 3e-5 * p_term)
     assert np.max(err) <= 0.0, np.unravel_index(np.argmax(err), err.shape)
     assert abs(float(host(loss)[0]) - loss_ref) < 1e-5 * loss_ref
+
+
+@pytest.mark.parametrize("vocab", [256, 65536, 409608])
+def test_lce_label_beyond_vocabulary_is_reported_and_ignored(vocab):
+    """Device labels cannot be checked by the host: a label equal to the
+    vocabulary size sets device error 4 and its row is ignored, bit for bit
+    as if it carried the ignore index (one CTA per row, a cluster of four,
+    and the two-pass kernel)."""
+    n, d = 16, 64
+    h = bf16_values(rnd(21, (n, d)))
+    w = bf16_values(rnd(22, (vocab, d), 0.5))
+    lab = np.random.default_rng(23).integers(0, vocab, n).astype(np.int32)
+    bad, ign = lab.copy(), lab.copy()
+    bad[5], ign[5] = vocab, sf.IGNORE_INDEX
+    assert sf.device_error() == 0
+    got = lce_run(h, w, bad, n, n_valid=n - 1)
+    assert sf.device_error() == 4
+    want = lce_run(h, w, ign, n, n_valid=n - 1)
+    assert sf.device_error() == 0
+    assert got[0] == want[0]
+    assert np.array_equal(got[1], want[1]) and np.array_equal(got[2], want[2])
+    assert not np.any(got[1][5])
 
 
 def test_lce_all_ignored_gives_zero():

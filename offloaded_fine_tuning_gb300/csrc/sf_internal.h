@@ -101,8 +101,9 @@ void rope_inplace(__nv_bfloat16* qkv, int64_t ld, int64_t tokens, int seq, int h
 // z 16-byte aligned): loss_rows[r] = lse - z[r, label] (0 when ignored) and
 // dz [rows, vocab] bf16 = (softmax(z) - onehot) * inv_n (0 on ignored rows).
 // A cluster of CTAs shares a row held in shared memory, so z is read once;
-// a wait that runs out writes kDevCeTimeout to *err.  Returns 0, or -1 when
-// the launch fails.
+// a wait that runs out writes kDevCeTimeout to *err, and a label >= vocab
+// writes kDevCeBadLabel (its row is then ignored).  Returns 0, or -1 when the
+// launch fails.
 int ce_rows_f32(const float* z, __nv_bfloat16* dz, const int32_t* labels, int64_t rows,
                 int64_t vocab, float inv_n, float* loss_rows, int* err, cudaStream_t st);
 // CTAs per row of the cross-entropy kernel for this vocabulary (0: one CTA

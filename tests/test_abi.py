@@ -75,3 +75,13 @@ def test_kernel_api_rejects_bad_arguments_without_launching(sf):
     assert sfp.op_attn_fwd(0, 0, 0, 1, 16, 4, 2, 96) == sfp.SF_EINVAL
     assert sfp.op_swiglu_fwd(0, 0, 4, 12) == sfp.SF_EINVAL
     assert sfp.lce_workspace_bytes(100, 1000, 64) >= 64 * 1000 * 2 + 400
+    # the workspace holds a chunk's fp32 logits and bf16 dZ, 256-aligned, then the row losses
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert sfp.lce_workspace_bytes(100, 1000, 64) == r256(4 * 64 * 1000) + r256(2 * 64 * 1000) + r256(4 * 100)
+    assert sfp.lce_workspace_bytes(50, 1000, 64) == r256(4 * 50 * 1000) + r256(2 * 50 * 1000) + r256(4 * 50)
+    # sf_op_lce: vocabulary not a multiple of 8, misaligned workspace, n_valid above n
+    a = 4096
+    assert sfp.op_lce(a, a, a, 16, 64, 1004, 16, 16, a, a, a, a) == sfp.SF_EINVAL
+    assert sfp.op_lce(a, a, a, 16, 64, 1000, 16, 16, a + 16, a, a, a) == sfp.SF_EINVAL
+    assert sfp.op_lce(a, a, a, 16, 64, 1000, 17, 16, a, a, a, a) == sfp.SF_EINVAL
+    assert sfp.lce_launches() == 0  # no call has launched anything on this thread

@@ -481,8 +481,10 @@ void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16*
 // ------------------------------------------------------------------ cross-entropy rows
 // Per row of fp32 logits z: lse = log sum_v exp(z_v), loss = lse - z_label and
 // dz = (exp(z - lse) - [v == label]) * inv_n as bf16 into its own buffer (the
-// operand of the dH and dW products); rows whose label is ignore (-100) get
-// dz = 0 and loss 0.
+// operand of the dH and dW products); rows whose label is negative (the
+// ignore index -100 among them) get dz = 0 and loss 0, and so does a row
+// whose label is at or beyond the vocabulary, which is also reported as
+// kDevCeBadLabel (the labels are device data that no host code has seen).
 //
 // Cluster form (rows of up to kCeMaxCluster slices of kCeSliceMax bytes):
 // the CTAs of one cluster share a row, each holding a contiguous slice of it

@@ -484,7 +484,8 @@ void swiglu_bwd(const __nv_bfloat16* dm, const __nv_bfloat16* ab, __nv_bfloat16*
 // operand of the dH and dW products); rows whose label is negative (the
 // ignore index -100 among them) get dz = 0 and loss 0, and so does a row
 // whose label is at or beyond the vocabulary, which is also reported as
-// kDevCeBadLabel (the labels are device data that no host code has seen).
+// kDevCeBadLabel (the kernel API takes labels in device memory, where the
+// host cannot check them).
 //
 // Cluster form (rows of up to kCeMaxCluster slices of kCeSliceMax bytes):
 // the CTAs of one cluster share a row, each holding a contiguous slice of it
